@@ -1,0 +1,151 @@
+"""fp64 CPU oracle of the delta-rule recurrent memory (DeltaNet, Gated DeltaNet,
+Kimi Delta Attention).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library never
+does, and this package imports nothing from it.
+
+The arithmetic lives in ``dro.c`` (a plain token-by-token loop in fp64, with the
+hand-derived reverse-time recurrence for the gradients); this module only builds
+it with gcc and marshals numpy arrays through ctypes.  What it computes is
+defined on the page "Linear Attention Architectures: Mechanisms, Trade-offs, and
+Cross-Layer Routing", section "Metodologia y Marco de Trabajo", item 1 (the
+unified recurrent-memory notation and its DeltaNet / Gated DeltaNet / Kimi Delta
+Attention bullets); the header of ``dro.c`` states each step.
+
+Parity status: every function here is pinned by ``tests/test_oracle.py``
+(explicit matrix unrolling, central finite differences, the beta = 0 closed
+form, exact recall, variant nesting, orthonormal keys, split/varlen chaining,
+a hand-worked scalar example).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dro.c")
+_LIB = os.path.join(_HERE, "libdro.so")
+_lock = threading.Lock()
+_lib = None
+
+VARIANTS = {"deltanet": 0, "gdn": 1, "kda": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile dro.c into libdro.so (gcc, OpenMP if available)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c99", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            common = [I, I, I, I, I, I, ctypes.c_double, P, I, P, I]
+            lib.dro_forward.argtypes = common + [P] * 8 + [I]
+            lib.dro_forward.restype = I
+            lib.dro_backward.argtypes = common + [P] * 14 + [I]
+            lib.dro_backward.restype = I
+            lib.dro_max_threads.argtypes = []
+            lib.dro_max_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().dro_max_threads())
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i32(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _dims(q, v, cu_seqlens):
+    B, T, H, dk = q.shape
+    dv = v.shape[3]
+    N = B if cu_seqlens is None else len(cu_seqlens) - 1
+    return B, T, H, dk, dv, N
+
+
+def forward(variant, q, k, v, beta, g=None, h0=None, scale=1.0, cu_seqlens=None,
+            units=None, nthreads=0):
+    """Run the recurrence forward.  Returns (o, hT) as fp64 numpy arrays.
+
+    Shapes: q, k [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H]; g [B,T,H] (GDN) or
+    [B,T,H,dk] (KDA) holding log(alpha); h0 [N,H,dk,dv] or None (zero state).
+    ``units`` restricts the work to the listed (sequence*H + head) pairs; the
+    other entries of the outputs stay zero.
+    """
+    vid = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    q, k, v, beta, g, h0 = map(_f64, (q, k, v, beta, g, h0))
+    cu = _i32(cu_seqlens)
+    un = _i32(units)
+    B, T, H, dk, dv, N = _dims(q, v, cu)
+    o = np.zeros((B, T, H, dv))
+    hT = np.zeros((N, H, dk, dv))
+    rc = _load().dro_forward(B, T, H, dk, dv, vid, float(scale), _ptr(cu), N,
+                             _ptr(un), 0 if un is None else len(un),
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                             _ptr(o), _ptr(hT), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle forward: bad shape or arguments")
+    return o, hT
+
+
+def backward(variant, q, k, v, beta, g, h0, dO, dhT=None, scale=1.0,
+             cu_seqlens=None, units=None, nthreads=0):
+    """Reverse-time gradients.  Returns dict dq, dk, dv, dbeta, dg (None for
+    DeltaNet), dh0 (fp64 numpy)."""
+    vid = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    q, k, v, beta, g, h0, dO, dhT = map(_f64, (q, k, v, beta, g, h0, dO, dhT))
+    cu = _i32(cu_seqlens)
+    un = _i32(units)
+    B, T, H, dk, dv, N = _dims(q, v, cu)
+    dq = np.zeros_like(q)
+    dk_ = np.zeros_like(k)
+    dv_ = np.zeros_like(v)
+    dbeta = np.zeros_like(beta)
+    dg = None if vid == 0 else np.zeros_like(g)
+    dh0 = np.zeros((N, H, dk, dv))
+    rc = _load().dro_backward(B, T, H, dk, dv, vid, float(scale), _ptr(cu), N,
+                              _ptr(un), 0 if un is None else len(un),
+                              _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                              _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_),
+                              _ptr(dbeta), _ptr(dg), _ptr(dh0), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle backward: bad shape or arguments")
+    return {"dq": dq, "dk": dk_, "dv": dv_, "dbeta": dbeta, "dg": dg, "dh0": dh0}
