@@ -1,0 +1,210 @@
+// dr_api.cu -- the C ABI of libdr.so (declared in include/dr.h): argument
+// validation, workspace sizing, the packed-sequence chunk plan, and dispatch
+// to the bf16 tensor-core path (tc_*.cu) or the fp32 CUDA-core path (simt.cu).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "dr.h"
+
+namespace dr {
+size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv);
+cudaError_t simt_fwd(const Params& p, cudaStream_t st);
+cudaError_t simt_bwd(const Params& p, cudaStream_t st);
+size_t tc_workspace_bytes(const Params& p);
+cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
+cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse);
+cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st);
+}  // namespace dr
+
+using dr::Params;
+
+namespace {
+
+constexpr size_t kHeader = 256;  // error word + padding at the start of the workspace
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+enum class Path { kNone, kTensor, kSimt };
+
+// Structural validity (DR_ERR_INVALID_ARG) and support (DR_ERR_UNSUPPORTED).
+int check_desc(const dr_desc* d, Path* path) {
+    if (!d) return DR_ERR_INVALID_ARG;
+    if (d->B < 0 || d->T < 0 || d->H < 1 || d->d_k < 1 || d->d_v < 1 || d->chunk < 1)
+        return DR_ERR_INVALID_ARG;
+    if (d->variant < DR_DELTANET || d->variant > DR_KDA) return DR_ERR_INVALID_ARG;
+    for (int t : {d->io_dtype, d->out_dtype, d->grad_dtype})
+        if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
+    if (!std::isfinite(d->scale)) return DR_ERR_INVALID_ARG;
+    if (d->flags & ~DR_FLAG_REUSE_FWD) return DR_ERR_INVALID_ARG;
+    if ((long long)d->B * d->T * d->H * (d->d_k > d->d_v ? d->d_k : d->d_v) >= (1ll << 40))
+        return DR_ERR_INVALID_ARG;
+    if (d->cu_seqlens) {
+        if (d->B != 1 || d->num_seqs < 0 || d->num_chunks < 0) return DR_ERR_INVALID_ARG;
+        if (d->num_seqs > 0 && !d->chunk_offsets) return DR_ERR_INVALID_ARG;
+        if (d->num_chunks > 0 && !d->chunk_table) return DR_ERR_INVALID_ARG;
+    } else {
+        if (d->num_seqs != d->B) return DR_ERR_INVALID_ARG;
+        if (d->chunk_table || d->chunk_offsets) return DR_ERR_INVALID_ARG;
+    }
+    *path = Path::kNone;
+    if (d->io_dtype == DR_BF16) {
+        if (d->d_k == d->d_v && (d->d_k == 64 || d->d_k == 128) && d->chunk == 64)
+            *path = Path::kTensor;
+    } else {
+        auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
+        if (ok(d->d_k) && ok(d->d_v) && ok(d->chunk)) *path = Path::kSimt;
+    }
+    return *path == Path::kNone ? DR_ERR_UNSUPPORTED : DR_OK;
+}
+
+Params make_params(const dr_desc* d) {
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = d->B; p.T = d->T; p.H = d->H; p.dk = d->d_k; p.dv = d->d_v; p.C = d->chunk;
+    p.variant = d->variant; p.io_dtype = d->io_dtype; p.out_dtype = d->out_dtype;
+    p.grad_dtype = d->grad_dtype; p.scale = d->scale;
+    if (d->cu_seqlens) {
+        p.N = d->num_seqs;
+        p.num_chunks = d->num_chunks;
+        p.chunks_per_seq = 0;
+        p.cu = d->cu_seqlens; p.ctab = d->chunk_table; p.coff = d->chunk_offsets;
+    } else {
+        p.N = d->B;
+        p.chunks_per_seq = (d->T + d->chunk - 1) / d->chunk;
+        p.num_chunks = p.N * p.chunks_per_seq;
+    }
+    return p;
+}
+
+size_t ws_bytes(const Params& p, Path path) {
+    if (path == Path::kSimt)
+        return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
+    return kHeader + dr::tc_workspace_bytes(p);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DR_OK : DR_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dr_error_string(int code) {
+    switch (code) {
+        case DR_OK: return "DR_OK";
+        case DR_ERR_INVALID_ARG: return "DR_ERR_INVALID_ARG: invalid argument";
+        case DR_ERR_UNSUPPORTED: return "DR_ERR_UNSUPPORTED: outside the supported set";
+        case DR_ERR_WORKSPACE: return "DR_ERR_WORKSPACE: workspace missing or too small";
+        case DR_ERR_ALIGNMENT: return "DR_ERR_ALIGNMENT: pointer not 16-byte aligned";
+        case DR_ERR_CUDA: return "DR_ERR_CUDA: CUDA launch or runtime failure";
+        case DR_ERR_TIMEOUT: return "DR_ERR_TIMEOUT: a bounded device wait ran out";
+        default: return "unknown dr status code";
+    }
+}
+
+size_t dr_workspace_bytes(const dr_desc* desc) {
+    Path path;
+    if (check_desc(desc, &path) != DR_OK) return 0;
+    return ws_bytes(make_params(desc), path);
+}
+
+int dr_plan_varlen(const int32_t* cu, int num_seqs, int chunk, int32_t* table, int32_t* offsets,
+                   int max_chunks, int* num_chunks) {
+    if (!cu || num_seqs < 0 || chunk < 1 || !num_chunks) return DR_ERR_INVALID_ARG;
+    if (cu[0] != 0) return DR_ERR_INVALID_ARG;
+    long long total = 0;
+    for (int n = 0; n < num_seqs; ++n) {
+        const long long len = (long long)cu[n + 1] - cu[n];
+        if (len < 0) return DR_ERR_INVALID_ARG;
+        total += (len + chunk - 1) / chunk;
+    }
+    if (total > 0x7fffffffll) return DR_ERR_INVALID_ARG;
+    *num_chunks = (int)total;
+    if (!table && !offsets) return DR_OK;
+    if (total > max_chunks) return DR_ERR_INVALID_ARG;
+    int c = 0;
+    for (int n = 0; n < num_seqs; ++n) {
+        if (offsets) offsets[n] = c;
+        for (int32_t t = cu[n]; t < cu[n + 1]; t += chunk, ++c) {
+            if (table) { table[2 * c] = n; table[2 * c + 1] = t; }
+        }
+    }
+    if (offsets) offsets[num_seqs] = c;
+    return DR_OK;
+}
+
+int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+           const float* g, const float* h0, void* o, float* hT, void* ws, size_t ws_size,
+           void* stream) {
+    Path path;
+    int rc = check_desc(desc, &path);
+    if (rc != DR_OK) return rc;
+    Params p = make_params(desc);
+    const long long tokens = (long long)p.B * p.T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
+    if (tokens > 0 && ((p.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, beta, g, h0, o, hT, ws};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    const size_t need = ws_bytes(p, path);
+    if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.hT = hT;
+    p.ws = static_cast<uint8_t*>(ws);
+    p.err = static_cast<int*>(ws);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
+    if (tokens == 0) {
+        if (hT) return cuda_status(dr::state_passthrough(h0, hT, (size_t)p.N * p.H * p.dk * p.dv, st));
+        return DR_OK;
+    }
+    if (path == Path::kSimt) return cuda_status(dr::simt_fwd(p, st));
+    return cuda_status(dr::tc_fwd(p, st, true));
+}
+
+int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+           const float* g, const float* h0, const void* dO, const float* dhT, void* dq, void* dk,
+           void* dv, float* dbeta, float* dg, float* dh0, void* ws, size_t ws_size,
+           void* stream) {
+    Path path;
+    int rc = check_desc(desc, &path);
+    if (rc != DR_OK) return rc;
+    Params p = make_params(desc);
+    const long long tokens = (long long)p.B * p.T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
+        return DR_ERR_INVALID_ARG;
+    if (tokens > 0 && ((p.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
+    if (tokens > 0 && ((p.variant == DR_DELTANET) != (dg == nullptr))) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    const size_t need = ws_bytes(p, path);
+    if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0;
+    p.dO = dO; p.dhT = dhT; p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dbeta = dbeta; p.dg = dg;
+    p.dh0 = dh0;
+    p.ws = static_cast<uint8_t*>(ws);
+    p.err = static_cast<int*>(ws);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
+    if (tokens == 0) {
+        if (dh0) return cuda_status(dr::state_passthrough(dhT, dh0, (size_t)p.N * p.H * p.dk * p.dv, st));
+        return DR_OK;
+    }
+    if (path == Path::kSimt) return cuda_status(dr::simt_bwd(p, st));
+    return cuda_status(dr::tc_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
+}
+
+int dr_check_status(const void* ws, void* stream) {
+    if (!ws) return DR_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return DR_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DR_ERR_CUDA;
+    return word == 0 ? DR_OK : DR_ERR_TIMEOUT;
+}
+
+}  // extern "C"

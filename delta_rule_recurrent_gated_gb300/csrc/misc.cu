@@ -1,0 +1,21 @@
+// misc.cu -- small helper kernels.
+#include "common.cuh"
+
+namespace dr {
+namespace {
+// dst = src (or 0 when src is null): the state of a sequence with no tokens
+// passes through unchanged (hT = h0, dh0 = dhT).
+__global__ void copy_or_zero(const float* __restrict__ src, float* __restrict__ dst, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src ? src[i] : 0.f;
+}
+}  // namespace
+
+cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st) {
+    if (n == 0 || !dst) return cudaSuccess;
+    const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    copy_or_zero<<<blocks, 256, 0, st>>>(src, dst, n);
+    return cudaGetLastError();
+}
+}  // namespace dr

@@ -1,0 +1,348 @@
+// simt.cu -- fp32 CUDA-core path (no tensor cores) of the chunkwise delta rule:
+// serves fp32 inputs, where the tolerance asks for fp32 arithmetic throughout.
+//
+// One CTA per (sequence, head) walks its chunks in order.  Each chunk of L <= C
+// tokens, starting from the state S (d_k x d_v, S = W^T), is evaluated in the
+// chunkwise form of the recurrence (decay before the residual, residual
+// r = v - (decayed W) k, write beta r k^T, read W q; page "Linear Attention
+// Architectures: Mechanisms, Trade-offs, and Cross-Layer Routing", section
+// "Metodologia y Marco de Trabajo", item 1):
+//   Gamma = within-chunk cumulative sum of the log-decay (per key channel)
+//   Kb = k e^{Gamma}, Kr = k e^{-Gamma}, Qb = q e^{Gamma}, KC = k e^{Gamma_L - Gamma}
+//   T  = (I + diag(beta) strict_lower(Kb Kr^T))^{-1}
+//   Wy = T diag(beta) Kb,  Ut = T diag(beta) v,  Aqk = tril(Qb Kr^T)
+//   Qt = scale (Qb - Aqk Wy),  Ot = scale Aqk Ut
+//   U  = Ut - Wy S,  O = Qt S + Ot,  S <- diag(e^{Gamma_L}) S + KC^T U
+// and the backward pass is the chain rule through exactly these steps.
+// Small matrices live in a per-CTA scratch slice of the workspace (L1/L2
+// resident); every helper is block-wide and ends with __syncthreads().
+#include "common.cuh"
+
+namespace dr {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBuf = 64 * 64;  // floats per scratch matrix (C, d_k, d_v <= 64)
+
+// C[m x n] = alpha * op(A) op(B) (+ C when acc).  op(A) is m x k.
+__device__ void mm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* Bm,
+                   int ldb, bool tb, int m, int n, int k, float alpha, bool acc) {
+    for (int idx = threadIdx.x; idx < m * n; idx += blockDim.x) {
+        const int i = idx / n, j = idx % n;
+        float s = 0.f;
+        for (int p = 0; p < k; ++p) {
+            const float a = ta ? A[p * lda + i] : A[i * lda + p];
+            const float b = tb ? Bm[j * ldb + p] : Bm[p * ldb + j];
+            s = fmaf(a, b, s);
+        }
+        Cm[i * ldc + j] = acc ? Cm[i * ldc + j] + alpha * s : alpha * s;
+    }
+    __syncthreads();
+}
+
+struct Scratch {
+    float* base;
+    __device__ float* operator()(int i) const { return base + (size_t)i * kBuf; }
+};
+
+enum {
+    bS, bQ, bK, bV, bGam, bKb, bKr, bQb, bKC, bA, bT, bbK, bbV, bWy, bUt, bAqk, bQt, bOt, bU,
+    bO, bVec, bTmp,
+    // backward only
+    bS0, bdS, bdSp, bdO, bdU, bdQt, bdWy, bdUt, bdKC, bdAqk, bdQb, bdKr, bdKb, bdT, bdA,
+    bdbK, bdbV, bdGam, bdVec,
+    kNumBufs
+};
+
+// Load one chunk's inputs into scratch and evaluate everything that does not
+// depend on the state (steps Gamma .. Ot above).
+__device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, int L) {
+    const int dk = p.dk, dv = p.dv, H = p.H, tid = threadIdx.x, nt = blockDim.x;
+    float* q = s(bQ); float* k = s(bK); float* v = s(bV); float* gm = s(bGam);
+    float* beta = s(bVec);  // [0, C): beta;  [C, C + dk): e^{Gamma_L}
+    for (int idx = tid; idx < L * dk; idx += nt) {
+        const int i = idx / dk, c = idx % dk;
+        const size_t e = ((size_t)(row0 + i) * H + h) * dk + c;
+        q[idx] = ld_any(p.q, e, p.io_dtype);
+        k[idx] = ld_any(p.k, e, p.io_dtype);
+    }
+    for (int idx = tid; idx < L * dv; idx += nt) {
+        const int i = idx / dv, c = idx % dv;
+        v[idx] = ld_any(p.v, ((size_t)(row0 + i) * H + h) * dv + c, p.io_dtype);
+    }
+    for (int i = tid; i < L; i += nt) beta[i] = p.beta[(size_t)(row0 + i) * H + h];
+    // Gamma: within-chunk inclusive cumulative sum of the log-decay
+    for (int c = tid; c < dk; c += nt) {
+        float acc = 0.f;
+        for (int i = 0; i < L; ++i) {
+            float gi = 0.f;
+            if (p.variant == DR_GDN) gi = p.g[(size_t)(row0 + i) * H + h];
+            else if (p.variant == DR_KDA) gi = p.g[((size_t)(row0 + i) * H + h) * dk + c];
+            acc += gi;
+            gm[i * dk + c] = acc;
+        }
+        beta[p.C + c] = expf(acc);
+    }
+    __syncthreads();
+    float* Kb = s(bKb); float* Kr = s(bKr); float* Qb = s(bQb); float* KC = s(bKC);
+    float* bK = s(bbK); float* bV = s(bbV);
+    for (int idx = tid; idx < L * dk; idx += nt) {
+        const int i = idx / dk, c = idx % dk;
+        const float G = gm[idx], GL = gm[(L - 1) * dk + c];
+        Kb[idx] = k[idx] * expf(G);
+        Kr[idx] = k[idx] * expf(-G);
+        Qb[idx] = q[idx] * expf(G);
+        KC[idx] = k[idx] * expf(GL - G);
+        bK[idx] = beta[i] * Kb[idx];
+    }
+    for (int idx = tid; idx < L * dv; idx += nt) bV[idx] = beta[idx / dv] * v[idx];
+    __syncthreads();
+    float* A = s(bA); float* T = s(bT);
+    mm(A, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);  // Gram (kept for backward)
+    // T = (I + diag(beta) strict_lower(Gram))^{-1}, forward substitution by rows
+    for (int i = 0; i < L; ++i) {
+        for (int n = tid; n < L; n += nt) {
+            float x = (n == i) ? 1.f : 0.f;
+            if (n < i)
+                for (int j = n; j < i; ++j) x -= beta[i] * A[i * L + j] * T[j * L + n];
+            T[i * L + n] = x;
+        }
+        __syncthreads();
+    }
+    float* Wy = s(bWy); float* Ut = s(bUt); float* Aqk = s(bAqk);
+    mm(Wy, dk, T, L, false, bK, dk, false, L, dk, L, 1.f, false);
+    mm(Ut, dv, T, L, false, bV, dv, false, L, dv, L, 1.f, false);
+    mm(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    for (int idx = tid; idx < L * L; idx += nt)
+        if (idx % L > idx / L) Aqk[idx] = 0.f;
+    __syncthreads();
+    float* Qt = s(bQt); float* Ot = s(bOt);
+    mm(Qt, dk, Aqk, L, false, Wy, dk, false, L, dk, L, -p.scale, false);
+    for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += p.scale * Qb[idx];
+    mm(Ot, dv, Aqk, L, false, Ut, dv, false, L, dv, L, p.scale, false);
+}
+
+// U = Ut - Wy S; O = Qt S + Ot; S <- diag(e^{Gamma_L}) S + KC^T U
+__device__ void chunk_scan(const Params& p, const Scratch& s, int L, float* S) {
+    const int dk = p.dk, dv = p.dv, tid = threadIdx.x, nt = blockDim.x;
+    float* U = s(bU); float* O = s(bO);
+    for (int idx = tid; idx < L * dv; idx += nt) { U[idx] = s(bUt)[idx]; O[idx] = s(bOt)[idx]; }
+    __syncthreads();
+    mm(U, dv, s(bWy), dk, false, S, dv, false, L, dv, dk, -1.f, true);
+    mm(O, dv, s(bQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    const float* gL = s(bVec) + p.C;
+    for (int idx = tid; idx < dk * dv; idx += nt) S[idx] *= gL[idx / dv];
+    __syncthreads();
+    mm(S, dv, s(bKC), dk, true, U, dv, false, dk, dv, L, 1.f, true);
+}
+
+__device__ void load_state(float* S, const float* h, int n, int hd, int H, int dk, int dv) {
+    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x)
+        S[idx] = h ? h[((size_t)n * H + hd) * dk * dv + idx] : 0.f;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scratch) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
+    const Scratch s{scratch + (size_t)u * kNumBufs * kBuf};
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+    float* S = s(bS);
+    load_state(S, p.h0, n, h, p.H, p.dk, p.dv);
+    for (int c = 0; c < nc; ++c) {
+        const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
+        chunk_prep(p, s, h, row0, L);
+        chunk_scan(p, s, L, S);
+        const float* O = s(bO);
+        for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
+            const int i = idx / p.dv, j = idx % p.dv;
+            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * p.dv + j, p.out_dtype, O[idx]);
+        }
+        __syncthreads();
+    }
+    if (p.hT)
+        for (int idx = threadIdx.x; idx < p.dk * p.dv; idx += blockDim.x)
+            p.hT[((size_t)n * p.H + h) * p.dk * p.dv + idx] = S[idx];
+}
+
+__global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scratch,
+                                                            float* states) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
+    const int dk = p.dk, dv = p.dv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
+    const Scratch s{scratch + (size_t)u * kNumBufs * kBuf};
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+    const size_t SS = (size_t)dk * dv;
+    // pass 1: the state at the start of every chunk
+    float* S = s(bS);
+    load_state(S, p.h0, n, h, p.H, dk, dv);
+    for (int c = 0; c < nc; ++c) {
+        const int row0 = srow + c * C, L = min(C, slen - c * C);
+        float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
+        for (int idx = tid; idx < dk * dv; idx += nt) dst[idx] = S[idx];
+        __syncthreads();
+        chunk_prep(p, s, h, row0, L);
+        chunk_scan(p, s, L, S);
+    }
+    // pass 2: reverse over chunks with dS = dL/dS_end
+    float* dS = s(bdS);
+    load_state(dS, p.dhT, n, h, p.H, dk, dv);
+    for (int c = nc - 1; c >= 0; --c) {
+        const int row0 = srow + c * C, L = min(C, slen - c * C);
+        float* S0 = s(bS0);
+        const float* src = states + ((size_t)(c0 + c) * p.H + h) * SS;
+        for (int idx = tid; idx < dk * dv; idx += nt) { S0[idx] = src[idx]; S[idx] = src[idx]; }
+        __syncthreads();
+        chunk_prep(p, s, h, row0, L);
+        chunk_scan(p, s, L, S);  // recomputes U (S is scratch here)
+        float* dO = s(bdO);
+        for (int idx = tid; idx < L * dv; idx += nt) {
+            const int i = idx / dv, j = idx % dv;
+            dO[idx] = ld_any(p.dO, ((size_t)(row0 + i) * p.H + h) * dv + j, p.io_dtype);
+        }
+        __syncthreads();
+        const float* beta = s(bVec);
+        const float* gL = s(bVec) + C;
+        float* dU = s(bdU); float* dSp = s(bdSp);
+        // dU = KC dS;  dS_prev = diag(gL) dS + Qt^T dO - Wy^T dU
+        mm(dU, dv, s(bKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
+        for (int idx = tid; idx < dk * dv; idx += nt) dSp[idx] = gL[idx / dv] * dS[idx];
+        __syncthreads();
+        mm(dSp, dv, s(bQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
+        mm(dSp, dv, s(bWy), dk, true, dU, dv, false, dk, dv, L, -1.f, true);
+        // state-side gradients of the chunk
+        float* dQt = s(bdQt); float* dWy = s(bdWy); float* dUt = s(bdUt); float* dKC = s(bdKC);
+        mm(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm(dWy, dk, dU, dv, false, S0, dv, true, L, dk, dv, -1.f, false);
+        mm(dKC, dk, s(bU), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
+        float* dVec = s(bdVec);  // [0, dk): d e^{Gamma_L} ; [C + ...] unused
+        for (int c2 = tid; c2 < dk; c2 += nt) {
+            float acc = 0.f;
+            for (int j = 0; j < dv; ++j) acc += dS[c2 * dv + j] * S0[c2 * dv + j];
+            dVec[c2] = acc;
+        }
+        for (int idx = tid; idx < L * dv; idx += nt) dUt[idx] = dU[idx];
+        __syncthreads();
+        // Qt = scale (Qb - Aqk Wy), Ot = scale Aqk Ut
+        const float sc = p.scale;
+        float* dAqk = s(bdAqk); float* dQb = s(bdQb);
+        mm(dAqk, L, dQt, dk, false, s(bWy), dk, true, L, L, dk, -sc, false);
+        mm(dAqk, L, dO, dv, false, s(bUt), dv, true, L, L, dv, sc, true);
+        for (int idx = tid; idx < L * L; idx += nt)
+            if (idx % L > idx / L) dAqk[idx] = 0.f;
+        __syncthreads();
+        mm(dWy, dk, s(bAqk), L, true, dQt, dk, false, L, dk, L, -sc, true);
+        mm(dUt, dv, s(bAqk), L, true, dO, dv, false, L, dv, L, sc, true);
+        for (int idx = tid; idx < L * dk; idx += nt) dQb[idx] = sc * dQt[idx];
+        __syncthreads();
+        // Aqk = tril(Qb Kr^T)
+        float* dKr = s(bdKr); float* dKb = s(bdKb);
+        mm(dQb, dk, dAqk, L, false, s(bKr), dk, false, L, dk, L, 1.f, true);
+        mm(dKr, dk, dAqk, L, true, s(bQb), dk, false, L, dk, L, 1.f, false);
+        // Wy = T bK, Ut = T bV
+        float* dT = s(bdT); float* dbK = s(bdbK); float* dbV = s(bdbV); float* dA = s(bdA);
+        float* tmp = s(bTmp);
+        mm(dT, L, dWy, dk, false, s(bbK), dk, true, L, L, dk, 1.f, false);
+        mm(dT, L, dUt, dv, false, s(bbV), dv, true, L, L, dv, 1.f, true);
+        mm(dbK, dk, s(bT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
+        mm(dbV, dv, s(bT), L, true, dUt, dv, false, L, dv, L, 1.f, false);
+        // T = (I + A)^{-1}: dA = -T^T dT T^T, strictly lower
+        mm(tmp, L, dT, L, false, s(bT), L, true, L, L, L, 1.f, false);
+        mm(dA, L, s(bT), L, true, tmp, L, false, L, L, L, -1.f, false);
+        for (int idx = tid; idx < L * L; idx += nt)
+            if (idx % L >= idx / L) dA[idx] = 0.f;
+        __syncthreads();
+        // A = diag(beta) strict_lower(Kb Kr^T) (Gram kept in bA)
+        float* db = dVec + 64;  // per-token dbeta partials
+        const float* Gm = s(bA);
+        for (int i = tid; i < L; i += nt) {
+            float acc = 0.f;
+            for (int j = 0; j < i; ++j) acc += dA[i * L + j] * Gm[i * L + j];
+            for (int c2 = 0; c2 < dk; ++c2) acc += dbK[i * dk + c2] * s(bKb)[i * dk + c2];
+            for (int j = 0; j < dv; ++j) acc += dbV[i * dv + j] * s(bV)[i * dv + j];
+            db[i] = acc;
+        }
+        for (int idx = tid; idx < L * L; idx += nt) dA[idx] *= beta[idx / L];
+        __syncthreads();
+        mm(dKb, dk, dA, L, false, s(bKr), dk, false, L, dk, L, 1.f, false);
+        mm(dKr, dk, dA, L, true, s(bKb), dk, false, L, dk, L, 1.f, true);
+        // decay chain -> dq, dk, dv, dbeta, dGamma
+        float* dGam = s(bdGam);
+        const float* gm = s(bGam);
+        for (int idx = tid; idx < L * dk; idx += nt) {
+            const int i = idx / dk, c2 = idx % dk;
+            dKb[idx] += beta[i] * dbK[idx];
+            const float G = gm[idx], GL = gm[(L - 1) * dk + c2];
+            const float eG = expf(G), enG = expf(-G), eC = expf(GL - G);
+            const size_t e = ((size_t)(row0 + i) * p.H + h) * dk + c2;
+            st_any(p.dq, e, p.grad_dtype, dQb[idx] * eG);
+            st_any(p.dk_, e, p.grad_dtype, dKb[idx] * eG + dKr[idx] * enG + dKC[idx] * eC);
+            dGam[idx] = dQb[idx] * s(bQb)[idx] + dKb[idx] * s(bKb)[idx] -
+                        dKr[idx] * s(bKr)[idx] - dKC[idx] * s(bKC)[idx];
+        }
+        for (int idx = tid; idx < L * dv; idx += nt) {
+            const int i = idx / dv, j = idx % dv;
+            st_any(p.dv_, ((size_t)(row0 + i) * p.H + h) * dv + j, p.grad_dtype,
+                   beta[i] * dbV[idx]);
+        }
+        for (int i = tid; i < L; i += nt) p.dbeta[(size_t)(row0 + i) * p.H + h] = db[i];
+        __syncthreads();
+        if (p.variant != DR_DELTANET) {
+            // Gamma_L terms, then dg = reverse cumulative sum of dGamma
+            for (int c2 = tid; c2 < dk; c2 += nt) {
+                float acc = dVec[c2] * gL[c2];
+                for (int i = 0; i < L; ++i) acc += dKC[i * dk + c2] * s(bKC)[i * dk + c2];
+                dGam[(L - 1) * dk + c2] += acc;
+                float run = 0.f;
+                for (int i = L - 1; i >= 0; --i) {
+                    run += dGam[i * dk + c2];
+                    dGam[i * dk + c2] = run;
+                }
+            }
+            __syncthreads();
+            if (p.variant == DR_KDA) {
+                for (int idx = tid; idx < L * dk; idx += nt) {
+                    const int i = idx / dk, c2 = idx % dk;
+                    p.dg[((size_t)(row0 + i) * p.H + h) * dk + c2] = dGam[idx];
+                }
+            } else {
+                for (int i = tid; i < L; i += nt) {
+                    float acc = 0.f;
+                    for (int c2 = 0; c2 < dk; ++c2) acc += dGam[i * dk + c2];
+                    p.dg[(size_t)(row0 + i) * p.H + h] = acc;
+                }
+            }
+        }
+        for (int idx = tid; idx < dk * dv; idx += nt) dS[idx] = dSp[idx];
+        __syncthreads();
+    }
+    if (p.dh0)
+        for (int idx = tid; idx < dk * dv; idx += nt)
+            p.dh0[((size_t)n * p.H + h) * SS + idx] = dS[idx];
+}
+
+}  // namespace
+
+size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv) {
+    return (size_t)units * kNumBufs * kBuf * sizeof(float) +
+           (size_t)num_chunks * H * dk * dv * sizeof(float);
+}
+
+cudaError_t simt_fwd(const Params& p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    simt_fwd_kernel<<<units, kThreads, 0, st>>>(p, scratch);
+    return cudaGetLastError();
+}
+
+cudaError_t simt_bwd(const Params& p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    float* states = scratch + (size_t)units * kNumBufs * kBuf;
+    simt_bwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, states);
+    return cudaGetLastError();
+}
+
+}  // namespace dr

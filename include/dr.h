@@ -1,0 +1,145 @@
+/*
+ * dr.h -- C ABI of libdr.so: chunkwise-parallel forward and backward of the
+ * delta-rule recurrent memory (DeltaNet, Gated DeltaNet, Kimi Delta Attention)
+ * on one GB300 GPU (sm_103a).
+ *
+ * The operation (page "Linear Attention Architectures: Mechanisms, Trade-offs,
+ * and Cross-Layer Routing", section "Metodologia y Marco de Trabajo", item 1,
+ * the unified recurrent-memory notation and its three variant bullets): per
+ * (sequence, head) a memory matrix W (d_v x d_k) is, token by token,
+ *   decayed   Wd_t = W_{t-1} diag(a_t)       a_t = 1 (DeltaNet), exp(g_t) * 1 (Gated
+ *                                            DeltaNet, one scalar gate), exp(g_t) per
+ *                                            key channel (Kimi Delta Attention)
+ *   corrected r_t  = v_t - Wd_t k_t          (the delta-rule residual r = v - vbar)
+ *   written   W_t  = Wd_t + beta_t r_t k_t^T
+ *   read      o_t  = scale * W_t q_t
+ * The gate enters as its logarithm g = log(alpha) <= 0.  beta_t, the read after
+ * the write and `scale` are the standard delta-rule reading of that notation.
+ *
+ * Memory: the caller allocates every buffer (device memory unless stated) and
+ * the workspace; the library never allocates, frees or synchronises inside
+ * dr_fwd / dr_bwd.  All work is enqueued on `stream` (a cudaStream_t passed as
+ * void*, NULL = legacy default stream) in stream order.  Calls are re-entrant;
+ * two calls that run concurrently must not share a workspace.
+ *
+ * Layouts (row-major, contiguous, every pointer 16-byte aligned):
+ *   q, k, dq, dk   [B, T, H, d_k]       io dtype (grad dtype for dq, dk)
+ *   v, dO, dv      [B, T, H, d_v]       io dtype (grad dtype for dv)
+ *   o              [B, T, H, d_v]       out dtype
+ *   beta, dbeta    [B, T, H]            fp32, beta in [0, 1]
+ *   g, dg          Gated DeltaNet [B, T, H]; KDA [B, T, H, d_k]; fp32; NULL for DeltaNet
+ *   h0, hT, dhT, dh0  [N, H, d_k, d_v]  fp32, the state S = W^T (d_v contiguous)
+ * N = B for dense batches.  For packed ragged sequences B == 1, T is the total
+ * length and cu_seqlens (N + 1 offsets) splits the T axis; every sequence
+ * starts from its own h0[n] (zero when h0 is NULL) and ends in hT[n].
+ *
+ * Errors: every entry point returns a dr_status_code.  When the host detects
+ * an error nothing is launched and no output is touched.  A launch failure is
+ * DR_ERR_CUDA.  Device-side waits are bounded: a wait that runs out records
+ * DR_ERR_TIMEOUT in the workspace, which dr_check_status reports.
+ */
+#ifndef DR_H
+#define DR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum dr_status_code {
+    DR_OK = 0,
+    DR_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad enum, bad cu_seqlens */
+    DR_ERR_UNSUPPORTED = 2,   /* valid but outside the supported set (below)         */
+    DR_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than dr_workspace_bytes   */
+    DR_ERR_ALIGNMENT = 4,     /* a pointer is not 16-byte aligned                    */
+    DR_ERR_CUDA = 5,          /* a CUDA call or launch failed                        */
+    DR_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out                  */
+};
+
+enum dr_variant { DR_DELTANET = 0, DR_GDN = 1, DR_KDA = 2 };
+enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
+
+/* dr_desc.flags */
+#define DR_FLAG_REUSE_FWD 1  /* dr_bwd: the workspace still holds the residuals
+                                written by dr_fwd for the same desc and inputs;
+                                skip their recomputation */
+
+/*
+ * Problem descriptor.  Supported set:
+ *   io bf16: d_k = d_v in {64, 128}, chunk = 64  (tensor-core path)
+ *   io fp32: d_k, d_v in {16, 32, 64}, chunk in {16, 32, 64}  (fp32 CUDA-core path)
+ *   any T >= 0 (a partial last chunk is fine), B >= 0, H >= 1.
+ */
+typedef struct dr_desc {
+    int B, T, H;
+    int d_k, d_v;
+    int chunk;                    /* tokens per chunk of the chunkwise form            */
+    int variant;                  /* enum dr_variant                                   */
+    int io_dtype;                 /* q, k, v, dO                                       */
+    int out_dtype;                /* o                                                 */
+    int grad_dtype;               /* dq, dk, dv                                        */
+    float scale;                  /* read scale (1.0 = the plain read o = W q)         */
+    int flags;                    /* DR_FLAG_*                                          */
+    int num_seqs;                 /* N: B for dense batches, or the packed count       */
+    const int32_t* cu_seqlens;    /* device [N+1] or NULL (dense)                      */
+    const int32_t* chunk_table;   /* device [num_chunks][2] = (sequence, first token),
+                                     from dr_plan_varlen; NULL for dense batches      */
+    const int32_t* chunk_offsets; /* device [N+1]: first chunk of each sequence        */
+    int num_chunks;               /* total chunks (packed layout only)                 */
+} dr_desc;
+
+/* Bytes of workspace dr_fwd and dr_bwd need for `desc` (the same for both).
+   Returns 0 when desc is invalid or unsupported. */
+size_t dr_workspace_bytes(const dr_desc* desc);
+
+/*
+ * Host-side chunk plan of packed ragged sequences (no GPU work).
+ * cu_seqlens_host: N + 1 non-decreasing offsets starting at 0.  Writes, for
+ * every chunk of every sequence in order, (sequence, first token) into
+ * chunk_table_host[2*i], [2*i+1] (chunks never straddle a sequence boundary;
+ * the last chunk of a sequence may be short; an empty sequence has none), and
+ * the index of each sequence's first chunk into chunk_offsets_host[0..N]
+ * (chunk_offsets_host[N] = total).  *num_chunks receives the total; when it
+ * exceeds max_chunks nothing is written and DR_ERR_INVALID_ARG is returned.
+ * chunk_table_host / chunk_offsets_host may be NULL to query the count only.
+ */
+int dr_plan_varlen(const int32_t* cu_seqlens_host, int num_seqs, int chunk,
+                   int32_t* chunk_table_host, int32_t* chunk_offsets_host, int max_chunks,
+                   int* num_chunks);
+
+/*
+ * Forward: o (and hT when non-NULL) from q, k, v, beta, g, h0 (h0 NULL = zero
+ * state).  Also leaves in the workspace the residuals dr_bwd can reuse
+ * (DR_FLAG_REUSE_FWD).
+ */
+int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+           const float* beta, const float* g, const float* h0, void* o, float* hT,
+           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: gradients of L = sum(dO * o) + sum(dhT * hT) with respect to q, k,
+ * v, beta, g (the log-gate) and h0.  dhT NULL means a zero final-state
+ * gradient; dh0 may be NULL when not needed; dg must be NULL for DeltaNet and
+ * non-NULL otherwise.  Gradients are with respect to the tensors as passed
+ * (q, k already normalised, beta after its sigmoid, g = log alpha).
+ */
+int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+           const float* beta, const float* g, const float* h0, const void* dO,
+           const float* dhT, void* dq, void* dk, void* dv, float* dbeta, float* dg,
+           float* dh0, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream` and report any device-side error recorded in the
+   workspace by the last call that used it (DR_OK or DR_ERR_TIMEOUT), or
+   DR_ERR_CUDA when the stream itself failed. */
+int dr_check_status(const void* workspace, void* stream);
+
+/* Human-readable name of a dr_status_code. */
+const char* dr_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DR_H */

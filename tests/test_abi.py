@@ -1,0 +1,163 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel is launched):
+the library loads, exports every entry point of include/dr.h, and rejects bad
+arguments with the documented codes before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from delta_rule_recurrent_gated_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from delta_rule_recurrent_gated_gb300 import build
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dr.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dr_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"dr_fwd", "dr_bwd", "dr_workspace_bytes", "dr_plan_varlen", "dr_check_status",
+            "dr_error_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dr.h but not exported"
+
+
+def desc(**kw):
+    d = B.DrDesc()
+    d.B, d.T, d.H, d.d_k, d.d_v, d.chunk = 2, 128, 4, 128, 128, 64
+    d.variant, d.io_dtype, d.out_dtype, d.grad_dtype = B.DR_GDN, B.DR_BF16, B.DR_F32, B.DR_F32
+    d.scale, d.flags, d.num_seqs = 1.0, 0, 2
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_struct_layout_matches_header(lib, tmp_path):
+    """The binding's dr_desc must agree field by field with the C compiler's."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not available")
+    names = [f[0] for f in B.DrDesc._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join(f'printf("%zu\\n", offsetof(dr_desc, {n}));' for n in names)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "dr.h"\n'
+                   'int main(void){' + body + 'printf("%zu\\n", sizeof(dr_desc));return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert out[:-1] == [getattr(B.DrDesc, n).offset for n in names]
+    assert out[-1] == ctypes.sizeof(B.DrDesc)
+
+
+def test_workspace_bytes(lib):
+    assert B.workspace_bytes(desc()) > 0
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16)) > 0
+    assert B.workspace_bytes(desc(H=0)) == 0
+    assert B.workspace_bytes(desc(d_k=96, d_v=96)) == 0          # unsupported
+    assert B.workspace_bytes(desc(chunk=32)) == 0                 # bf16 path needs chunk 64
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=128, d_v=128, chunk=64)) == 0
+
+
+def call_fwd(d, ptrs=None, ws=None, ws_bytes=1 << 40):
+    p = dict(q=16, k=16, v=16, beta=16, g=16, h0=None, o=16, hT=None)
+    if ptrs:
+        p.update(ptrs)
+    return B.dr_fwd(d, p["q"], p["k"], p["v"], p["beta"], p["g"], p["h0"], p["o"], p["hT"],
+                    16 if ws is None else ws, ws_bytes, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert call_fwd(desc(variant=7)) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(B=-1)) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(io_dtype=5)) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(scale=float("nan"))) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(flags=8)) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(num_seqs=3)) == B.DR_ERR_INVALID_ARG      # dense: N must equal B
+    assert call_fwd(desc(), ptrs={"q": None}) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(), ptrs={"g": None}) == B.DR_ERR_INVALID_ARG       # GDN needs g
+    assert call_fwd(desc(variant=B.DR_DELTANET)) == B.DR_ERR_INVALID_ARG    # DeltaNet: g NULL
+    assert call_fwd(desc(d_k=96, d_v=96)) == B.DR_ERR_UNSUPPORTED
+    assert call_fwd(desc(), ptrs={"k": 24}) == B.DR_ERR_ALIGNMENT
+    assert call_fwd(desc(), ptrs={"hT": 8}) == B.DR_ERR_ALIGNMENT
+    assert call_fwd(desc(), ws=0) == B.DR_ERR_WORKSPACE
+    assert call_fwd(desc(), ws_bytes=100) == B.DR_ERR_WORKSPACE
+    # packed layout needs B == 1 and the chunk tables
+    assert call_fwd(desc(B=2, cu_seqlens=16, num_seqs=2, chunk_offsets=16)) == B.DR_ERR_INVALID_ARG
+    assert call_fwd(desc(B=1, cu_seqlens=16, num_seqs=2, num_chunks=3,
+                         chunk_offsets=16)) == B.DR_ERR_INVALID_ARG
+
+
+def test_bwd_argument_errors(lib):
+    def bwd(d, **kw):
+        p = dict(q=16, k=16, v=16, beta=16, g=16, h0=None, dO=16, dhT=None, dq=16, dk=16,
+                 dv=16, dbeta=16, dg=16, dh0=None)
+        p.update(kw)
+        return B.dr_bwd(d, *p.values(), 16, 1 << 40, None)
+    assert bwd(desc(), dO=None) == B.DR_ERR_INVALID_ARG
+    assert bwd(desc(), dg=None) == B.DR_ERR_INVALID_ARG
+    assert bwd(desc(variant=B.DR_DELTANET), g=None) == B.DR_ERR_INVALID_ARG  # dg must be NULL
+    assert bwd(desc(), dh0=4) == B.DR_ERR_ALIGNMENT
+    assert bwd(desc(d_k=64, d_v=128)) == B.DR_ERR_UNSUPPORTED
+
+
+def test_error_strings(lib):
+    for c in range(7):
+        assert B.error_string(c).startswith("DR_")
+    assert "unknown" in B.error_string(99)
+
+
+def python_plan(cu, chunk):
+    table, offs = [], []
+    for n in range(len(cu) - 1):
+        offs.append(len(table))
+        t = cu[n]
+        while t < cu[n + 1]:
+            table.append((n, t))
+            t += chunk
+    offs.append(len(table))
+    return table, offs
+
+
+@pytest.mark.parametrize("lens", [[5], [64], [65, 0, 130, 1], [0, 0], [256, 4000, 33, 64, 63]])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_plan_varlen_is_exact(lib, lens, chunk):
+    cu = np.cumsum([0] + lens).astype(np.int32)
+    table, offs, n = B.plan_varlen(cu, chunk)
+    rt, ro = python_plan(cu.tolist(), chunk)
+    assert n == len(rt)
+    assert table.tolist() == [list(x) for x in rt]
+    assert offs.tolist() == ro
+    # every token covered exactly once, no chunk straddles a boundary
+    cover = np.zeros(cu[-1], dtype=np.int32)
+    for s, t0 in table:
+        end = min(t0 + chunk, cu[s + 1])
+        assert cu[s] <= t0 < cu[s + 1]
+        cover[t0:end] += 1
+    assert np.all(cover == 1)
+
+
+def test_plan_varlen_errors(lib):
+    n = ctypes.c_int(0)
+    bad = np.array([1, 5], dtype=np.int32)
+    assert lib.dr_plan_varlen(bad.ctypes.data, 1, 64, None, None, 0, ctypes.byref(n)) == B.DR_ERR_INVALID_ARG
+    dec = np.array([0, 9, 4], dtype=np.int32)
+    assert lib.dr_plan_varlen(dec.ctypes.data, 2, 64, None, None, 0, ctypes.byref(n)) == B.DR_ERR_INVALID_ARG
+    ok = np.array([0, 200], dtype=np.int32)
+    tab = np.zeros(4, dtype=np.int32)
+    assert lib.dr_plan_varlen(ok.ctypes.data, 1, 64, tab.ctypes.data, None, 2, ctypes.byref(n)) == B.DR_ERR_INVALID_ARG
+    assert n.value == 4
