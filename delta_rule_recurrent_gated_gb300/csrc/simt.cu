@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
             for (int j = 0; j < dv; ++j) acc += dbV[i * dv + j] * s(bV)[i * dv + j];
             db[i] = acc;
         }
+        __syncthreads();
         for (int idx = tid; idx < L * L; idx += nt) dA[idx] *= beta[idx / L];
         __syncthreads();
         mm(dKb, dk, dA, L, false, s(bKr), dk, false, L, dk, L, 1.f, false);
