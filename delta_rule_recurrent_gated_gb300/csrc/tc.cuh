@@ -197,3 +197,104 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 }  // namespace tc
+
+namespace tc {
+
+// ---------------------------------------------------------------- bulk copy (untiled)
+// Global -> shared copy of `bytes` (multiple of 16, both addresses 16-aligned),
+// completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- operand tiles
+// An SW128 tile in shared memory: `rows` x `cols` bf16, cols a multiple of 64.
+struct Tile {
+    uint32_t saddr;
+    int rows;
+};
+// Descriptor of the 16-wide K slice starting at kk when the tile is used
+// K-major (the tile's columns are the contraction index).
+__device__ __forceinline__ uint64_t desc_kmajor(const Tile& t, int kk) {
+    return sdesc_sw128(t.saddr + (uint32_t)((kk >> 6) * (t.rows * 128) + (kk & 63) * 2), 16, 1024);
+}
+// Descriptor of the 16-row K slice starting at kk when the tile is used
+// MN-major (the tile's rows are the contraction index).
+__device__ __forceinline__ uint64_t desc_mnmajor(const Tile& t, int kk) {
+    return sdesc_sw128(t.saddr + (uint32_t)(kk * 128), (uint32_t)(t.rows * 128), 1024);
+}
+// D[tmem] (+)= op(A) op(B), M x N, contraction K (multiple of 16).
+//   a_rows_are_k == false: A tile is [M][K];  true: A tile is [K][M] (uses A^T).
+//   b_rows_are_k == false: B tile is [N][K];  true: B tile is [K][N].
+// i.e. with both false D = A B^T.  Issued by a single thread.
+__device__ __forceinline__ void mma_tiles(uint32_t d_tmem, const Tile& A, bool a_rows_are_k,
+                                          const Tile& B, bool b_rows_are_k, int M, int N, int K,
+                                          bool accumulate) {
+    const uint32_t idesc = idesc_bf16(M, N, a_rows_are_k, b_rows_are_k);
+    for (int kk = 0; kk < K; kk += 16) {
+        const uint64_t ad = a_rows_are_k ? desc_mnmajor(A, kk) : desc_kmajor(A, kk);
+        const uint64_t bd = b_rows_are_k ? desc_mnmajor(B, kk) : desc_kmajor(B, kk);
+        mma_bf16(d_tmem, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ __nv_bfloat16* tile_elem(uint8_t* base, int row, int col, int rows) {
+    return reinterpret_cast<__nv_bfloat16*>(base + sw128_offset(row, col, rows));
+}
+// Write 16 consecutive values (col0 multiple of 16) of one tile row as bf16.
+__device__ __forceinline__ void tile_store16(uint8_t* base, int row, int col0, int rows,
+                                             const float (&v)[16]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * h + 0], v[8 * h + 1]);
+        u.y = pack_bf16(v[8 * h + 2], v[8 * h + 3]);
+        u.z = pack_bf16(v[8 * h + 4], v[8 * h + 5]);
+        u.w = pack_bf16(v[8 * h + 6], v[8 * h + 7]);
+        *reinterpret_cast<uint4*>(base + sw128_offset(row, col0 + 8 * h, rows)) = u;
+    }
+}
+// Read 16 consecutive values (col0 multiple of 16) of one tile row.
+__device__ __forceinline__ void tile_load16(const uint8_t* base, int row, int col0, int rows,
+                                            float (&v)[16]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint4 u =
+            *reinterpret_cast<const uint4*>(base + sw128_offset(row, col0 + 8 * h, rows));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+            v[8 * h + 2 * j] = __low2float(b);
+            v[8 * h + 2 * j + 1] = __high2float(b);
+        }
+    }
+}
+// Unpack 8 bf16 held in a uint4.
+__device__ __forceinline__ void unpack8(const uint4& u, float* v) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+        v[2 * j] = __low2float(b);
+        v[2 * j + 1] = __high2float(b);
+    }
+}
+
+// TMEM lane base of the calling warp (32 lanes per warp quarter)
+__device__ __forceinline__ uint32_t warp_lane_base(uint32_t tmem) {
+    return tmem + ((uint32_t)((threadIdx.x >> 5) & 3) * 32u << 16);
+}
+// Row of the accumulator held by this thread for an M = 64 product (rows
+// 16w..16w+15 sit in lanes 0..15 of warp quarter w), or -1.
+__device__ __forceinline__ int m64_row() {
+    const int lane = threadIdx.x & 31;
+    return lane < 16 ? (int)((threadIdx.x >> 5) & 3) * 16 + lane : -1;
+}
+
+}  // namespace tc

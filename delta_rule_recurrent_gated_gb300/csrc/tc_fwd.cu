@@ -1,0 +1,590 @@
+// tc_fwd.cu -- bf16 tensor-core forward of the chunkwise delta rule (sm_103a).
+//
+// The recurrence (page "Linear Attention Architectures: Mechanisms, Trade-offs,
+// and Cross-Layer Routing", section "Metodologia y Marco de Trabajo", item 1:
+// decay the memory before the residual, residual r = v - (decayed W) k, write
+// beta r k^T, read W q) is evaluated per 64-token chunk in its UT/WY form.  With
+// Gamma the within-chunk cumulative log-decay per key channel:
+//   Kb = k e^{Gamma}, Kr = k e^{-Gamma}, Qb = q e^{Gamma}, KC = k e^{Gamma_last - Gamma}
+//   T  = (I + diag(beta) strict_lower(Kb Kr^T))^{-1}          (the UT inverse)
+//   Wy = T diag(beta) Kb,  Ut = T diag(beta) v,  Aqk = tril(Qb Kr^T)
+//   Qt = scale (Qb - Aqk Wy),  Ot = scale Aqk Ut
+// and, from the state S at the chunk start (W = S^T),
+//   U = Ut - Wy S  (the writes beta r),  O = Qt S + Ot,
+//   S_next = diag(e^{Gamma_last}) S + KC^T U.
+//
+// Kernel 1, tc_prep: one CTA per (chunk, head), fully parallel.  TMA loads the
+// q/k/v tiles, CUDA cores apply the decay, tcgen05 computes the two Gram
+// products, CUDA cores invert the unit-lower-triangular 64x64 matrix (one
+// column per thread, forward substitution), tcgen05 forms Wy, Ut, Aqk Wy,
+// Aqk Ut.  Writes Wy, Qt, KC (tile images), Ut^T, Ot^T, T and e^{Gamma_last}.
+// Kernel 2, tc_scan_fwd: one CTA per (sequence, head, value tile of BV rows),
+// sequential over the sequence's chunks.  The state slice W[v0:v0+BV, :] stays
+// in fp32 registers (one row per thread); per chunk two tcgen05 products
+// (W Wy^T, W Qt^T) give U and O, and one more (U^T KC) the state increment.
+// Also stores the chunk-start state S and U for the backward pass.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+#include "tc_layout.cuh"
+
+namespace dr {
+using namespace tc;
+
+namespace {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+template <int VAR>
+__device__ __forceinline__ float gate_at(const Params& p, int row, int h, int c) {
+    if (VAR == DR_GDN) return p.g[(size_t)row * p.H + h];
+    return p.g[((size_t)row * p.H + h) * p.dk + c];
+}
+
+__device__ __forceinline__ void record_timeout(const Params& p) {
+    if (threadIdx.x == 0) atomicExch(p.err, kErrTimeout);
+}
+
+// ============================================================== tc_prep
+template <int D>
+struct PrepSmem {
+    static constexpr int kTile = 64 * D * 2;
+    static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kX = 3 * kTile, kY = 4 * kTile;
+    static constexpr int kAq = 5 * kTile, kT = kAq + 8192;
+    static constexpr int kAf = (D == 128) ? kX : kT + 8192;  // fp32 [64][64] (16 KB)
+    static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384;
+    static constexpr int kBytes = kBeta + 256 + 1024;  // + alignment slack
+};
+
+template <int D, int VAR>
+__global__ void __launch_bounds__(128, 1)
+    tc_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const Params p, const TcLayout L) {
+    using S = PrepSmem<D>;
+    constexpr int kTile = S::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* Qs = sm + S::kQ;   // q -> Qb
+    uint8_t* Ks = sm + S::kK;   // k -> Kr -> Ut
+    uint8_t* Vs = sm + S::kV;   // v -> beta v
+    uint8_t* Xs = sm + S::kX;   // Kb -> (A fp32 when D == 128) -> Wy
+    uint8_t* Ys = sm + S::kY;   // beta Kb
+    uint8_t* Aqs = sm + S::kAq; // tril(Qb Kr^T) [64][64]
+    uint8_t* Ts = sm + S::kT;   // T [64][64]
+    float* Af = reinterpret_cast<float*>(sm + S::kAf);
+    float* beta_s = reinterpret_cast<float*>(sm + S::kBeta);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_base;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    int seq, row0, len;
+    chunk_info(p, chunk, seq, row0, len);
+    const size_t rec = (size_t)chunk * p.H + h;
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+        prefetch_tmap(&mq);
+        prefetch_tmap(&mk);
+        prefetch_tmap(&mv);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = warp_lane_base(tm);
+    const int r = m64_row();
+    bool ok = true;
+
+    do {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile);
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
+            }
+        }
+        if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
+        ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+
+        // rows past the end of the sequence hold another sequence's tokens: zero them
+        {
+            const int pad = 64 - len;
+            const int per_tile = (D / 64) * pad * 8;
+            for (int w = tid; w < 3 * per_tile; w += 128) {
+                const int t = w / per_tile, rem = w % per_tile;
+                const int kb = rem / (pad * 8), rr = len + (rem % (pad * 8)) / 8, ch = rem % 8;
+                uint8_t* base = (t == 0 ? Qs : t == 1 ? Ks : Vs) + kb * 8192;
+                *reinterpret_cast<uint4*>(base + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncthreads();
+
+        // decay factors, one thread per key channel walking the chunk's tokens
+        for (int c = tid; c < D; c += 128) {
+            float GL = 0.f;
+            if (VAR != DR_DELTANET)
+                for (int i = 0; i < len; ++i) GL += gate_at<VAR>(p, row0 + i, h, c);
+            L.gC[rec * D + c] = VAR != DR_DELTANET ? expf(GL) : 1.f;
+            uint8_t* kc_img = L.KC + rec * kTile;
+            float G = 0.f;
+            for (int i = 0; i < 64; ++i) {
+                float e = 1.f, ei = 1.f, ec = 1.f;
+                if (VAR != DR_DELTANET) {
+                    if (i < len) G += gate_at<VAR>(p, row0 + i, h, c);
+                    e = expf(G);
+                    ei = expf(-G);
+                    ec = expf(GL - G);
+                }
+                const uint32_t off = sw128_offset(i, c, 64);
+                __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(Qs + off);
+                __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(Ks + off);
+                __nv_bfloat16* vp = reinterpret_cast<__nv_bfloat16*>(Vs + off);
+                const float kv = __bfloat162float(*kp), qv = __bfloat162float(*qp);
+                const float b = beta_s[i];
+                *qp = __float2bfloat16_rn(qv * e);
+                *kp = __float2bfloat16_rn(kv * ei);
+                *reinterpret_cast<__nv_bfloat16*>(Xs + off) = __float2bfloat16_rn(kv * e);
+                *reinterpret_cast<__nv_bfloat16*>(Ys + off) = __float2bfloat16_rn(b * kv * e);
+                *vp = __float2bfloat16_rn(b * __bfloat162float(*vp));
+                *reinterpret_cast<__nv_bfloat16*>(kc_img + off) = __float2bfloat16_rn(kv * ec);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+
+        // Gram = Kb Kr^T -> cols [0,64);  Qb Kr^T -> cols [64,128)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tX{smem_u32(Xs), 64}, tK{smem_u32(Ks), 64}, tQ{smem_u32(Qs), 64};
+            mma_tiles(tm + 0, tX, false, tK, false, 64, 64, D, false);
+            mma_tiles(tm + 64, tQ, false, tK, false, 64, 64, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+        // A = diag(beta) strict_lower(Gram) (fp32) and the masked Aqk tile
+        for (int cb = 0; cb < 4; ++cb) {
+            float g16[16], a16[16];
+            tmem_ld16(tl + cb * 16, g16);
+            tmem_ld16(tl + 64 + cb * 16, a16);
+            tmem_ld_wait();
+            if (r >= 0) {
+                const float br = beta_s[r];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = cb * 16 + j;
+                    Af[r * 64 + col] = col < r ? br * g16[j] : 0.f;
+                    a16[j] = col <= r ? a16[j] : 0.f;
+                }
+                tile_store16(Aqs, r, cb * 16, 64, a16);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // T = (I + A)^{-1}: thread n solves column n by forward substitution
+        if (tid < 64) {
+            const int n = tid;
+            float x[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                float s0 = (i == n) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int j = 0; j + 3 < i; j += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(&Af[i * 64 + j]);
+                    s0 = fmaf(-a.x, x[j], s0);
+                    s1 = fmaf(-a.y, x[j + 1], s1);
+                    s2 = fmaf(-a.z, x[j + 2], s2);
+                    s3 = fmaf(-a.w, x[j + 3], s3);
+                }
+#pragma unroll
+                for (int j = i & ~3; j < i; ++j) s0 = fmaf(-Af[i * 64 + j], x[j], s0);
+                x[i] = (s0 + s1) + (s2 + s3);
+            }
+            uint8_t* t_img = L.T + rec * 8192;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(x[i]);
+                const uint32_t off = sw128_offset(i, n, 64);
+                *reinterpret_cast<__nv_bfloat16*>(Ts + off) = b;
+                *reinterpret_cast<__nv_bfloat16*>(t_img + off) = b;
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+
+        // Wy = T (beta Kb) -> cols [0,D);  Ut = T (beta v) -> cols [D,2D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tT{smem_u32(Ts), 64}, tY{smem_u32(Ys), 64}, tV{smem_u32(Vs), 64};
+            mma_tiles(tm + 0, tT, false, tY, true, 64, D, 64, false);
+            mma_tiles(tm + D, tT, false, tV, true, 64, D, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+        {
+            uint8_t* wy_img = L.Wy + rec * kTile;
+            __nv_bfloat16* utT = reinterpret_cast<__nv_bfloat16*>(L.UtT + rec * kTile);
+            for (int cb = 0; cb < D / 16; ++cb) {
+                float w16[16], u16[16];
+                tmem_ld16(tl + cb * 16, w16);
+                tmem_ld16(tl + D + cb * 16, u16);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    tile_store16(Xs, r, cb * 16, 64, w16);
+                    tile_store16(wy_img, r, cb * 16, 64, w16);
+                    tile_store16(Ks, r, cb * 16, 64, u16);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        utT[(cb * 16 + j) * 64 + r] = __float2bfloat16_rn(u16[j]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // Aqk Wy -> cols [0,D);  Aqk Ut -> cols [D,2D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), 64};
+            mma_tiles(tm + 0, tA, false, tW, true, 64, D, 64, false);
+            mma_tiles(tm + D, tA, false, tU, true, 64, D, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+        {
+            uint8_t* qt_img = L.Qt + rec * kTile;
+            __nv_bfloat16* otT = reinterpret_cast<__nv_bfloat16*>(L.OtT + rec * kTile);
+            const float sc = p.scale;
+            for (int cb = 0; cb < D / 16; ++cb) {
+                float w16[16], u16[16], qb[16];
+                tmem_ld16(tl + cb * 16, w16);
+                tmem_ld16(tl + D + cb * 16, u16);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    tile_load16(Qs, r, cb * 16, 64, qb);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) qb[j] = sc * (qb[j] - w16[j]);
+                    tile_store16(qt_img, r, cb * 16, 64, qb);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        otT[(cb * 16 + j) * 64 + r] = __float2bfloat16_rn(sc * u16[j]);
+                }
+            }
+        }
+    } while (0);
+
+    if (!ok) {
+        record_timeout(p);
+        mbar_wait(&bar_ld, 0, kWaitLimitNs);  // let an outstanding copy land before exit
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ============================================================== tc_scan_fwd
+template <int D, int BV>
+struct ScanSmem {
+    static constexpr int kTile = 64 * D * 2;
+    static constexpr int kW = 0;                       // [BV][D] state (bf16 operand)
+    static constexpr int kWy = BV * D * 2;             // [64][D]
+    static constexpr int kQt = kWy + kTile;
+    static constexpr int kKC = kQt + kTile;
+    static constexpr int kUs = kKC + kTile;            // [BV][64] U^T operand
+    static constexpr int kUt = kUs + BV * 128;         // [BV][64] plain Ut^T rows
+    static constexpr int kOt = kUt + BV * 128;         // [BV][64] plain Ot^T rows
+    static constexpr int kG = kOt + BV * 128;          // [D] fp32 e^{Gamma_last}
+    static constexpr int kBytes = kG + D * 4 + 1024;
+};
+
+template <int D, int BV>
+__global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, const TcLayout L,
+                                                             int write_o) {
+    using S = ScanSmem<D, BV>;
+    constexpr int kTile = S::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* Ws = sm + S::kW;
+    uint8_t* Wys = sm + S::kWy;
+    uint8_t* Qts = sm + S::kQt;
+    uint8_t* KCs = sm + S::kKC;
+    uint8_t* Us = sm + S::kUs;
+    const uint8_t* UtTs = sm + S::kUt;
+    const uint8_t* OtTs = sm + S::kOt;
+    const float* gCs = reinterpret_cast<const float*>(sm + S::kG);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_base;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
+    const int v0 = blockIdx.y * BV;
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = warp_lane_base(tm);
+    const int r = (BV == 128) ? tid : m64_row();  // value row of this thread (or -1)
+    const int v = v0 + (r < 0 ? 0 : r);
+    const size_t state_off = ((size_t)n * p.H + h) * D * D;
+
+    float W[D];  // W[v, :] = S[:, v], fp32
+#pragma unroll
+    for (int c = 0; c < D; ++c) W[c] = (p.h0 && r >= 0) ? p.h0[state_off + (size_t)c * D + v] : 0.f;
+    if (r >= 0) {
+#pragma unroll
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float t[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
+            tile_store16(Ws, r, cb * 16, BV, t);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    bool ok = true;
+    for (int ci = 0; ci < nc && ok; ++ci) {
+        const int chunk = c0 + ci;
+        const size_t rec = (size_t)chunk * p.H + h;
+        const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * BV * 128 + D * 4);
+            bulk_g2s(Wys, L.Wy + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(Qts, L.Qt + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(KCs, L.KC + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(sm + S::kUt, L.UtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld);
+            bulk_g2s(sm + S::kOt, L.OtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld);
+            bulk_g2s(sm + S::kG, L.gC + rec * D, D * 4, &bar_ld);
+        }
+        // the chunk-start state, for the backward pass
+        if (r >= 0) {
+            uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
+#pragma unroll
+            for (int c = 0; c < D; ++c)
+                *reinterpret_cast<__nv_bfloat16*>(s_img + sw128_offset(c, v, D)) =
+                    __float2bfloat16_rn(W[c]);
+        }
+        ok = mbar_wait(&bar_ld, ci & 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+
+        // W Wy^T -> cols [0,64) ;  W Qt^T -> cols [64,128)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tW{smem_u32(Ws), BV}, tWy{smem_u32(Wys), 64}, tQt{smem_u32(Qts), 64};
+            mma_tiles(tm + 0, tW, false, tWy, false, BV, 64, D, false);
+            mma_tiles(tm + 64, tW, false, tQt, false, BV, 64, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+        {
+            uint8_t* u_img = L.U + rec * kTile;
+            for (int g = 0; g < 4; ++g) {
+                float acc[16], oacc[16];
+                tmem_ld16(tl + g * 16, acc);
+                tmem_ld16(tl + 64 + g * 16, oacc);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    float ut[16], ot[16];
+                    const uint4* up = reinterpret_cast<const uint4*>(UtTs + r * 128 + g * 32);
+                    const uint4* op = reinterpret_cast<const uint4*>(OtTs + r * 128 + g * 32);
+                    unpack8(up[0], ut);
+                    unpack8(up[1], ut + 8);
+                    unpack8(op[0], ot);
+                    unpack8(op[1], ot + 8);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        acc[j] = ut[j] - acc[j];   // U
+                        oacc[j] = ot[j] + oacc[j]; // O
+                    }
+                    tile_store16(Us, r, g * 16, BV, acc);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = g * 16 + j;
+                        *reinterpret_cast<__nv_bfloat16*>(u_img + sw128_offset(i, v, 64)) =
+                            __float2bfloat16_rn(acc[j]);
+                        if (write_o && i < len)
+                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype,
+                                   oacc[j]);
+                    }
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // U^T KC -> cols [128, 128+D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(KCs), 64};
+            mma_tiles(tm + 128, tU, false, tKC, true, BV, D, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+#pragma unroll
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float acc[16];
+            tmem_ld16(tl + 128 + cb * 16, acc);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int c = cb * 16 + j;
+                W[c] = fmaf(W[c], gCs[c], acc[j]);
+                acc[j] = W[c];
+            }
+            if (r >= 0) tile_store16(Ws, r, cb * 16, BV, acc);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (ok) {
+        if (p.hT && r >= 0) {
+#pragma unroll
+            for (int c = 0; c < D; ++c) p.hT[state_off + (size_t)c * D + v] = W[c];
+        }
+    } else {
+        record_timeout(p);
+        mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        mbar_wait(&bar_ld, 1, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ============================================================== host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+// [rows, H, D] bf16 tensor, box = 64 channels x 1 head x 64 rows, 128B swizzle
+bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t tc_records(const Params& p) { return (size_t)p.num_chunks * p.H; }
+
+TcLayout tc_layout(const Params& p) {
+    return tc_layout_at(p.ws + 256, tc_records(p), p.dk);
+}
+
+size_t tc_workspace_bytes(const Params& p) { return tc_layout_bytes(tc_records(p), p.dk); }
+
+template <int D, int VAR>
+cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    const long long rows = (long long)p.B * p.T;
+    if (!make_token_map(&mq, p.q, D, p.H, rows) || !make_token_map(&mk, p.k, D, p.H, rows) ||
+        !make_token_map(&mv, p.v, D, p.H, rows))
+        return cudaErrorInvalidValue;
+    constexpr int smem = PrepSmem<D>::kBytes;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = set_smem(tc_prep_kernel<D, VAR>, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    if (p.num_chunks == 0) return cudaSuccess;
+    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, p, L);
+    return cudaGetLastError();
+}
+
+template <int D, int BV>
+cudaError_t launch_scan_fwd(const Params& p, const TcLayout& L, cudaStream_t st, bool write_o) {
+    constexpr int smem = ScanSmem<D, BV>::kBytes;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = set_smem(tc_scan_fwd_kernel<D, BV>, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    if (p.N * p.H == 0) return cudaSuccess;
+    tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L, write_o ? 1 : 0);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t tc_fwd_d(const Params& p, cudaStream_t st, bool write_o) {
+    const TcLayout L = tc_layout(p);
+    cudaError_t e;
+    switch (p.variant) {
+        case DR_DELTANET: e = launch_prep<D, DR_DELTANET>(p, L, st); break;
+        case DR_GDN: e = launch_prep<D, DR_GDN>(p, L, st); break;
+        default: e = launch_prep<D, DR_KDA>(p, L, st); break;
+    }
+    if (e != cudaSuccess) return e;
+    return launch_scan_fwd<D, 64>(p, L, st, write_o);
+}
+
+cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o) {
+    return p.dk == 128 ? tc_fwd_d<128>(p, st, write_o) : tc_fwd_d<64>(p, st, write_o);
+}
+
+}  // namespace dr

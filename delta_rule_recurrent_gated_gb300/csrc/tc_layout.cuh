@@ -1,0 +1,59 @@
+// tc_layout.cuh -- workspace layout of the bf16 tensor-core path.
+//
+// Every per-chunk intermediate is kept per (chunk, head) record rec = chunk*H + h.
+// "Tile images" are byte-for-byte copies of SW128 shared-memory tiles (see
+// tc.cuh) so a kernel fetches one with a single untiled bulk copy.
+//   Wy, Qt, KC, U, dU : [64 tokens][D] tile images           (64*D*2 bytes)
+//   UtT, OtT          : [D][64] plain bf16, transposed         (D*64*2 bytes)
+//   T                 : [64][64] tile image of the UT inverse  (8 KB)
+//   S, dS             : [D rows = key channel][D cols = value channel] tile images
+//                       of the state at the chunk start / of dL/d(state at the
+//                       chunk end)                              (D*D*2 bytes)
+//   gC                : [D] fp32, e^{Gamma} at the chunk's last token
+#pragma once
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace dr {
+
+struct TcLayout {
+    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS;
+    float* gC;
+};
+
+__host__ __device__ inline size_t tc_align(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+// Byte offsets of the arrays for `recs` records of head size D, starting at 0.
+struct TcSizes {
+    size_t kd, dd, cc, g;
+    __host__ __device__ explicit TcSizes(int D)
+        : kd((size_t)64 * D * 2), dd((size_t)D * D * 2), cc(64 * 64 * 2), g((size_t)D * 4) {}
+};
+
+__host__ inline size_t tc_layout_bytes(size_t recs, int D) {
+    TcSizes s(D);
+    return tc_align(recs * s.kd) * 7 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
+           tc_align(recs * s.g);
+}
+
+__host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
+    TcSizes s(D);
+    TcLayout L;
+    uint8_t* p = base;
+    auto take = [&](size_t n) { uint8_t* r = p; p += tc_align(n); return r; };
+    L.Wy = take(recs * s.kd);
+    L.Qt = take(recs * s.kd);
+    L.KC = take(recs * s.kd);
+    L.U = take(recs * s.kd);
+    L.dU = take(recs * s.kd);
+    L.UtT = take(recs * s.kd);
+    L.OtT = take(recs * s.kd);
+    L.T = take(recs * s.cc);
+    L.S = take(recs * s.dd);
+    L.dS = take(recs * s.dd);
+    L.gC = reinterpret_cast<float*>(take(recs * s.g));
+    return L;
+}
+
+}  // namespace dr

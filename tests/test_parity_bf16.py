@@ -1,0 +1,37 @@
+"""GPU parity of the bf16 tensor-core path against the fp64 oracle, through the
+C ABI, at sizes the oracle finishes in seconds (several chunks, ragged tails,
+packed sequences, empty sequences) and at the full workload sizes on sampled
+(sequence, head) units.  Tolerance: tests/parity.py."""
+import numpy as np
+import pytest
+
+from delta_rule_recurrent_gated_gb300 import inputs
+
+from parity import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["deltanet", "gdn", "kda"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_small(variant, d):
+    w = inputs.small(variant, B=2, T=200, H=3, dk=d, dv=d)
+    x = inputs.make(w, seed=3)
+    compare(w, x, run_gpu(w, x, backward=False), run_oracle(w, x, backward=False))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("T", [1, 63, 64, 65])
+def test_forward_short_sequences(variant, T):
+    w = inputs.small(variant, B=3, T=T, H=2, dk=64, dv=64)
+    x = inputs.make(w, seed=4)
+    compare(w, x, run_gpu(w, x, backward=False), run_oracle(w, x, backward=False))
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_forward_packed(variant):
+    w = inputs.small(variant, H=2, dk=128, dv=128, lengths=[100, 0, 64, 1, 191, 7])
+    x = inputs.make(w, seed=5)
+    compare(w, x, run_gpu(w, x, backward=False), run_oracle(w, x, backward=False))
