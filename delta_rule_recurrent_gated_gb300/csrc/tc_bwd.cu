@@ -1,0 +1,827 @@
+// tc_bwd.cu -- bf16 tensor-core backward of the chunkwise delta rule (sm_103a).
+//
+// Chain rule through the chunk steps of tc_fwd.cu, per chunk with state S at
+// its start and dS = dL/d(state at its end):
+//   dU   = KC dS                         dS_prev = diag(e^{Gamma_last}) dS + Qt^T dO - Wy^T dU
+//   dQt  = dO S^T,  dWyA = dU S^T,  dKC = U dS^T,  dgC = rowsum(dS * S)
+//   dAqk = scale tril(dO Ut^T - dQt Wy^T) = scale tril(P T^T),
+//          P = (dO v^T - dQt Kb^T) diag(beta)
+//   dWy  = -dWyA - scale Aqk^T dQt,       dUt = dU + scale Aqk^T dO
+//   dT   = (dWy Kb^T + dUt v^T) diag(beta)
+//   d(beta Kb) = T^T dWy,  d(beta v) = T^T dUt
+//   dA   = -T^T (dT T^T)  (strictly lower),  dG = diag(beta) dA
+//   dKb  = dG Kr + beta d(beta Kb),  dKr = dG^T Kb + dAqk^T Qb,  dQb = scale dQt + dAqk Kr
+// then the decay: dq = dQb e^{Gamma}, dk = dKb e^{Gamma} + dKr e^{-Gamma} + dKC e^{Gamma_last-Gamma},
+// dGamma = dQb Qb + dKb Kb - dKr Kr - dKC KC (+ sum_i dKC KC + dgC e^{Gamma_last} at the
+// last token), dg = reverse cumulative sum of dGamma within the chunk.
+//
+// Kernels: tc_scan_bwd (reverse over chunks, one CTA per (sequence, head, value
+// tile), dS kept in fp32 registers), tc_bwd_state (chunk-parallel, the four
+// state-side products), tc_bwd_chunk (chunk-parallel, everything else).
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+#include "tc_layout.cuh"
+
+namespace dr {
+using namespace tc;
+
+bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
+TcLayout tc_layout(const Params& p);
+cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
+
+namespace {
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+__device__ __forceinline__ void record_timeout(const Params& p) {
+    if (threadIdx.x == 0) atomicExch(p.err, kErrTimeout);
+}
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+__device__ __forceinline__ void zero_pad_rows(uint8_t* tile, int D, int len) {
+    const int pad = 64 - len;
+    const int n = (D / 64) * pad * 8;
+    for (int w = threadIdx.x; w < n; w += blockDim.x) {
+        const int kb = w / (pad * 8), rr = len + (w % (pad * 8)) / 8, ch = w % 8;
+        *reinterpret_cast<uint4*>(tile + kb * 8192 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// ============================================================== tc_scan_bwd
+template <int D, int BV>
+struct BScanSmem {
+    static constexpr int kTile = 64 * D * 2;
+    static constexpr int kW = 0;                 // [BV][D]  dS^T slice (bf16 operand)
+    static constexpr int kKC = BV * D * 2;       // [64][D]
+    static constexpr int kQt = kKC + kTile;
+    static constexpr int kWy = kQt + kTile;
+    static constexpr int kdO = kWy + kTile;      // [BV][64] dO^T
+    static constexpr int kdU = kdO + BV * 128;   // [BV][64] -dU^T
+    static constexpr int kG = kdU + BV * 128;    // [D] fp32
+    static constexpr int kBytes = kG + D * 4 + 1024;
+};
+
+template <int D, int BV>
+__global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, const TcLayout L) {
+    using S = BScanSmem<D, BV>;
+    constexpr int kTile = S::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* Ws = sm + S::kW;
+    uint8_t* KCs = sm + S::kKC;
+    uint8_t* Qts = sm + S::kQt;
+    uint8_t* Wys = sm + S::kWy;
+    uint8_t* dOs = sm + S::kdO;
+    uint8_t* dUs = sm + S::kdU;
+    const float* gCs = reinterpret_cast<const float*>(sm + S::kG);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_base;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
+    const int v0 = blockIdx.y * BV;
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = warp_lane_base(tm);
+    const int r = (BV == 128) ? tid : m64_row();
+    const int v = v0 + (r < 0 ? 0 : r);
+    const size_t state_off = ((size_t)n * p.H + h) * D * D;
+
+    float W[D];  // dS[:, v] (the gradient of the state at the current chunk end)
+#pragma unroll
+    for (int c = 0; c < D; ++c) W[c] = (p.dhT && r >= 0) ? p.dhT[state_off + (size_t)c * D + v] : 0.f;
+    if (r >= 0) {
+#pragma unroll
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float t[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
+            tile_store16(Ws, r, cb * 16, BV, t);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    bool ok = true;
+    int it = 0;
+    for (int ci = nc - 1; ci >= 0 && ok; --ci, ++it) {
+        const size_t rec = (size_t)(c0 + ci) * p.H + h;
+        const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + D * 4);
+            bulk_g2s(KCs, L.KC + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(Qts, L.Qt + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(Wys, L.Wy + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(sm + S::kG, L.gC + rec * D, D * 4, &bar_ld);
+        }
+        if (r >= 0) {
+            uint8_t* ds_img = L.dS + rec * (size_t)D * D * 2;
+#pragma unroll
+            for (int c = 0; c < D; ++c)
+                *reinterpret_cast<__nv_bfloat16*>(ds_img + sw128_offset(c, v, D)) =
+                    __float2bfloat16_rn(W[c]);
+            for (int g = 0; g < 4; ++g) {
+                float t[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int i = g * 16 + j;
+                    t[j] = i < len ? ld_any(p.dO, ((size_t)(row0 + i) * p.H + h) * D + v, p.io_dtype)
+                                   : 0.f;
+                }
+                tile_store16(dOs, r, g * 16, BV, t);
+            }
+        }
+        fence_async_smem();
+        ok = mbar_wait(&bar_ld, it & 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+
+        // dU^T = dS^T KC^T -> cols [0,64)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tW{smem_u32(Ws), BV}, tK{smem_u32(KCs), 64};
+            mma_tiles(tm + 0, tW, false, tK, false, BV, 64, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        {
+            uint8_t* du_img = L.dU + rec * kTile;
+            for (int g = 0; g < 4; ++g) {
+                float acc[16];
+                tmem_ld16(tl + g * 16, acc);
+                tmem_ld_wait();
+                if (r >= 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        *reinterpret_cast<__nv_bfloat16*>(du_img + sw128_offset(g * 16 + j, v, 64)) =
+                            __float2bfloat16_rn(acc[j]);
+                        acc[j] = -acc[j];
+                    }
+                    tile_store16(dUs, r, g * 16, BV, acc);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // dO^T Qt - dU^T Wy -> cols [64, 64+D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tO{smem_u32(dOs), BV}, tU{smem_u32(dUs), BV}, tQ{smem_u32(Qts), 64},
+                tWy{smem_u32(Wys), 64};
+            mma_tiles(tm + 64, tO, false, tQ, true, BV, D, 64, false);
+            mma_tiles(tm + 64, tU, false, tWy, true, BV, D, 64, true);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float acc[16];
+            tmem_ld16(tl + 64 + cb * 16, acc);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int c = cb * 16 + j;
+                W[c] = fmaf(W[c], gCs[c], acc[j]);
+                acc[j] = W[c];
+            }
+            if (r >= 0) tile_store16(Ws, r, cb * 16, BV, acc);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (ok) {
+        if (p.dh0 && r >= 0) {
+#pragma unroll
+            for (int c = 0; c < D; ++c) p.dh0[state_off + (size_t)c * D + v] = W[c];
+        }
+    } else {
+        record_timeout(p);
+        mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        mbar_wait(&bar_ld, 1, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ============================================================== tc_bwd_state
+template <int D>
+struct BStateSmem {
+    static constexpr int kTile = 64 * D * 2, kDD = D * D * 2;
+    static constexpr int kdO = 0, kS = kTile, kdS = kS + kDD, kU = kdS + kDD, kdU = kU + kTile;
+    static constexpr int kBytes = kdU + kTile + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    tc_bwd_state_kernel(const __grid_constant__ CUtensorMap mdo, const Params p, const TcLayout L) {
+    using S = BStateSmem<D>;
+    constexpr int kTile = S::kTile, kDD = S::kDD;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* dOs = sm + S::kdO;
+    uint8_t* Ss = sm + S::kS;
+    uint8_t* dSs = sm + S::kdS;
+    uint8_t* Us = sm + S::kU;
+    uint8_t* dUs = sm + S::kdU;
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    int seq, row0, len;
+    chunk_info(p, chunk, seq, row0, len);
+    const size_t rec = (size_t)chunk * p.H + h;
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+        prefetch_tmap(&mdo);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = warp_lane_base(tm);
+    const int r = m64_row();
+    bool ok = true;
+    do {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * kDD);
+            for (int kb = 0; kb < D / 64; ++kb)
+                tma_load_3d(dOs + kb * 8192, &mdo, &bar_ld, kb * 64, h, row0);
+            bulk_g2s(Ss, L.S + rec * kDD, kDD, &bar_ld);
+            bulk_g2s(dSs, L.dS + rec * kDD, kDD, &bar_ld);
+            bulk_g2s(Us, L.U + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(dUs, L.dU + rec * kTile, kTile, &bar_ld);
+        }
+        ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        zero_pad_rows(dOs, D, len);
+        fence_async_smem();
+        __syncthreads();
+        // dO S^T -> [0,D) ; dU S^T -> [D,2D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tO{smem_u32(dOs), 64}, tS{smem_u32(Ss), D}, tdU{smem_u32(dUs), 64};
+            mma_tiles(tm + 0, tO, false, tS, false, 64, D, D, false);
+            mma_tiles(tm + D, tdU, false, tS, false, 64, D, D, false);
+            mma_commit(&bar_mma);
+        }
+        // dgC[c] = sum_v dS[c, v] S[c, v]  (overlaps the MMAs)
+        for (int c = tid; c < D; c += 128) {
+            float acc = 0.f;
+            for (int vb = 0; vb < D; vb += 16) {
+                float a[16], b[16];
+                tile_load16(Ss, c, vb, D, a);
+                tile_load16(dSs, c, vb, D, b);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc = fmaf(a[j], b[j], acc);
+            }
+            L.dgC[rec * D + c] = acc;
+        }
+        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float a[16], b[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + D + cb * 16, b);
+            tmem_ld_wait();
+            if (r >= 0) {
+                tile_store16(L.dQt + rec * kTile, r, cb * 16, 64, a);
+                tile_store16(L.dWyA + rec * kTile, r, cb * 16, 64, b);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // U dS^T -> [0,D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tU{smem_u32(Us), 64}, tdS{smem_u32(dSs), D};
+            mma_tiles(tm + 0, tU, false, tdS, false, 64, D, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float a[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld_wait();
+            if (r >= 0) tile_store16(L.dKC + rec * kTile, r, cb * 16, 64, a);
+        }
+    } while (0);
+    if (!ok) {
+        record_timeout(p);
+        mbar_wait(&bar_ld, 0, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+// ============================================================== tc_bwd_chunk
+template <int D, int VAR>
+struct BChunkSmem {
+    static constexpr int kTile = 64 * D * 2, kCC = 8192;
+    static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kdQ = 4 * kTile,
+                         kKb = 5 * kTile, kdWy = 6 * kTile, kdUt = 7 * kTile;
+    static constexpr int kT = 8 * kTile, kAq = kT + kCC, kB8a = kAq + kCC, kB8b = kB8a + kCC,
+                         kdAq = kB8b + kCC;
+    static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][D]
+    static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * D * 4 : 0);
+    // small arrays: beta[64], gamma_last[D], dgC[D], E[D], rowsum[64], Gamma_row[64]
+    static constexpr int kBytes = kSmall + (64 * 3 + D * 3) * 4 + 1024;
+};
+
+template <int D, int VAR>
+__global__ void __launch_bounds__(128, 1)
+    tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                        const Params p, const TcLayout L) {
+    using S = BChunkSmem<D, VAR>;
+    constexpr int kTile = S::kTile;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* Qs = sm + S::kQ;     // q -> Qb
+    uint8_t* Ks = sm + S::kK;     // k -> Kr
+    uint8_t* Vs = sm + S::kV;     // v
+    uint8_t* dOs = sm + S::kdO;
+    uint8_t* dQs = sm + S::kdQ;   // dQt = dO S^T
+    uint8_t* Kbs = sm + S::kKb;   // Kb
+    uint8_t* dWys = sm + S::kdWy;
+    uint8_t* dUts = sm + S::kdUt;
+    uint8_t* Ts = sm + S::kT;
+    uint8_t* Aqs = sm + S::kAq;   // tril(Qb Kr^T)
+    uint8_t* B8a = sm + S::kB8a;  // P, then X = dT T^T
+    uint8_t* B8b = sm + S::kB8b;  // dT, then dG
+    uint8_t* dAqs = sm + S::kdAq; // dAqk
+    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: Gamma, then dGamma
+    float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
+    float* gC_s = beta_s + 64;
+    float* dgC_s = gC_s + D;
+    float* E_s = dgC_s + D;
+    float* rowsum = E_s + D;
+    float* Grow = rowsum + 64;    // GDN: Gamma per row
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_base;
+
+    constexpr uint32_t R_dbK = 128, R_dbV = 128 + D, R_dQ = 128 + 2 * D, R_dKr = 128 + D;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    int seq, row0, len;
+    chunk_info(p, chunk, seq, row0, len);
+    const size_t rec = (size_t)chunk * p.H + h;
+    const float sc = p.scale;
+
+    if (tid == 0) {
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+        prefetch_tmap(&mq);
+        prefetch_tmap(&mk);
+        prefetch_tmap(&mv);
+        prefetch_tmap(&mdo);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = warp_lane_base(tm);
+    const int r = m64_row();
+    bool ok = true;
+    uint32_t mph = 0;  // bar_mma phase
+    auto mma_done = [&]() -> bool {
+        const bool good = mbar_wait(&bar_mma, mph, kWaitLimitNs);
+        mph ^= 1;
+        return good;
+    };
+
+    do {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 5 * kTile + 8192 + 2 * D * 4);
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(dOs + kb * 8192, &mdo, &bar_ld, kb * 64, h, row0);
+            }
+            bulk_g2s(dQs, L.dQt + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(Ts, L.T + rec * 8192, 8192, &bar_ld);
+            bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_ld);
+            bulk_g2s(dgC_s, L.dgC + rec * D, D * 4, &bar_ld);
+        }
+        if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
+        for (int c = tid; c < D; c += 128) E_s[c] = 0.f;
+        ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        zero_pad_rows(Qs, D, len);
+        zero_pad_rows(Ks, D, len);
+        zero_pad_rows(Vs, D, len);
+        zero_pad_rows(dOs, D, len);
+        __syncthreads();
+
+        // E1: decay factors per key channel
+        for (int c = tid; c < D; c += 128) {
+            float G = 0.f;
+            for (int i = 0; i < 64; ++i) {
+                float e = 1.f, ei = 1.f;
+                if (VAR != DR_DELTANET) {
+                    if (i < len) {
+                        G += (VAR == DR_GDN) ? p.g[(size_t)(row0 + i) * p.H + h]
+                                             : p.g[((size_t)(row0 + i) * p.H + h) * D + c];
+                    }
+                    e = expf(G);
+                    ei = expf(-G);
+                    if (VAR == DR_KDA) Gam[i * D + c] = G;
+                    if (VAR == DR_GDN && c == 0) Grow[i] = G;
+                }
+                const uint32_t off = sw128_offset(i, c, 64);
+                __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(Qs + off);
+                __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(Ks + off);
+                const float kv = __bfloat162float(*kp);
+                *qp = __float2bfloat16_rn(__bfloat162float(*qp) * e);
+                *kp = __float2bfloat16_rn(kv * ei);
+                *reinterpret_cast<__nv_bfloat16*>(Kbs + off) = __float2bfloat16_rn(kv * e);
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+
+        // M1: Qb Kr^T -> [0,64) ; dO v^T -> [64,128) ; dQt Kb^T -> [128,192)
+        if (tid == 0) {
+            tc_fence_after();
+            mma_tiles(tm + 0, Tile{smem_u32(Qs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + 64, Tile{smem_u32(dOs), 64}, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + 128, Tile{smem_u32(dQs), 64}, false, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < 4; ++cb) {
+            float a[16], p1[16], p2[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + 64 + cb * 16, p1);
+            tmem_ld16(tl + 128 + cb * 16, p2);
+            tmem_ld_wait();
+            if (r >= 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = cb * 16 + j;
+                    a[j] = col <= r ? a[j] : 0.f;
+                    p1[j] = beta_s[col] * (p1[j] - p2[j]);
+                }
+                tile_store16(Aqs, r, cb * 16, 64, a);
+                tile_store16(B8a, r, cb * 16, 64, p1);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M2: P T^T -> [0,64) ; Aqk^T dQt -> [64,64+D) ; Aqk^T dO -> [64+D,64+2D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tAq{smem_u32(Aqs), 64};
+            mma_tiles(tm + 0, Tile{smem_u32(B8a), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
+            mma_tiles(tm + 64, tAq, true, Tile{smem_u32(dQs), 64}, true, 64, D, 64, false);
+            mma_tiles(tm + 64 + D, tAq, true, Tile{smem_u32(dOs), 64}, true, 64, D, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < 4; ++cb) {
+            float a[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld_wait();
+            if (r >= 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = (cb * 16 + j <= r) ? sc * a[j] : 0.f;
+                tile_store16(dAqs, r, cb * 16, 64, a);
+            }
+        }
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float a[16], b[16];
+            tmem_ld16(tl + 64 + cb * 16, a);
+            tmem_ld16(tl + 64 + D + cb * 16, b);
+            tmem_ld_wait();
+            if (r >= 0) {
+                float wa[16], du[16];
+                tile_load16(L.dWyA + rec * kTile, r, cb * 16, 64, wa);
+                tile_load16(L.dU + rec * kTile, r, cb * 16, 64, du);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    a[j] = -wa[j] - sc * a[j];  // dWy
+                    b[j] = du[j] + sc * b[j];   // dUt
+                }
+                tile_store16(dWys, r, cb * 16, 64, a);
+                tile_store16(dUts, r, cb * 16, 64, b);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M3: dWy Kb^T -> [0,64) ; dUt v^T -> [64,128) ; T^T dWy -> R_dbK ; T^T dUt -> R_dbV ;
+        //     dAqk Kr -> R_dQ
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tT{smem_u32(Ts), 64}, tdW{smem_u32(dWys), 64}, tdU{smem_u32(dUts), 64};
+            mma_tiles(tm + 0, tdW, false, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + 64, tdU, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + R_dbK, tT, true, tdW, true, 64, D, 64, false);
+            mma_tiles(tm + R_dbV, tT, true, tdU, true, 64, D, 64, false);
+            mma_tiles(tm + R_dQ, Tile{smem_u32(dAqs), 64}, false, Tile{smem_u32(Ks), 64}, true, 64, D, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        float dbeta_acc = 0.f;
+        for (int cb = 0; cb < 4; ++cb) {
+            float a[16], b[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + 64 + cb * 16, b);
+            tmem_ld_wait();
+            if (r >= 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = beta_s[cb * 16 + j] * (a[j] + b[j]);  // dT
+                tile_store16(B8b, r, cb * 16, 64, a);
+            }
+        }
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float a[16];
+            tmem_ld16(tl + R_dbV + cb * 16, a);
+            tmem_ld_wait();
+            if (r >= 0) {
+                float vv[16];
+                tile_load16(Vs, r, cb * 16, 64, vv);
+                const float br = beta_s[r];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    dbeta_acc = fmaf(a[j], vv[j], dbeta_acc);
+                    if (r < len)
+                        st_any(p.dv_, ((size_t)(row0 + r) * p.H + h) * D + cb * 16 + j,
+                               p.grad_dtype, br * a[j]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M4: X = dT T^T -> [0,64)
+        if (tid == 0) {
+            tc_fence_after();
+            mma_tiles(tm + 0, Tile{smem_u32(B8b), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < 4; ++cb) {
+            float a[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld_wait();
+            if (r >= 0) tile_store16(B8a, r, cb * 16, 64, a);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M5: T^T X -> [0,64) (dA = -it) ; Gram Kb Kr^T -> [64,128)
+        if (tid == 0) {
+            tc_fence_after();
+            mma_tiles(tm + 0, Tile{smem_u32(Ts), 64}, true, Tile{smem_u32(B8a), 64}, true, 64, 64, 64, false);
+            mma_tiles(tm + 64, Tile{smem_u32(Kbs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int cb = 0; cb < 4; ++cb) {
+            float a[16], gm[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + 64 + cb * 16, gm);
+            tmem_ld_wait();
+            if (r >= 0) {
+                const float br = beta_s[r];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float dA = (cb * 16 + j < r) ? -a[j] : 0.f;
+                    dbeta_acc = fmaf(dA, gm[j], dbeta_acc);
+                    a[j] = br * dA;  // dG
+                }
+                tile_store16(B8b, r, cb * 16, 64, a);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M6: dG Kr -> [0,D) ; dG^T Kb + dAqk^T Qb -> R_dKr
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tG{smem_u32(B8b), 64};
+            mma_tiles(tm + 0, tG, false, Tile{smem_u32(Ks), 64}, true, 64, D, 64, false);
+            mma_tiles(tm + R_dKr, tG, true, Tile{smem_u32(Kbs), 64}, true, 64, D, 64, false);
+            mma_tiles(tm + R_dKr, Tile{smem_u32(dAqs), 64}, true, Tile{smem_u32(Qs), 64}, true, 64, D, 64, true);
+            mma_commit(&bar_mma);
+        }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+
+        // E7: the decay chain, per row
+        {
+            const uint8_t* dkc_img = L.dKC + rec * kTile;
+            float grow = 0.f;
+            float Gr = 0.f;
+            if (VAR == DR_GDN && r >= 0) Gr = Grow[r];
+            const float br = r >= 0 ? beta_s[r] : 0.f;
+            for (int cb = 0; cb < D / 16; ++cb) {
+                float dq_[16], dbk[16], dkb[16], dkr[16];
+                tmem_ld16(tl + R_dQ + cb * 16, dq_);
+                tmem_ld16(tl + R_dbK + cb * 16, dbk);
+                tmem_ld16(tl + 0 + cb * 16, dkb);
+                tmem_ld16(tl + R_dKr + cb * 16, dkr);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    float qb[16], kb[16], kr[16], dqt[16], dkc[16];
+                    tile_load16(Qs, r, cb * 16, 64, qb);
+                    tile_load16(Kbs, r, cb * 16, 64, kb);
+                    tile_load16(Ks, r, cb * 16, 64, kr);
+                    tile_load16(dQs, r, cb * 16, 64, dqt);
+                    tile_load16(dkc_img, r, cb * 16, 64, dkc);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int c = cb * 16 + j;
+                        float G = 0.f;
+                        if (VAR == DR_KDA) G = Gam[r * D + c];
+                        if (VAR == DR_GDN) G = Gr;
+                        const float e = VAR == DR_DELTANET ? 1.f : expf(G);
+                        const float ei = VAR == DR_DELTANET ? 1.f : expf(-G);
+                        const float gc = gC_s[c];
+                        const float dQb = sc * dqt[j] + dq_[j];
+                        const float dKb = dkb[j] + br * dbk[j];
+                        const float KC = kr[j] * gc;
+                        dbeta_acc = fmaf(dbk[j], kb[j], dbeta_acc);
+                        const float dG = dQb * qb[j] + dKb * kb[j] - dkr[j] * kr[j] - dkc[j] * KC;
+                        if (VAR == DR_KDA) {
+                            Gam[r * D + c] = dG;
+                            atomicAdd(&E_s[c], dkc[j] * KC);
+                        } else if (VAR == DR_GDN) {
+                            grow += dG;
+                            atomicAdd(&E_s[c], dkc[j] * KC);
+                        }
+                        if (r < len) {
+                            const size_t eidx = ((size_t)(row0 + r) * p.H + h) * D + c;
+                            st_any(p.dq, eidx, p.grad_dtype, dQb * e);
+                            st_any(p.dk_, eidx, p.grad_dtype, dKb * e + dkr[j] * ei + dkc[j] * gc * ei);
+                        }
+                    }
+                }
+            }
+            if (r >= 0) {
+                if (VAR == DR_GDN) rowsum[r] = grow;
+                if (r < len) p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc;
+            }
+        }
+        __syncthreads();
+
+        // E8: dg = reverse cumulative sum of dGamma within the chunk
+        if (VAR == DR_KDA) {
+            for (int c = tid; c < D; c += 128) {
+                float run = E_s[c] + dgC_s[c] * gC_s[c];
+                for (int i = len - 1; i >= 0; --i) {
+                    run += Gam[i * D + c];
+                    p.dg[((size_t)(row0 + i) * p.H + h) * D + c] = run;
+                }
+            }
+        } else if (VAR == DR_GDN) {
+            if (warp == 0) {
+                float e = 0.f;
+                for (int c = threadIdx.x; c < D; c += 32) e += E_s[c] + dgC_s[c] * gC_s[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+                if (threadIdx.x == 0) {
+                    float run = e;
+                    for (int i = len - 1; i >= 0; --i) {
+                        run += rowsum[i];
+                        p.dg[(size_t)(row0 + i) * p.H + h] = run;
+                    }
+                }
+            }
+        }
+    } while (0);
+    if (!ok) {
+        record_timeout(p);
+        mbar_wait(&bar_ld, 0, kWaitLimitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+template <int D>
+cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
+    if (!reuse) {
+        cudaError_t e = tc_fwd(p, st, false);
+        if (e != cudaSuccess) return e;
+    }
+    const TcLayout L = tc_layout(p);
+    const long long rows = (long long)p.B * p.T;
+    CUtensorMap mq, mk, mv, mdo;
+    if (!make_token_map(&mq, p.q, D, p.H, rows) || !make_token_map(&mk, p.k, D, p.H, rows) ||
+        !make_token_map(&mv, p.v, D, p.H, rows) || !make_token_map(&mdo, p.dO, D, p.H, rows))
+        return cudaErrorInvalidValue;
+    {
+        constexpr int BV = 64;
+        constexpr int smem = BScanSmem<D, BV>::kBytes;
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = set_smem(tc_scan_bwd_kernel<D, BV>, smem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        tc_scan_bwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (p.num_chunks == 0) return cudaSuccess;
+    {
+        constexpr int smem = BStateSmem<D>::kBytes;
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = set_smem(tc_bwd_state_kernel<D>, smem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        tc_bwd_state_kernel<D><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mdo, p, L);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    auto chunk_launch = [&](auto kernel, int smem, bool& attr) -> cudaError_t {
+        if (!attr) {
+            cudaError_t e = set_smem(kernel, smem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        kernel<<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mdo, p, L);
+        return cudaGetLastError();
+    };
+    static bool a0 = false, a1 = false, a2 = false;
+    switch (p.variant) {
+        case DR_DELTANET:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET>, BChunkSmem<D, DR_DELTANET>::kBytes, a0);
+        case DR_GDN:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN>, BChunkSmem<D, DR_GDN>::kBytes, a1);
+        default:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA>, BChunkSmem<D, DR_KDA>::kBytes, a2);
+    }
+}
+
+}  // namespace
+
+cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse) {
+    return p.dk == 128 ? tc_bwd_d<128>(p, st, reuse) : tc_bwd_d<64>(p, st, reuse);
+}
+
+}  // namespace dr

@@ -35,3 +35,36 @@ def test_forward_packed(variant):
     w = inputs.small(variant, H=2, dk=128, dv=128, lengths=[100, 0, 64, 1, 191, 7])
     x = inputs.make(w, seed=5)
     compare(w, x, run_gpu(w, x, backward=False), run_oracle(w, x, backward=False))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_bwd_small(variant, d):
+    w = inputs.small(variant, B=2, T=200, H=3, dk=d, dv=d)
+    x = inputs.make(w, seed=6)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("T", [1, 64, 130])
+def test_fwd_bwd_short_and_tail(variant, T):
+    w = inputs.small(variant, B=2, T=T, H=2, dk=64, dv=64, h0=False, dhT=False)
+    x = inputs.make(w, seed=7)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fwd_bwd_packed(variant):
+    w = inputs.small(variant, H=2, dk=128, dv=128, lengths=[100, 0, 64, 1, 191, 7])
+    x = inputs.make(w, seed=8)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_backward_recompute_matches_reuse(variant):
+    w = inputs.small(variant, B=2, T=300, H=2, dk=128, dv=128)
+    x = inputs.make(w, seed=9)
+    a = run_gpu(w, x, reuse=True)
+    b = run_gpu(w, x, reuse=False)
+    for n in ("dq", "dk", "dv", "dbeta", "dg", "dh0"):
+        assert np.array_equal(a[n], b[n]), n
