@@ -1,0 +1,381 @@
+"""Benchmark of one delta-rule token-mixer layer: forward + backward tokens/s.
+
+One step = dr_fwd + dr_bwd (the backward reusing the forward's residuals)
+through the C ABI over one batch of synthetic inputs already resident in HBM.
+Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle is
+timed instead, on a bounded sample of the same workload, on the host cores.
+
+Multi-GPU: the layer has no cross-sequence exchange, so N ranks run N
+independent replicas of the workload (weak scaling); the only collectives are
+the timing barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "gdn_h0_b8_t4096_h16_d128"
+METRIC = "fwd+bwd tokens/s per delta-rule layer (T=4096,H=16,d=128)"
+
+
+def algorithmic(w, N):
+    """Per-step algorithmic FLOPs and bytes of the whole path (fwd + bwd), per
+    token per head: F = 24 C dk + 14 C dv + 22 dk dv + 16/3 C^2 and
+    bytes = 3 s (2 dk + dv) + 2 s dv + 12 + 3 G (s = io bytes, G = gate bytes),
+    plus 5 dk dv 4 bytes of state per sequence and head when states are used."""
+    C, dk, dv = w.chunk, w.dk, w.dv
+    s = 2 if w.io == "bf16" else 4
+    G = {"deltanet": 0, "gdn": 4, "kda": 4 * dk}[w.variant]
+    th = w.B * w.T * w.H
+    flops = th * (24 * C * dk + 14 * C * dv + 22 * dk * dv + 16.0 / 3.0 * C * C)
+    byts = th * (3 * s * (2 * dk + dv) + 2 * s * dv + 12 + 3 * G)
+    if w.h0:
+        byts += 5 * dk * dv * 4 * N * w.H
+    return flops, byts
+
+
+def kernel_bytes(name, w, N):
+    """Bytes a kernel must move by design (its inputs and outputs), per launch."""
+    D, H, th = w.dk, w.H, w.B * w.T * w.H
+    chunks = (w.T + 63) // 64 * w.B
+    recs = chunks * H
+    tile, dd = 64 * D * 2, D * D * 2
+    g = {"deltanet": 0, "gdn": 4, "kda": 4 * D}[w.variant]
+    if name == "tc_prep":            # q, k, v, beta, g in; Wy, Qt, KC, Ut^T, Ot^T, T, gC out
+        return th * (3 * D * 2 + 4 + g) + recs * (5 * tile + 8192 + D * 4)
+    if name == "tc_scan_fwd":        # Wy, Qt, KC, Ut^T, Ot^T, gC in; o, U, S out
+        return recs * (5 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
+    if name == "tc_scan_bwd":        # KC, Qt, Wy, gC, dO in; dU, dS out
+        return recs * (3 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
+    if name == "tc_bwd_state":       # dO, S, dS, U, dU in; dQt, dWyA, dKC, dgC out
+        return th * D * 2 + recs * (2 * dd + 2 * tile) + recs * (3 * tile + D * 4)
+    if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, dQt, T, gC, dgC, dWyA, dU, dKC in;
+        return (th * (4 * D * 2 + 4 + g) + recs * (4 * tile + 8192 + 2 * D * 4)
+                + th * (3 * D * 2 + 4 + g))   # dq, dk, dv, dbeta, dg out
+    return 0
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    """Time the fp64 oracle (forward + backward, as it stands) on whole
+    (sequence, head) units of the workload on the host cores, and scale the
+    result to tokens/s of the layer (a token carries H heads)."""
+    import numpy as np
+    import oracle
+    threads = oracle.max_threads()
+    N = x["N"]
+    total_units = N * w.H
+    a = dict(q=x["q"], k=x["k"], v=x["v"], beta=x["beta"], g=x["g"], h0=x["h0"],
+             cu_seqlens=x["cu_seqlens"])
+
+    def run(units):
+        oracle.forward(w.variant, units=units, **a)
+        oracle.backward(w.variant, dO=x["dO"], dhT=x["dhT"], units=units, **a)
+
+    n1 = min(total_units, threads)
+    t0 = time.perf_counter()
+    run(np.arange(n1, dtype=np.int32))
+    dt1 = max(time.perf_counter() - t0, 1e-3)
+    batches = max(0, min(int(budget_s / dt1) - 1, total_units // max(n1, 1) - 1))
+    n2 = batches * n1
+    dt2 = 0.0
+    if n2 > 0:
+        t0 = time.perf_counter()
+        run(np.arange(n1, n1 + n2, dtype=np.int32))
+        dt2 = time.perf_counter() - t0
+    units = n1 + n2
+    secs = dt1 + dt2
+    tok_per_unit = w.T if x["cu_seqlens"] is None else w.T / max(N, 1)
+    tokens_per_s = units * tok_per_unit / secs / w.H
+    return {"value": tokens_per_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{units} of {total_units} (sequence, head) units of {w.name}, "
+                      f"fp64 forward+backward, {secs:.1f} s on {threads} threads"}
+
+
+def dist_setup():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from delta_rule_recurrent_gated_gb300 import inputs
+    x = inputs.make(w, seed=0)
+    vals = []
+    base = None
+    per_step = max(2.0, 90.0 / max(args.steps + args.warmup, 1))
+    for i in range(args.warmup + args.steps):
+        base = cpu_baseline(w, x, budget_s=per_step)
+        if i >= args.warmup:
+            vals.append(base["value"])
+    value = sum(vals) / len(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * w.tokens / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "variant": w.variant, "global_batch": w.B,
+                       "seq_len": w.T, "heads": w.H, "d_k": w.dk, "d_v": w.dv,
+                       "parallelism": "host cores (OpenMP over sequence x head)"},
+            "cpu_baseline": dict(base, value=value),
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from delta_rule_recurrent_gated_gb300 import inputs
+    w = inputs.get(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    from delta_rule_recurrent_gated_gb300 import binding
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    x = inputs.make(w, seed=rank)
+    N = x["N"]
+    prob = binding.Problem(w.variant, w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io,
+                           out="bf16", grad="bf16", scale=w.scale,
+                           cu_seqlens=x["cu_seqlens"], device=dev)
+    t = {n: (v.to(dev) if torch.is_tensor(v) and n != "cu_seqlens" else v) for n, v in x.items()}
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(N, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+    grads = {
+        "dq": torch.empty(w.B, w.T, w.H, w.dk, dtype=torch.bfloat16, device=dev),
+        "dk": torch.empty(w.B, w.T, w.H, w.dk, dtype=torch.bfloat16, device=dev),
+        "dv": torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev),
+        "dbeta": torch.empty(w.B, w.T, w.H, dtype=torch.float32, device=dev),
+        "dg": None if t["g"] is None else torch.empty_like(t["g"]),
+        "dh0": torch.empty(N, w.H, w.dk, w.dv, dtype=torch.float32, device=dev),
+    }
+
+    def step(src):
+        prob.forward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], o=o, hT=hT)
+        prob.backward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], src["dO"],
+                      src["dhT"], reuse_fwd=True, out=grads)
+
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if not dist:
+            return v
+        tt = torch.tensor([v], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize(dev)
+    assert prob.status() == binding.DR_OK
+
+    # timed region: K steps, per-kernel events recorded on the launching stream
+    binding.trace_enable(8 * args.steps + 8)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    st = prob.status()
+    assert st == binding.DR_OK, binding.error_string(st)
+    launches = binding.trace_read()
+    binding.trace_enable(0)
+    per = {}
+    for nm, kms in launches:
+        tot, n = per.get(nm, (0.0, 0))
+        per[nm] = (tot + kms, n + 1)
+
+    tokens = w.tokens * world
+    value = tokens / (ms / 1e3)
+    hbm, tflops, peak_src = measured_peaks()
+    flops, byts = algorithmic(w, N)
+    t_roof = max(flops / (tflops * 1e12), byts / (hbm * 1e9))
+    roof = None
+    if per:
+        name, (tot, n) = max(per.items(), key=lambda kv: kv[1][0])
+        avg_s = tot / n / 1e3
+        kb = kernel_bytes(name, w, N)
+        ach = kb / avg_s / 1e9
+        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
+                "traffic": None, "avg_launch_ms": tot / n, "bytes_per_launch": kb}
+    kern = {k: {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(v[0] for v in per.values())}
+            for k, (tot, n) in per.items()}
+
+    # end to end through the public API from pinned host buffers, copies inside
+    e2e = None
+    if not args.no_e2e:
+        names = [n for n, v in x.items() if torch.is_tensor(v) and n != "cu_seqlens"]
+        host_in = {n: x[n].pin_memory() for n in names}
+        dev_in = dict(t)
+        for n in names:
+            dev_in[n] = torch.empty_like(t[n])
+        outs_dev = [o, hT] + [grads[n] for n in ("dq", "dk", "dv", "dbeta", "dg", "dh0")
+                              if grads[n] is not None]
+        outs_host = [torch.empty(v.shape, dtype=v.dtype).pin_memory() for v in outs_dev]
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in outs_host)
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step(dev_in)
+            for hv, dv_ in zip(outs_host, outs_dev):
+                hv.copy_(dv_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        e2e = {"value": tokens / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    base = None if args.no_cpu_baseline else cpu_baseline(w, x)
+    in_bytes = sum(v.numel() * v.element_size() for n, v in t.items()
+                   if torch.is_tensor(v) and n != "cu_seqlens")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "variant": w.variant, "global_batch": w.B * world,
+                   "seq_len": w.T, "heads": w.H, "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB per step > 129 MB)"},
+        "roofline": roof,
+        "path_roofline": {"flops_per_step": flops, "bytes_per_step": byts,
+                          "t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3),
+                          "peaks": {"hbm_gbs": hbm, "bf16_tflops": tflops, "source": peak_src}},
+        "kernels": kern,
+        "cpu_baseline": base,
+        "e2e": e2e,
+        "gpu_launches": len(launches),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -65,6 +65,14 @@ def load(path: str = LIB_PATH):
     lib.dr_check_status.restype = I
     lib.dr_error_string.argtypes = [I]
     lib.dr_error_string.restype = ctypes.c_char_p
+    lib.dr_trace_enable.argtypes = [I]
+    lib.dr_trace_enable.restype = I
+    lib.dr_trace_count.argtypes = []
+    lib.dr_trace_count.restype = I
+    lib.dr_trace_reset.argtypes = []
+    lib.dr_trace_reset.restype = None
+    lib.dr_trace_get.argtypes = [I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]
+    lib.dr_trace_get.restype = I
     _lib = lib
     return lib
 
@@ -111,6 +119,22 @@ def dr_bwd(desc, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, 
 
 def check_status(ws, stream) -> int:
     return load().dr_check_status(ws, stream)
+
+
+def trace_enable(max_launches: int) -> None:
+    _check(load().dr_trace_enable(int(max_launches)), "dr_trace_enable")
+
+
+def trace_read():
+    """[(kernel name, milliseconds)] of the traced launches, in launch order."""
+    lib = load()
+    out = []
+    for i in range(lib.dr_trace_count()):
+        name = ctypes.c_char_p()
+        ms = ctypes.c_float()
+        _check(lib.dr_trace_get(i, ctypes.byref(name), ctypes.byref(ms)), "dr_trace_get")
+        out.append((name.value.decode(), float(ms.value)))
+    return out
 
 
 # ------------------------------------------------------------------ torch-level helpers

@@ -1,5 +1,6 @@
 // misc.cu -- small helper kernels.
 #include "common.cuh"
+#include "trace.cuh"
 
 namespace dr {
 namespace {
@@ -15,6 +16,7 @@ __global__ void copy_or_zero(const float* __restrict__ src, float* __restrict__ 
 cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st) {
     if (n == 0 || !dst) return cudaSuccess;
     const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    TraceScope ts("copy_or_zero", st);
     copy_or_zero<<<blocks, 256, 0, st>>>(src, dst, n);
     return cudaGetLastError();
 }

@@ -17,6 +17,7 @@
 // Small matrices live in a per-CTA scratch slice of the workspace (L1/L2
 // resident); every helper is block-wide and ends with __syncthreads().
 #include "common.cuh"
+#include "trace.cuh"
 
 namespace dr {
 namespace {
@@ -333,6 +334,7 @@ cudaError_t simt_fwd(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    TraceScope ts("simt_fwd", st);
     simt_fwd_kernel<<<units, kThreads, 0, st>>>(p, scratch);
     return cudaGetLastError();
 }
@@ -342,6 +344,7 @@ cudaError_t simt_bwd(const Params& p, cudaStream_t st) {
     if (units == 0) return cudaSuccess;
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
     float* states = scratch + (size_t)units * kNumBufs * kBuf;
+    TraceScope ts("simt_bwd", st);
     simt_bwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, states);
     return cudaGetLastError();
 }

@@ -23,6 +23,7 @@
 #include "common.cuh"
 #include "tc.cuh"
 #include "tc_layout.cuh"
+#include "trace.cuh"
 
 namespace dr {
 using namespace tc;
@@ -361,7 +362,7 @@ struct BChunkSmem {
                          kdAq = kB8b + kCC;
     static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][D]
     static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * D * 4 : 0);
-    // small arrays: beta[64], gamma_last[D], dgC[D], E[D], rowsum[64], Gamma_row[64]
+    // small arrays: beta[64], gamma_last[D], dgC[D], (spare D), rowsum[64], Gamma_row[64]
     static constexpr int kBytes = kSmall + (64 * 3 + D * 3) * 4 + 1024;
 };
 
@@ -391,8 +392,7 @@ __global__ void __launch_bounds__(128, 1)
     float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
     float* gC_s = beta_s + 64;
     float* dgC_s = gC_s + D;
-    float* E_s = dgC_s + D;
-    float* rowsum = E_s + D;
+    float* rowsum = dgC_s + 2 * D;
     float* Grow = rowsum + 64;    // GDN: Gamma per row
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base;
@@ -447,7 +447,6 @@ __global__ void __launch_bounds__(128, 1)
             bulk_g2s(dgC_s, L.dgC + rec * D, D * 4, &bar_ld);
         }
         if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
-        for (int c = tid; c < D; c += 128) E_s[c] = 0.f;
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         zero_pad_rows(Qs, D, len);
@@ -672,7 +671,10 @@ __global__ void __launch_bounds__(128, 1)
         // E7: the decay chain, per row
         {
             const uint8_t* dkc_img = L.dKC + rec * kTile;
-            float grow = 0.f;
+            // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows;
+            // the v and dO tiles (contiguous, 64 x D fp32 together) are free by now
+            float* Fa = reinterpret_cast<float*>(Vs);
+            float grow = 0.f, frow = 0.f;
             float Gr = 0.f;
             if (VAR == DR_GDN && r >= 0) Gr = Grow[r];
             const float br = r >= 0 ? beta_s[r] : 0.f;
@@ -706,10 +708,10 @@ __global__ void __launch_bounds__(128, 1)
                         const float dG = dQb * qb[j] + dKb * kb[j] - dkr[j] * kr[j] - dkc[j] * KC;
                         if (VAR == DR_KDA) {
                             Gam[r * D + c] = dG;
-                            atomicAdd(&E_s[c], dkc[j] * KC);
+                            Fa[r * D + c] = dkc[j] * KC;
                         } else if (VAR == DR_GDN) {
                             grow += dG;
-                            atomicAdd(&E_s[c], dkc[j] * KC);
+                            frow = fmaf(dkc[j], KC, frow);
                         }
                         if (r < len) {
                             const size_t eidx = ((size_t)(row0 + r) * p.H + h) * D + c;
@@ -720,7 +722,10 @@ __global__ void __launch_bounds__(128, 1)
                 }
             }
             if (r >= 0) {
-                if (VAR == DR_GDN) rowsum[r] = grow;
+                if (VAR == DR_GDN) {
+                    rowsum[r] = grow;
+                    Grow[r] = frow;  // this row's Gamma was read above; reuse the slot
+                }
                 if (r < len) p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc;
             }
         }
@@ -729,7 +734,9 @@ __global__ void __launch_bounds__(128, 1)
         // E8: dg = reverse cumulative sum of dGamma within the chunk
         if (VAR == DR_KDA) {
             for (int c = tid; c < D; c += 128) {
-                float run = E_s[c] + dgC_s[c] * gC_s[c];
+                float run = dgC_s[c] * gC_s[c];
+                const float* Fa = reinterpret_cast<const float*>(Vs);
+                for (int i = 0; i < 64; ++i) run += Fa[i * D + c];
                 for (int i = len - 1; i >= 0; --i) {
                     run += Gam[i * D + c];
                     p.dg[((size_t)(row0 + i) * p.H + h) * D + c] = run;
@@ -738,10 +745,11 @@ __global__ void __launch_bounds__(128, 1)
         } else if (VAR == DR_GDN) {
             if (warp == 0) {
                 float e = 0.f;
-                for (int c = threadIdx.x; c < D; c += 32) e += E_s[c] + dgC_s[c] * gC_s[c];
+                for (int c = threadIdx.x; c < D; c += 32) e += dgC_s[c] * gC_s[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
                 if (threadIdx.x == 0) {
+                    for (int i = 0; i < 64; ++i) e += Grow[i];
                     float run = e;
                     for (int i = len - 1; i >= 0; --i) {
                         run += rowsum[i];
@@ -781,7 +789,10 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        tc_scan_bwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L);
+        {
+            TraceScope ts("tc_scan_bwd", st);
+            tc_scan_bwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -794,7 +805,10 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        tc_bwd_state_kernel<D><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mdo, p, L);
+        {
+            TraceScope ts("tc_bwd_state", st);
+            tc_bwd_state_kernel<D><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mdo, p, L);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -804,7 +818,10 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
             if (e != cudaSuccess) return e;
             attr = true;
         }
-        kernel<<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mdo, p, L);
+        {
+            TraceScope ts("tc_bwd_chunk", st);
+            kernel<<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mdo, p, L);
+        }
         return cudaGetLastError();
     };
     static bool a0 = false, a1 = false, a2 = false;

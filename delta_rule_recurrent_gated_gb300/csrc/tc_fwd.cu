@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "tc.cuh"
 #include "tc_layout.cuh"
+#include "trace.cuh"
 
 namespace dr {
 using namespace tc;
@@ -552,6 +553,7 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
         attr = true;
     }
     if (p.num_chunks == 0) return cudaSuccess;
+    TraceScope ts("tc_prep", st);
     tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, p, L);
     return cudaGetLastError();
 }
@@ -566,6 +568,7 @@ cudaError_t launch_scan_fwd(const Params& p, const TcLayout& L, cudaStream_t st,
         attr = true;
     }
     if (p.N * p.H == 0) return cudaSuccess;
+    TraceScope ts("tc_scan_fwd", st);
     tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L, write_o ? 1 : 0);
     return cudaGetLastError();
 }

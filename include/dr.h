@@ -135,6 +135,20 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
    DR_ERR_CUDA when the stream itself failed. */
 int dr_check_status(const void* workspace, void* stream);
 
+/*
+ * Kernel-level timing.  dr_trace_enable(n) (n > 0) creates n pairs of CUDA
+ * events; while enabled, each of the next n kernel launches made by dr_fwd /
+ * dr_bwd is bracketed by an event pair recorded on the call's stream.
+ * dr_trace_enable(0) disables tracing and destroys the events;
+ * dr_trace_reset() reuses them from the first slot.  dr_trace_get(i, ...)
+ * waits for launch i to finish and returns its kernel name and device
+ * duration in milliseconds.  Host-global state: not for concurrent callers.
+ */
+int dr_trace_enable(int max_launches);
+int dr_trace_count(void);
+void dr_trace_reset(void);
+int dr_trace_get(int index, const char** kernel_name, float* milliseconds);
+
 /* Human-readable name of a dr_status_code. */
 const char* dr_error_string(int code);
 

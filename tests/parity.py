@@ -43,7 +43,8 @@ def run_gpu(w: inputs.Workload, x: dict, reuse=True, out="f32", grad="f32", dev=
     torch.cuda.synchronize()
     st = prob.status()
     assert st == binding.DR_OK, binding.error_string(st)
-    return {n: (None if val is None else val.double().cpu().numpy()) for n, val in res.items()}
+    # fp32 on the host is exact for the fp32 / bf16 values the library writes
+    return {n: (None if val is None else val.float().cpu().numpy()) for n, val in res.items()}
 
 
 def run_oracle(w: inputs.Workload, x: dict, units=None, backward=True):
@@ -91,7 +92,7 @@ def compare(w, x, got: dict, ref: dict, units=None, fields=FIELDS):
             m = unit_mask(w, x, units, n, r.shape)
             r, g = r[m], g[m]
         assert np.all(np.isfinite(g)), f"{n}: non-finite values"
-        err = float(np.max(np.abs(g - r))) if r.size else 0.0
+        err = float(np.max(np.abs(g.astype(np.float64) - r))) if r.size else 0.0
         tol = tolerance(w, r)
         report[n] = (err, tol)
     bad = {n: v for n, v in report.items() if not v[0] <= v[1]}
