@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdr.so")
 
 DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_WORKSPACE, DR_ERR_ALIGNMENT, \
-    DR_ERR_CUDA, DR_ERR_TIMEOUT = range(7)
+    DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_SCRATCH_LIMIT = range(8)
 DR_DELTANET, DR_GDN, DR_KDA = 0, 1, 2
 DR_BF16, DR_F32 = 0, 1
 DR_FLAG_REUSE_FWD = 1
@@ -65,6 +65,8 @@ def load(path: str = LIB_PATH):
     lib.dr_check_status.restype = I
     lib.dr_error_string.argtypes = [I]
     lib.dr_error_string.restype = ctypes.c_char_p
+    lib.dr_fwd_noalloc.argtypes = [D] + [P] * 8 + [P]
+    lib.dr_fwd_noalloc.restype = I
     lib.dr_trace_enable.argtypes = [I]
     lib.dr_trace_enable.restype = I
     lib.dr_trace_count.argtypes = []

@@ -16,6 +16,8 @@ size_t tc_workspace_bytes(const Params& p);
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
 cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse);
 cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st);
+int simt_noalloc_max_units();
+cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st);
 }  // namespace dr
 
 using dr::Params;
@@ -101,6 +103,9 @@ const char* dr_error_string(int code) {
         case DR_ERR_ALIGNMENT: return "DR_ERR_ALIGNMENT: pointer not 16-byte aligned";
         case DR_ERR_CUDA: return "DR_ERR_CUDA: CUDA launch or runtime failure";
         case DR_ERR_TIMEOUT: return "DR_ERR_TIMEOUT: a bounded device wait ran out";
+        case DR_ERR_SCRATCH_LIMIT:
+            return "DR_ERR_SCRATCH_LIMIT: problem larger than the library's static scratch "
+                   "(dr_fwd_noalloc)";
         default: return "unknown dr status code";
     }
 }
@@ -195,6 +200,30 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
     }
     if (path == Path::kSimt) return cuda_status(dr::simt_bwd(p, st));
     return cuda_status(dr::tc_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
+}
+
+int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void* v,
+                   const float* beta, const float* g, const float* h0, void* o, float* hT,
+                   void* stream) {
+    Path path;
+    int rc = check_desc(desc, &path);
+    if (rc != DR_OK) return rc;
+    if (path != Path::kSimt) return DR_ERR_UNSUPPORTED;
+    Params p = make_params(desc);
+    const long long tokens = (long long)p.B * p.T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
+    if (tokens > 0 && ((p.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, beta, g, h0, o, hT};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    if ((long long)p.N * p.H > dr::simt_noalloc_max_units()) return DR_ERR_SCRATCH_LIMIT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.hT = hT;
+    if (tokens == 0) {
+        if (hT) return cuda_status(dr::state_passthrough(h0, hT, (size_t)p.N * p.H * p.dk * p.dv, st));
+        return DR_OK;
+    }
+    return cuda_status(dr::simt_fwd_noalloc(p, st));
 }
 
 int dr_check_status(const void* ws, void* stream) {

@@ -16,6 +16,8 @@
 // and the backward pass is the chain rule through exactly these steps.
 // Small matrices live in a per-CTA scratch slice of the workspace (L1/L2
 // resident); every helper is block-wide and ends with __syncthreads().
+#include <mutex>
+
 #include "common.cuh"
 #include "trace.cuh"
 
@@ -346,6 +348,88 @@ cudaError_t simt_bwd(const Params& p, cudaStream_t st) {
     float* states = scratch + (size_t)units * kNumBufs * kBuf;
     TraceScope ts("simt_bwd", st);
     simt_bwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, states);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Forward without a caller-supplied workspace (dr_fwd_noalloc in dr.h).
+//
+// Some callers cannot allocate device memory at the point where they run this
+// layer: code that is handed only its input and output buffers by a host
+// framework, or that runs where a cudaMalloc would synchronise the device or
+// is not allowed.  For them the scratch of the fp32 forward kernel lives in
+// one file-scope device array owned by the library instead of the workspace.
+// The array is a fixed kNoAllocScratchBytes on every GPU that loads the
+// library and stays allocated until the process exits.  All calls share it:
+// two calls whose kernels overlap on the GPU (different streams or devices
+// sharing a context) race on it.  The kernel writes every scratch word before
+// it reads it, so stale contents from an earlier call never leak into a result
+// and nothing needs clearing.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;       // 16 MiB per GPU
+constexpr int kNoAllocBufs = bTmp + 1;                          // forward-only buffers
+constexpr size_t kNoAllocUnitFloats = (size_t)kNoAllocBufs * kBuf;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+namespace {
+// The forward kernel of this file with a forward-only per-unit scratch stride.
+__global__ void __launch_bounds__(kThreads) simt_fwd_noalloc_kernel(Params p, float* scratch) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
+    const Scratch s{scratch + (size_t)u * kNoAllocUnitFloats};
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+    float* S = s(bS);
+    load_state(S, p.h0, n, h, p.H, p.dk, p.dv);
+    for (int c = 0; c < nc; ++c) {
+        const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
+        chunk_prep(p, s, h, row0, L);
+        chunk_scan(p, s, L, S);
+        const float* O = s(bO);
+        for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
+            const int i = idx / p.dv, j = idx % p.dv;
+            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * p.dv + j, p.out_dtype, O[idx]);
+        }
+        __syncthreads();
+    }
+    if (p.hT)
+        for (int idx = threadIdx.x; idx < p.dk * p.dv; idx += blockDim.x)
+            p.hT[((size_t)n * p.H + h) * p.dk * p.dv + idx] = S[idx];
+}
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  The host-side name of the array is only a stand-in for the
+// symbol; the kernel must receive this address.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+cudaError_t noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+// Largest number of (sequence, head) units the static scratch holds.
+int simt_noalloc_max_units() { return (int)(kNoAllocScratchBytes / (kNoAllocUnitFloats * sizeof(float))); }
+
+cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    float* scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    TraceScope ts("simt_fwd_noalloc", st);
+    simt_fwd_noalloc_kernel<<<units, kThreads, 0, st>>>(p, scratch);
     return cudaGetLastError();
 }
 

@@ -55,7 +55,8 @@ enum dr_status_code {
     DR_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than dr_workspace_bytes   */
     DR_ERR_ALIGNMENT = 4,     /* a pointer is not 16-byte aligned                    */
     DR_ERR_CUDA = 5,          /* a CUDA call or launch failed                        */
-    DR_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out                  */
+    DR_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out                  */
+    DR_ERR_SCRATCH_LIMIT = 7  /* dr_fwd_noalloc: problem larger than its static scratch */
 };
 
 enum dr_variant { DR_DELTANET = 0, DR_GDN = 1, DR_KDA = 2 };
@@ -129,6 +130,34 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
            const float* beta, const float* g, const float* h0, const void* dO,
            const float* dhT, void* dq, void* dk, void* dv, float* dbeta, float* dg,
            float* dh0, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Forward for callers that cannot allocate device memory.  The paper has no
+ * counterpart; this is an interface convenience of the library.
+ *
+ * Some callers cannot call cudaMalloc where they run this layer (a plugin
+ * handed only its input and output buffers by its host framework, or code
+ * that must not trigger an allocation and the device synchronisation it may
+ * bring).  dr_fwd_noalloc computes the same o and hT as dr_fwd, with the
+ * fp32 CUDA-core kernel (io fp32 only; the supported set of dr_fwd for fp32
+ * inputs), but takes no workspace: its scratch is a 16 MiB array that the
+ * library keeps in the global memory of every GPU that loads it, for the life
+ * of the process.  It allocates nothing itself.
+ *   - Size limit: N * H (sequences times heads) must not exceed 46; larger
+ *     problems return DR_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current (a runtime symbol query); make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one array: calls whose kernels can overlap on the
+ *     GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller.  Contents left by an earlier call are never
+ *     read before being overwritten.
+ *   - It writes no workspace, so dr_bwd cannot reuse its residuals.
+ * Errors as dr_fwd, plus DR_ERR_UNSUPPORTED for bf16 inputs.
+ */
+int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void* v,
+                   const float* beta, const float* g, const float* h0, void* o, float* hT,
+                   void* stream);
 
 /* Synchronise `stream` and report any device-side error recorded in the
    workspace by the last call that used it (DR_OK or DR_ERR_TIMEOUT), or
