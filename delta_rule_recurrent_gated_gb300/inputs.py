@@ -56,6 +56,9 @@ WORKLOADS = {
     "gdn_varlen_t32768_h16_d128": Workload("gdn_varlen_t32768_h16_d128", "gdn", 1, 32768,
                                            16, 128, 128, h0=True, varlen_total=32768),
 }
+# a two-sequence case of the same layer, for kernel profiling (inputs still exceed L2)
+WORKLOADS["gdn_b2_t4096_h16_d128"] = Workload("gdn_b2_t4096_h16_d128", "gdn", 2, 4096, 16, 128, 128,
+                                              h0=True)
 for _v in ("deltanet", "gdn", "kda"):
     for _T, _B in ((4096, 16), (8192, 8), (16384, 4), (32768, 2)):
         _n = f"sweep_{_v}_b{_B}_t{_T}_h16_d128"
