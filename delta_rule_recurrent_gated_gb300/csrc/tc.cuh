@@ -298,3 +298,26 @@ __device__ __forceinline__ int m64_row() {
 }
 
 }  // namespace tc
+
+namespace tc {
+// ---------------------------------------------------------------- bulk copy shared -> global
+// Untiled copy of `bytes` (multiple of 16, 16-aligned) from shared to global
+// memory through the bulk-copy engine, tracked as a bulk async-group of the
+// issuing thread.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until the sources of all committed bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until all committed bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+}  // namespace tc

@@ -58,29 +58,26 @@ template <int D, int BV>
 struct BScanSmem {
     static constexpr int kTile = 64 * D * 2;
     static constexpr int kW = 0;                 // [BV][D]  dS^T slice (bf16 operand)
-    static constexpr int kKC = BV * D * 2;       // [64][D]
-    static constexpr int kQt = kKC + kTile;
-    static constexpr int kWy = kQt + kTile;
-    static constexpr int kdO = kWy + kTile;      // [BV][64] dO^T
-    static constexpr int kdU = kdO + BV * 128;   // [BV][64] -dU^T
-    static constexpr int kG = kdU + BV * 128;    // [D] fp32
-    static constexpr int kBytes = kG + D * 4 + 1024;
+    static constexpr int kdU = BV * D * 2;       // [BV][64] -dU^T operand
+    static constexpr int kStage0 = kdU + BV * 128;
+    // stage layout: KC, Qt, Wy [64][D] tiles; dO [64 tokens][BV] tile; gC [D] fp32
+    static constexpr int kKC = 0, kQt = kTile, kWy = 2 * kTile, kdO = 3 * kTile,
+                         kG = kdO + BV * 128;
+    static constexpr int kStageBytes = (kG + D * 4 + 1023) / 1024 * 1024;
+    static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
+    static constexpr uint32_t kStageTx = 3 * kTile + BV * 128 + D * 4;
 };
 
 template <int D, int BV>
-__global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, const TcLayout L) {
+__global__ void __launch_bounds__(128, 1)
+    tc_scan_bwd_kernel(const __grid_constant__ CUtensorMap mdo, const Params p, const TcLayout L) {
     using S = BScanSmem<D, BV>;
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Ws = sm + S::kW;
-    uint8_t* KCs = sm + S::kKC;
-    uint8_t* Qts = sm + S::kQt;
-    uint8_t* Wys = sm + S::kWy;
-    uint8_t* dOs = sm + S::kdO;
     uint8_t* dUs = sm + S::kdU;
-    const float* gCs = reinterpret_cast<const float*>(sm + S::kG);
-    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint64_t bar_ld[2], bar_mma;
     __shared__ uint32_t tmem_base;
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -90,9 +87,11 @@ __global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, con
     seq_chunks(p, n, c0, nc, srow, slen);
 
     if (tid == 0) {
-        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_ld[0], 1);
+        mbar_init(&bar_ld[1], 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
+        prefetch_tmap(&mdo);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -106,6 +105,24 @@ __global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, con
     const int r = (BV == 128) ? tid : m64_row();
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
+    int issued[2] = {0, 0}, waited[2] = {0, 0};
+
+    // iteration it handles chunk nc-1-it, in stage it & 1
+    auto load_iter = [&](int it) {
+        const int s = it & 1, ci = nc - 1 - it;
+        uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
+        const size_t rec = (size_t)(c0 + ci) * p.H + h;
+        const int row0 = srow + ci * 64;
+        mbar_arrive_expect_tx(&bar_ld[s], S::kStageTx);
+        bulk_g2s(st + S::kKC, L.KC + rec * kTile, kTile, &bar_ld[s]);
+        bulk_g2s(st + S::kQt, L.Qt + rec * kTile, kTile, &bar_ld[s]);
+        bulk_g2s(st + S::kWy, L.Wy + rec * kTile, kTile, &bar_ld[s]);
+        for (int kb = 0; kb < BV / 64; ++kb)
+            tma_load_3d(st + S::kdO + kb * 8192, &mdo, &bar_ld[s], v0 + kb * 64, h, row0);
+        bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
+        ++issued[s];
+    };
+    if (tid == 0 && nc > 0) load_iter(0);
 
     float W[D];  // dS[:, v] (the gradient of the state at the current chunk end)
 #pragma unroll
@@ -123,81 +140,62 @@ __global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, con
     __syncthreads();
 
     bool ok = true;
-    int it = 0;
-    for (int ci = nc - 1; ci >= 0 && ok; --ci, ++it) {
+    for (int it = 0; it < nc && ok; ++it) {
+        const int s = it & 1, ci = nc - 1 - it;
+        const uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
-        const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + D * 4);
-            bulk_g2s(KCs, L.KC + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(Qts, L.Qt + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(Wys, L.Wy + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(sm + S::kG, L.gC + rec * D, D * 4, &bar_ld);
-        }
-        if (r >= 0) {
+            if (it + 1 < nc) load_iter(it + 1);
+            // rows [v0, v0+BV) of the W-layout image of dS at this chunk's end
             uint8_t* ds_img = L.dS + rec * (size_t)D * D * 2;
-#pragma unroll
-            for (int c = 0; c < D; ++c)
-                *reinterpret_cast<__nv_bfloat16*>(ds_img + sw128_offset(c, v, D)) =
-                    __float2bfloat16_rn(W[c]);
-            for (int g = 0; g < 4; ++g) {
-                float t[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int i = g * 16 + j;
-                    t[j] = i < len ? ld_any(p.dO, ((size_t)(row0 + i) * p.H + h) * D + v, p.io_dtype)
-                                   : 0.f;
-                }
-                tile_store16(dOs, r, g * 16, BV, t);
-            }
+            for (int kb = 0; kb < D / 64; ++kb)
+                bulk_s2g(ds_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
+            bulk_commit();
         }
-        fence_async_smem();
-        ok = mbar_wait(&bar_ld, it & 1, kWaitLimitNs);
+        ok = mbar_wait(&bar_ld[s], (it >> 1) & 1, kWaitLimitNs);
+        if (tid == 0) ++waited[s];
         if (__syncthreads_or(!ok)) break;
 
         // dU^T = dS^T KC^T -> cols [0,64)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tW{smem_u32(Ws), BV}, tK{smem_u32(KCs), 64};
+            const Tile tW{smem_u32(Ws), BV}, tK{smem_u32(st + S::kKC), 64};
             mma_tiles(tm + 0, tW, false, tK, false, BV, 64, D, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        {
-            uint8_t* du_img = L.dU + rec * kTile;
-            for (int g = 0; g < 4; ++g) {
-                float acc[16];
-                tmem_ld16(tl + g * 16, acc);
-                tmem_ld_wait();
-                if (r >= 0) {
+        for (int g = 0; g < 4; ++g) {
+            float acc[16];
+            tmem_ld16(tl + g * 16, acc);
+            tmem_ld_wait();
+            if (r >= 0) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        *reinterpret_cast<__nv_bfloat16*>(du_img + sw128_offset(g * 16 + j, v, 64)) =
-                            __float2bfloat16_rn(acc[j]);
-                        acc[j] = -acc[j];
-                    }
-                    tile_store16(dUs, r, g * 16, BV, acc);
-                }
+                for (int j = 0; j < 16; ++j) acc[j] = -acc[j];
+                tile_store16(dUs, r, g * 16, BV, acc);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // dO^T Qt - dU^T Wy -> cols [64, 64+D)
+        // dO^T Qt - dU^T Wy -> cols [64, 64+D); -dU^T rows [v0, v0+BV) of its image
         if (tid == 0) {
             tc_fence_after();
-            const Tile tO{smem_u32(dOs), BV}, tU{smem_u32(dUs), BV}, tQ{smem_u32(Qts), 64},
-                tWy{smem_u32(Wys), 64};
-            mma_tiles(tm + 64, tO, false, tQ, true, BV, D, 64, false);
+            const Tile tO{smem_u32(st + S::kdO), 64}, tU{smem_u32(dUs), BV},
+                tQ{smem_u32(st + S::kQt), 64}, tWy{smem_u32(st + S::kWy), 64};
+            mma_tiles(tm + 64, tO, true, tQ, true, BV, D, 64, false);
             mma_tiles(tm + 64, tU, false, tWy, true, BV, D, 64, true);
             mma_commit(&bar_mma);
+            bulk_s2g(L.dU + rec * kTile + (size_t)v0 * 128, dUs, BV * 128);
+            bulk_commit();
         }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (tid == 0) bulk_wait_read();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG);
 #pragma unroll
         for (int cb = 0; cb < D / 16; ++cb) {
             float acc[16];
@@ -223,9 +221,11 @@ __global__ void __launch_bounds__(128, 1) tc_scan_bwd_kernel(const Params p, con
         }
     } else {
         record_timeout(p);
-        mbar_wait(&bar_ld, 0, kWaitLimitNs);
-        mbar_wait(&bar_ld, 1, kWaitLimitNs);
+        if (tid == 0)
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > waited[s]) mbar_wait(&bar_ld[s], waited[s] & 1, kWaitLimitNs);
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -291,24 +291,21 @@ __global__ void __launch_bounds__(128, 1)
         zero_pad_rows(dOs, D, len);
         fence_async_smem();
         __syncthreads();
-        // dO S^T -> [0,D) ; dU S^T -> [D,2D)
+        // S and dS arrive in W layout ([value][key]); U and dU as U^T / -dU^T ([value][token]).
+        // dO S^T -> [0,D) ; (-dU) S^T -> [D,2D)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tO{smem_u32(dOs), 64}, tS{smem_u32(Ss), D}, tdU{smem_u32(dUs), 64};
-            mma_tiles(tm + 0, tO, false, tS, false, 64, D, D, false);
-            mma_tiles(tm + D, tdU, false, tS, false, 64, D, D, false);
+            const Tile tO{smem_u32(dOs), 64}, tS{smem_u32(Ss), D}, tdU{smem_u32(dUs), D};
+            mma_tiles(tm + 0, tO, false, tS, true, 64, D, D, false);
+            mma_tiles(tm + D, tdU, true, tS, true, 64, D, D, false);
             mma_commit(&bar_mma);
         }
         // dgC[c] = sum_v dS[c, v] S[c, v]  (overlaps the MMAs)
         for (int c = tid; c < D; c += 128) {
             float acc = 0.f;
-            for (int vb = 0; vb < D; vb += 16) {
-                float a[16], b[16];
-                tile_load16(Ss, c, vb, D, a);
-                tile_load16(dSs, c, vb, D, b);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc = fmaf(a[j], b[j], acc);
-            }
+            for (int vv = 0; vv < D; ++vv)
+                acc = fmaf(__bfloat162float(*tile_elem(Ss, vv, c, D)),
+                           __bfloat162float(*tile_elem(dSs, vv, c, D)), acc);
             L.dgC[rec * D + c] = acc;
         }
         ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
@@ -320,6 +317,8 @@ __global__ void __launch_bounds__(128, 1)
             tmem_ld16(tl + D + cb * 16, b);
             tmem_ld_wait();
             if (r >= 0) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) b[j] = -b[j];
                 tile_store16(L.dQt + rec * kTile, r, cb * 16, 64, a);
                 tile_store16(L.dWyA + rec * kTile, r, cb * 16, 64, b);
             }
@@ -329,8 +328,8 @@ __global__ void __launch_bounds__(128, 1)
         // U dS^T -> [0,D)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tU{smem_u32(Us), 64}, tdS{smem_u32(dSs), D};
-            mma_tiles(tm + 0, tU, false, tdS, false, 64, D, D, false);
+            const Tile tU{smem_u32(Us), D}, tdS{smem_u32(dSs), D};
+            mma_tiles(tm + 0, tU, true, tdS, true, 64, D, D, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
@@ -394,7 +393,7 @@ __global__ void __launch_bounds__(128, 1)
     float* dgC_s = gC_s + D;
     float* rowsum = dgC_s + 2 * D;
     float* Grow = rowsum + 64;    // GDN: Gamma per row
-    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint64_t bar_ld, bar_mma, bar_kc;
     __shared__ uint32_t tmem_base;
 
     constexpr uint32_t R_dbK = 128, R_dbV = 128 + D, R_dQ = 128 + 2 * D, R_dKr = 128 + D;
@@ -408,6 +407,7 @@ __global__ void __launch_bounds__(128, 1)
     if (tid == 0) {
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_kc, 1);
         fence_barrier_init();
         prefetch_tmap(&mq);
         prefetch_tmap(&mk);
@@ -434,7 +434,9 @@ __global__ void __launch_bounds__(128, 1)
 
     do {
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 5 * kTile + 8192 + 2 * D * 4);
+            mbar_arrive_expect_tx(&bar_ld, 7 * kTile + 8192 + 2 * D * 4);
+            bulk_g2s(dWys, L.dWyA + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_ld);
             for (int kb = 0; kb < D / 64; ++kb) {
                 tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
                 tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
@@ -457,14 +459,21 @@ __global__ void __launch_bounds__(128, 1)
 
         // E1: decay factors per key channel
         for (int c = tid; c < D; c += 128) {
+            // all of this channel's gate values in flight at once
+            float gl[64];
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                gl[i] = 0.f;
+                if (VAR != DR_DELTANET && i < len)
+                    gl[i] = (VAR == DR_GDN) ? p.g[(size_t)(row0 + i) * p.H + h]
+                                            : p.g[((size_t)(row0 + i) * p.H + h) * D + c];
+            }
             float G = 0.f;
+#pragma unroll
             for (int i = 0; i < 64; ++i) {
                 float e = 1.f, ei = 1.f;
                 if (VAR != DR_DELTANET) {
-                    if (i < len) {
-                        G += (VAR == DR_GDN) ? p.g[(size_t)(row0 + i) * p.H + h]
-                                             : p.g[((size_t)(row0 + i) * p.H + h) * D + c];
-                    }
+                    G += gl[i];
                     e = expf(G);
                     ei = expf(-G);
                     if (VAR == DR_KDA) Gam[i * D + c] = G;
@@ -526,6 +535,10 @@ __global__ void __launch_bounds__(128, 1)
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        if (tid == 0) {  // dO is consumed: bring dKC into its buffer for the last phase
+            mbar_arrive_expect_tx(&bar_kc, kTile);
+            bulk_g2s(dOs, L.dKC + rec * kTile, kTile, &bar_kc);
+        }
         for (int cb = 0; cb < 4; ++cb) {
             float a[16];
             tmem_ld16(tl + cb * 16, a);
@@ -542,16 +555,17 @@ __global__ void __launch_bounds__(128, 1)
             tmem_ld16(tl + 64 + D + cb * 16, b);
             tmem_ld_wait();
             if (r >= 0) {
-                float wa[16], du[16];
-                tile_load16(L.dWyA + rec * kTile, r, cb * 16, 64, wa);
-                tile_load16(L.dU + rec * kTile, r, cb * 16, 64, du);
+                float wa[16];
+                tile_load16(dWys, r, cb * 16, 64, wa);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[j] = -wa[j] - sc * a[j];  // dWy
+                tile_store16(dWys, r, cb * 16, 64, a);
+                // dUts holds -dU^T ([value][token]); this thread owns column r
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    a[j] = -wa[j] - sc * a[j];  // dWy
-                    b[j] = du[j] + sc * b[j];   // dUt
+                    __nv_bfloat16* e = tile_elem(dUts, cb * 16 + j, r, D);
+                    *e = __float2bfloat16_rn(sc * b[j] - __bfloat162float(*e));  // dUt^T
                 }
-                tile_store16(dWys, r, cb * 16, 64, a);
-                tile_store16(dUts, r, cb * 16, 64, b);
             }
         }
         fence_async_smem();
@@ -562,11 +576,11 @@ __global__ void __launch_bounds__(128, 1)
         //     dAqk Kr -> R_dQ
         if (tid == 0) {
             tc_fence_after();
-            const Tile tT{smem_u32(Ts), 64}, tdW{smem_u32(dWys), 64}, tdU{smem_u32(dUts), 64};
+            const Tile tT{smem_u32(Ts), 64}, tdW{smem_u32(dWys), 64}, tdU{smem_u32(dUts), D};
             mma_tiles(tm + 0, tdW, false, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
-            mma_tiles(tm + 64, tdU, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + 64, tdU, true, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
             mma_tiles(tm + R_dbK, tT, true, tdW, true, 64, D, 64, false);
-            mma_tiles(tm + R_dbV, tT, true, tdU, true, 64, D, 64, false);
+            mma_tiles(tm + R_dbV, tT, true, tdU, false, 64, D, 64, false);
             mma_tiles(tm + R_dQ, Tile{smem_u32(dAqs), 64}, false, Tile{smem_u32(Ks), 64}, true, 64, D, 64, false);
             mma_commit(&bar_mma);
         }
@@ -669,11 +683,13 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
 
         // E7: the decay chain, per row
+        ok = mbar_wait(&bar_kc, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
         {
-            const uint8_t* dkc_img = L.dKC + rec * kTile;
-            // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows;
-            // the v and dO tiles (contiguous, 64 x D fp32 together) are free by now
-            float* Fa = reinterpret_cast<float*>(Vs);
+            const uint8_t* dkc_img = dOs;
+            // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows, in
+            // the T / Aqk / P / dG / dAqk tiles (40 KB contiguous), all consumed by now
+            float* Fa = reinterpret_cast<float*>(Ts);
             float grow = 0.f, frow = 0.f;
             float Gr = 0.f;
             if (VAR == DR_GDN && r >= 0) Gr = Grow[r];
@@ -735,7 +751,7 @@ __global__ void __launch_bounds__(128, 1)
         if (VAR == DR_KDA) {
             for (int c = tid; c < D; c += 128) {
                 float run = dgC_s[c] * gC_s[c];
-                const float* Fa = reinterpret_cast<const float*>(Vs);
+                const float* Fa = reinterpret_cast<const float*>(Ts);
                 for (int i = 0; i < 64; ++i) run += Fa[i * D + c];
                 for (int i = len - 1; i >= 0; --i) {
                     run += Gam[i * D + c];
@@ -762,6 +778,7 @@ __global__ void __launch_bounds__(128, 1)
     if (!ok) {
         record_timeout(p);
         mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        mbar_wait(&bar_kc, 0, kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -781,19 +798,23 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         !make_token_map(&mv, p.v, D, p.H, rows) || !make_token_map(&mdo, p.dO, D, p.H, rows))
         return cudaErrorInvalidValue;
     {
-        constexpr int BV = 64;
-        constexpr int smem = BScanSmem<D, BV>::kBytes;
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = set_smem(tc_scan_bwd_kernel<D, BV>, smem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        {
+        auto launch_scan = [&](auto kernel, int bv, int smem, bool& attr) -> cudaError_t {
+            if (!attr) {
+                cudaError_t e = set_smem(kernel, smem);
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
             TraceScope ts("tc_scan_bwd", st);
-            tc_scan_bwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L);
-        }
-        cudaError_t e = cudaGetLastError();
+            kernel<<<dim3(p.N * p.H, D / bv), 128, smem, st>>>(mdo, p, L);
+            return cudaGetLastError();
+        };
+        static bool s64 = false, s128 = false;
+        cudaError_t e;
+        if (D == 128 && p.N * p.H >= 120)
+            e = launch_scan(tc_scan_bwd_kernel<D, (D == 128 ? 128 : 64)>, D == 128 ? 128 : 64,
+                            BScanSmem<D, (D == 128 ? 128 : 64)>::kBytes, s128);
+        else
+            e = launch_scan(tc_scan_bwd_kernel<D, 64>, 64, BScanSmem<D, 64>::kBytes, s64);
         if (e != cudaSuccess) return e;
     }
     if (p.num_chunks == 0) return cudaSuccess;

@@ -134,16 +134,22 @@ __global__ void __launch_bounds__(128, 1)
 
         // decay factors, one thread per key channel walking the chunk's tokens
         for (int c = tid; c < D; c += 128) {
+            // all of this channel's gate values in flight at once
+            float gl[64];
             float GL = 0.f;
-            if (VAR != DR_DELTANET)
-                for (int i = 0; i < len; ++i) GL += gate_at<VAR>(p, row0 + i, h, c);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                gl[i] = (VAR != DR_DELTANET && i < len) ? gate_at<VAR>(p, row0 + i, h, c) : 0.f;
+                GL += gl[i];
+            }
             L.gC[rec * D + c] = VAR != DR_DELTANET ? expf(GL) : 1.f;
             uint8_t* kc_img = L.KC + rec * kTile;
             float G = 0.f;
+#pragma unroll
             for (int i = 0; i < 64; ++i) {
                 float e = 1.f, ei = 1.f, ec = 1.f;
                 if (VAR != DR_DELTANET) {
-                    if (i < len) G += gate_at<VAR>(p, row0 + i, h, c);
+                    G += gl[i];
                     e = expf(G);
                     ei = expf(-G);
                     ec = expf(GL - G);
@@ -306,18 +312,20 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ============================================================== tc_scan_fwd
+// Shared memory: the state operand, the U^T operand, and two stages of the
+// per-chunk inputs so the next chunk's tiles load while this chunk computes.
 template <int D, int BV>
 struct ScanSmem {
     static constexpr int kTile = 64 * D * 2;
-    static constexpr int kW = 0;                       // [BV][D] state (bf16 operand)
-    static constexpr int kWy = BV * D * 2;             // [64][D]
-    static constexpr int kQt = kWy + kTile;
-    static constexpr int kKC = kQt + kTile;
-    static constexpr int kUs = kKC + kTile;            // [BV][64] U^T operand
-    static constexpr int kUt = kUs + BV * 128;         // [BV][64] plain Ut^T rows
-    static constexpr int kOt = kUt + BV * 128;         // [BV][64] plain Ot^T rows
-    static constexpr int kG = kOt + BV * 128;          // [D] fp32 e^{Gamma_last}
-    static constexpr int kBytes = kG + D * 4 + 1024;
+    static constexpr int kW = 0;                       // [BV][D] state W (bf16 operand)
+    static constexpr int kUs = BV * D * 2;             // [BV][64] U^T operand
+    static constexpr int kStage0 = kUs + BV * 128;
+    // stage layout: Wy, Qt, KC [64][D] tiles; Ut^T, Ot^T rows [BV][64]; gC [D] fp32
+    static constexpr int kWy = 0, kQt = kTile, kKC = 2 * kTile, kUt = 3 * kTile,
+                         kOt = kUt + BV * 128, kG = kOt + BV * 128;
+    static constexpr int kStageBytes = (kG + D * 4 + 1023) / 1024 * 1024;
+    static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
+    static constexpr uint32_t kStageTx = 3 * kTile + 2 * BV * 128 + D * 4;
 };
 
 template <int D, int BV>
@@ -328,14 +336,8 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Ws = sm + S::kW;
-    uint8_t* Wys = sm + S::kWy;
-    uint8_t* Qts = sm + S::kQt;
-    uint8_t* KCs = sm + S::kKC;
     uint8_t* Us = sm + S::kUs;
-    const uint8_t* UtTs = sm + S::kUt;
-    const uint8_t* OtTs = sm + S::kOt;
-    const float* gCs = reinterpret_cast<const float*>(sm + S::kG);
-    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint64_t bar_ld[2], bar_mma;
     __shared__ uint32_t tmem_base;
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -345,7 +347,8 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     seq_chunks(p, n, c0, nc, srow, slen);
 
     if (tid == 0) {
-        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_ld[0], 1);
+        mbar_init(&bar_ld[1], 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
@@ -361,6 +364,22 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     const int r = (BV == 128) ? tid : m64_row();  // value row of this thread (or -1)
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
+    int issued[2] = {0, 0}, waited[2] = {0, 0};   // bulk-load phases per stage (thread 0)
+
+    auto load_chunk = [&](int ci) {  // thread 0: fetch chunk ci into stage ci & 1
+        const int s = ci & 1;
+        uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
+        const size_t rec = (size_t)(c0 + ci) * p.H + h;
+        mbar_arrive_expect_tx(&bar_ld[s], S::kStageTx);
+        bulk_g2s(st + S::kWy, L.Wy + rec * kTile, kTile, &bar_ld[s]);
+        bulk_g2s(st + S::kQt, L.Qt + rec * kTile, kTile, &bar_ld[s]);
+        bulk_g2s(st + S::kKC, L.KC + rec * kTile, kTile, &bar_ld[s]);
+        bulk_g2s(st + S::kUt, L.UtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
+        bulk_g2s(st + S::kOt, L.OtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
+        bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
+        ++issued[s];
+    };
+    if (tid == 0 && nc > 0) load_chunk(0);
 
     float W[D];  // W[v, :] = S[:, v], fp32
 #pragma unroll
@@ -379,33 +398,26 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
 
     bool ok = true;
     for (int ci = 0; ci < nc && ok; ++ci) {
-        const int chunk = c0 + ci;
-        const size_t rec = (size_t)chunk * p.H + h;
+        const int s = ci & 1;
+        const uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
+        const size_t rec = (size_t)(c0 + ci) * p.H + h;
         const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * BV * 128 + D * 4);
-            bulk_g2s(Wys, L.Wy + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(Qts, L.Qt + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(KCs, L.KC + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(sm + S::kUt, L.UtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld);
-            bulk_g2s(sm + S::kOt, L.OtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld);
-            bulk_g2s(sm + S::kG, L.gC + rec * D, D * 4, &bar_ld);
-        }
-        // the chunk-start state, for the backward pass
-        if (r >= 0) {
+            if (ci + 1 < nc) load_chunk(ci + 1);  // stage s^1 was released at the end of ci-1
+            // the chunk-start state rows [v0, v0+BV) of the W-layout state image
             uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
-#pragma unroll
-            for (int c = 0; c < D; ++c)
-                *reinterpret_cast<__nv_bfloat16*>(s_img + sw128_offset(c, v, D)) =
-                    __float2bfloat16_rn(W[c]);
+            for (int kb = 0; kb < D / 64; ++kb)
+                bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
+            bulk_commit();
         }
-        ok = mbar_wait(&bar_ld, ci & 1, kWaitLimitNs);
+        ok = mbar_wait(&bar_ld[s], (ci >> 1) & 1, kWaitLimitNs);
+        if (tid == 0) ++waited[s];
         if (__syncthreads_or(!ok)) break;
 
         // W Wy^T -> cols [0,64) ;  W Qt^T -> cols [64,128)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tW{smem_u32(Ws), BV}, tWy{smem_u32(Wys), 64}, tQt{smem_u32(Qts), 64};
+            const Tile tW{smem_u32(Ws), BV}, tWy{smem_u32(st + S::kWy), 64}, tQt{smem_u32(st + S::kQt), 64};
             mma_tiles(tm + 0, tW, false, tWy, false, BV, 64, D, false);
             mma_tiles(tm + 64, tW, false, tQt, false, BV, 64, D, false);
             mma_commit(&bar_mma);
@@ -414,35 +426,31 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        {
-            uint8_t* u_img = L.U + rec * kTile;
-            for (int g = 0; g < 4; ++g) {
-                float acc[16], oacc[16];
-                tmem_ld16(tl + g * 16, acc);
-                tmem_ld16(tl + 64 + g * 16, oacc);
-                tmem_ld_wait();
-                if (r >= 0) {
-                    float ut[16], ot[16];
-                    const uint4* up = reinterpret_cast<const uint4*>(UtTs + r * 128 + g * 32);
-                    const uint4* op = reinterpret_cast<const uint4*>(OtTs + r * 128 + g * 32);
-                    unpack8(up[0], ut);
-                    unpack8(up[1], ut + 8);
-                    unpack8(op[0], ot);
-                    unpack8(op[1], ot + 8);
+        for (int g = 0; g < 4; ++g) {
+            float acc[16], oacc[16];
+            tmem_ld16(tl + g * 16, acc);
+            tmem_ld16(tl + 64 + g * 16, oacc);
+            tmem_ld_wait();
+            if (r >= 0) {
+                float ut[16], ot[16];
+                const uint4* up = reinterpret_cast<const uint4*>(st + S::kUt + r * 128 + g * 32);
+                const uint4* op = reinterpret_cast<const uint4*>(st + S::kOt + r * 128 + g * 32);
+                unpack8(up[0], ut);
+                unpack8(up[1], ut + 8);
+                unpack8(op[0], ot);
+                unpack8(op[1], ot + 8);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        acc[j] = ut[j] - acc[j];   // U
-                        oacc[j] = ot[j] + oacc[j]; // O
-                    }
-                    tile_store16(Us, r, g * 16, BV, acc);
+                for (int j = 0; j < 16; ++j) {
+                    acc[j] = ut[j] - acc[j];    // U
+                    oacc[j] = ot[j] + oacc[j];  // O
+                }
+                tile_store16(Us, r, g * 16, BV, acc);
+                if (write_o) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int i = g * 16 + j;
-                        *reinterpret_cast<__nv_bfloat16*>(u_img + sw128_offset(i, v, 64)) =
-                            __float2bfloat16_rn(acc[j]);
-                        if (write_o && i < len)
-                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype,
-                                   oacc[j]);
+                        if (i < len)
+                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype, oacc[j]);
                     }
                 }
             }
@@ -451,17 +459,21 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         tc_fence_before();
         __syncthreads();
 
-        // U^T KC -> cols [128, 128+D)
+        // U^T KC -> cols [128, 128+D); U^T rows [v0, v0+BV) of the U^T image
         if (tid == 0) {
             tc_fence_after();
-            const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(KCs), 64};
+            const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(st + S::kKC), 64};
             mma_tiles(tm + 128, tU, false, tKC, true, BV, D, 64, false);
             mma_commit(&bar_mma);
+            bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
+            bulk_commit();
         }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+        if (tid == 0) bulk_wait_read();  // Ws and Us are rewritten below / next chunk
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG);
 #pragma unroll
         for (int cb = 0; cb < D / 16; ++cb) {
             float acc[16];
@@ -487,9 +499,11 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         }
     } else {
         record_timeout(p);
-        mbar_wait(&bar_ld, 0, kWaitLimitNs);
-        mbar_wait(&bar_ld, 1, kWaitLimitNs);
+        if (tid == 0)
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > waited[s]) mbar_wait(&bar_ld[s], waited[s] & 1, kWaitLimitNs);
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -583,6 +597,11 @@ cudaError_t tc_fwd_d(const Params& p, cudaStream_t st, bool write_o) {
         default: e = launch_prep<D, DR_KDA>(p, L, st); break;
     }
     if (e != cudaSuccess) return e;
+    // one 128-row value tile per (sequence, head) when that already fills the SMs; two
+    // 64-row tiles otherwise (more CTAs for few, long sequences)
+    if constexpr (D == 128) {
+        if (p.N * p.H >= 120) return launch_scan_fwd<D, 128>(p, L, st, write_o);
+    }
     return launch_scan_fwd<D, 64>(p, L, st, write_o);
 }
 

@@ -3,12 +3,13 @@
 // Every per-chunk intermediate is kept per (chunk, head) record rec = chunk*H + h.
 // "Tile images" are byte-for-byte copies of SW128 shared-memory tiles (see
 // tc.cuh) so a kernel fetches one with a single untiled bulk copy.
-//   Wy, Qt, KC, U, dU : [64 tokens][D] tile images           (64*D*2 bytes)
+//   Wy, Qt, KC        : [64 tokens][D] tile images             (64*D*2 bytes)
+//   U, dU             : [D value channels][64 tokens] tile images of U^T and -dU^T
 //   UtT, OtT          : [D][64] plain bf16, transposed         (D*64*2 bytes)
 //   T                 : [64][64] tile image of the UT inverse  (8 KB)
-//   S, dS             : [D rows = key channel][D cols = value channel] tile images
-//                       of the state at the chunk start / of dL/d(state at the
-//                       chunk end)                              (D*D*2 bytes)
+//   S, dS             : [D rows = value channel][D cols = key channel] tile images
+//                       (W layout) of the state at the chunk start / of dL/d(state
+//                       at the chunk end)                       (D*D*2 bytes)
 //   gC                : [D] fp32, e^{Gamma} at the chunk's last token
 //   dQt, dWyA, dKC    : [64][D] tile images of dO S^T, dU S^T and U dS^T
 //                       (the state-side pieces of the chunk's gradient)
