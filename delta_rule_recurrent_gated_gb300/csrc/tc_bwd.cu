@@ -457,36 +457,71 @@ __global__ void __launch_bounds__(128, 1)
         zero_pad_rows(dOs, D, len);
         __syncthreads();
 
-        // E1: decay factors per key channel
-        for (int c = tid; c < D; c += 128) {
-            // all of this channel's gate values in flight at once
-            float gl[64];
+        // E1a: within-chunk cumulative log-decay (KDA: per key channel into Gam;
+        // GDN: per token into Grow); rows past the sequence end add nothing
+        if (VAR == DR_KDA) {
+            for (int c = tid; c < D; c += 128) {
+                float gl[64];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                gl[i] = 0.f;
-                if (VAR != DR_DELTANET && i < len)
-                    gl[i] = (VAR == DR_GDN) ? p.g[(size_t)(row0 + i) * p.H + h]
-                                            : p.g[((size_t)(row0 + i) * p.H + h) * D + c];
-            }
-            float G = 0.f;
+                for (int i = 0; i < 64; ++i)
+                    gl[i] = i < len ? p.g[((size_t)(row0 + i) * p.H + h) * D + c] : 0.f;
+                float G = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float e = 1.f, ei = 1.f;
-                if (VAR != DR_DELTANET) {
+                for (int i = 0; i < 64; ++i) {
                     G += gl[i];
-                    e = expf(G);
-                    ei = expf(-G);
-                    if (VAR == DR_KDA) Gam[i * D + c] = G;
-                    if (VAR == DR_GDN && c == 0) Grow[i] = G;
+                    Gam[i * D + c] = G;
                 }
-                const uint32_t off = sw128_offset(i, c, 64);
-                __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(Qs + off);
-                __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(Ks + off);
-                const float kv = __bfloat162float(*kp);
-                *qp = __float2bfloat16_rn(__bfloat162float(*qp) * e);
-                *kp = __float2bfloat16_rn(kv * ei);
-                *reinterpret_cast<__nv_bfloat16*>(Kbs + off) = __float2bfloat16_rn(kv * e);
             }
+        } else if (VAR == DR_GDN) {
+            if (warp == 0) {
+                const int lane = tid & 31;
+                const float a0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
+                const float a1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+                float x = a0 + a1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                Grow[2 * lane + 1] = x;
+                Grow[2 * lane] = x - a1;
+            }
+        }
+        __syncthreads();
+        // E1b: Qb = q e^G, Kr = k e^-G, Kb = k e^G, eight channels per step
+        for (int w = tid; w < 64 * (D / 8); w += 128) {
+            const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
+            const uint32_t off = sw128_offset(i, c8, 64);
+            const uint4 qv = *reinterpret_cast<const uint4*>(Qs + off);
+            const uint4 kv = *reinterpret_cast<const uint4*>(Ks + off);
+            if (VAR == DR_DELTANET) {
+                *reinterpret_cast<uint4*>(Kbs + off) = kv;
+                continue;
+            }
+            float q8[8], k8[8], G8[8];
+            unpack8(qv, q8);
+            unpack8(kv, k8);
+            if (VAR == DR_KDA) {
+                const float4 g0 = *reinterpret_cast<const float4*>(&Gam[i * D + c8]);
+                const float4 g1 = *reinterpret_cast<const float4*>(&Gam[i * D + c8 + 4]);
+                G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
+                G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) G8[j] = Grow[i];
+            }
+            uint32_t wq[4], wr[4], wb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float e0 = expf(G8[2 * j]), e1 = expf(G8[2 * j + 1]);
+                const float i0 = expf(-G8[2 * j]), i1 = expf(-G8[2 * j + 1]);
+                wq[j] = pack_bf16(q8[2 * j] * e0, q8[2 * j + 1] * e1);
+                wr[j] = pack_bf16(k8[2 * j] * i0, k8[2 * j + 1] * i1);
+                wb[j] = pack_bf16(k8[2 * j] * e0, k8[2 * j + 1] * e1);
+            }
+            *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
+            *reinterpret_cast<uint4*>(Kbs + off) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
         fence_async_smem();
         __syncthreads();
@@ -529,7 +564,8 @@ __global__ void __launch_bounds__(128, 1)
             const Tile tAq{smem_u32(Aqs), 64};
             mma_tiles(tm + 0, Tile{smem_u32(B8a), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
             mma_tiles(tm + 64, tAq, true, Tile{smem_u32(dQs), 64}, true, 64, D, 64, false);
-            mma_tiles(tm + 64 + D, tAq, true, Tile{smem_u32(dOs), 64}, true, 64, D, 64, false);
+            // dUt^T - (-dU^T) = scale-free dO^T Aqk, rows = value channels (M = D)
+            mma_tiles(tm + 64 + D, Tile{smem_u32(dOs), 64}, true, tAq, true, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mma_done();
@@ -550,9 +586,8 @@ __global__ void __launch_bounds__(128, 1)
             }
         }
         for (int cb = 0; cb < D / 16; ++cb) {
-            float a[16], b[16];
+            float a[16];
             tmem_ld16(tl + 64 + cb * 16, a);
-            tmem_ld16(tl + 64 + D + cb * 16, b);
             tmem_ld_wait();
             if (r >= 0) {
                 float wa[16];
@@ -560,11 +595,21 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) a[j] = -wa[j] - sc * a[j];  // dWy
                 tile_store16(dWys, r, cb * 16, 64, a);
-                // dUts holds -dU^T ([value][token]); this thread owns column r
+            }
+        }
+        {
+            // dUts holds -dU^T ([value][token]); the accumulator rows are value channels
+            const int rv = (D == 128) ? tid : r;
+            for (int g = 0; g < 4; ++g) {
+                float b[16];
+                tmem_ld16(tl + 64 + D + g * 16, b);
+                tmem_ld_wait();
+                if (rv >= 0) {
+                    float nd[16];
+                    tile_load16(dUts, rv, g * 16, D, nd);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    __nv_bfloat16* e = tile_elem(dUts, cb * 16 + j, r, D);
-                    *e = __float2bfloat16_rn(sc * b[j] - __bfloat162float(*e));  // dUt^T
+                    for (int j = 0; j < 16; ++j) b[j] = sc * b[j] - nd[j];  // dUt^T
+                    tile_store16(dUts, rv, g * 16, D, b);
                 }
             }
         }
@@ -610,10 +655,9 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     dbeta_acc = fmaf(a[j], vv[j], dbeta_acc);
-                    if (r < len)
-                        st_any(p.dv_, ((size_t)(row0 + r) * p.H + h) * D + cb * 16 + j,
-                               p.grad_dtype, br * a[j]);
+                    a[j] *= br;
                 }
+                if (r < len) store_row16(p.dv_, ((size_t)(row0 + r) * p.H + h) * D + cb * 16, p.grad_dtype, a);
             }
         }
         fence_async_smem();
@@ -708,6 +752,7 @@ __global__ void __launch_bounds__(128, 1)
                     tile_load16(Ks, r, cb * 16, 64, kr);
                     tile_load16(dQs, r, cb * 16, 64, dqt);
                     tile_load16(dkc_img, r, cb * 16, 64, dkc);
+                    float oq[16], ok_[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int c = cb * 16 + j;
@@ -729,11 +774,13 @@ __global__ void __launch_bounds__(128, 1)
                             grow += dG;
                             frow = fmaf(dkc[j], KC, frow);
                         }
-                        if (r < len) {
-                            const size_t eidx = ((size_t)(row0 + r) * p.H + h) * D + c;
-                            st_any(p.dq, eidx, p.grad_dtype, dQb * e);
-                            st_any(p.dk_, eidx, p.grad_dtype, dKb * e + dkr[j] * ei + dkc[j] * gc * ei);
-                        }
+                        oq[j] = dQb * e;
+                        ok_[j] = dKb * e + dkr[j] * ei + dkc[j] * gc * ei;
+                    }
+                    if (r < len) {
+                        const size_t eidx = ((size_t)(row0 + r) * p.H + h) * D + cb * 16;
+                        store_row16(p.dq, eidx, p.grad_dtype, oq);
+                        store_row16(p.dk_, eidx, p.grad_dtype, ok_);
                     }
                 }
             }

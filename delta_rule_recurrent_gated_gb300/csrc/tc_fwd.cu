@@ -57,7 +57,8 @@ struct PrepSmem {
     static constexpr int kAq = 5 * kTile, kT = kAq + 8192;
     static constexpr int kAf = (D == 128) ? kX : kT + 8192;  // fp32 [64][64] (16 KB)
     static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384;
-    static constexpr int kBytes = kBeta + 256 + 1024;  // + alignment slack
+    static constexpr int kGL = kBeta + 256;              // [D] fp32 Gamma at the last token
+    static constexpr int kBytes = kGL + D * 4 + 1024;    // + alignment slack
 };
 
 template <int D, int VAR>
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* Ts = sm + S::kT;   // T [64][64]
     float* Af = reinterpret_cast<float*>(sm + S::kAf);
     float* beta_s = reinterpret_cast<float*>(sm + S::kBeta);
+    float* GLs = reinterpret_cast<float*>(sm + S::kGL);
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base;
 
@@ -132,40 +134,71 @@ __global__ void __launch_bounds__(128, 1)
         }
         __syncthreads();
 
-        // decay factors, one thread per key channel walking the chunk's tokens
-        for (int c = tid; c < D; c += 128) {
-            // all of this channel's gate values in flight at once
+        // decay: the cumulative log-decay per key channel (thread c holds its channel's
+        // gates in registers), staged 32 rows at a time in the still-unused Aqk / T
+        // buffers, then an elementwise pass eight channels wide
+        {
+            float* Gb = reinterpret_cast<float*>(Aqs);  // [32][D] fp32
             float gl[64];
-            float GL = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                gl[i] = (VAR != DR_DELTANET && i < len) ? gate_at<VAR>(p, row0 + i, h, c) : 0.f;
-                GL += gl[i];
-            }
-            L.gC[rec * D + c] = VAR != DR_DELTANET ? expf(GL) : 1.f;
-            uint8_t* kc_img = L.KC + rec * kTile;
             float G = 0.f;
+            if (tid < D) {
+                float GL = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float e = 1.f, ei = 1.f, ec = 1.f;
-                if (VAR != DR_DELTANET) {
-                    G += gl[i];
-                    e = expf(G);
-                    ei = expf(-G);
-                    ec = expf(GL - G);
+                for (int i = 0; i < 64; ++i) {
+                    gl[i] = (VAR != DR_DELTANET && i < len) ? gate_at<VAR>(p, row0 + i, h, tid) : 0.f;
+                    GL += gl[i];
                 }
-                const uint32_t off = sw128_offset(i, c, 64);
-                __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(Qs + off);
-                __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(Ks + off);
-                __nv_bfloat16* vp = reinterpret_cast<__nv_bfloat16*>(Vs + off);
-                const float kv = __bfloat162float(*kp), qv = __bfloat162float(*qp);
-                const float b = beta_s[i];
-                *qp = __float2bfloat16_rn(qv * e);
-                *kp = __float2bfloat16_rn(kv * ei);
-                *reinterpret_cast<__nv_bfloat16*>(Xs + off) = __float2bfloat16_rn(kv * e);
-                *reinterpret_cast<__nv_bfloat16*>(Ys + off) = __float2bfloat16_rn(b * kv * e);
-                *vp = __float2bfloat16_rn(b * __bfloat162float(*vp));
-                *reinterpret_cast<__nv_bfloat16*>(kc_img + off) = __float2bfloat16_rn(kv * ec);
+                L.gC[rec * D + tid] = VAR != DR_DELTANET ? expf(GL) : 1.f;
+                GLs[tid] = GL;
+            }
+            uint8_t* kc_img = L.KC + rec * kTile;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                if (tid < D) {
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) {
+                        G += gl[32 * half + ii];
+                        Gb[ii * D + tid] = G;
+                    }
+                }
+                __syncthreads();
+                for (int w = tid; w < 32 * (D / 8); w += 128) {
+                    const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
+                    const uint32_t off = sw128_offset(i, c8, 64);
+                    float q8[8], k8[8], v8[8];
+                    unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
+                    unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
+                    unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
+                    const float b = beta_s[i];
+                    uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float e[2] = {1.f, 1.f}, ei[2] = {1.f, 1.f}, ec[2] = {1.f, 1.f};
+                        if (VAR != DR_DELTANET) {
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                const float Gv = Gb[ii * D + c8 + 2 * j + t];
+                                e[t] = expf(Gv);
+                                ei[t] = expf(-Gv);
+                                ec[t] = expf(GLs[c8 + 2 * j + t] - Gv);
+                            }
+                        }
+                        const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
+                        wq[j] = pack_bf16(q8[2 * j] * e[0], q8[2 * j + 1] * e[1]);
+                        wr[j] = pack_bf16(k0 * ei[0], k1 * ei[1]);
+                        wb[j] = pack_bf16(k0 * e[0], k1 * e[1]);
+                        wy[j] = pack_bf16(b * k0 * e[0], b * k1 * e[1]);
+                        wv[j] = pack_bf16(b * v8[2 * j], b * v8[2 * j + 1]);
+                        wc[j] = pack_bf16(k0 * ec[0], k1 * ec[1]);
+                    }
+                    *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
+                    *reinterpret_cast<uint4*>(Xs + off) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+                    *reinterpret_cast<uint4*>(Ys + off) = make_uint4(wy[0], wy[1], wy[2], wy[3]);
+                    *reinterpret_cast<uint4*>(Vs + off) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    *reinterpret_cast<uint4*>(kc_img + off) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
+                }
+                __syncthreads();
             }
         }
         fence_async_smem();
@@ -194,7 +227,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = cb * 16 + j;
-                    Af[r * 64 + col] = col < r ? br * g16[j] : 0.f;
+                    Af[col * 64 + r] = col < r ? br * g16[j] : 0.f;  // column-major A
                     a16[j] = col <= r ? a16[j] : 0.f;
                 }
                 tile_store16(Aqs, r, cb * 16, 64, a16);
@@ -203,24 +236,25 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_before();
         __syncthreads();
 
-        // T = (I + A)^{-1}: thread n solves column n by forward substitution
+        // T = (I + A)^{-1}: thread n solves column n of (I + A) x = e_n, right-looking:
+        // once x_j is final, every later row's partial sum takes its A[i][j] x_j term,
+        // so the dependent chain is one FMA per row
         if (tid < 64) {
             const int n = tid;
             float x[64];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float s0 = (i == n) ? 1.f : 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            for (int i = 0; i < 64; ++i) x[i] = (i == n) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j + 3 < i; j += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(&Af[i * 64 + j]);
-                    s0 = fmaf(-a.x, x[j], s0);
-                    s1 = fmaf(-a.y, x[j + 1], s1);
-                    s2 = fmaf(-a.z, x[j + 2], s2);
-                    s3 = fmaf(-a.w, x[j + 3], s3);
+            for (int j = 0; j < 63; ++j) {
+                const float xj = x[j];
+#pragma unroll
+                for (int i4 = (j + 1) & ~3; i4 < 64; i4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(&Af[j * 64 + i4]);
+                    if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
+                    if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
+                    if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
+                    if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
                 }
-#pragma unroll
-                for (int j = i & ~3; j < i; ++j) s0 = fmaf(-Af[i * 64 + j], x[j], s0);
-                x[i] = (s0 + s1) + (s2 + s3);
             }
             uint8_t* t_img = L.T + rec * 8192;
 #pragma unroll
