@@ -352,6 +352,10 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ============================================================== tc_bwd_chunk
+// 256 threads: warps w and w+4 read the same TMEM lane quarter (the same
+// accumulator rows of an M = 64 product) and split its columns between them.
+constexpr int kChunkThreads = 256;
+
 template <int D, int VAR>
 struct BChunkSmem {
     static constexpr int kTile = 64 * D * 2, kCC = 8192;
@@ -361,12 +365,13 @@ struct BChunkSmem {
                          kdAq = kB8b + kCC;
     static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][D]
     static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * D * 4 : 0);
-    // small arrays: beta[64], gamma_last[D], dgC[D], (spare D), rowsum[64], Gamma_row[64]
-    static constexpr int kBytes = kSmall + (64 * 3 + D * 3) * 4 + 1024;
+    // small arrays: beta[64], e^{Gamma_last}[D], dgC[D], rowsum[64], Gamma_row[64],
+    // e^{Gamma_row}[64], e^{-Gamma_row}[64], per-row partials of the second warp half [3][64]
+    static constexpr int kBytes = kSmall + (64 * 8 + D * 2) * 4 + 1024;
 };
 
 template <int D, int VAR>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                         const Params p, const TcLayout L) {
@@ -377,27 +382,30 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* Qs = sm + S::kQ;     // q -> Qb
     uint8_t* Ks = sm + S::kK;     // k -> Kr
     uint8_t* Vs = sm + S::kV;     // v
-    uint8_t* dOs = sm + S::kdO;
+    uint8_t* dOs = sm + S::kdO;   // dO, later dKC
     uint8_t* dQs = sm + S::kdQ;   // dQt = dO S^T
     uint8_t* Kbs = sm + S::kKb;   // Kb
-    uint8_t* dWys = sm + S::kdWy;
-    uint8_t* dUts = sm + S::kdUt;
+    uint8_t* dWys = sm + S::kdWy; // dWyA -> dWy
+    uint8_t* dUts = sm + S::kdUt; // -dU^T -> dUt^T  ([value][token])
     uint8_t* Ts = sm + S::kT;
     uint8_t* Aqs = sm + S::kAq;   // tril(Qb Kr^T)
     uint8_t* B8a = sm + S::kB8a;  // P, then X = dT T^T
     uint8_t* B8b = sm + S::kB8b;  // dT, then dG
     uint8_t* dAqs = sm + S::kdAq; // dAqk
-    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: Gamma, then dGamma
+    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g, Gamma, then dGamma
     float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
     float* gC_s = beta_s + 64;
     float* dgC_s = gC_s + D;
-    float* rowsum = dgC_s + 2 * D;
-    float* Grow = rowsum + 64;    // GDN: Gamma per row
+    float* rowsum = dgC_s + D;
+    float* Grow = rowsum + 64;    // GDN: Gamma per row, later sum of dKC*KC per row
+    float* Erow = Grow + 64;      // GDN: e^{Gamma} per row
+    float* Eirow = Erow + 64;     // GDN: e^{-Gamma} per row
+    float* part = Eirow + 64;     // [3][64] partial row sums of warps 4..7
     __shared__ uint64_t bar_ld, bar_mma, bar_kc;
     __shared__ uint32_t tmem_base;
 
     constexpr uint32_t R_dbK = 128, R_dbV = 128 + D, R_dQ = 128 + 2 * D, R_dKr = 128 + D;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2;
     const int chunk = blockIdx.x, h = blockIdx.y;
     int seq, row0, len;
     chunk_info(p, chunk, seq, row0, len);
@@ -434,7 +442,8 @@ __global__ void __launch_bounds__(128, 1)
 
     do {
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 7 * kTile + 8192 + 2 * D * 4);
+            const uint32_t gbytes = VAR == DR_KDA ? (uint32_t)len * D * 4 : 0u;
+            mbar_arrive_expect_tx(&bar_ld, 7 * kTile + 8192 + 2 * D * 4 + gbytes);
             bulk_g2s(dWys, L.dWyA + rec * kTile, kTile, &bar_ld);
             bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_ld);
             for (int kb = 0; kb < D / 64; ++kb) {
@@ -448,6 +457,11 @@ __global__ void __launch_bounds__(128, 1)
             bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_ld);
             bulk_g2s(dgC_s, L.dgC + rec * D, D * 4, &bar_ld);
         }
+        __syncthreads();  // the expected byte count is registered before the gate rows go out
+        if (VAR == DR_KDA && warp == 1) {
+            for (int i = tid & 31; i < len; i += 32)
+                bulk_g2s(Gam + i * D, p.g + ((size_t)(row0 + i) * p.H + h) * D, D * 4, &bar_ld);
+        }
         if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
@@ -455,20 +469,15 @@ __global__ void __launch_bounds__(128, 1)
         zero_pad_rows(Ks, D, len);
         zero_pad_rows(Vs, D, len);
         zero_pad_rows(dOs, D, len);
-        __syncthreads();
 
-        // E1a: within-chunk cumulative log-decay (KDA: per key channel into Gam;
-        // GDN: per token into Grow); rows past the sequence end add nothing
+        // E1a: within-chunk cumulative log-decay (KDA: per key channel, in place in Gam;
+        // GDN: per token, with its two exponentials); rows past the end add nothing
         if (VAR == DR_KDA) {
-            for (int c = tid; c < D; c += 128) {
-                float gl[64];
-#pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    gl[i] = i < len ? p.g[((size_t)(row0 + i) * p.H + h) * D + c] : 0.f;
+            for (int c = tid; c < D; c += kChunkThreads) {
                 float G = 0.f;
-#pragma unroll
+#pragma unroll 8
                 for (int i = 0; i < 64; ++i) {
-                    G += gl[i];
+                    if (i < len) G += Gam[i * D + c];
                     Gam[i * D + c] = G;
                 }
             }
@@ -483,13 +492,19 @@ __global__ void __launch_bounds__(128, 1)
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
-                Grow[2 * lane + 1] = x;
-                Grow[2 * lane] = x - a1;
+                const float g0 = x - a1, g1 = x;
+                Grow[2 * lane] = g0;
+                Grow[2 * lane + 1] = g1;
+                const float e0 = expf(g0), e1 = expf(g1);
+                Erow[2 * lane] = e0;
+                Erow[2 * lane + 1] = e1;
+                Eirow[2 * lane] = __frcp_rn(e0);
+                Eirow[2 * lane + 1] = __frcp_rn(e1);
             }
         }
         __syncthreads();
         // E1b: Qb = q e^G, Kr = k e^-G, Kb = k e^G, eight channels per step
-        for (int w = tid; w < 64 * (D / 8); w += 128) {
+        for (int w = tid; w < 64 * (D / 8); w += kChunkThreads) {
             const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
             const uint32_t off = sw128_offset(i, c8, 64);
             const uint4 qv = *reinterpret_cast<const uint4*>(Qs + off);
@@ -498,26 +513,32 @@ __global__ void __launch_bounds__(128, 1)
                 *reinterpret_cast<uint4*>(Kbs + off) = kv;
                 continue;
             }
-            float q8[8], k8[8], G8[8];
+            float q8[8], k8[8], e8[8], i8[8];
             unpack8(qv, q8);
             unpack8(kv, k8);
             if (VAR == DR_KDA) {
                 const float4 g0 = *reinterpret_cast<const float4*>(&Gam[i * D + c8]);
                 const float4 g1 = *reinterpret_cast<const float4*>(&Gam[i * D + c8 + 4]);
-                G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
-                G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
-            } else {
+                const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) G8[j] = Grow[i];
+                for (int j = 0; j < 8; ++j) {
+                    e8[j] = expf(G8[j]);
+                    i8[j] = __frcp_rn(e8[j]);
+                }
+            } else {
+                const float e = Erow[i], ei = Eirow[i];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    e8[j] = e;
+                    i8[j] = ei;
+                }
             }
             uint32_t wq[4], wr[4], wb[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float e0 = expf(G8[2 * j]), e1 = expf(G8[2 * j + 1]);
-                const float i0 = expf(-G8[2 * j]), i1 = expf(-G8[2 * j + 1]);
-                wq[j] = pack_bf16(q8[2 * j] * e0, q8[2 * j + 1] * e1);
-                wr[j] = pack_bf16(k8[2 * j] * i0, k8[2 * j + 1] * i1);
-                wb[j] = pack_bf16(k8[2 * j] * e0, k8[2 * j + 1] * e1);
+                wq[j] = pack_bf16(q8[2 * j] * e8[2 * j], q8[2 * j + 1] * e8[2 * j + 1]);
+                wr[j] = pack_bf16(k8[2 * j] * i8[2 * j], k8[2 * j + 1] * i8[2 * j + 1]);
+                wb[j] = pack_bf16(k8[2 * j] * e8[2 * j], k8[2 * j + 1] * e8[2 * j + 1]);
             }
             *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
             *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
@@ -537,7 +558,7 @@ __global__ void __launch_bounds__(128, 1)
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = half; cb < 4; cb += 2) {
             float a[16], p1[16], p2[16];
             tmem_ld16(tl + cb * 16, a);
             tmem_ld16(tl + 64 + cb * 16, p1);
@@ -558,13 +579,12 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_before();
         __syncthreads();
 
-        // M2: P T^T -> [0,64) ; Aqk^T dQt -> [64,64+D) ; Aqk^T dO -> [64+D,64+2D)
+        // M2: P T^T -> [0,64) ; Aqk^T dQt -> [64,64+D) ; dO^T Aqk -> [64+D, 128+D) (M = D)
         if (tid == 0) {
             tc_fence_after();
             const Tile tAq{smem_u32(Aqs), 64};
             mma_tiles(tm + 0, Tile{smem_u32(B8a), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
             mma_tiles(tm + 64, tAq, true, Tile{smem_u32(dQs), 64}, true, 64, D, 64, false);
-            // dUt^T - (-dU^T) = scale-free dO^T Aqk, rows = value channels (M = D)
             mma_tiles(tm + 64 + D, Tile{smem_u32(dOs), 64}, true, tAq, true, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
@@ -575,7 +595,7 @@ __global__ void __launch_bounds__(128, 1)
             mbar_arrive_expect_tx(&bar_kc, kTile);
             bulk_g2s(dOs, L.dKC + rec * kTile, kTile, &bar_kc);
         }
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = half; cb < 4; cb += 2) {
             float a[16];
             tmem_ld16(tl + cb * 16, a);
             tmem_ld_wait();
@@ -585,7 +605,7 @@ __global__ void __launch_bounds__(128, 1)
                 tile_store16(dAqs, r, cb * 16, 64, a);
             }
         }
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = half; cb < D / 16; cb += 2) {
             float a[16];
             tmem_ld16(tl + 64 + cb * 16, a);
             tmem_ld_wait();
@@ -599,8 +619,8 @@ __global__ void __launch_bounds__(128, 1)
         }
         {
             // dUts holds -dU^T ([value][token]); the accumulator rows are value channels
-            const int rv = (D == 128) ? tid : r;
-            for (int g = 0; g < 4; ++g) {
+            const int rv = (D == 128) ? (tid & 127) : r;
+            for (int g = half; g < 4; g += 2) {
                 float b[16];
                 tmem_ld16(tl + 64 + D + g * 16, b);
                 tmem_ld_wait();
@@ -633,7 +653,7 @@ __global__ void __launch_bounds__(128, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
         float dbeta_acc = 0.f;
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = half; cb < 4; cb += 2) {
             float a[16], b[16];
             tmem_ld16(tl + cb * 16, a);
             tmem_ld16(tl + 64 + cb * 16, b);
@@ -644,7 +664,7 @@ __global__ void __launch_bounds__(128, 1)
                 tile_store16(B8b, r, cb * 16, 64, a);
             }
         }
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = half; cb < D / 16; cb += 2) {
             float a[16];
             tmem_ld16(tl + R_dbV + cb * 16, a);
             tmem_ld_wait();
@@ -673,7 +693,7 @@ __global__ void __launch_bounds__(128, 1)
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = half; cb < 4; cb += 2) {
             float a[16];
             tmem_ld16(tl + cb * 16, a);
             tmem_ld_wait();
@@ -693,7 +713,7 @@ __global__ void __launch_bounds__(128, 1)
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = half; cb < 4; cb += 2) {
             float a[16], gm[16];
             tmem_ld16(tl + cb * 16, a);
             tmem_ld16(tl + 64 + cb * 16, gm);
@@ -723,22 +743,23 @@ __global__ void __launch_bounds__(128, 1)
             mma_commit(&bar_mma);
         }
         ok = mma_done();
+        ok = ok && mbar_wait(&bar_kc, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        // E7: the decay chain, per row
-        ok = mbar_wait(&bar_kc, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
+        // E7: the decay chain, per row; each warp half takes every other 16-column block
         {
-            const uint8_t* dkc_img = dOs;
             // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows, in
             // the T / Aqk / P / dG / dAqk tiles (40 KB contiguous), all consumed by now
             float* Fa = reinterpret_cast<float*>(Ts);
             float grow = 0.f, frow = 0.f;
-            float Gr = 0.f;
-            if (VAR == DR_GDN && r >= 0) Gr = Grow[r];
+            float er = 1.f, eir = 1.f;
+            if (VAR == DR_GDN && r >= 0) {
+                er = Erow[r];
+                eir = Eirow[r];
+            }
             const float br = r >= 0 ? beta_s[r] : 0.f;
-            for (int cb = 0; cb < D / 16; ++cb) {
+            for (int cb = half; cb < D / 16; cb += 2) {
                 float dq_[16], dbk[16], dkb[16], dkr[16];
                 tmem_ld16(tl + R_dQ + cb * 16, dq_);
                 tmem_ld16(tl + R_dbK + cb * 16, dbk);
@@ -751,16 +772,16 @@ __global__ void __launch_bounds__(128, 1)
                     tile_load16(Kbs, r, cb * 16, 64, kb);
                     tile_load16(Ks, r, cb * 16, 64, kr);
                     tile_load16(dQs, r, cb * 16, 64, dqt);
-                    tile_load16(dkc_img, r, cb * 16, 64, dkc);
+                    tile_load16(dOs, r, cb * 16, 64, dkc);
                     float oq[16], ok_[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int c = cb * 16 + j;
-                        float G = 0.f;
-                        if (VAR == DR_KDA) G = Gam[r * D + c];
-                        if (VAR == DR_GDN) G = Gr;
-                        const float e = VAR == DR_DELTANET ? 1.f : expf(G);
-                        const float ei = VAR == DR_DELTANET ? 1.f : expf(-G);
+                        float e = er, ei = eir;
+                        if (VAR == DR_KDA) {
+                            e = expf(Gam[r * D + c]);
+                            ei = __frcp_rn(e);
+                        }
                         const float gc = gC_s[c];
                         const float dQb = sc * dqt[j] + dq_[j];
                         const float dKb = dkb[j] + br * dbk[j];
@@ -784,10 +805,18 @@ __global__ void __launch_bounds__(128, 1)
                     }
                 }
             }
-            if (r >= 0) {
+            // combine the two warp halves' row partials in a fixed order
+            if (half == 1 && r >= 0) {
+                part[r] = dbeta_acc;
+                part[64 + r] = grow;
+                part[128 + r] = frow;
+            }
+            __syncthreads();
+            if (half == 0 && r >= 0) {
+                dbeta_acc += part[r];
                 if (VAR == DR_GDN) {
-                    rowsum[r] = grow;
-                    Grow[r] = frow;  // this row's Gamma was read above; reuse the slot
+                    rowsum[r] = grow + part[64 + r];
+                    Grow[r] = frow + part[128 + r];  // this row's Gamma is no longer needed
                 }
                 if (r < len) p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc;
             }
@@ -796,7 +825,7 @@ __global__ void __launch_bounds__(128, 1)
 
         // E8: dg = reverse cumulative sum of dGamma within the chunk
         if (VAR == DR_KDA) {
-            for (int c = tid; c < D; c += 128) {
+            for (int c = tid; c < D; c += kChunkThreads) {
                 float run = dgC_s[c] * gC_s[c];
                 const float* Fa = reinterpret_cast<const float*>(Ts);
                 for (int i = 0; i < 64; ++i) run += Fa[i * D + c];
@@ -888,7 +917,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         }
         {
             TraceScope ts("tc_bwd_chunk", st);
-            kernel<<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mdo, p, L);
+            kernel<<<dim3(p.num_chunks, p.H), kChunkThreads, smem, st>>>(mq, mk, mv, mdo, p, L);
         }
         return cudaGetLastError();
     };

@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(128, 1)
                     gl[i] = (VAR != DR_DELTANET && i < len) ? gate_at<VAR>(p, row0 + i, h, tid) : 0.f;
                     GL += gl[i];
                 }
-                L.gC[rec * D + tid] = VAR != DR_DELTANET ? expf(GL) : 1.f;
-                GLs[tid] = GL;
+                const float eGL = VAR != DR_DELTANET ? expf(GL) : 1.f;
+                L.gC[rec * D + tid] = eGL;
+                GLs[tid] = eGL;  // e^{Gamma_last} per channel
             }
             uint8_t* kc_img = L.KC + rec * kTile;
 #pragma unroll
@@ -177,10 +178,9 @@ __global__ void __launch_bounds__(128, 1)
                         if (VAR != DR_DELTANET) {
 #pragma unroll
                             for (int t = 0; t < 2; ++t) {
-                                const float Gv = Gb[ii * D + c8 + 2 * j + t];
-                                e[t] = expf(Gv);
-                                ei[t] = expf(-Gv);
-                                ec[t] = expf(GLs[c8 + 2 * j + t] - Gv);
+                                e[t] = expf(Gb[ii * D + c8 + 2 * j + t]);
+                                ei[t] = __frcp_rn(e[t]);
+                                ec[t] = GLs[c8 + 2 * j + t] * ei[t];
                             }
                         }
                         const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
