@@ -16,8 +16,8 @@
 // last token), dg = reverse cumulative sum of dGamma within the chunk.
 //
 // Kernels: tc_scan_bwd (reverse over chunks, one CTA per (sequence, head, value
-// tile), dS kept in fp32 registers), tc_bwd_state (chunk-parallel, the four
-// state-side products), tc_bwd_chunk (chunk-parallel, everything else).
+// tile), dS kept in fp32 registers) and tc_bwd_chunk (chunk-parallel: first the
+// state-side products dO S^T, dU S^T, U dS^T and rowsum(dS * S), then the rest).
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -231,126 +231,6 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 
-// ============================================================== tc_bwd_state
-template <int D>
-struct BStateSmem {
-    static constexpr int kTile = 64 * D * 2, kDD = D * D * 2;
-    static constexpr int kdO = 0, kS = kTile, kdS = kS + kDD, kU = kdS + kDD, kdU = kU + kTile;
-    static constexpr int kBytes = kdU + kTile + 1024;
-};
-
-template <int D>
-__global__ void __launch_bounds__(128, 1)
-    tc_bwd_state_kernel(const __grid_constant__ CUtensorMap mdo, const Params p, const TcLayout L) {
-    using S = BStateSmem<D>;
-    constexpr int kTile = S::kTile, kDD = S::kDD;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = align1024(smem_raw);
-    uint8_t* dOs = sm + S::kdO;
-    uint8_t* Ss = sm + S::kS;
-    uint8_t* dSs = sm + S::kdS;
-    uint8_t* Us = sm + S::kU;
-    uint8_t* dUs = sm + S::kdU;
-    __shared__ uint64_t bar_ld, bar_mma;
-    __shared__ uint32_t tmem_base;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    int seq, row0, len;
-    chunk_info(p, chunk, seq, row0, len);
-    const size_t rec = (size_t)chunk * p.H + h;
-
-    if (tid == 0) {
-        mbar_init(&bar_ld, 1);
-        mbar_init(&bar_mma, 1);
-        fence_barrier_init();
-        prefetch_tmap(&mdo);
-    }
-    if (warp == 0) {
-        tmem_alloc(&tmem_base, 256);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = tmem_base;
-    const uint32_t tl = warp_lane_base(tm);
-    const int r = m64_row();
-    bool ok = true;
-    do {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * kDD);
-            for (int kb = 0; kb < D / 64; ++kb)
-                tma_load_3d(dOs + kb * 8192, &mdo, &bar_ld, kb * 64, h, row0);
-            bulk_g2s(Ss, L.S + rec * kDD, kDD, &bar_ld);
-            bulk_g2s(dSs, L.dS + rec * kDD, kDD, &bar_ld);
-            bulk_g2s(Us, L.U + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(dUs, L.dU + rec * kTile, kTile, &bar_ld);
-        }
-        ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        zero_pad_rows(dOs, D, len);
-        fence_async_smem();
-        __syncthreads();
-        // S and dS arrive in W layout ([value][key]); U and dU as U^T / -dU^T ([value][token]).
-        // dO S^T -> [0,D) ; (-dU) S^T -> [D,2D)
-        if (tid == 0) {
-            tc_fence_after();
-            const Tile tO{smem_u32(dOs), 64}, tS{smem_u32(Ss), D}, tdU{smem_u32(dUs), D};
-            mma_tiles(tm + 0, tO, false, tS, true, 64, D, D, false);
-            mma_tiles(tm + D, tdU, true, tS, true, 64, D, D, false);
-            mma_commit(&bar_mma);
-        }
-        // dgC[c] = sum_v dS[c, v] S[c, v]  (overlaps the MMAs)
-        for (int c = tid; c < D; c += 128) {
-            float acc = 0.f;
-            for (int vv = 0; vv < D; ++vv)
-                acc = fmaf(__bfloat162float(*tile_elem(Ss, vv, c, D)),
-                           __bfloat162float(*tile_elem(dSs, vv, c, D)), acc);
-            L.dgC[rec * D + c] = acc;
-        }
-        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
-        for (int cb = 0; cb < D / 16; ++cb) {
-            float a[16], b[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld16(tl + D + cb * 16, b);
-            tmem_ld_wait();
-            if (r >= 0) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) b[j] = -b[j];
-                tile_store16(L.dQt + rec * kTile, r, cb * 16, 64, a);
-                tile_store16(L.dWyA + rec * kTile, r, cb * 16, 64, b);
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-        // U dS^T -> [0,D)
-        if (tid == 0) {
-            tc_fence_after();
-            const Tile tU{smem_u32(Us), D}, tdS{smem_u32(dSs), D};
-            mma_tiles(tm + 0, tU, true, tdS, true, 64, D, D, false);
-            mma_commit(&bar_mma);
-        }
-        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
-        for (int cb = 0; cb < D / 16; ++cb) {
-            float a[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld_wait();
-            if (r >= 0) tile_store16(L.dKC + rec * kTile, r, cb * 16, 64, a);
-        }
-    } while (0);
-    if (!ok) {
-        record_timeout(p);
-        mbar_wait(&bar_ld, 0, kWaitLimitNs);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
-}
-
 // ============================================================== tc_bwd_chunk
 // 256 threads: warps w and w+4 read the same TMEM lane quarter (the same
 // accumulator rows of an M = 64 product) and split its columns between them.
@@ -441,21 +321,23 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
 
     do {
+        // Phase A: what the state-side products need.  S sits in the Aqk / P / dG / dAqk
+        // tiles, dS in the Kb / dWy tiles and U^T in the v tile, all idle until later.
+        uint8_t* Sst = Aqs;   // [D][D] W-layout state at the chunk start
+        uint8_t* dSst = Kbs;  // [D][D] W-layout state gradient at the chunk end
+        uint8_t* Ust = Vs;    // [D][64] U^T
+        constexpr uint32_t kDD = D * D * 2;
         if (tid == 0) {
             const uint32_t gbytes = VAR == DR_KDA ? (uint32_t)len * D * 4 : 0u;
-            mbar_arrive_expect_tx(&bar_ld, 7 * kTile + 8192 + 2 * D * 4 + gbytes);
-            bulk_g2s(dWys, L.dWyA + rec * kTile, kTile, &bar_ld);
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * kDD + 8192 + D * 4 + gbytes);
             bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_ld);
-            for (int kb = 0; kb < D / 64; ++kb) {
-                tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
-                tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
-                tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
+            bulk_g2s(Ust, L.U + rec * kTile, kTile, &bar_ld);
+            bulk_g2s(Sst, L.S + rec * kDD, kDD, &bar_ld);
+            bulk_g2s(dSst, L.dS + rec * kDD, kDD, &bar_ld);
+            for (int kb = 0; kb < D / 64; ++kb)
                 tma_load_3d(dOs + kb * 8192, &mdo, &bar_ld, kb * 64, h, row0);
-            }
-            bulk_g2s(dQs, L.dQt + rec * kTile, kTile, &bar_ld);
             bulk_g2s(Ts, L.T + rec * 8192, 8192, &bar_ld);
             bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_ld);
-            bulk_g2s(dgC_s, L.dgC + rec * D, D * 4, &bar_ld);
         }
         __syncthreads();  // the expected byte count is registered before the gate rows go out
         if (VAR == DR_KDA && warp == 1) {
@@ -465,13 +347,29 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
-        zero_pad_rows(Qs, D, len);
-        zero_pad_rows(Ks, D, len);
-        zero_pad_rows(Vs, D, len);
         zero_pad_rows(dOs, D, len);
+        fence_async_smem();
+        __syncthreads();
 
-        // E1a: within-chunk cumulative log-decay (KDA: per key channel, in place in Gam;
-        // GDN: per token, with its two exponentials); rows past the end add nothing
+        // M0: dO S^T -> [0,D) ; -dU S^T -> [D,2D) ; U dS^T -> [2D,3D)
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tS{smem_u32(Sst), D}, tdS{smem_u32(dSst), D};
+            mma_tiles(tm + 0, Tile{smem_u32(dOs), 64}, false, tS, true, 64, D, D, false);
+            mma_tiles(tm + D, Tile{smem_u32(dUts), D}, true, tS, true, 64, D, D, false);
+            mma_tiles(tm + 2 * D, Tile{smem_u32(Ust), D}, true, tdS, true, 64, D, D, false);
+            mma_commit(&bar_mma);
+        }
+        // while M0 runs: dgC[c] = sum_v dS[c, v] S[c, v], and the cumulative log-decay
+        // (KDA: per key channel, in place in Gam; GDN: per token, with its two
+        // exponentials); rows past the end of the sequence add nothing
+        for (int c = tid; c < D; c += kChunkThreads) {
+            float acc = 0.f;
+            for (int vv = 0; vv < D; ++vv)
+                acc = fmaf(__bfloat162float(*tile_elem(Sst, vv, c, D)),
+                           __bfloat162float(*tile_elem(dSst, vv, c, D)), acc);
+            dgC_s[c] = acc;
+        }
         if (VAR == DR_KDA) {
             for (int c = tid; c < D; c += kChunkThreads) {
                 float G = 0.f;
@@ -502,6 +400,38 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 Eirow[2 * lane + 1] = __frcp_rn(e1);
             }
         }
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        // Phase B: q, k, v (v replaces U^T, which M0 has consumed)
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile);
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
+                tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
+            }
+        }
+        // E0: dQt -> its tile, -dWyA -> the dWy tile (dS is consumed), dKC -> its
+        // workspace image (reloaded for the last phase)
+        for (int cb = half; cb < D / 16; cb += 2) {
+            float a[16], b[16], c_[16];
+            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + D + cb * 16, b);
+            tmem_ld16(tl + 2 * D + cb * 16, c_);
+            tmem_ld_wait();
+            if (r >= 0) {
+                tile_store16(dQs, r, cb * 16, 64, a);
+                tile_store16(dWys, r, cb * 16, 64, b);
+                tile_store16(L.dKC + rec * kTile, r, cb * 16, 64, c_);
+            }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // dKC image -> bulk reload
+        ok = mbar_wait(&bar_ld, 1, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        zero_pad_rows(Qs, D, len);
+        zero_pad_rows(Ks, D, len);
+        zero_pad_rows(Vs, D, len);
         __syncthreads();
         // E1b: Qb = q e^G, Kr = k e^-G, Kb = k e^G, eight channels per step
         for (int w = tid; w < 64 * (D / 8); w += kChunkThreads) {
@@ -613,7 +543,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 float wa[16];
                 tile_load16(dWys, r, cb * 16, 64, wa);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = -wa[j] - sc * a[j];  // dWy
+                for (int j = 0; j < 16; ++j) a[j] = wa[j] - sc * a[j];  // dWy (the tile held -dWyA)
                 tile_store16(dWys, r, cb * 16, 64, a);
             }
         }
@@ -854,6 +784,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     if (!ok) {
         record_timeout(p);
         mbar_wait(&bar_ld, 0, kWaitLimitNs);
+        mbar_wait(&bar_ld, 1, kWaitLimitNs);
         mbar_wait(&bar_kc, 0, kWaitLimitNs);
     }
     tc_fence_before();
@@ -894,21 +825,6 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         if (e != cudaSuccess) return e;
     }
     if (p.num_chunks == 0) return cudaSuccess;
-    {
-        constexpr int smem = BStateSmem<D>::kBytes;
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = set_smem(tc_bwd_state_kernel<D>, smem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        {
-            TraceScope ts("tc_bwd_state", st);
-            tc_bwd_state_kernel<D><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mdo, p, L);
-        }
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     auto chunk_launch = [&](auto kernel, int smem, bool& attr) -> cudaError_t {
         if (!attr) {
             cudaError_t e = set_smem(kernel, smem);

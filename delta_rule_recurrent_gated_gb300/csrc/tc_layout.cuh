@@ -11,9 +11,8 @@
 //                       (W layout) of the state at the chunk start / of dL/d(state
 //                       at the chunk end)                       (D*D*2 bytes)
 //   gC                : [D] fp32, e^{Gamma} at the chunk's last token
-//   dQt, dWyA, dKC    : [64][D] tile images of dO S^T, dU S^T and U dS^T
-//                       (the state-side pieces of the chunk's gradient)
-//   dgC               : [D] fp32, sum over value channels of dS * S
+//   dKC               : [64][D] tile image of U dS^T, written and reread by the
+//                       backward chunk kernel
 #pragma once
 #include <cstdint>
 
@@ -22,8 +21,8 @@
 namespace dr {
 
 struct TcLayout {
-    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS, *dQt, *dWyA, *dKC;
-    float *gC, *dgC;
+    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS, *dKC;
+    float* gC;
 };
 
 __host__ __device__ inline size_t tc_align(size_t x) { return (x + 1023) & ~(size_t)1023; }
@@ -37,8 +36,8 @@ struct TcSizes {
 
 __host__ inline size_t tc_layout_bytes(size_t recs, int D) {
     TcSizes s(D);
-    return tc_align(recs * s.kd) * 10 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
-           tc_align(recs * s.g) * 2;
+    return tc_align(recs * s.kd) * 8 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
+           tc_align(recs * s.g);
 }
 
 __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
@@ -56,11 +55,8 @@ __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
     L.T = take(recs * s.cc);
     L.S = take(recs * s.dd);
     L.dS = take(recs * s.dd);
-    L.dQt = take(recs * s.kd);
-    L.dWyA = take(recs * s.kd);
     L.dKC = take(recs * s.kd);
     L.gC = reinterpret_cast<float*>(take(recs * s.g));
-    L.dgC = reinterpret_cast<float*>(take(recs * s.g));
     return L;
 }
 
