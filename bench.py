@@ -55,11 +55,10 @@ def kernel_bytes(name, w, N):
         return recs * (5 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
     if name == "tc_scan_bwd":        # KC, Qt, Wy, gC, dO in; dU, dS out
         return recs * (3 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
-    if name == "tc_bwd_state":       # dO, S, dS, U, dU in; dQt, dWyA, dKC, dgC out
-        return th * D * 2 + recs * (2 * dd + 2 * tile) + recs * (3 * tile + D * 4)
-    if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, dQt, T, gC, dgC, dWyA, dU, dKC in;
-        return (th * (4 * D * 2 + 4 + g) + recs * (4 * tile + 8192 + 2 * D * 4)
-                + th * (3 * D * 2 + 4 + g))   # dq, dk, dv, dbeta, dg out
+    if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, U^T, -dU^T, S, dS, T, gC in;
+        return (th * (4 * D * 2 + 4 + g) + recs * (2 * tile + 2 * dd + 8192 + D * 4)
+                + recs * 2 * tile                       # dKC image written and reread
+                + th * (3 * D * 2 + 4 + g))             # dq, dk, dv, dbeta, dg out
     return 0
 
 
