@@ -64,10 +64,12 @@ struct PrepSmem {
     static constexpr int kBytes = kGL + D * 4 + 1024;    // + alignment slack
 };
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;
+// warps w and w + 4 (when present) read the same TMEM lanes and split the columns
+constexpr int kHalves = kPrepThreads / 128;
 
 template <int D, int VAR>
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const Params p, const TcLayout L) {
     using S = PrepSmem<D>;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         tc_fence_after();
 
         // A = diag(beta) strict_lower(Gram) (fp32) and the masked Aqk tile
-        for (int cb = half; cb < 4; cb += 2) {
+        for (int cb = half; cb < 4; cb += kHalves) {
             float g16[16], a16[16];
             tmem_ld16(tl + cb * 16, g16);
             tmem_ld16(tl + 64 + cb * 16, a16);
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         {
             uint8_t* wy_img = L.Wy + rec * kTile;
             __nv_bfloat16* utT = reinterpret_cast<__nv_bfloat16*>(L.UtT + rec * kTile);
-            for (int cb = half; cb < D / 16; cb += 2) {
+            for (int cb = half; cb < D / 16; cb += kHalves) {
                 float w16[16], u16[16];
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld16(tl + D + cb * 16, u16);
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             uint8_t* qt_img = L.Qt + rec * kTile;
             __nv_bfloat16* otT = reinterpret_cast<__nv_bfloat16*>(L.OtT + rec * kTile);
             const float sc = p.scale;
-            for (int cb = half; cb < D / 16; cb += 2) {
+            for (int cb = half; cb < D / 16; cb += kHalves) {
                 float w16[16], u16[16], qb[16];
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld16(tl + D + cb * 16, u16);
