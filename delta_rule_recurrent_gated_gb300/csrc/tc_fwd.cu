@@ -56,20 +56,13 @@ struct PrepSmem {
     static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kX = 3 * kTile, kY = 4 * kTile;
     static constexpr int kAq = 5 * kTile, kT = kAq + 8192;
     static constexpr int kAf = (D == 128) ? kX : kT + 8192;  // fp32 [64][64] (16 KB)
-    // fp32 [64][64] blocks of T during the inversion (16 KB): the k tile once the Gram
-    // products are done (D = 128), else a region of its own
-    static constexpr int kTf = (D == 128) ? kK : kAf + 16384;
-    static constexpr int kBeta = (D == 128) ? kT + 8192 : kTf + 16384;
+    static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384;
     static constexpr int kGL = kBeta + 256;              // [D] fp32 Gamma at the last token
     static constexpr int kBytes = kGL + D * 4 + 1024;    // + alignment slack
 };
 
-constexpr int kPrepThreads = 128;
-// warps w and w + 4 (when present) read the same TMEM lanes and split the columns
-constexpr int kHalves = kPrepThreads / 128;
-
 template <int D, int VAR>
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(128, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const Params p, const TcLayout L) {
     using S = PrepSmem<D>;
@@ -89,7 +82,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base;
 
-    const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int chunk = blockIdx.x, h = blockIdx.y;
     int seq, row0, len;
     chunk_info(p, chunk, seq, row0, len);
@@ -132,7 +125,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         {
             const int pad = 64 - len;
             const int per_tile = (D / 64) * pad * 8;
-            for (int w = tid; w < 3 * per_tile; w += kPrepThreads) {
+            for (int w = tid; w < 3 * per_tile; w += 128) {
                 const int t = w / per_tile, rem = w % per_tile;
                 const int kb = rem / (pad * 8), rr = len + (rem % (pad * 8)) / 8, ch = rem % 8;
                 uint8_t* base = (t == 0 ? Qs : t == 1 ? Ks : Vs) + kb * 8192;
@@ -170,7 +163,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                     }
                 }
                 __syncthreads();
-                for (int w = tid; w < 32 * (D / 8); w += kPrepThreads) {
+                for (int w = tid; w < 32 * (D / 8); w += 128) {
                     const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
                     const uint32_t off = sw128_offset(i, c8, 64);
                     float q8[8], k8[8], v8[8];
@@ -224,7 +217,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_after();
 
         // A = diag(beta) strict_lower(Gram) (fp32) and the masked Aqk tile
-        for (int cb = half; cb < 4; cb += kHalves) {
+        for (int cb = 0; cb < 4; ++cb) {
             float g16[16], a16[16];
             tmem_ld16(tl + cb * 16, g16);
             tmem_ld16(tl + 64 + cb * 16, a16);
@@ -243,64 +236,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // T = (I + A)^{-1}, blocked 2 x 2 with 32-row blocks:
-        //   T11 = (I + A11)^{-1}, T22 = (I + A22)^{-1}  (threads 0..63, one column each,
-        //   right-looking forward substitution);  T21 = -T22 (A21 T11)  (all threads)
-        {
-            float* Tf = reinterpret_cast<float*>(sm + S::kTf);  // row-major [64][64]
-            float* Yf = reinterpret_cast<float*>(Ts);           // [32][32] A21 T11
-            if (tid < 64) {
-                const int b = tid & 32, n = tid & 31;  // diagonal block origin, column
-                float x[32];
+        // T = (I + A)^{-1}: thread n solves column n of (I + A) x = e_n, right-looking:
+        // once x_j is final, every later row's partial sum takes its A[i][j] x_j term,
+        // so the dependent chain is one FMA per row
+        if (tid < 64) {
+            const int n = tid;
+            float x[64];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = (i == n) ? 1.f : 0.f;
+            for (int i = 0; i < 64; ++i) x[i] = (i == n) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j < 31; ++j) {
-                    const float xj = x[j];
+            for (int j = 0; j < 63; ++j) {
+                const float xj = x[j];
 #pragma unroll
-                    for (int i4 = (j + 1) & ~3; i4 < 32; i4 += 4) {
-                        const float4 a = *reinterpret_cast<const float4*>(&Af[(b + j) * 64 + b + i4]);
-                        if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
-                        if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
-                        if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
-                        if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
-                    }
+                for (int i4 = (j + 1) & ~3; i4 < 64; i4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(&Af[j * 64 + i4]);
+                    if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
+                    if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
+                    if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
+                    if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
                 }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) Tf[(b + i) * 64 + b + n] = x[i];
             }
-            __syncthreads();
-            // Y = A21 T11: Y[i][j] = sum_{k >= j} A[32+i][k] T11[k][j]
-            for (int o = tid; o < 32 * 32; o += kPrepThreads) {
-                const int i = o >> 5, j = o & 31;
-                float acc = 0.f;
-                for (int k = j; k < 32; ++k) acc = fmaf(Af[k * 64 + 32 + i], Tf[k * 64 + j], acc);
-                Yf[i * 32 + j] = acc;
-            }
-            __syncthreads();
-            // T21[i][j] = -sum_{k <= i} T22[i][k] Y[k][j]; write the whole T as bf16
-            for (int o = tid; o < 32 * 32; o += kPrepThreads) {
-                const int i = o >> 5, j = o & 31;
-                float acc = 0.f;
-                for (int k = 0; k <= i; ++k) acc = fmaf(Tf[(32 + i) * 64 + 32 + k], Yf[k * 32 + j], acc);
-                Tf[(32 + i) * 64 + j] = -acc;
-            }
-            __syncthreads();
             uint8_t* t_img = L.T + rec * 8192;
-            for (int o = tid; o < 64 * 8; o += kPrepThreads) {
-                const int i = o >> 3, c8 = (o & 7) * 8;
-                uint32_t w4[4];
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    // the block above the diagonal blocks (rows < 32, columns >= 32) is zero
-                    const int c = c8 + 2 * t;
-                    const bool z = (i < 32 && c >= 32);
-                    w4[t] = pack_bf16(z ? 0.f : Tf[i * 64 + c], z ? 0.f : Tf[i * 64 + c + 1]);
-                }
-                const uint4 u = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                const uint32_t off = sw128_offset(i, c8, 64);
-                *reinterpret_cast<uint4*>(Ts + off) = u;
-                *reinterpret_cast<uint4*>(t_img + off) = u;
+            for (int i = 0; i < 64; ++i) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(x[i]);
+                const uint32_t off = sw128_offset(i, n, 64);
+                *reinterpret_cast<__nv_bfloat16*>(Ts + off) = b;
+                *reinterpret_cast<__nv_bfloat16*>(t_img + off) = b;
             }
         }
         fence_async_smem();
@@ -321,7 +283,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         {
             uint8_t* wy_img = L.Wy + rec * kTile;
             __nv_bfloat16* utT = reinterpret_cast<__nv_bfloat16*>(L.UtT + rec * kTile);
-            for (int cb = half; cb < D / 16; cb += kHalves) {
+            for (int cb = 0; cb < D / 16; ++cb) {
                 float w16[16], u16[16];
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld16(tl + D + cb * 16, u16);
@@ -356,7 +318,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             uint8_t* qt_img = L.Qt + rec * kTile;
             __nv_bfloat16* otT = reinterpret_cast<__nv_bfloat16*>(L.OtT + rec * kTile);
             const float sc = p.scale;
-            for (int cb = half; cb < D / 16; cb += kHalves) {
+            for (int cb = 0; cb < D / 16; ++cb) {
                 float w16[16], u16[16], qb[16];
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld16(tl + D + cb * 16, u16);
@@ -640,7 +602,7 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
     }
     if (p.num_chunks == 0) return cudaSuccess;
     TraceScope ts("tc_prep", st);
-    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), kPrepThreads, smem, st>>>(mq, mk, mv, p, L);
+    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, p, L);
     return cudaGetLastError();
 }
 
