@@ -460,33 +460,25 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        for (int g = 0; g < 4; ++g) {
-            float acc[16], oacc[16];
+        // U = Ut - W Wy^T  (on the serial chain: it feeds the state update)
+        for (int g = 0; g < 4; g += 2) {
+            float acc[16], acc2[16];
             tmem_ld16(tl + g * 16, acc);
-            tmem_ld16(tl + 64 + g * 16, oacc);
+            tmem_ld16(tl + (g + 1) * 16, acc2);
             tmem_ld_wait();
             if (r >= 0) {
-                float ut[16], ot[16];
+                float ut[16];
                 const uint4* up = reinterpret_cast<const uint4*>(st + S::kUt + r * 128 + g * 32);
-                const uint4* op = reinterpret_cast<const uint4*>(st + S::kOt + r * 128 + g * 32);
                 unpack8(up[0], ut);
                 unpack8(up[1], ut + 8);
-                unpack8(op[0], ot);
-                unpack8(op[1], ot + 8);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    acc[j] = ut[j] - acc[j];    // U
-                    oacc[j] = ot[j] + oacc[j];  // O
-                }
+                for (int j = 0; j < 16; ++j) acc[j] = ut[j] - acc[j];
                 tile_store16(Us, r, g * 16, BV, acc);
-                if (write_o) {
+                unpack8(up[2], ut);
+                unpack8(up[3], ut + 8);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = g * 16 + j;
-                        if (i < len)
-                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype, oacc[j]);
-                    }
-                }
+                for (int j = 0; j < 16; ++j) acc2[j] = ut[j] - acc2[j];
+                tile_store16(Us, r, (g + 1) * 16, BV, acc2);
             }
         }
         fence_async_smem();
@@ -502,6 +494,27 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
             bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
             bulk_commit();
         }
+        // O = Ot + W Qt^T while the state-update product runs
+        if (write_o) {
+            tc_fence_after();
+            for (int g = 0; g < 4; ++g) {
+                float oacc[16];
+                tmem_ld16(tl + 64 + g * 16, oacc);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    float ot[16];
+                    const uint4* op = reinterpret_cast<const uint4*>(st + S::kOt + r * 128 + g * 32);
+                    unpack8(op[0], ot);
+                    unpack8(op[1], ot + 8);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = g * 16 + j;
+                        if (i < len)
+                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype, ot[j] + oacc[j]);
+                    }
+                }
+            }
+        }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
         if (tid == 0) bulk_wait_read();  // Ws and Us are rewritten below / next chunk
         if (__syncthreads_or(!ok)) break;
@@ -509,17 +522,23 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
 
         const float* gCs = reinterpret_cast<const float*>(st + S::kG);
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb) {
-            float acc[16];
+        for (int cb = 0; cb < D / 16; cb += 2) {
+            float acc[16], acc2[16];
             tmem_ld16(tl + 128 + cb * 16, acc);
+            tmem_ld16(tl + 128 + (cb + 1) * 16, acc2);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int c = cb * 16 + j;
                 W[c] = fmaf(W[c], gCs[c], acc[j]);
                 acc[j] = W[c];
+                W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                acc2[j] = W[c + 16];
             }
-            if (r >= 0) tile_store16(Ws, r, cb * 16, BV, acc);
+            if (r >= 0) {
+                tile_store16(Ws, r, cb * 16, BV, acc);
+                tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
+            }
         }
         fence_async_smem();
         tc_fence_before();
