@@ -753,31 +753,50 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         __syncthreads();
 
-        // E8: dg = reverse cumulative sum of dGamma within the chunk
+        // E8: dg_i = (dgC e^{Gamma_last} + sum_rows dKC KC) + sum_{j >= i} dGamma_j
         if (VAR == DR_KDA) {
-            for (int c = tid; c < D; c += kChunkThreads) {
-                float run = dgC_s[c] * gC_s[c];
-                const float* Fa = reinterpret_cast<const float*>(Ts);
-                for (int i = 0; i < 64; ++i) run += Fa[i * D + c];
-                for (int i = len - 1; i >= 0; --i) {
+            // P threads per key channel, each owning 64 / P consecutive rows
+            constexpr int P = kChunkThreads / D, R = 64 / P;
+            const int c = tid % D, pt = tid / D, i0 = pt * R;
+            const float* Fa = reinterpret_cast<const float*>(Ts);
+            float* Sp = reinterpret_cast<float*>(Ts + 64 * D * 4);  // [P][D] row sums of dGamma
+            float* Fp = Sp + P * D;                                 // [P][D] row sums of dKC KC
+            float sg = 0.f, sf = 0.f;
+            for (int i = i0; i < i0 + R; ++i) {
+                sf += Fa[i * D + c];
+                if (i < len) sg += Gam[i * D + c];
+            }
+            Sp[pt * D + c] = sg;
+            Fp[pt * D + c] = sf;
+            __syncthreads();
+            float run = dgC_s[c] * gC_s[c];
+            for (int q = 0; q < P; ++q) {
+                run += Fp[q * D + c];
+                if (q > pt) run += Sp[q * D + c];
+            }
+            for (int i = i0 + R - 1; i >= i0; --i) {
+                if (i < len) {
                     run += Gam[i * D + c];
                     p.dg[((size_t)(row0 + i) * p.H + h) * D + c] = run;
                 }
             }
         } else if (VAR == DR_GDN) {
             if (warp == 0) {
-                float e = 0.f;
-                for (int c = threadIdx.x; c < D; c += 32) e += dgC_s[c] * gC_s[c];
+                const int lane = tid & 31;
+                float e = Grow[lane] + Grow[lane + 32];  // per-row sums of dKC KC
+                for (int c = lane; c < D; c += 32) e += dgC_s[c] * gC_s[c];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-                if (threadIdx.x == 0) {
-                    for (int i = 0; i < 64; ++i) e += Grow[i];
-                    float run = e;
-                    for (int i = len - 1; i >= 0; --i) {
-                        run += rowsum[i];
-                        p.dg[(size_t)(row0 + i) * p.H + h] = run;
-                    }
+                const float a0 = 2 * lane < len ? rowsum[2 * lane] : 0.f;
+                const float a1 = 2 * lane + 1 < len ? rowsum[2 * lane + 1] : 0.f;
+                float x = a0 + a1;  // suffix sum over lanes >= this one
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_down_sync(0xffffffffu, x, o);
+                    if (lane + o < 32) x += y;
                 }
+                if (2 * lane < len) p.dg[(size_t)(row0 + 2 * lane) * p.H + h] = e + x;
+                if (2 * lane + 1 < len) p.dg[(size_t)(row0 + 2 * lane + 1) * p.H + h] = e + x - a0;
             }
         }
     } while (0);
