@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     uint8_t* B8a = sm + S::kB8a;  // P, then X = dT T^T
     uint8_t* B8b = sm + S::kB8b;  // dT, then dG
     uint8_t* dAqs = sm + S::kdAq; // dAqk
-    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g, Gamma, then dGamma
+    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g, Gamma, e^Gamma, dGamma
     float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
     float* gC_s = beta_s + 64;
     float* dgC_s = gC_s + D;
@@ -371,14 +371,23 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dgC_s[c] = acc;
         }
         if (VAR == DR_KDA) {
-            for (int c = tid; c < D; c += kChunkThreads) {
-                float G = 0.f;
+            // kChunkThreads / D threads per channel, each a contiguous block of rows, then
+            // every block adds the totals of the blocks above it
+            constexpr int P = kChunkThreads / D, R = 64 / P;
+            const int c = tid % D, pt = tid / D;
+            float* tot = reinterpret_cast<float*>(Qs);  // [P][D]; q arrives only after M0
+            float G = 0.f;
 #pragma unroll 8
-                for (int i = 0; i < 64; ++i) {
-                    if (i < len) G += Gam[i * D + c];
-                    Gam[i * D + c] = G;
-                }
+            for (int i = pt * R; i < pt * R + R; ++i) {
+                if (i < len) G += Gam[i * D + c];
+                Gam[i * D + c] = G;
             }
+            tot[pt * D + c] = G;
+            __syncthreads();
+            float off = 0.f;
+            for (int q = 0; q < pt; ++q) off += tot[q * D + c];
+            if (pt > 0)
+                for (int i = pt * R; i < pt * R + R; ++i) Gam[i * D + c] += off;
         } else if (VAR == DR_GDN) {
             if (warp == 0) {
                 const int lane = tid & 31;
@@ -447,14 +456,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             unpack8(qv, q8);
             unpack8(kv, k8);
             if (VAR == DR_KDA) {
-                const float4 g0 = *reinterpret_cast<const float4*>(&Gam[i * D + c8]);
-                const float4 g1 = *reinterpret_cast<const float4*>(&Gam[i * D + c8 + 4]);
+                float4* gp = reinterpret_cast<float4*>(&Gam[i * D + c8]);
+                const float4 g0 = gp[0], g1 = gp[1];
                 const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     e8[j] = expf(G8[j]);
                     i8[j] = __frcp_rn(e8[j]);
                 }
+                gp[0] = make_float4(e8[0], e8[1], e8[2], e8[3]);  // e^Gamma from here on
+                gp[1] = make_float4(e8[4], e8[5], e8[6], e8[7]);
             } else {
                 const float e = Erow[i], ei = Eirow[i];
 #pragma unroll
@@ -709,7 +720,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                         const int c = cb * 16 + j;
                         float e = er, ei = eir;
                         if (VAR == DR_KDA) {
-                            e = expf(Gam[r * D + c]);
+                            e = Gam[r * D + c];  // e^Gamma, stored by the decay pass
                             ei = __frcp_rn(e);
                         }
                         const float gc = gC_s[c];

@@ -68,3 +68,12 @@ def test_backward_recompute_matches_reuse(variant):
     b = run_gpu(w, x, reuse=False)
     for n in ("dq", "dk", "dv", "dbeta", "dg", "dh0"):
         assert np.array_equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("io,d,chunk", [("bf16", 128, 64), ("f32", 32, 16)])
+def test_fwd_bwd_read_scale(variant, io, d, chunk):
+    w = inputs.replace(inputs.small(variant, B=2, T=150, H=2, dk=d, dv=d, chunk=chunk, io=io),
+                       scale=0.375)
+    x = inputs.make(w, seed=10)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
