@@ -191,6 +191,10 @@ __device__ __forceinline__ void sw128_store8(uint8_t* tile, int row, int k, int 
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, k, rows)) = v;
 }
 
+// Reciprocal through the hardware approximation (about 1 ulp): used for e^{-Gamma}
+// from e^{Gamma}, where the result is rounded to bf16 or multiplies bf16 data.
+__device__ __forceinline__ float fast_rcp(float x) { return __fdividef(1.f, x); }
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);

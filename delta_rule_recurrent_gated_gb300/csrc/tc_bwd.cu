@@ -402,11 +402,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 const float g0 = x - a1, g1 = x;
                 Grow[2 * lane] = g0;
                 Grow[2 * lane + 1] = g1;
-                const float e0 = expf(g0), e1 = expf(g1);
+                const float e0 = __expf(g0), e1 = __expf(g1);
                 Erow[2 * lane] = e0;
                 Erow[2 * lane + 1] = e1;
-                Eirow[2 * lane] = __frcp_rn(e0);
-                Eirow[2 * lane + 1] = __frcp_rn(e1);
+                Eirow[2 * lane] = fast_rcp(e0);
+                Eirow[2 * lane + 1] = fast_rcp(e1);
             }
         }
         ok = mma_done();
@@ -461,8 +461,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    e8[j] = expf(G8[j]);
-                    i8[j] = __frcp_rn(e8[j]);
+                    e8[j] = __expf(G8[j]);
+                    i8[j] = fast_rcp(e8[j]);
                 }
                 gp[0] = make_float4(e8[0], e8[1], e8[2], e8[3]);  // e^Gamma from here on
                 gp[1] = make_float4(e8[4], e8[5], e8[6], e8[7]);
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                         float e = er, ei = eir;
                         if (VAR == DR_KDA) {
                             e = Gam[r * D + c];  // e^Gamma, stored by the decay pass
-                            ei = __frcp_rn(e);
+                            ei = fast_rcp(e);
                         }
                         const float gc = gC_s[c];
                         const float dQb = sc * dqt[j] + dq_[j];

@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(128, 1)
                         if (VAR != DR_DELTANET) {
 #pragma unroll
                             for (int t = 0; t < 2; ++t) {
-                                e[t] = expf(Gb[ii * D + c8 + 2 * j + t]);
-                                ei[t] = __frcp_rn(e[t]);
+                                e[t] = __expf(Gb[ii * D + c8 + 2 * j + t]);
+                                ei[t] = fast_rcp(e[t]);
                                 ec[t] = GLs[c8 + 2 * j + t] * ei[t];
                             }
                         }
@@ -362,9 +362,17 @@ struct ScanSmem {
     static constexpr uint32_t kStageTx = 3 * kTile + 2 * BV * 128 + D * 4;
 };
 
+// 256 threads: warps 0-3 carry the state chain (U, the state-update product, W);
+// warps 4-7 read the output accumulator of the same rows and store o meanwhile.
+constexpr int kScanFwdThreads = 256;
+
+__device__ __forceinline__ void state_warps_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 template <int D, int BV>
-__global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, const TcLayout L,
-                                                             int write_o) {
+__global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const Params p, const TcLayout L,
+                                                                         int write_o) {
     using S = ScanSmem<D, BV>;
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
@@ -373,8 +381,10 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     uint8_t* Us = sm + S::kUs;
     __shared__ uint64_t bar_ld[2], bar_mma;
     __shared__ uint32_t tmem_base;
+    __shared__ int s_fail;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool state_warp = warp < 4;
     const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
     const int v0 = blockIdx.y * BV;
     int c0, nc, srow, slen;
@@ -385,6 +395,7 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         mbar_init(&bar_ld[1], 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
+        s_fail = 0;
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = (BV == 128) ? tid : m64_row();  // value row of this thread (or -1)
+    const int r = (BV == 128) ? (tid & 127) : m64_row();  // value row (or -1)
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
     int issued[2] = {0, 0}, waited[2] = {0, 0};   // bulk-load phases per stage (thread 0)
@@ -415,10 +426,11 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
     };
     if (tid == 0 && nc > 0) load_chunk(0);
 
-    float W[D];  // W[v, :] = S[:, v], fp32
+    float W[D];  // W[v, :] = S[:, v], fp32 (state warps)
 #pragma unroll
-    for (int c = 0; c < D; ++c) W[c] = (p.h0 && r >= 0) ? p.h0[state_off + (size_t)c * D + v] : 0.f;
-    if (r >= 0) {
+    for (int c = 0; c < D; ++c)
+        W[c] = (p.h0 && r >= 0 && state_warp) ? p.h0[state_off + (size_t)c * D + v] : 0.f;
+    if (r >= 0 && state_warp) {
 #pragma unroll
         for (int cb = 0; cb < D / 16; ++cb) {
             float t[16];
@@ -460,43 +472,69 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        // U = Ut - W Wy^T  (on the serial chain: it feeds the state update)
-        for (int g = 0; g < 4; g += 2) {
-            float acc[16], acc2[16];
-            tmem_ld16(tl + g * 16, acc);
-            tmem_ld16(tl + (g + 1) * 16, acc2);
-            tmem_ld_wait();
-            if (r >= 0) {
-                float ut[16];
-                const uint4* up = reinterpret_cast<const uint4*>(st + S::kUt + r * 128 + g * 32);
-                unpack8(up[0], ut);
-                unpack8(up[1], ut + 8);
+        if (state_warp) {
+            // U = Ut - W Wy^T
+            for (int g = 0; g < 4; g += 2) {
+                float acc[16], acc2[16];
+                tmem_ld16(tl + g * 16, acc);
+                tmem_ld16(tl + (g + 1) * 16, acc2);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    float ut[16];
+                    const uint4* up = reinterpret_cast<const uint4*>(st + S::kUt + r * 128 + g * 32);
+                    unpack8(up[0], ut);
+                    unpack8(up[1], ut + 8);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = ut[j] - acc[j];
-                tile_store16(Us, r, g * 16, BV, acc);
-                unpack8(up[2], ut);
-                unpack8(up[3], ut + 8);
+                    for (int j = 0; j < 16; ++j) acc[j] = ut[j] - acc[j];
+                    tile_store16(Us, r, g * 16, BV, acc);
+                    unpack8(up[2], ut);
+                    unpack8(up[3], ut + 8);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc2[j] = ut[j] - acc2[j];
-                tile_store16(Us, r, (g + 1) * 16, BV, acc2);
+                    for (int j = 0; j < 16; ++j) acc2[j] = ut[j] - acc2[j];
+                    tile_store16(Us, r, (g + 1) * 16, BV, acc2);
+                }
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // U^T KC -> cols [128, 128+D); U^T rows [v0, v0+BV) of the U^T image
-        if (tid == 0) {
+            fence_async_smem();
+            tc_fence_before();
+            state_warps_sync();
+            // U^T KC -> cols [128, 128+D); U^T rows [v0, v0+BV) of the U^T image
+            if (tid == 0) {
+                tc_fence_after();
+                const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(st + S::kKC), 64};
+                mma_tiles(tm + 128, tU, false, tKC, true, BV, D, 64, false);
+                mma_commit(&bar_mma);
+                bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
+                bulk_commit();
+            }
+            const bool ok2 = mbar_wait(&bar_mma, 1, kWaitLimitNs);
+            if (tid == 0) bulk_wait_read();  // Ws and Us are rewritten below / next chunk
+            state_warps_sync();
             tc_fence_after();
-            const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(st + S::kKC), 64};
-            mma_tiles(tm + 128, tU, false, tKC, true, BV, D, 64, false);
-            mma_commit(&bar_mma);
-            bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
-            bulk_commit();
-        }
-        // O = Ot + W Qt^T while the state-update product runs
-        if (write_o) {
-            tc_fence_after();
+            if (!ok2) s_fail = 1;
+            const float* gCs = reinterpret_cast<const float*>(st + S::kG);
+#pragma unroll
+            for (int cb = 0; cb < D / 16; cb += 2) {
+                float acc[16], acc2[16];
+                tmem_ld16(tl + 128 + cb * 16, acc);
+                tmem_ld16(tl + 128 + (cb + 1) * 16, acc2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int c = cb * 16 + j;
+                    W[c] = fmaf(W[c], gCs[c], acc[j]);
+                    acc[j] = W[c];
+                    W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                    acc2[j] = W[c + 16];
+                }
+                if (r >= 0) {
+                    tile_store16(Ws, r, cb * 16, BV, acc);
+                    tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
+                }
+            }
+        } else if (write_o) {
+            // O = Ot + W Qt^T for rows r, while the state chain proceeds
+            const size_t stride = (size_t)p.H * D;
+            const size_t base = ((size_t)row0 * p.H + h) * D + v;
             for (int g = 0; g < 4; ++g) {
                 float oacc[16];
                 tmem_ld16(tl + 64 + g * 16, oacc);
@@ -506,47 +544,31 @@ __global__ void __launch_bounds__(128, 1) tc_scan_fwd_kernel(const Params p, con
                     const uint4* op = reinterpret_cast<const uint4*>(st + S::kOt + r * 128 + g * 32);
                     unpack8(op[0], ot);
                     unpack8(op[1], ot + 8);
+                    const int jmax = min(16, len - g * 16);
+                    if (p.out_dtype == DR_F32) {
+                        float* dst = static_cast<float*>(p.o) + base + (size_t)g * 16 * stride;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = g * 16 + j;
-                        if (i < len)
-                            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * D + v, p.out_dtype, ot[j] + oacc[j]);
+                        for (int j = 0; j < 16; ++j)
+                            if (j < jmax) dst[(size_t)j * stride] = ot[j] + oacc[j];
+                    } else {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + base + (size_t)g * 16 * stride;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < jmax) dst[(size_t)j * stride] = __float2bfloat16_rn(ot[j] + oacc[j]);
                     }
                 }
             }
         }
-        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
-        if (tid == 0) bulk_wait_read();  // Ws and Us are rewritten below / next chunk
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
-
-        const float* gCs = reinterpret_cast<const float*>(st + S::kG);
-#pragma unroll
-        for (int cb = 0; cb < D / 16; cb += 2) {
-            float acc[16], acc2[16];
-            tmem_ld16(tl + 128 + cb * 16, acc);
-            tmem_ld16(tl + 128 + (cb + 1) * 16, acc2);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int c = cb * 16 + j;
-                W[c] = fmaf(W[c], gCs[c], acc[j]);
-                acc[j] = W[c];
-                W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
-                acc2[j] = W[c + 16];
-            }
-            if (r >= 0) {
-                tile_store16(Ws, r, cb * 16, BV, acc);
-                tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
-            }
-        }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(s_fail != 0)) {
+            ok = false;
+            break;
+        }
     }
 
     if (ok) {
-        if (p.hT && r >= 0) {
+        if (p.hT && r >= 0 && state_warp) {
 #pragma unroll
             for (int c = 0; c < D; ++c) p.hT[state_off + (size_t)c * D + v] = W[c];
         }
@@ -636,7 +658,7 @@ cudaError_t launch_scan_fwd(const Params& p, const TcLayout& L, cudaStream_t st,
     }
     if (p.N * p.H == 0) return cudaSuccess;
     TraceScope ts("tc_scan_fwd", st);
-    tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), 128, smem, st>>>(p, L, write_o ? 1 : 0);
+    tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), kScanFwdThreads, smem, st>>>(p, L, write_o ? 1 : 0);
     return cudaGetLastError();
 }
 
