@@ -244,7 +244,8 @@ struct BChunkSmem {
     static constexpr int kT = 8 * kTile, kAq = kT + kCC, kB8a = kAq + kCC, kB8b = kB8a + kCC,
                          kdAq = kB8b + kCC;
     static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][D]
-    static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * D * 4 : 0);
+    static constexpr int kGS = D + 4;  // row stride of the per-channel fp32 arrays
+    static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * kGS * 4 : 0);
     // small arrays: beta[64], e^{Gamma_last}[D], dgC[D], rowsum[64], Gamma_row[64],
     // e^{Gamma_row}[64], e^{-Gamma_row}[64], per-row partials of the second warp half [3][64]
     static constexpr int kBytes = kSmall + (64 * 8 + D * 2) * 4 + 1024;
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         __syncthreads();  // the expected byte count is registered before the gate rows go out
         if (VAR == DR_KDA && warp == 1) {
             for (int i = tid & 31; i < len; i += 32)
-                bulk_g2s(Gam + i * D, p.g + ((size_t)(row0 + i) * p.H + h) * D, D * 4, &bar_ld);
+                bulk_g2s(Gam + i * S::kGS, p.g + ((size_t)(row0 + i) * p.H + h) * D, D * 4, &bar_ld);
         }
         if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
@@ -379,15 +380,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             float G = 0.f;
 #pragma unroll 8
             for (int i = pt * R; i < pt * R + R; ++i) {
-                if (i < len) G += Gam[i * D + c];
-                Gam[i * D + c] = G;
+                if (i < len) G += Gam[i * S::kGS + c];
+                Gam[i * S::kGS + c] = G;
             }
             tot[pt * D + c] = G;
             __syncthreads();
             float off = 0.f;
             for (int q = 0; q < pt; ++q) off += tot[q * D + c];
             if (pt > 0)
-                for (int i = pt * R; i < pt * R + R; ++i) Gam[i * D + c] += off;
+                for (int i = pt * R; i < pt * R + R; ++i) Gam[i * S::kGS + c] += off;
         } else if (VAR == DR_GDN) {
             if (warp == 0) {
                 const int lane = tid & 31;
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             unpack8(qv, q8);
             unpack8(kv, k8);
             if (VAR == DR_KDA) {
-                float4* gp = reinterpret_cast<float4*>(&Gam[i * D + c8]);
+                float4* gp = reinterpret_cast<float4*>(&Gam[i * S::kGS + c8]);
                 const float4 g0 = gp[0], g1 = gp[1];
                 const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
@@ -691,7 +692,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // E7: the decay chain, per row; each warp half takes every other 16-column block
         {
             // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows, in
-            // the T / Aqk / P / dG / dAqk tiles (40 KB contiguous), all consumed by now
+            // the T / Aqk / P / dG / dAqk tiles (40 KB contiguous), all consumed by now;
+            // rows padded to kGS floats so that lanes owning different rows hit different banks
             float* Fa = reinterpret_cast<float*>(Ts);
             float grow = 0.f, frow = 0.f;
             float er = 1.f, eir = 1.f;
@@ -720,7 +722,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                         const int c = cb * 16 + j;
                         float e = er, ei = eir;
                         if (VAR == DR_KDA) {
-                            e = Gam[r * D + c];  // e^Gamma, stored by the decay pass
+                            e = Gam[r * S::kGS + c];  // e^Gamma, stored by the decay pass
                             ei = fast_rcp(e);
                         }
                         const float gc = gC_s[c];
@@ -730,8 +732,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                         dbeta_acc = fmaf(dbk[j], kb[j], dbeta_acc);
                         const float dG = dQb * qb[j] + dKb * kb[j] - dkr[j] * kr[j] - dkc[j] * KC;
                         if (VAR == DR_KDA) {
-                            Gam[r * D + c] = dG;
-                            Fa[r * D + c] = dkc[j] * KC;
+                            Gam[r * S::kGS + c] = dG;
+                            Fa[r * S::kGS + c] = dkc[j] * KC;
                         } else if (VAR == DR_GDN) {
                             grow += dG;
                             frow = fmaf(dkc[j], KC, frow);
@@ -770,12 +772,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             constexpr int P = kChunkThreads / D, R = 64 / P;
             const int c = tid % D, pt = tid / D, i0 = pt * R;
             const float* Fa = reinterpret_cast<const float*>(Ts);
-            float* Sp = reinterpret_cast<float*>(Ts + 64 * D * 4);  // [P][D] row sums of dGamma
+            float* Sp = reinterpret_cast<float*>(Ts + 64 * S::kGS * 4);  // [P][D] row sums of dGamma
             float* Fp = Sp + P * D;                                 // [P][D] row sums of dKC KC
             float sg = 0.f, sf = 0.f;
             for (int i = i0; i < i0 + R; ++i) {
-                sf += Fa[i * D + c];
-                if (i < len) sg += Gam[i * D + c];
+                sf += Fa[i * S::kGS + c];
+                if (i < len) sg += Gam[i * S::kGS + c];
             }
             Sp[pt * D + c] = sg;
             Fp[pt * D + c] = sf;
@@ -787,7 +789,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             }
             for (int i = i0 + R - 1; i >= i0; --i) {
                 if (i < len) {
-                    run += Gam[i * D + c];
+                    run += Gam[i * S::kGS + c];
                     p.dg[((size_t)(row0 + i) * p.H + h) * D + c] = run;
                 }
             }

@@ -171,6 +171,16 @@ __global__ void __launch_bounds__(128, 1)
                     unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
                     unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
                     const float b = beta_s[i];
+                    float G8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L8[8];
+                    if (VAR != DR_DELTANET) {
+                        const float4* gp = reinterpret_cast<const float4*>(&Gb[ii * D + c8]);
+                        const float4* lp = reinterpret_cast<const float4*>(&GLs[c8]);
+                        const float4 g0 = gp[0], g1 = gp[1], l0 = lp[0], l1 = lp[1];
+                        G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
+                        G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
+                        L8[0] = l0.x; L8[1] = l0.y; L8[2] = l0.z; L8[3] = l0.w;
+                        L8[4] = l1.x; L8[5] = l1.y; L8[6] = l1.z; L8[7] = l1.w;
+                    }
                     uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -178,9 +188,9 @@ __global__ void __launch_bounds__(128, 1)
                         if (VAR != DR_DELTANET) {
 #pragma unroll
                             for (int t = 0; t < 2; ++t) {
-                                e[t] = __expf(Gb[ii * D + c8 + 2 * j + t]);
+                                e[t] = __expf(G8[2 * j + t]);
                                 ei[t] = fast_rcp(e[t]);
-                                ec[t] = GLs[c8 + 2 * j + t] * ei[t];
+                                ec[t] = L8[2 * j + t] * ei[t];
                             }
                         }
                         const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
