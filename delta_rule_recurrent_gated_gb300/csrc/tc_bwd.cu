@@ -29,6 +29,7 @@ namespace dr {
 using namespace tc;
 
 bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
+bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
 TcLayout tc_layout(const Params& p);
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
 
@@ -232,30 +233,86 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ============================================================== tc_bwd_chunk
-// 256 threads: warps w and w+4 read the same TMEM lane quarter (the same
-// accumulator rows of an M = 64 product) and split its columns between them.
+// 256 threads.  Two accumulator shapes alternate:
+//  * token-by-token products (M = 64): row i of the accumulator sits in lane
+//    16*(i/16) + i%16 of warp quarter i/16; warps w and w+4 split its columns;
+//  * channel-by-token products (M = D, the transposes of every d-wide result):
+//    channel c sits in lane c (D = 128) or in the M = 64 lane of row c (D = 64);
+//    warps w and w+4 take tokens [0,32) and [32,64).  Everything per element of
+//    the d-wide results (dv, dq, dk, KDA's dGamma and its reverse cumulative sum)
+//    then runs on full warps, with 32 consecutive channels of one token per
+//    warp store, and the sums over channels are warp transpose-reductions.
 constexpr int kChunkThreads = 256;
 
 template <int D, int VAR>
 struct BChunkSmem {
     static constexpr int kTile = 64 * D * 2, kCC = 8192;
+    // [64][D] token-row tiles: q -> Qb, k -> Kr, v, dO, Kb
+    // [D][64] channel-row tiles: U^T -> dQt^T, -dWyA^T -> dWy^T, -dU^T -> dUt^T
     static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kdQ = 4 * kTile,
                          kKb = 5 * kTile, kdWy = 6 * kTile, kdUt = 7 * kTile;
     static constexpr int kT = 8 * kTile, kAq = kT + kCC, kB8a = kAq + kCC, kB8b = kB8a + kCC,
                          kdAq = kB8b + kCC;
-    static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][D]
-    static constexpr int kGS = D + 4;  // row stride of the per-channel fp32 arrays
-    static constexpr int kSmall = kGam + (VAR == DR_KDA ? 64 * kGS * 4 : 0);
-    // small arrays: beta[64], e^{Gamma_last}[D], dgC[D], rowsum[64], Gamma_row[64],
-    // e^{Gamma_row}[64], e^{-Gamma_row}[64], per-row partials of the second warp half [3][64]
-    static constexpr int kBytes = kSmall + (64 * 8 + D * 2) * 4 + 1024;
+    static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][kGS]
+    static constexpr int kGS = D;  // row stride of the per-channel fp32 array (a dense TMA box)
+    static constexpr int kX = kGam + (VAR == DR_KDA ? 64 * kGS * 4 : 0);  // fp32 scratch, 8 KB
+    static constexpr int kSmall = kX + 8192;
+    // small arrays: beta[64], e^{Gamma_last}[D], dgC[D], dGamma per row[64],
+    // e^{Gamma} per row[64], e^{-Gamma} per row[64], dbeta partials of warps 4..7 [64]
+    static constexpr int kBytes = kSmall + (64 * 5 + D * 2) * 4 + 1024;
 };
+
+// Sum over the 32 lanes of v[lane][k] for every k: on return lane L holds the
+// sum for k = L.  Five exchange rounds, 31 shuffles, fixed order.
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int k = 0; k < s; ++k) {
+            const float send = up ? v[k] : v[k + s];
+            const float keep = up ? v[k + s] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+// A [64][D] output block staged in shared memory in the output's own element type,
+// tokens [0,32) in one buffer and [32,64) in another (a token's D values contiguous);
+// `sb` points at this thread's channel in the row of the first token of its half.
+template <int D, bool F32>
+__device__ __forceinline__ void stage_put(uint8_t* sb, int k, float x) {
+    if (F32)
+        reinterpret_cast<float*>(sb)[k * D] = x;
+    else
+        reinterpret_cast<__nv_bfloat16*>(sb)[k * D] = __float2bfloat16_rn(x);
+}
+// The whole block, after the staging writes and a block barrier: 16-byte loads from
+// the staging rows, 16-byte stores to the token rows (rows past `len` are not written).
+template <int D, bool F32>
+__device__ __forceinline__ void stage_copy_out(void* out, const uint8_t* lo, const uint8_t* hi,
+                                               const Params& p, int row0, int len, int h) {
+    constexpr int kRow = D * (F32 ? 4 : 2), kChunks = kRow / 16;
+    for (int w = threadIdx.x; w < len * kChunks; w += kChunkThreads) {
+        const int i = w / kChunks, c = w % kChunks;
+        const uint8_t* src = (i < 32 ? lo + i * kRow : hi + (i - 32) * kRow) + c * 16;
+        *reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + ((size_t)(row0 + i) * p.H + h) * kRow +
+                                  c * 16) = *reinterpret_cast<const uint4*>(src);
+    }
+}
 
 template <int D, int VAR>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-                        const Params p, const TcLayout L) {
+                        const __grid_constant__ CUtensorMap mg, const Params p, const TcLayout L) {
     using S = BChunkSmem<D, VAR>;
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
@@ -263,45 +320,50 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     uint8_t* Qs = sm + S::kQ;     // q -> Qb
     uint8_t* Ks = sm + S::kK;     // k -> Kr
     uint8_t* Vs = sm + S::kV;     // v
-    uint8_t* dOs = sm + S::kdO;   // dO, later dKC
-    uint8_t* dQs = sm + S::kdQ;   // dQt = dO S^T
+    uint8_t* dOs = sm + S::kdO;   // dO
+    uint8_t* dQs = sm + S::kdQ;   // U^T, then dQt^T = S dO^T
     uint8_t* Kbs = sm + S::kKb;   // Kb
-    uint8_t* dWys = sm + S::kdWy; // dWyA -> dWy
-    uint8_t* dUts = sm + S::kdUt; // -dU^T -> dUt^T  ([value][token])
+    uint8_t* dWys = sm + S::kdWy; // -dWyA^T -> dWy^T
+    uint8_t* dUts = sm + S::kdUt; // -dU^T -> dUt^T
     uint8_t* Ts = sm + S::kT;
     uint8_t* Aqs = sm + S::kAq;   // tril(Qb Kr^T)
     uint8_t* B8a = sm + S::kB8a;  // P, then X = dT T^T
-    uint8_t* B8b = sm + S::kB8b;  // dT, then dG
+    uint8_t* B8b = sm + S::kB8b;  // dT^T, then dG
     uint8_t* dAqs = sm + S::kdAq; // dAqk
-    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g, Gamma, e^Gamma, dGamma
+    float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g -> Gamma -> e^Gamma
+    float* Xs = reinterpret_cast<float*>(sm + S::kX);
     float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
     float* gC_s = beta_s + 64;
     float* dgC_s = gC_s + D;
-    float* rowsum = dgC_s + D;
-    float* Grow = rowsum + 64;    // GDN: Gamma per row, later sum of dKC*KC per row
-    float* Erow = Grow + 64;      // GDN: e^{Gamma} per row
+    float* rowsum = dgC_s + D;    // GDN: dGamma per row
+    float* Erow = rowsum + 64;    // GDN: e^{Gamma} per row
     float* Eirow = Erow + 64;     // GDN: e^{-Gamma} per row
-    float* part = Eirow + 64;     // [3][64] partial row sums of warps 4..7
-    __shared__ uint64_t bar_ld, bar_mma, bar_kc;
+    float* part = Eirow + 64;     // dbeta partials of warps 4..7
+    __shared__ uint64_t bar_st, bar_tok, bar_mma;
     __shared__ uint32_t tmem_base;
 
-    constexpr uint32_t R_dbK = 128, R_dbV = 128 + D, R_dQ = 128 + 2 * D, R_dKr = 128 + D;
-    const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2;
+    // TMEM columns, 64 each.  C0 / C1 / C2 are reused phase by phase; the others hold
+    // one result from its product to its last reader.
+    constexpr uint32_t C0 = 0, C1 = 64, C2 = 128, C3 = 192, C4 = 256, C_dQ = 320, C6 = 384,
+                       C_dKC = 448;
+    const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2, lane = tid & 31;
     const int chunk = blockIdx.x, h = blockIdx.y;
     int seq, row0, len;
     chunk_info(p, chunk, seq, row0, len);
     const size_t rec = (size_t)chunk * p.H + h;
     const float sc = p.scale;
+    const bool f32out = p.grad_dtype == DR_F32;
 
     if (tid == 0) {
-        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_st, 1);
+        mbar_init(&bar_tok, 1);
         mbar_init(&bar_mma, 1);
-        mbar_init(&bar_kc, 1);
         fence_barrier_init();
         prefetch_tmap(&mq);
         prefetch_tmap(&mk);
         prefetch_tmap(&mv);
         prefetch_tmap(&mdo);
+        if (VAR == DR_KDA) prefetch_tmap(&mg);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -312,7 +374,21 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = m64_row();
+    const int r = m64_row();                            // row of an M = 64 accumulator, or -1
+    const int cl = D == 128 ? (tid & 127) : r;          // channel of an M = D accumulator, or -1
+    const int t0 = 32 * half;                           // first token of this thread's column half
+    // Element (t0 + k, cl) of a [64][D] SW128 token tile sits at xo[k % 8] + 128 k: the
+    // swizzle depends on the row only through k % 8 because t0 is a multiple of 8.
+    uint32_t xo[8];
+    {
+        const int c = cl < 0 ? 0 : cl;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            xo[k] = (uint32_t)((c >> 6) * 8192 + t0 * 128 + ((((c >> 3) & 7) ^ k) << 4) + (c & 7) * 2);
+    }
+    auto tok = [&](const uint8_t* tile, int k) -> float {
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + xo[k & 7] + k * 128));
+    };
     bool ok = true;
     uint32_t mph = 0;  // bar_mma phase
     auto mma_done = [&]() -> bool {
@@ -320,146 +396,149 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         mph ^= 1;
         return good;
     };
+    // e^{Gamma} and e^{-Gamma} of token t0 + k for this thread's channel
+    const float* gam_t = Gam + t0 * S::kGS + (cl < 0 ? 0 : cl);
+    // 16 consecutive per-token values starting at token t0 + k0 (k0 multiple of 4)
+    auto load16 = [&](const float* src, int k0, float (&v)[16]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 x = *reinterpret_cast<const float4*>(src + t0 + k0 + 4 * q);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    };
+    // e^{Gamma} and e^{-Gamma} of tokens t0 + 16 b .. + 15 for this thread's channel
+    auto decay16 = [&](int b, float (&e)[16], float (&ei)[16]) {
+        if (VAR == DR_KDA) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                e[j] = gam_t[(16 * b + j) * S::kGS];  // e^Gamma, stored by the decay pass
+                ei[j] = fast_rcp(e[j]);
+            }
+        } else if (VAR == DR_GDN) {
+            load16(Erow, 16 * b, e);
+            load16(Eirow, 16 * b, ei);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) e[j] = ei[j] = 1.f;
+        }
+    };
+    // staging base of this thread: its half's buffer, its channel
+    auto stage_base = [&](uint8_t* lo, uint8_t* hi, bool f32) -> uint8_t* {
+        return (half ? hi : lo) + (cl < 0 ? 0 : cl) * (f32 ? 4 : 2);
+    };
+    // dGamma of this thread's channel and tokens (KDA), or its share of each token's
+    // dGamma (GDN), is accumulated in TMEM columns C1 + t0 .. + 31 from E4 on
+    float fsum = 0.f;  // sum over this thread's tokens of dKC * KC
 
     do {
-        // Phase A: what the state-side products need.  S sits in the Aqk / P / dG / dAqk
-        // tiles, dS in the Kb / dWy tiles and U^T in the v tile, all idle until later.
+        // Two load groups, token side first so that the decay pass and the first
+        // token-by-token products run while the state side arrives.  Token side: q, k,
+        // v, dO, the gates (KDA: one [64][D] fp32 box) and e^{Gamma_last}.  State side:
+        // S in the Aqk / P / dG / dAqk tiles, dS in the Kb / dWy tiles, U^T in the dQt
+        // tile (all idle until the state-side products have read them), -dU^T, T.
         uint8_t* Sst = Aqs;   // [D][D] W-layout state at the chunk start
         uint8_t* dSst = Kbs;  // [D][D] W-layout state gradient at the chunk end
-        uint8_t* Ust = Vs;    // [D][64] U^T
+        uint8_t* Ust = dQs;   // [D][64] U^T
         constexpr uint32_t kDD = D * D * 2;
+        // per-token scalars first, so that they do not queue behind the tile copies
+        const float beta_ld = (tid >= 64 && tid < 128 && tid - 64 < len)
+                                  ? p.beta[(size_t)(row0 + tid - 64) * p.H + h] : 0.f;
+        float gl0 = 0.f, gl1 = 0.f;  // GDN: this lane's two log-decays (warp 1)
+        if (VAR == DR_GDN && warp == 1) {
+            gl0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
+            gl1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+        }
         if (tid == 0) {
-            const uint32_t gbytes = VAR == DR_KDA ? (uint32_t)len * D * 4 : 0u;
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + 2 * kDD + 8192 + D * 4 + gbytes);
-            bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(Ust, L.U + rec * kTile, kTile, &bar_ld);
-            bulk_g2s(Sst, L.S + rec * kDD, kDD, &bar_ld);
-            bulk_g2s(dSst, L.dS + rec * kDD, kDD, &bar_ld);
-            for (int kb = 0; kb < D / 64; ++kb)
-                tma_load_3d(dOs + kb * 8192, &mdo, &bar_ld, kb * 64, h, row0);
-            bulk_g2s(Ts, L.T + rec * 8192, 8192, &bar_ld);
-            bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_ld);
-        }
-        __syncthreads();  // the expected byte count is registered before the gate rows go out
-        if (VAR == DR_KDA && warp == 1) {
-            for (int i = tid & 31; i < len; i += 32)
-                bulk_g2s(Gam + i * S::kGS, p.g + ((size_t)(row0 + i) * p.H + h) * D, D * 4, &bar_ld);
-        }
-        if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
-        ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        zero_pad_rows(dOs, D, len);
-        fence_async_smem();
-        __syncthreads();
-
-        // M0: dO S^T -> [0,D) ; -dU S^T -> [D,2D) ; U dS^T -> [2D,3D)
-        if (tid == 0) {
-            tc_fence_after();
-            const Tile tS{smem_u32(Sst), D}, tdS{smem_u32(dSst), D};
-            mma_tiles(tm + 0, Tile{smem_u32(dOs), 64}, false, tS, true, 64, D, D, false);
-            mma_tiles(tm + D, Tile{smem_u32(dUts), D}, true, tS, true, 64, D, D, false);
-            mma_tiles(tm + 2 * D, Tile{smem_u32(Ust), D}, true, tdS, true, 64, D, D, false);
-            mma_commit(&bar_mma);
-        }
-        // while M0 runs: dgC[c] = sum_v dS[c, v] S[c, v], and the cumulative log-decay
-        // (KDA: per key channel, in place in Gam; GDN: per token, with its two
-        // exponentials); rows past the end of the sequence add nothing
-        for (int c = tid; c < D; c += kChunkThreads) {
-            float acc = 0.f;
-            for (int vv = 0; vv < D; ++vv)
-                acc = fmaf(__bfloat162float(*tile_elem(Sst, vv, c, D)),
-                           __bfloat162float(*tile_elem(dSst, vv, c, D)), acc);
-            dgC_s[c] = acc;
-        }
-        if (VAR == DR_KDA) {
-            // kChunkThreads / D threads per channel, each a contiguous block of rows, then
-            // every block adds the totals of the blocks above it
-            constexpr int P = kChunkThreads / D, R = 64 / P;
-            const int c = tid % D, pt = tid / D;
-            float* tot = reinterpret_cast<float*>(Qs);  // [P][D]; q arrives only after M0
-            float G = 0.f;
-#pragma unroll 8
-            for (int i = pt * R; i < pt * R + R; ++i) {
-                if (i < len) G += Gam[i * S::kGS + c];
-                Gam[i * S::kGS + c] = G;
+            mbar_arrive_expect_tx(&bar_tok, 4 * kTile + D * 4 + (VAR == DR_KDA ? 64 * D * 4 : 0));
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_load_3d(Qs + kb * 8192, &mq, &bar_tok, kb * 64, h, row0);
+                tma_load_3d(Ks + kb * 8192, &mk, &bar_tok, kb * 64, h, row0);
+                tma_load_3d(Vs + kb * 8192, &mv, &bar_tok, kb * 64, h, row0);
+                tma_load_3d(dOs + kb * 8192, &mdo, &bar_tok, kb * 64, h, row0);
             }
+            if (VAR == DR_KDA) tma_load_3d(Gam, &mg, &bar_tok, 0, h, row0);
+            bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_tok);
+            mbar_arrive_expect_tx(&bar_st, 2 * kTile + 2 * kDD + 8192);
+            bulk_g2s(Sst, L.S + rec * kDD, kDD, &bar_st);
+            bulk_g2s(dSst, L.dS + rec * kDD, kDD, &bar_st);
+            bulk_g2s(Ust, L.U + rec * kTile, kTile, &bar_st);
+            bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_st);
+            bulk_g2s(Ts, L.T + rec * 8192, 8192, &bar_st);
+        }
+        if (tid >= 64 && tid < 128) beta_s[tid - 64] = beta_ld;
+        ok = mbar_wait(&bar_tok, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+        zero_pad_rows(Qs, D, len);
+        zero_pad_rows(Ks, D, len);
+        zero_pad_rows(Vs, D, len);
+        zero_pad_rows(dOs, D, len);
+        // cumulative log-decay: KDA per key channel, in place in Gam (rows past the end of
+        // the sequence repeat the total); GDN per token, with its two exponentials
+        float* tot = Xs + 1024;  // KDA: [P][D] block totals
+        constexpr int kP = kChunkThreads / D, kR = 64 / kP;  // KDA: threads per channel, rows each
+        if (VAR == DR_KDA) {
+            // kP threads per channel, each the cumulative sum of a contiguous block of kR
+            // rows; the decay pass adds the totals of the blocks above
+            const int c = tid % D, pt = tid / D;
+            float v[kR];
+#pragma unroll
+            for (int t = 0; t < kR; ++t) v[t] = Gam[(pt * kR + t) * S::kGS + c];
+            float G = 0.f;
+#pragma unroll
+            for (int t = 0; t < kR; ++t) {
+                if (pt * kR + t < len) G += v[t];
+                v[t] = G;
+            }
+#pragma unroll
+            for (int t = 0; t < kR; ++t) Gam[(pt * kR + t) * S::kGS + c] = v[t];
             tot[pt * D + c] = G;
-            __syncthreads();
-            float off = 0.f;
-            for (int q = 0; q < pt; ++q) off += tot[q * D + c];
-            if (pt > 0)
-                for (int i = pt * R; i < pt * R + R; ++i) Gam[i * S::kGS + c] += off;
         } else if (VAR == DR_GDN) {
-            if (warp == 0) {
-                const int lane = tid & 31;
-                const float a0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-                const float a1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
-                float x = a0 + a1;
+            if (warp == 1) {
+                float x = gl0 + gl1;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
-                const float g0 = x - a1, g1 = x;
-                Grow[2 * lane] = g0;
-                Grow[2 * lane + 1] = g1;
-                const float e0 = __expf(g0), e1 = __expf(g1);
+                const float e0 = __expf(x - gl1), e1 = __expf(x);
                 Erow[2 * lane] = e0;
                 Erow[2 * lane + 1] = e1;
                 Eirow[2 * lane] = fast_rcp(e0);
                 Eirow[2 * lane + 1] = fast_rcp(e1);
             }
         }
-        ok = mma_done();
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
-        // Phase B: q, k, v (v replaces U^T, which M0 has consumed)
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile);
-            for (int kb = 0; kb < D / 64; ++kb) {
-                tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
-                tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
-                tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
-            }
-        }
-        // E0: dQt -> its tile, -dWyA -> the dWy tile (dS is consumed), dKC -> its
-        // workspace image (reloaded for the last phase)
-        for (int cb = half; cb < D / 16; cb += 2) {
-            float a[16], b[16], c_[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld16(tl + D + cb * 16, b);
-            tmem_ld16(tl + 2 * D + cb * 16, c_);
-            tmem_ld_wait();
-            if (r >= 0) {
-                tile_store16(dQs, r, cb * 16, 64, a);
-                tile_store16(dWys, r, cb * 16, 64, b);
-                tile_store16(L.dKC + rec * kTile, r, cb * 16, 64, c_);
-            }
-        }
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // dKC image -> bulk reload
-        ok = mbar_wait(&bar_ld, 1, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        zero_pad_rows(Qs, D, len);
-        zero_pad_rows(Ks, D, len);
-        zero_pad_rows(Vs, D, len);
         __syncthreads();
-        // E1b: Qb = q e^G, Kr = k e^-G, Kb = k e^G, eight channels per step
-        for (int w = tid; w < 64 * (D / 8); w += kChunkThreads) {
+        // decay pass: Qb = q e^G and Kr = k e^-G in place; Kb = k e^G is held in registers
+        // until the state-side products have read dS out of the Kb tile
+        constexpr int kPer = 64 * (D / 8) / kChunkThreads;
+        uint4 kbr[kPer];
+#pragma unroll
+        for (int n = 0; n < kPer; ++n) {
+            const int w = tid + n * kChunkThreads;
             const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
             const uint32_t off = sw128_offset(i, c8, 64);
-            const uint4 qv = *reinterpret_cast<const uint4*>(Qs + off);
             const uint4 kv = *reinterpret_cast<const uint4*>(Ks + off);
             if (VAR == DR_DELTANET) {
-                *reinterpret_cast<uint4*>(Kbs + off) = kv;
+                kbr[n] = kv;
                 continue;
             }
+            const uint4 qv = *reinterpret_cast<const uint4*>(Qs + off);
             float q8[8], k8[8], e8[8], i8[8];
             unpack8(qv, q8);
             unpack8(kv, k8);
             if (VAR == DR_KDA) {
                 float4* gp = reinterpret_cast<float4*>(&Gam[i * S::kGS + c8]);
                 const float4 g0 = gp[0], g1 = gp[1];
-                const float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                for (int q = 0; q < i / kR; ++q) {  // totals of the row blocks above
+                    const float4* tp = reinterpret_cast<const float4*>(tot + q * D + c8);
+                    const float4 t0v = tp[0], t1v = tp[1];
+                    G8[0] += t0v.x, G8[1] += t0v.y, G8[2] += t0v.z, G8[3] += t0v.w;
+                    G8[4] += t1v.x, G8[5] += t1v.y, G8[6] += t1v.z, G8[7] += t1v.w;
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     e8[j] = __expf(G8[j]);
@@ -484,27 +563,99 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             }
             *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
             *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
-            *reinterpret_cast<uint4*>(Kbs + off) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+            kbr[n] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
         fence_async_smem();
         __syncthreads();
-
-        // M1: Qb Kr^T -> [0,64) ; dO v^T -> [64,128) ; dQt Kb^T -> [128,192)
+        // MA: Qb Kr^T -> C3 ; dO v^T -> C4
         if (tid == 0) {
             tc_fence_after();
-            mma_tiles(tm + 0, Tile{smem_u32(Qs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
-            mma_tiles(tm + 64, Tile{smem_u32(dOs), 64}, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
-            mma_tiles(tm + 128, Tile{smem_u32(dQs), 64}, false, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + C3, Tile{smem_u32(Qs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + C4, Tile{smem_u32(dOs), 64}, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
+        }
+        ok = mbar_wait(&bar_st, 0, kWaitLimitNs);
+        if (__syncthreads_or(!ok)) break;
+
+        // M0 (M = D): dQt^T = S dO^T -> C0 ; -dWyA^T = S (-dU)^T -> C1 ; dKC^T = dS U^T -> C_dKC
+        if (tid == 0) {
+            tc_fence_after();
+            const Tile tS{smem_u32(Sst), D};
+            mma_tiles(tm + C0, tS, true, Tile{smem_u32(dOs), 64}, false, D, 64, D, false);
+            mma_tiles(tm + C1, tS, true, Tile{smem_u32(dUts), D}, true, D, 64, D, false);
+            mma_tiles(tm + C_dKC, Tile{smem_u32(dSst), D}, true, Tile{smem_u32(Ust), D}, true, D, 64, D,
+                      false);
+            mma_commit(&bar_mma);
+        }
+        // while M0 runs: dgC[c] = sum_v dS[c, v] S[c, v] (eight channels by a block of
+        // value rows per thread, partials added in a fixed order after the wait)
+        {
+            constexpr int kOct = D / 8, kGroups = kChunkThreads / kOct, kRows = D / kGroups;
+            const int c8 = (tid % kOct) * 8, g = tid / kOct;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < kRows; ++t) {
+                const uint32_t off = sw128_offset(g * kRows + t, c8, D);
+                float s8[8], d8[8];
+                unpack8(*reinterpret_cast<const uint4*>(Sst + off), s8);
+                unpack8(*reinterpret_cast<const uint4*>(dSst + off), d8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(s8[j], d8[j], acc[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 16);
+            if ((lane & 16) == 0) {
+                const int pg = warp * (16 / kOct) + lane / kOct;  // 128 / kOct partial rows
+#pragma unroll
+                for (int j = 0; j < 8; ++j) Xs[pg * D + c8 + j] = acc[j];
+            }
+        }
+        ok = mma_done();  // MA and M0
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+        for (int c = tid; c < D; c += kChunkThreads) {
+            float a = 0.f;
+            for (int q = 0; q < 128 / (D / 8); ++q) a += Xs[q * D + c];
+            dgC_s[c] = a;
+        }
+        // E0: Kb into its tile; dQt^T -> its tile (U^T is consumed), -dWyA^T -> the dWy
+        // tile (dS is consumed)
+#pragma unroll
+        for (int n = 0; n < kPer; ++n) {
+            const int w = tid + n * kChunkThreads;
+            *reinterpret_cast<uint4*>(Kbs + sw128_offset(w / (D / 8), (w % (D / 8)) * 8, 64)) = kbr[n];
+        }
+#pragma unroll 1
+        for (int b = 0; b < 2; ++b) {
+            float a[16], c_[16];
+            tmem_ld16(tl + C0 + t0 + 16 * b, a);
+            tmem_ld16(tl + C1 + t0 + 16 * b, c_);
+            tmem_ld_wait();
+            if (cl >= 0) {
+                tile_store16(dQs, cl, t0 + 16 * b, D, a);
+                tile_store16(dWys, cl, t0 + 16 * b, D, c_);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M1: dQt Kb^T -> C2 ; Gram Kb Kr^T -> C6 (read in E6)
+        if (tid == 0) {
+            tc_fence_after();
+            mma_tiles(tm + C2, Tile{smem_u32(dQs), D}, true, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + C6, Tile{smem_u32(Kbs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
             mma_commit(&bar_mma);
         }
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        // E2: Aqk = tril(Qb Kr^T) ; P = (dO v^T - dQt Kb^T) diag(beta)
+#pragma unroll 1
         for (int cb = half; cb < 4; cb += 2) {
             float a[16], p1[16], p2[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld16(tl + 64 + cb * 16, p1);
-            tmem_ld16(tl + 128 + cb * 16, p2);
+            tmem_ld16(tl + C3 + cb * 16, a);
+            tmem_ld16(tl + C4 + cb * 16, p1);
+            tmem_ld16(tl + C2 + cb * 16, p2);
             tmem_ld_wait();
             if (r >= 0) {
 #pragma unroll
@@ -521,25 +672,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // M2: P T^T -> [0,64) ; Aqk^T dQt -> [64,64+D) ; dO^T Aqk -> [64+D, 128+D) (M = D)
+        // M2: P T^T -> C0 ; dQt^T Aqk -> C1 (M = D) ; dO^T Aqk -> C2 (M = D)
         if (tid == 0) {
             tc_fence_after();
             const Tile tAq{smem_u32(Aqs), 64};
-            mma_tiles(tm + 0, Tile{smem_u32(B8a), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
-            mma_tiles(tm + 64, tAq, true, Tile{smem_u32(dQs), 64}, true, 64, D, 64, false);
-            mma_tiles(tm + 64 + D, Tile{smem_u32(dOs), 64}, true, tAq, true, D, 64, 64, false);
+            mma_tiles(tm + C0, Tile{smem_u32(B8a), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
+            mma_tiles(tm + C1, Tile{smem_u32(dQs), D}, false, tAq, true, D, 64, 64, false);
+            mma_tiles(tm + C2, Tile{smem_u32(dOs), 64}, true, tAq, true, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        if (tid == 0) {  // dO is consumed: bring dKC into its buffer for the last phase
-            mbar_arrive_expect_tx(&bar_kc, kTile);
-            bulk_g2s(dOs, L.dKC + rec * kTile, kTile, &bar_kc);
-        }
+#pragma unroll 1
         for (int cb = half; cb < 4; cb += 2) {
             float a[16];
-            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + C0 + cb * 16, a);
             tmem_ld_wait();
             if (r >= 0) {
 #pragma unroll
@@ -547,97 +695,120 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tile_store16(dAqs, r, cb * 16, 64, a);
             }
         }
-        for (int cb = half; cb < D / 16; cb += 2) {
-            float a[16];
-            tmem_ld16(tl + 64 + cb * 16, a);
+#pragma unroll 1
+        for (int b = 0; b < 2; ++b) {
+            float a[16], u[16];
+            tmem_ld16(tl + C1 + t0 + 16 * b, a);
+            tmem_ld16(tl + C2 + t0 + 16 * b, u);
             tmem_ld_wait();
-            if (r >= 0) {
-                float wa[16];
-                tile_load16(dWys, r, cb * 16, 64, wa);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = wa[j] - sc * a[j];  // dWy (the tile held -dWyA)
-                tile_store16(dWys, r, cb * 16, 64, a);
-            }
-        }
-        {
-            // dUts holds -dU^T ([value][token]); the accumulator rows are value channels
-            const int rv = (D == 128) ? (tid & 127) : r;
-            for (int g = half; g < 4; g += 2) {
-                float b[16];
-                tmem_ld16(tl + 64 + D + g * 16, b);
-                tmem_ld_wait();
-                if (rv >= 0) {
-                    float nd[16];
-                    tile_load16(dUts, rv, g * 16, D, nd);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) b[j] = sc * b[j] - nd[j];  // dUt^T
-                    tile_store16(dUts, rv, g * 16, D, b);
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // M3: dWy Kb^T -> [0,64) ; dUt v^T -> [64,128) ; T^T dWy -> R_dbK ; T^T dUt -> R_dbV ;
-        //     dAqk Kr -> R_dQ
-        if (tid == 0) {
-            tc_fence_after();
-            const Tile tT{smem_u32(Ts), 64}, tdW{smem_u32(dWys), 64}, tdU{smem_u32(dUts), D};
-            mma_tiles(tm + 0, tdW, false, Tile{smem_u32(Kbs), 64}, false, 64, 64, D, false);
-            mma_tiles(tm + 64, tdU, true, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
-            mma_tiles(tm + R_dbK, tT, true, tdW, true, 64, D, 64, false);
-            mma_tiles(tm + R_dbV, tT, true, tdU, false, 64, D, 64, false);
-            mma_tiles(tm + R_dQ, Tile{smem_u32(dAqs), 64}, false, Tile{smem_u32(Ks), 64}, true, 64, D, 64, false);
-            mma_commit(&bar_mma);
-        }
-        ok = mma_done();
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
-        float dbeta_acc = 0.f;
-        for (int cb = half; cb < 4; cb += 2) {
-            float a[16], b[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld16(tl + 64 + cb * 16, b);
-            tmem_ld_wait();
-            if (r >= 0) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = beta_s[cb * 16 + j] * (a[j] + b[j]);  // dT
-                tile_store16(B8b, r, cb * 16, 64, a);
-            }
-        }
-        for (int cb = half; cb < D / 16; cb += 2) {
-            float a[16];
-            tmem_ld16(tl + R_dbV + cb * 16, a);
-            tmem_ld_wait();
-            if (r >= 0) {
-                float vv[16];
-                tile_load16(Vs, r, cb * 16, 64, vv);
-                const float br = beta_s[r];
+            if (cl >= 0) {
+                float wa[16], nd[16];
+                tile_load16(dWys, cl, t0 + 16 * b, D, wa);
+                tile_load16(dUts, cl, t0 + 16 * b, D, nd);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    dbeta_acc = fmaf(a[j], vv[j], dbeta_acc);
-                    a[j] *= br;
+                    a[j] = wa[j] - sc * a[j];  // dWy^T (the tile held -dWyA^T)
+                    u[j] = sc * u[j] - nd[j];  // dUt^T (the tile held -dU^T)
                 }
-                if (r < len) store_row16(p.dv_, ((size_t)(row0 + r) * p.H + h) * D + cb * 16, p.grad_dtype, a);
+                tile_store16(dWys, cl, t0 + 16 * b, D, a);
+                tile_store16(dUts, cl, t0 + 16 * b, D, u);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // M4: X = dT T^T -> [0,64)
+        // M3: Kb dWy^T -> C0 ; v dUt^T -> C1 ; dUt^T T -> C3 (dbV^T) ; dWy^T T -> C4 (dbK^T) ;
+        //     Kr^T dAqk^T -> C_dQ  (the last three M = D)
         if (tid == 0) {
             tc_fence_after();
-            mma_tiles(tm + 0, Tile{smem_u32(B8b), 64}, false, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
+            const Tile tT{smem_u32(Ts), 64}, tdW{smem_u32(dWys), D}, tdU{smem_u32(dUts), D};
+            mma_tiles(tm + C0, Tile{smem_u32(Kbs), 64}, false, tdW, true, 64, 64, D, false);
+            mma_tiles(tm + C1, Tile{smem_u32(Vs), 64}, false, tdU, true, 64, 64, D, false);
+            mma_tiles(tm + C3, tdU, false, tT, true, D, 64, 64, false);
+            mma_tiles(tm + C4, tdW, false, tT, true, D, 64, 64, false);
+            mma_tiles(tm + C_dQ, Tile{smem_u32(Ks), 64}, true, Tile{smem_u32(dAqs), 64}, false, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        // E4, token rows j: dT^T[j][i] = beta_j (Kb dWy^T + v dUt^T)[j][i], and the key and
+        // value parts of dbeta_j = sum_c dbK[j,c] Kb[j,c] + sum_v dbV[j,v] v[j,v]
+        //                        = sum_i T[i,j] (dWy Kb^T + dUt v^T)[i,j]
+        float dbeta_acc = 0.f;
+        {
+            // column r of T: element (16 cb + j, r) at xr[j % 8] + 128 (16 cb + j)
+            uint32_t xr[8];
+            const int rc = r < 0 ? 0 : r;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xr[k] = (uint32_t)(((((rc >> 3) & 7) ^ k) << 4) + (rc & 7) * 2);
+#pragma unroll 1
+            for (int n = 0; n < 2; ++n) {
+                const int cb = half + 2 * n;
+                float a[16], b[16];
+                tmem_ld16(tl + C0 + cb * 16, a);
+                tmem_ld16(tl + C1 + cb * 16, b);
+                tmem_ld_wait();
+                if (r >= 0) {
+                    const float br = beta_s[r];
+                    const uint8_t* tcol = Ts + cb * 16 * 128;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float s = a[j] + b[j];
+                        const float tij = __bfloat162float(
+                            *reinterpret_cast<const __nv_bfloat16*>(tcol + xr[j & 7] + j * 128));
+                        dbeta_acc = fmaf(tij, s, dbeta_acc);
+                        a[j] = br * s;
+                    }
+                    tile_store16(B8b, r, cb * 16, 64, a);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // M4: X = dT T^T -> C0
+        if (tid == 0) {
+            tc_fence_after();
+            mma_tiles(tm + C0, Tile{smem_u32(B8b), 64}, true, Tile{smem_u32(Ts), 64}, false, 64, 64, 64, false);
+            mma_commit(&bar_mma);
+        }
+        // while M4 runs: dv[j, v] = beta_j dbV^T[v][j], staged in the v / dO tiles (both
+        // consumed) and written out
+        auto dv_stage = [&](auto f32) {
+            constexpr bool F32 = decltype(f32)::value;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                uint8_t* sb = stage_base(Vs, dOs, F32) + 16 * b * D * (F32 ? 4 : 2);
+                float a[16];
+                tmem_ld16(tl + C3 + t0 + 16 * b, a);
+                tmem_ld_wait();
+                if (cl >= 0) {
+                    float bt[16];
+                    load16(beta_s, 16 * b, bt);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stage_put<D, F32>(sb, j, bt[j] * a[j]);
+                }
+            }
+        };
+        if (f32out)
+            dv_stage(BoolTag<true>{});
+        else
+            dv_stage(BoolTag<false>{});
+        __syncthreads();
+        if (f32out)
+            stage_copy_out<D, true>(p.dv_, Vs, dOs, p, row0, len, h);
+        else
+            stage_copy_out<D, false>(p.dv_, Vs, dOs, p, row0, len, h);
+        ok = mma_done();
+        if (__syncthreads_or(!ok)) break;
+        tc_fence_after();
+#pragma unroll 1
         for (int cb = half; cb < 4; cb += 2) {
             float a[16];
-            tmem_ld16(tl + cb * 16, a);
+            tmem_ld16(tl + C0 + cb * 16, a);
             tmem_ld_wait();
             if (r >= 0) tile_store16(B8a, r, cb * 16, 64, a);
         }
@@ -645,20 +816,60 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // M5: T^T X -> [0,64) (dA = -it) ; Gram Kb Kr^T -> [64,128)
+        // M5: T^T X -> C0 (dA = -it)
         if (tid == 0) {
             tc_fence_after();
-            mma_tiles(tm + 0, Tile{smem_u32(Ts), 64}, true, Tile{smem_u32(B8a), 64}, true, 64, 64, 64, false);
-            mma_tiles(tm + 64, Tile{smem_u32(Kbs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
+            mma_tiles(tm + C0, Tile{smem_u32(Ts), 64}, true, Tile{smem_u32(B8a), 64}, true, 64, 64, 64, false);
             mma_commit(&bar_mma);
         }
+        // while M5 runs: dq = (scale dQt + dAqk Kr) e^{Gamma}, staged in the dUt / dWy tiles
+        // (consumed), and the dQb Qb - dKC KC part of dGamma.  Tokens past the end of the
+        // sequence have zero q and k rows, so they add nothing to dGamma.
+        auto dq_stage = [&](auto f32) {
+            constexpr bool F32 = decltype(f32)::value;
+            const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                uint8_t* sb = stage_base(dUts, dWys, F32) + 16 * b * D * (F32 ? 4 : 2);
+                float dq_[16], dkc[16], dqt[16], g[16];
+                tmem_ld16(tl + C_dQ + t0 + 16 * b, dq_);
+                tmem_ld16(tl + C_dKC + t0 + 16 * b, dkc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) g[j] = 0.f;
+                if (cl >= 0) {
+                    tile_load16(dQs, cl, t0 + 16 * b, D, dqt);
+                    float e16[16], ei16[16];
+                    decay16(b, e16, ei16);
+                    const uint8_t* qrow = Qs + 16 * b * 128;
+                    const uint8_t* krow = Ks + 16 * b * 128;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float qb = tok(qrow, j), kr = tok(krow, j);
+                        const float dQb = fmaf(sc, dqt[j], dq_[j]);
+                        const float f = dkc[j] * (kr * gc);
+                        g[j] = dQb * qb - f;
+                        fsum += f;
+                        stage_put<D, F32>(sb, j, dQb * e16[j]);
+                    }
+                }
+                tmem_st16(tl + C1 + t0 + 16 * b, g);
+            }
+            tmem_st_wait();
+        };
+        if (f32out)
+            dq_stage(BoolTag<true>{});
+        else
+            dq_stage(BoolTag<false>{});
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        // E6: dA = -T^T X (strictly lower), the A part of dbeta, dG = diag(beta) dA
+#pragma unroll 1
         for (int cb = half; cb < 4; cb += 2) {
             float a[16], gm[16];
-            tmem_ld16(tl + cb * 16, a);
-            tmem_ld16(tl + 64 + cb * 16, gm);
+            tmem_ld16(tl + C0 + cb * 16, a);
+            tmem_ld16(tl + C6 + cb * 16, gm);
             tmem_ld_wait();
             if (r >= 0) {
                 const float br = beta_s[r];
@@ -671,135 +882,134 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tile_store16(B8b, r, cb * 16, 64, a);
             }
         }
+        if (half == 1 && r >= 0) part[r] = dbeta_acc;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // M6: dG Kr -> [0,D) ; dG^T Kb + dAqk^T Qb -> R_dKr
+        // M6 (M = D): Kr^T dG^T -> C6 (dKb') ; Kb^T dG + Qb^T dAqk -> C2 (dKr')
         if (tid == 0) {
             tc_fence_after();
             const Tile tG{smem_u32(B8b), 64};
-            mma_tiles(tm + 0, tG, false, Tile{smem_u32(Ks), 64}, true, 64, D, 64, false);
-            mma_tiles(tm + R_dKr, tG, true, Tile{smem_u32(Kbs), 64}, true, 64, D, 64, false);
-            mma_tiles(tm + R_dKr, Tile{smem_u32(dAqs), 64}, true, Tile{smem_u32(Qs), 64}, true, 64, D, 64, true);
+            mma_tiles(tm + C6, Tile{smem_u32(Ks), 64}, true, tG, false, D, 64, 64, false);
+            mma_tiles(tm + C2, Tile{smem_u32(Kbs), 64}, true, tG, true, D, 64, 64, false);
+            mma_tiles(tm + C2, Tile{smem_u32(Qs), 64}, true, Tile{smem_u32(dAqs), 64}, true, D, 64, 64, true);
             mma_commit(&bar_mma);
         }
+        // while M6 runs: dbeta and the staged dq go out
+        if (half == 0 && r >= 0 && r < len)
+            p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc + part[r];
+        if (f32out)
+            stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
+        else
+            stage_copy_out<D, false>(p.dq, dUts, dWys, p, row0, len, h);
         ok = mma_done();
-        ok = ok && mbar_wait(&bar_kc, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        // E7: the decay chain, per row; each warp half takes every other 16-column block
-        {
-            // KDA: per-(row, channel) dKC * KC kept for a fixed-order sum over rows, in
-            // the T / Aqk / P / dG / dAqk tiles (40 KB contiguous), all consumed by now;
-            // rows padded to kGS floats so that lanes owning different rows hit different banks
-            float* Fa = reinterpret_cast<float*>(Ts);
-            float grow = 0.f, frow = 0.f;
-            float er = 1.f, eir = 1.f;
-            if (VAR == DR_GDN && r >= 0) {
-                er = Erow[r];
-                eir = Eirow[r];
-            }
-            const float br = r >= 0 ? beta_s[r] : 0.f;
-            for (int cb = half; cb < D / 16; cb += 2) {
-                float dq_[16], dbk[16], dkb[16], dkr[16];
-                tmem_ld16(tl + R_dQ + cb * 16, dq_);
-                tmem_ld16(tl + R_dbK + cb * 16, dbk);
-                tmem_ld16(tl + 0 + cb * 16, dkb);
-                tmem_ld16(tl + R_dKr + cb * 16, dkr);
+        // E7: dk = (dKb' + beta dbK) e^{Gamma} + (dKr' + dKC e^{Gamma_last}) e^{-Gamma}, staged
+        // in the T / Aqk / P / dG tiles (consumed), and the dKb Kb - dKr Kr part of dGamma
+        auto dk_stage = [&](auto f32) {
+            constexpr bool F32 = decltype(f32)::value;
+            const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                uint8_t* sb = stage_base(Ts, B8a, F32) + 16 * b * D * (F32 ? 4 : 2);
+                float dbk[16], dkb[16], dkr[16], dkc[16], g[16];
+                tmem_ld16(tl + C4 + t0 + 16 * b, dbk);
+                tmem_ld16(tl + C6 + t0 + 16 * b, dkb);
+                tmem_ld16(tl + C2 + t0 + 16 * b, dkr);
+                tmem_ld16(tl + C_dKC + t0 + 16 * b, dkc);
+                tmem_ld16(tl + C1 + t0 + 16 * b, g);
                 tmem_ld_wait();
-                if (r >= 0) {
-                    float qb[16], kb[16], kr[16], dqt[16], dkc[16];
-                    tile_load16(Qs, r, cb * 16, 64, qb);
-                    tile_load16(Kbs, r, cb * 16, 64, kb);
-                    tile_load16(Ks, r, cb * 16, 64, kr);
-                    tile_load16(dQs, r, cb * 16, 64, dqt);
-                    tile_load16(dOs, r, cb * 16, 64, dkc);
-                    float oq[16], ok_[16];
+                if (cl >= 0) {
+                    float e16[16], ei16[16], bt[16];
+                    decay16(b, e16, ei16);
+                    load16(beta_s, 16 * b, bt);
+                    const uint8_t* kbrow = Kbs + 16 * b * 128;
+                    const uint8_t* krow = Ks + 16 * b * 128;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int c = cb * 16 + j;
-                        float e = er, ei = eir;
-                        if (VAR == DR_KDA) {
-                            e = Gam[r * S::kGS + c];  // e^Gamma, stored by the decay pass
-                            ei = fast_rcp(e);
-                        }
-                        const float gc = gC_s[c];
-                        const float dQb = sc * dqt[j] + dq_[j];
-                        const float dKb = dkb[j] + br * dbk[j];
-                        const float KC = kr[j] * gc;
-                        dbeta_acc = fmaf(dbk[j], kb[j], dbeta_acc);
-                        const float dG = dQb * qb[j] + dKb * kb[j] - dkr[j] * kr[j] - dkc[j] * KC;
-                        if (VAR == DR_KDA) {
-                            Gam[r * S::kGS + c] = dG;
-                            Fa[r * S::kGS + c] = dkc[j] * KC;
-                        } else if (VAR == DR_GDN) {
-                            grow += dG;
-                            frow = fmaf(dkc[j], KC, frow);
-                        }
-                        oq[j] = dQb * e;
-                        ok_[j] = dKb * e + dkr[j] * ei + dkc[j] * gc * ei;
-                    }
-                    if (r < len) {
-                        const size_t eidx = ((size_t)(row0 + r) * p.H + h) * D + cb * 16;
-                        store_row16(p.dq, eidx, p.grad_dtype, oq);
-                        store_row16(p.dk_, eidx, p.grad_dtype, ok_);
+                        const float kb = tok(kbrow, j), kr = tok(krow, j);
+                        const float dKb = fmaf(bt[j], dbk[j], dkb[j]);
+                        g[j] += dKb * kb - dkr[j] * kr;
+                        stage_put<D, F32>(sb, j, dKb * e16[j] + fmaf(dkc[j], gc, dkr[j]) * ei16[j]);
                     }
                 }
+                tmem_st16(tl + C1 + t0 + 16 * b, g);
             }
-            // combine the two warp halves' row partials in a fixed order
-            if (half == 1 && r >= 0) {
-                part[r] = dbeta_acc;
-                part[64 + r] = grow;
-                part[128 + r] = frow;
-            }
-            __syncthreads();
-            if (half == 0 && r >= 0) {
-                dbeta_acc += part[r];
-                if (VAR == DR_GDN) {
-                    rowsum[r] = grow + part[64 + r];
-                    Grow[r] = frow + part[128 + r];  // this row's Gamma is no longer needed
-                }
-                if (r < len) p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc;
-            }
-        }
+            tmem_st_wait();
+        };
+        if (f32out)
+            dk_stage(BoolTag<true>{});
+        else
+            dk_stage(BoolTag<false>{});
         __syncthreads();
+        if (f32out)
+            stage_copy_out<D, true>(p.dk_, Ts, B8a, p, row0, len, h);
+        else
+            stage_copy_out<D, false>(p.dk_, Ts, B8a, p, row0, len, h);
 
         // E8: dg_i = (dgC e^{Gamma_last} + sum_rows dKC KC) + sum_{j >= i} dGamma_j
+        float dG[32];
+        if (VAR != DR_DELTANET) {
+            float g0[16], g1[16];
+            tc_fence_after();
+            tmem_ld16(tl + C1 + t0, g0);
+            tmem_ld16(tl + C1 + t0 + 16, g1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                dG[j] = g0[j];
+                dG[16 + j] = g1[j];
+            }
+        }
         if (VAR == DR_KDA) {
-            // P threads per key channel, each owning 64 / P consecutive rows
-            constexpr int P = kChunkThreads / D, R = 64 / P;
-            const int c = tid % D, pt = tid / D, i0 = pt * R;
-            const float* Fa = reinterpret_cast<const float*>(Ts);
-            float* Sp = reinterpret_cast<float*>(Ts + 64 * S::kGS * 4);  // [P][D] row sums of dGamma
-            float* Fp = Sp + P * D;                                 // [P][D] row sums of dKC KC
-            float sg = 0.f, sf = 0.f;
-            for (int i = i0; i < i0 + R; ++i) {
-                sf += Fa[i * S::kGS + c];
-                if (i < len) sg += Gam[i * S::kGS + c];
+            // the two token halves of a channel exchange their totals
+            float* sg1 = Xs;        // [D] sum of dGamma over tokens [32, 64)
+            float* f0 = Xs + D;     // [D] sum of dKC KC over tokens [0, 32)
+            float* f1 = Xs + 2 * D; // [D] ... over tokens [32, 64)
+            float sg = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) sg += dG[k];
+            if (cl >= 0) {
+                if (half == 1) {
+                    sg1[cl] = sg;
+                    f1[cl] = fsum;
+                } else {
+                    f0[cl] = fsum;
+                }
             }
-            Sp[pt * D + c] = sg;
-            Fp[pt * D + c] = sf;
             __syncthreads();
-            float run = dgC_s[c] * gC_s[c];
-            for (int q = 0; q < P; ++q) {
-                run += Fp[q * D + c];
-                if (q > pt) run += Sp[q * D + c];
-            }
-            for (int i = i0 + R - 1; i >= i0; --i) {
-                if (i < len) {
-                    run += Gam[i * S::kGS + c];
-                    p.dg[((size_t)(row0 + i) * p.H + h) * D + c] = run;
+            if (cl >= 0) {
+                float run = dgC_s[cl] * gC_s[cl] + f0[cl] + f1[cl];
+                if (half == 0) run += sg1[cl];
+#pragma unroll
+                for (int k = 31; k >= 0; --k) {
+                    const int i = t0 + k;
+                    run += dG[k];
+                    if (i < len) p.dg[((size_t)(row0 + i) * p.H + h) * D + cl] = run;
                 }
             }
         } else if (VAR == DR_GDN) {
-            if (warp == 0) {
-                const int lane = tid & 31;
-                float e = Grow[lane] + Grow[lane + 32];  // per-row sums of dKC KC
-                for (int c = lane; c < D; c += 32) e += dgC_s[c] * gC_s[c];
+            float* red = Xs;          // [4 channel quarters][64 rows]
+            float* fw = Xs + 256;     // [8 warps]
+            const float rs = warp_transpose_sum(dG);  // row t0 + lane, this warp's channels
+            red[(warp & 3) * 64 + t0 + lane] = rs;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            for (int o = 16; o > 0; o >>= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
+            if (lane == 0) fw[warp] = fsum;
+            __syncthreads();
+            if (tid < 64) rowsum[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+            __syncthreads();
+            if (warp == 0) {
+                float e = 0.f;
+                for (int w = 0; w < kChunkThreads / 32; ++w) e += fw[w];
+                float ec = 0.f;
+                for (int c = lane; c < D; c += 32) ec += dgC_s[c] * gC_s[c];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ec += __shfl_xor_sync(0xffffffffu, ec, o);
+                e += ec;
                 const float a0 = 2 * lane < len ? rowsum[2 * lane] : 0.f;
                 const float a1 = 2 * lane + 1 < len ? rowsum[2 * lane + 1] : 0.f;
                 float x = a0 + a1;  // suffix sum over lanes >= this one
@@ -815,9 +1025,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     } while (0);
     if (!ok) {
         record_timeout(p);
-        mbar_wait(&bar_ld, 0, kWaitLimitNs);
-        mbar_wait(&bar_ld, 1, kWaitLimitNs);
-        mbar_wait(&bar_kc, 0, kWaitLimitNs);
+        mbar_wait(&bar_st, 0, kWaitLimitNs);
+        mbar_wait(&bar_tok, 0, kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -832,9 +1041,11 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
     }
     const TcLayout L = tc_layout(p);
     const long long rows = (long long)p.B * p.T;
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mg;
     if (!make_token_map(&mq, p.q, D, p.H, rows) || !make_token_map(&mk, p.k, D, p.H, rows) ||
         !make_token_map(&mv, p.v, D, p.H, rows) || !make_token_map(&mdo, p.dO, D, p.H, rows))
+        return cudaErrorInvalidValue;
+    if (p.variant == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows) : !make_token_map(&mg, p.q, D, p.H, rows))
         return cudaErrorInvalidValue;
     {
         auto launch_scan = [&](auto kernel, int bv, int smem, bool& attr) -> cudaError_t {
@@ -865,7 +1076,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         }
         {
             TraceScope ts("tc_bwd_chunk", st);
-            kernel<<<dim3(p.num_chunks, p.H), kChunkThreads, smem, st>>>(mq, mk, mv, mdo, p, L);
+            kernel<<<dim3(p.num_chunks, p.H), kChunkThreads, smem, st>>>(mq, mk, mv, mdo, mg, p, L);
         }
         return cudaGetLastError();
     };

@@ -629,6 +629,21 @@ bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 per-key-channel gates [rows][H][D]: one box is the D gates of 64 tokens of one
+// head, dense (no swizzle) in shared memory
+bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t tc_records(const Params& p) { return (size_t)p.num_chunks * p.H; }
 
 TcLayout tc_layout(const Params& p) {

@@ -11,8 +11,6 @@
 //                       (W layout) of the state at the chunk start / of dL/d(state
 //                       at the chunk end)                       (D*D*2 bytes)
 //   gC                : [D] fp32, e^{Gamma} at the chunk's last token
-//   dKC               : [64][D] tile image of U dS^T, written and reread by the
-//                       backward chunk kernel
 #pragma once
 #include <cstdint>
 
@@ -21,7 +19,7 @@
 namespace dr {
 
 struct TcLayout {
-    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS, *dKC;
+    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS;
     float* gC;
 };
 
@@ -36,7 +34,7 @@ struct TcSizes {
 
 __host__ inline size_t tc_layout_bytes(size_t recs, int D) {
     TcSizes s(D);
-    return tc_align(recs * s.kd) * 8 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
+    return tc_align(recs * s.kd) * 7 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
            tc_align(recs * s.g);
 }
 
@@ -55,7 +53,6 @@ __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
     L.T = take(recs * s.cc);
     L.S = take(recs * s.dd);
     L.dS = take(recs * s.dd);
-    L.dKC = take(recs * s.kd);
     L.gC = reinterpret_cast<float*>(take(recs * s.g));
     return L;
 }
