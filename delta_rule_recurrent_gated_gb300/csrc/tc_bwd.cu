@@ -247,19 +247,23 @@ constexpr int kChunkThreads = 256;
 template <int D, int VAR>
 struct BChunkSmem {
     static constexpr int kTile = 64 * D * 2, kCC = 8192;
+    // Eight tile buffers P0..P7 of kTile bytes.  P1 holds k -> Kr, P2 v, P3 dO; the roles
+    // of P0 and P4..P7 alternate between consecutive work items of a CTA (ChunkRoles), so
+    // that the next item's inputs can be copied in while this item finishes.
     // [64][D] token-row tiles: q -> Qb, k -> Kr, v, dO, Kb
-    // [D][64] channel-row tiles: U^T -> dQt^T, -dWyA^T -> dWy^T, -dU^T -> dUt^T
-    static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kdQ = 4 * kTile,
-                         kKb = 5 * kTile, kdWy = 6 * kTile, kdUt = 7 * kTile;
+    // [D][64] channel-row tiles: U^T, dQt^T, -dWyA^T -> dWy^T, -dU^T -> dUt^T
+    static constexpr int kK = kTile, kV = 2 * kTile, kdO = 3 * kTile;
+    // five 8 KB tiles: T, then Aqk / P-X / dT-dG / dAqk, which hold S before those
     static constexpr int kT = 8 * kTile, kAq = kT + kCC, kB8a = kAq + kCC, kB8b = kB8a + kCC,
                          kdAq = kB8b + kCC;
     static constexpr int kGam = kdAq + kCC;                         // KDA: fp32 [64][kGS]
     static constexpr int kGS = D;  // row stride of the per-channel fp32 array (a dense TMA box)
     static constexpr int kX = kGam + (VAR == DR_KDA ? 64 * kGS * 4 : 0);  // fp32 scratch, 8 KB
     static constexpr int kSmall = kX + 8192;
-    // small arrays: beta[64], e^{Gamma_last}[D], dgC[D], dGamma per row[64],
-    // e^{Gamma} per row[64], e^{-Gamma} per row[64], dbeta partials of warps 4..7 [64]
-    static constexpr int kBytes = kSmall + (64 * 5 + D * 2) * 4 + 1024;
+    // small arrays: beta[64], e^{Gamma_last}[2][D] (this item's and the next one's),
+    // dgC[D], dGamma per row[64], e^{Gamma} per row[64], e^{-Gamma} per row[64], dbeta
+    // partials of warps 4..7 [64]
+    static constexpr int kBytes = kSmall + (64 * 5 + D * 3) * 4 + 1024;
 };
 
 // Sum over the 32 lanes of v[lane][k] for every k: on return lane L holds the
@@ -308,6 +312,20 @@ __device__ __forceinline__ void stage_copy_out(void* out, const uint8_t* lo, con
     }
 }
 
+// Buffer roles of one work item.  Even items: q in P0, U^T in P4 (then dQt^T), dS in
+// P5..P6 (then Kb in P5, dWy^T in P6), -dU^T in P7.  Odd items: q in P5, U^T in P0 (then
+// Kb), dS in P6..P7 (then dQt^T in P6, dWy^T in P7), -dU^T in P4.  What an even item
+// still reads after its last product (Kb, Kr) and where it stages dk (P2, P3) is
+// disjoint from where the next odd item's state goes, and the reverse.
+struct ChunkRoles {
+    uint8_t *Q, *U, *dQ, *dS, *Kb, *dWy, *dUt;
+};
+__device__ __forceinline__ ChunkRoles chunk_roles(uint8_t* sm, int kTile, bool odd) {
+    auto P = [&](int i) { return sm + i * kTile; };
+    if (odd) return ChunkRoles{P(5), P(0), P(6), P(6), P(0), P(7), P(4)};
+    return ChunkRoles{P(0), P(4), P(4), P(5), P(5), P(6), P(7)};
+}
+
 template <int D, int VAR>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -317,14 +335,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    uint8_t* Qs = sm + S::kQ;     // q -> Qb
     uint8_t* Ks = sm + S::kK;     // k -> Kr
-    uint8_t* Vs = sm + S::kV;     // v
-    uint8_t* dOs = sm + S::kdO;   // dO
-    uint8_t* dQs = sm + S::kdQ;   // U^T, then dQt^T = S dO^T
-    uint8_t* Kbs = sm + S::kKb;   // Kb
-    uint8_t* dWys = sm + S::kdWy; // -dWyA^T -> dWy^T
-    uint8_t* dUts = sm + S::kdUt; // -dU^T -> dUt^T
+    uint8_t* Vs = sm + S::kV;     // v, then dv and dk staging
+    uint8_t* dOs = sm + S::kdO;   // dO, then dv and dk staging
     uint8_t* Ts = sm + S::kT;
     uint8_t* Aqs = sm + S::kAq;   // tril(Qb Kr^T)
     uint8_t* B8a = sm + S::kB8a;  // P, then X = dT T^T
@@ -333,8 +346,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     float* Gam = reinterpret_cast<float*>(sm + S::kGam);  // KDA: g -> Gamma -> e^Gamma
     float* Xs = reinterpret_cast<float*>(sm + S::kX);
     float* beta_s = reinterpret_cast<float*>(sm + S::kSmall);
-    float* gC_s = beta_s + 64;
-    float* dgC_s = gC_s + D;
+    float* gC_b = beta_s + 64;    // [2][D]
+    float* dgC_s = gC_b + 2 * D;
     float* rowsum = dgC_s + D;    // GDN: dGamma per row
     float* Erow = rowsum + 64;    // GDN: e^{Gamma} per row
     float* Eirow = Erow + 64;     // GDN: e^{-Gamma} per row
@@ -347,10 +360,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     constexpr uint32_t C0 = 0, C1 = 64, C2 = 128, C3 = 192, C4 = 256, C_dQ = 320, C6 = 384,
                        C_dKC = 448;
     const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2, lane = tid & 31;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    int seq, row0, len;
-    chunk_info(p, chunk, seq, row0, len);
-    const size_t rec = (size_t)chunk * p.H + h;
+    const int nitems = p.num_chunks * p.H;  // work item = (chunk, head), item = chunk * H + h
     const float sc = p.scale;
     const bool f32out = p.grad_dtype == DR_F32;
 
@@ -410,13 +420,17 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
     };
     // e^{Gamma} and e^{-Gamma} of tokens t0 + 16 b .. + 15 for this thread's channel
-    auto decay16 = [&](int b, float (&e)[16], float (&ei)[16]) {
+    auto decay16 = [&](int b, float (&e)[16], float (&ei)[16], bool from_tmem = false) {
         if (VAR == DR_KDA) {
+            if (from_tmem) {
+                tmem_ld16(tl + C3 + t0 + 16 * b, e);  // copied there by the dq stage
+                tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                e[j] = gam_t[(16 * b + j) * S::kGS];  // e^Gamma, stored by the decay pass
-                ei[j] = fast_rcp(e[j]);
+                for (int j = 0; j < 16; ++j) e[j] = gam_t[(16 * b + j) * S::kGS];  // e^Gamma, from the decay pass
             }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ei[j] = fast_rcp(e[j]);
         } else if (VAR == DR_GDN) {
             load16(Erow, 16 * b, e);
             load16(Eirow, 16 * b, ei);
@@ -433,43 +447,82 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     // dGamma (GDN), is accumulated in TMEM columns C1 + t0 .. + 31 from E4 on
     float fsum = 0.f;  // sum over this thread's tokens of dKC * KC
 
-    do {
-        // Two load groups, token side first so that the decay pass and the first
-        // token-by-token products run while the state side arrives.  Token side: q, k,
-        // v, dO, the gates (KDA: one [64][D] fp32 box) and e^{Gamma_last}.  State side:
-        // S in the Aqk / P / dG / dAqk tiles, dS in the Kb / dWy tiles, U^T in the dQt
-        // tile (all idle until the state-side products have read them), -dU^T, T.
-        uint8_t* Sst = Aqs;   // [D][D] W-layout state at the chunk start
-        uint8_t* dSst = Kbs;  // [D][D] W-layout state gradient at the chunk end
-        uint8_t* Ust = dQs;   // [D][64] U^T
-        constexpr uint32_t kDD = D * D * 2;
-        // per-token scalars first, so that they do not queue behind the tile copies
-        const float beta_ld = (tid >= 64 && tid < 128 && tid - 64 < len)
-                                  ? p.beta[(size_t)(row0 + tid - 64) * p.H + h] : 0.f;
-        float gl0 = 0.f, gl1 = 0.f;  // GDN: this lane's two log-decays (warp 1)
+    constexpr uint32_t kDD = D * D * 2;
+    uint8_t* Sst = Aqs;  // [D][D] W-layout state at the chunk start, in the four 8 KB tiles
+    // State-side copies of an item: S, dS, U^T, -dU^T, T, e^{Gamma_last} (and KDA's
+    // gates, one [64][D] fp32 box) on bar_st; token side q, k, v, dO on bar_tok.
+    auto issue_state = [&](int itm, bool odd) {
+        const int c = itm / p.H, hh = itm % p.H;
+        int sq, r0, ln;
+        chunk_info(p, c, sq, r0, ln);
+        const size_t rc = (size_t)c * p.H + hh;
+        const ChunkRoles R = chunk_roles(sm, kTile, odd);
+        mbar_arrive_expect_tx(&bar_st, 2 * kTile + 2 * kDD + 8192 + D * 4 + (VAR == DR_KDA ? 64 * D * 4 : 0));
+        bulk_g2s(Sst, L.S + rc * kDD, kDD, &bar_st);
+        bulk_g2s(R.dS, L.dS + rc * kDD, kDD, &bar_st);
+        bulk_g2s(R.U, L.U + rc * kTile, kTile, &bar_st);
+        bulk_g2s(R.dUt, L.dU + rc * kTile, kTile, &bar_st);
+        bulk_g2s(Ts, L.T + rc * 8192, 8192, &bar_st);
+        bulk_g2s(gC_b + (odd ? D : 0), L.gC + rc * D, D * 4, &bar_st);
+        if (VAR == DR_KDA) tma_load_3d(Gam, &mg, &bar_st, 0, hh, r0);
+    };
+    auto issue_tok = [&](int itm, bool odd) {
+        const int c = itm / p.H, hh = itm % p.H;
+        int sq, r0, ln;
+        chunk_info(p, c, sq, r0, ln);
+        const ChunkRoles R = chunk_roles(sm, kTile, odd);
+        mbar_arrive_expect_tx(&bar_tok, 4 * kTile);
+        for (int kb = 0; kb < D / 64; ++kb) {
+            tma_load_3d(R.Q + kb * 8192, &mq, &bar_tok, kb * 64, hh, r0);
+            tma_load_3d(Ks + kb * 8192, &mk, &bar_tok, kb * 64, hh, r0);
+            tma_load_3d(Vs + kb * 8192, &mv, &bar_tok, kb * 64, hh, r0);
+            tma_load_3d(dOs + kb * 8192, &mdo, &bar_tok, kb * 64, hh, r0);
+        }
+    };
+    // per-token scalars of an item, read into registers ahead of time: beta (threads
+    // 64..127) and GDN's log-decays (two per lane of warp 1)
+    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f;
+    auto load_scalars = [&](int itm) {
+        const int c = itm / p.H, hh = itm % p.H;
+        int sq, r0, ln;
+        chunk_info(p, c, sq, r0, ln);
+        beta_ld = (tid >= 64 && tid < 128 && tid - 64 < ln) ? p.beta[(size_t)(r0 + tid - 64) * p.H + hh] : 0.f;
         if (VAR == DR_GDN && warp == 1) {
-            gl0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-            gl1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+            gl0 = 2 * lane < ln ? p.g[(size_t)(r0 + 2 * lane) * p.H + hh] : 0.f;
+            gl1 = 2 * lane + 1 < ln ? p.g[(size_t)(r0 + 2 * lane + 1) * p.H + hh] : 0.f;
         }
+    };
+    uint32_t n_st = 0, n_tok = 0;  // copy groups issued on bar_st / bar_tok
+    if ((int)blockIdx.x < nitems) {
+        load_scalars(blockIdx.x);
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_tok, 4 * kTile + D * 4 + (VAR == DR_KDA ? 64 * D * 4 : 0));
-            for (int kb = 0; kb < D / 64; ++kb) {
-                tma_load_3d(Qs + kb * 8192, &mq, &bar_tok, kb * 64, h, row0);
-                tma_load_3d(Ks + kb * 8192, &mk, &bar_tok, kb * 64, h, row0);
-                tma_load_3d(Vs + kb * 8192, &mv, &bar_tok, kb * 64, h, row0);
-                tma_load_3d(dOs + kb * 8192, &mdo, &bar_tok, kb * 64, h, row0);
-            }
-            if (VAR == DR_KDA) tma_load_3d(Gam, &mg, &bar_tok, 0, h, row0);
-            bulk_g2s(gC_s, L.gC + rec * D, D * 4, &bar_tok);
-            mbar_arrive_expect_tx(&bar_st, 2 * kTile + 2 * kDD + 8192);
-            bulk_g2s(Sst, L.S + rec * kDD, kDD, &bar_st);
-            bulk_g2s(dSst, L.dS + rec * kDD, kDD, &bar_st);
-            bulk_g2s(Ust, L.U + rec * kTile, kTile, &bar_st);
-            bulk_g2s(dUts, L.dU + rec * kTile, kTile, &bar_st);
-            bulk_g2s(Ts, L.T + rec * 8192, 8192, &bar_st);
+            issue_tok(blockIdx.x, false);
+            issue_state(blockIdx.x, false);
         }
+        n_st = n_tok = 1;
+    }
+
+    int it = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++it) {
+        const bool odd = it & 1;
+        const uint32_t ph = (uint32_t)(it & 1);
+        const int chunk = item / p.H, h = item % p.H;
+        int seq, row0, len;
+        chunk_info(p, chunk, seq, row0, len);
+        const int next = item + gridDim.x;
+        const ChunkRoles R = chunk_roles(sm, kTile, odd);
+        uint8_t* Qs = R.Q;      // q -> Qb
+        uint8_t* Ust = R.U;     // [D][64] U^T
+        uint8_t* dQs = R.dQ;    // dQt^T = S dO^T
+        uint8_t* dSst = R.dS;   // [D][D] W-layout state gradient at the chunk end
+        uint8_t* Kbs = R.Kb;    // Kb
+        uint8_t* dWys = R.dWy;  // -dWyA^T -> dWy^T
+        uint8_t* dUts = R.dUt;  // -dU^T -> dUt^T
+        float* gC_s = gC_b + (odd ? D : 0);
+        fsum = 0.f;
         if (tid >= 64 && tid < 128) beta_s[tid - 64] = beta_ld;
-        ok = mbar_wait(&bar_tok, 0, kWaitLimitNs);
+        ok = mbar_wait(&bar_tok, ph, kWaitLimitNs);
+        if (VAR == DR_KDA) ok = ok && mbar_wait(&bar_st, ph, kWaitLimitNs);  // the gates
         if (__syncthreads_or(!ok)) break;
         zero_pad_rows(Qs, D, len);
         zero_pad_rows(Ks, D, len);
@@ -573,7 +626,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             mma_tiles(tm + C3, Tile{smem_u32(Qs), 64}, false, Tile{smem_u32(Ks), 64}, false, 64, 64, D, false);
             mma_tiles(tm + C4, Tile{smem_u32(dOs), 64}, false, Tile{smem_u32(Vs), 64}, false, 64, 64, D, false);
         }
-        ok = mbar_wait(&bar_st, 0, kWaitLimitNs);
+        ok = mbar_wait(&bar_st, ph, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
 
         // M0 (M = D): dQt^T = S dO^T -> C0 ; -dWyA^T = S (-dU)^T -> C1 ; dKC^T = dS U^T -> C_dKC
@@ -837,10 +890,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) g[j] = 0.f;
+                float e16[16], ei16[16];
+                decay16(b, e16, ei16);
                 if (cl >= 0) {
                     tile_load16(dQs, cl, t0 + 16 * b, D, dqt);
-                    float e16[16], ei16[16];
-                    decay16(b, e16, ei16);
                     const uint8_t* qrow = Qs + 16 * b * 128;
                     const uint8_t* krow = Ks + 16 * b * 128;
 #pragma unroll
@@ -854,6 +907,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                     }
                 }
                 tmem_st16(tl + C1 + t0 + 16 * b, g);
+                if (VAR == DR_KDA) tmem_st16(tl + C3 + t0 + 16 * b, e16);  // for the dk stage
             }
             tmem_st_wait();
         };
@@ -903,18 +957,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
         else
             stage_copy_out<D, false>(p.dq, dUts, dWys, p, row0, len, h);
+        fence_async_smem();  // generic accesses of the buffers the next item's state goes to
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
+        // the next item's state side goes into what this item no longer reads
+        if (tid == 0 && next < nitems) issue_state(next, !odd);
+        n_st += next < nitems;
 
         // E7: dk = (dKb' + beta dbK) e^{Gamma} + (dKr' + dKC e^{Gamma_last}) e^{-Gamma}, staged
-        // in the T / Aqk / P / dG tiles (consumed), and the dKb Kb - dKr Kr part of dGamma
+        // in the v / dO tiles (consumed), and the dKb Kb - dKr Kr part of dGamma
         auto dk_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
             const float gc = cl >= 0 ? gC_s[cl] : 0.f;
 #pragma unroll 1
             for (int b = 0; b < 2; ++b) {
-                uint8_t* sb = stage_base(Ts, B8a, F32) + 16 * b * D * (F32 ? 4 : 2);
+                uint8_t* sb = stage_base(Vs, dOs, F32) + 16 * b * D * (F32 ? 4 : 2);
                 float dbk[16], dkb[16], dkr[16], dkc[16], g[16];
                 tmem_ld16(tl + C4 + t0 + 16 * b, dbk);
                 tmem_ld16(tl + C6 + t0 + 16 * b, dkb);
@@ -922,9 +980,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tmem_ld16(tl + C_dKC + t0 + 16 * b, dkc);
                 tmem_ld16(tl + C1 + t0 + 16 * b, g);
                 tmem_ld_wait();
+                float e16[16], ei16[16];
+                decay16(b, e16, ei16, true);
                 if (cl >= 0) {
-                    float e16[16], ei16[16], bt[16];
-                    decay16(b, e16, ei16);
+                    float bt[16];
                     load16(beta_s, 16 * b, bt);
                     const uint8_t* kbrow = Kbs + 16 * b * 128;
                     const uint8_t* krow = Ks + 16 * b * 128;
@@ -946,9 +1005,17 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dk_stage(BoolTag<false>{});
         __syncthreads();
         if (f32out)
-            stage_copy_out<D, true>(p.dk_, Ts, B8a, p, row0, len, h);
+            stage_copy_out<D, true>(p.dk_, Vs, dOs, p, row0, len, h);
         else
-            stage_copy_out<D, false>(p.dk_, Ts, B8a, p, row0, len, h);
+            stage_copy_out<D, false>(p.dk_, Vs, dOs, p, row0, len, h);
+        // the next item's token side goes into the Kb / Kr / staging tiles
+        fence_async_smem();
+        __syncthreads();
+        if (next < nitems) {
+            if (tid == 0) issue_tok(next, !odd);
+            load_scalars(next);
+            ++n_tok;
+        }
 
         // E8: dg_i = (dgC e^{Gamma_last} + sum_rows dKC KC) + sum_{j >= i} dGamma_j
         float dG[32];
@@ -1022,11 +1089,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 if (2 * lane + 1 < len) p.dg[(size_t)(row0 + 2 * lane + 1) * p.H + h] = e + x - a0;
             }
         }
-    } while (0);
+        tc_fence_before();
+        __syncthreads();  // Xs, TMEM and the small arrays are reused by the next item
+    }
     if (!ok) {
+        // leave no copy in flight: wait (bounded) for every group issued and not yet waited
         record_timeout(p);
-        mbar_wait(&bar_st, 0, kWaitLimitNs);
-        mbar_wait(&bar_tok, 0, kWaitLimitNs);
+        for (uint32_t q = (uint32_t)it; q < n_st; ++q) mbar_wait(&bar_st, q & 1, kWaitLimitNs);
+        for (uint32_t q = (uint32_t)it; q < n_tok; ++q) mbar_wait(&bar_tok, q & 1, kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -1074,9 +1144,19 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
             if (e != cudaSuccess) return e;
             attr = true;
         }
+        // persistent: one CTA per SM, each taking work items (chunk, head) in a stride
+        static int nsm = 0;
+        if (nsm == 0) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            if (nsm <= 0) nsm = 1;
+        }
+        const long long items = (long long)p.num_chunks * p.H;
+        const int grid = (int)(items < nsm ? items : nsm);
         {
             TraceScope ts("tc_bwd_chunk", st);
-            kernel<<<dim3(p.num_chunks, p.H), kChunkThreads, smem, st>>>(mq, mk, mv, mdo, mg, p, L);
+            kernel<<<grid, kChunkThreads, smem, st>>>(mq, mk, mv, mdo, mg, p, L);
         }
         return cudaGetLastError();
     };
