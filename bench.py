@@ -57,7 +57,6 @@ def kernel_bytes(name, w, N):
         return recs * (3 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
     if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, U^T, -dU^T, S, dS, T, gC in;
         return (th * (4 * D * 2 + 4 + g) + recs * (2 * tile + 2 * dd + 8192 + D * 4)
-                + recs * 2 * tile                       # dKC image written and reread
                 + th * (3 * D * 2 + 4 + g))             # dq, dk, dv, dbeta, dg out
     return 0
 

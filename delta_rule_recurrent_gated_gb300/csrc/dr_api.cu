@@ -26,8 +26,6 @@ namespace {
 
 constexpr size_t kHeader = 256;  // error word + padding at the start of the workspace
 
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 enum class Path { kNone, kTensor, kSimt };

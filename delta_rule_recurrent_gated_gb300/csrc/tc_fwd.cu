@@ -56,7 +56,9 @@ struct PrepSmem {
     static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kX = 3 * kTile, kY = 4 * kTile;
     static constexpr int kAq = 5 * kTile, kT = kAq + 8192;
     static constexpr int kAf = (D == 128) ? kX : kT + 8192;  // fp32 [64][64] (16 KB)
-    static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384;
+    // fp32 blocks of the inverse (12 KB): the consumed Kr tile when it is large enough
+    static constexpr int kInv = (D == 128) ? kK : kT + 8192 + 16384;
+    static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384 + 12288;
     static constexpr int kGL = kBeta + 256;              // [D] fp32 Gamma at the last token
     static constexpr int kBytes = kGL + D * 4 + 1024;    // + alignment slack
 };
@@ -134,7 +136,67 @@ __global__ void __launch_bounds__(128, 1)
         }
         __syncthreads();
 
-        // decay: the cumulative log-decay per key channel (thread c holds its channel's
+        // decay, per token (DeltaNet, GDN): warp 0 scans the 64 log-decays, two per lane, and
+        // keeps e^{Gamma}, e^{-Gamma} and e^{Gamma_last - Gamma} per token in the still-unused
+        // Aqk tile; then an elementwise pass eight channels wide
+        if (VAR != DR_KDA) {
+            float* Er = reinterpret_cast<float*>(Aqs);  // [3][64]
+            if (warp == 0) {
+                const int lane = tid & 31;
+                float a0 = 0.f, a1 = 0.f;
+                if (VAR == DR_GDN) {
+                    a0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
+                    a1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+                }
+                float x = a0 + a1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                const float GL = __shfl_sync(0xffffffffu, x, 31);
+                const float eGL = VAR != DR_DELTANET ? expf(GL) : 1.f;
+                const float e0 = VAR != DR_DELTANET ? __expf(x - a1) : 1.f;
+                const float e1 = VAR != DR_DELTANET ? __expf(x) : 1.f;
+                const float i0 = fast_rcp(e0), i1 = fast_rcp(e1);
+                Er[2 * lane] = e0;
+                Er[2 * lane + 1] = e1;
+                Er[64 + 2 * lane] = i0;
+                Er[64 + 2 * lane + 1] = i1;
+                Er[128 + 2 * lane] = eGL * i0;
+                Er[128 + 2 * lane + 1] = eGL * i1;
+                for (int c = lane; c < D; c += 32) L.gC[rec * D + c] = eGL;  // e^{Gamma_last}
+            }
+            __syncthreads();
+            uint8_t* kc_img = L.KC + rec * kTile;
+            for (int w = tid; w < 64 * (D / 8); w += 128) {
+                const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
+                const uint32_t off = sw128_offset(i, c8, 64);
+                float q8[8], k8[8], v8[8];
+                unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
+                unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
+                unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
+                const float b = beta_s[i], e = Er[i], ei = Er[64 + i], ec = Er[128 + i];
+                uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
+                    wq[j] = pack_bf16(q8[2 * j] * e, q8[2 * j + 1] * e);
+                    wr[j] = pack_bf16(k0 * ei, k1 * ei);
+                    wb[j] = pack_bf16(k0 * e, k1 * e);
+                    wy[j] = pack_bf16(b * k0 * e, b * k1 * e);
+                    wv[j] = pack_bf16(b * v8[2 * j], b * v8[2 * j + 1]);
+                    wc[j] = pack_bf16(k0 * ec, k1 * ec);
+                }
+                *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
+                *reinterpret_cast<uint4*>(Xs + off) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+                *reinterpret_cast<uint4*>(Ys + off) = make_uint4(wy[0], wy[1], wy[2], wy[3]);
+                *reinterpret_cast<uint4*>(Vs + off) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                *reinterpret_cast<uint4*>(kc_img + off) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
+            }
+        } else
+        // decay, per key channel (KDA): the cumulative log-decay (thread c holds its channel's
         // gates in registers), staged 32 rows at a time in the still-unused Aqk / T
         // buffers, then an elementwise pass eight channels wide
         {
@@ -246,33 +308,81 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_before();
         __syncthreads();
 
-        // T = (I + A)^{-1}: thread n solves column n of (I + A) x = e_n, right-looking:
-        // once x_j is final, every later row's partial sum takes its A[i][j] x_j term,
-        // so the dependent chain is one FMA per row
-        if (tid < 64) {
-            const int n = tid;
-            float x[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = (i == n) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < 63; ++j) {
-                const float xj = x[j];
-#pragma unroll
-                for (int i4 = (j + 1) & ~3; i4 < 64; i4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(&Af[j * 64 + i4]);
-                    if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
-                    if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
-                    if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
-                    if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
-                }
-            }
+        // T = (I + A)^{-1} by 2 x 2 blocks of 32: T11 = (I + A11)^{-1} and T22 = (I + A22)^{-1}
+        // side by side (thread n of each half solves column n, right-looking, so the
+        // dependent chain is one FMA per row), then T21 = -T22 (A21 T11) on all threads.
+        // fp32 throughout.
+        {
+            float* T11 = reinterpret_cast<float*>(sm + S::kInv);  // [32][32] row-major
+            float* T22 = T11 + 1024;                     // [32][32] row-major
+            float* Y = T22 + 1024;                       // [32][32] row-major, A21 T11
             uint8_t* t_img = L.T + rec * 8192;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const __nv_bfloat16 b = __float2bfloat16_rn(x[i]);
+            auto put_t = [&](int i, int n, float x) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(x);
                 const uint32_t off = sw128_offset(i, n, 64);
                 *reinterpret_cast<__nv_bfloat16*>(Ts + off) = b;
                 *reinterpret_cast<__nv_bfloat16*>(t_img + off) = b;
+            };
+            if (tid < 64) {
+                const int o = tid & 32, n = tid & 31;
+                float x[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = (i == n) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < 31; ++j) {
+                    const float xj = x[j];
+                    const float* col = Af + (o + j) * 64 + o;
+#pragma unroll
+                    for (int i4 = (j + 1) & ~3; i4 < 32; i4 += 4) {
+                        const float4 a = *reinterpret_cast<const float4*>(col + i4);
+                        if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
+                        if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
+                        if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
+                        if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
+                    }
+                }
+                float* Tb = o ? T22 : T11;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    Tb[i * 32 + n] = x[i];
+                    put_t(o + i, o + n, x[i]);
+                    put_t(i, 32 + n, 0.f);  // T12 = 0 (written twice, the same value)
+                }
+            }
+            __syncthreads();
+            // Y = A21 T11: thread (rows i0..i0+7, column n); A21[i][k] = Af[k * 64 + 32 + i]
+            const int n = tid & 31, i0 = (tid >> 5) * 8;
+            {
+                float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float t = T11[k * 32 + n];
+                    const float4 a0 = *reinterpret_cast<const float4*>(Af + k * 64 + 32 + i0);
+                    const float4 a1 = *reinterpret_cast<const float4*>(Af + k * 64 + 36 + i0);
+                    y[0] = fmaf(a0.x, t, y[0]);
+                    y[1] = fmaf(a0.y, t, y[1]);
+                    y[2] = fmaf(a0.z, t, y[2]);
+                    y[3] = fmaf(a0.w, t, y[3]);
+                    y[4] = fmaf(a1.x, t, y[4]);
+                    y[5] = fmaf(a1.y, t, y[5]);
+                    y[6] = fmaf(a1.z, t, y[6]);
+                    y[7] = fmaf(a1.w, t, y[7]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) Y[(i0 + q) * 32 + n] = y[q];
+            }
+            __syncthreads();
+            // T21 = -T22 Y
+            {
+                float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float yk = Y[k * 32 + n];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) z[q] = fmaf(T22[(i0 + q) * 32 + k], yk, z[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) put_t(32 + i0 + q, n, -z[q]);
             }
         }
         fence_async_smem();
