@@ -12,6 +12,7 @@ the timing barrier and the max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -40,6 +41,33 @@ def algorithmic(w, N):
     if w.h0:
         byts += 5 * dk * dv * 4 * N * w.H
     return flops, byts
+
+
+# DRAM bytes (read + write) per work item (chunk x head) from one ncu capture, with the
+# sha256 of the kernel source it was taken on; reported only while the source is unchanged.
+# profiles/tc_bwd_chunk_gdn_b2_t4096_h16_d128.md: 435.6 MB for 2048 items.
+MEASURED_TRAFFIC = {
+    ("tc_bwd_chunk", "gdn", 128): (435.567360e6 / 2048,
+                                   "delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
+                                   "0494880d9c6a8eab8f00e722d596cd0581f0fa427675ff08f94d69a9f70f6492"),
+}
+
+
+def measured_traffic(name, w):
+    """DRAM bytes per launch of `name` on workload w from the recorded capture, or None."""
+    rec = MEASURED_TRAFFIC.get((name, w.variant, w.dk))
+    if rec is None:
+        return None
+    per_item, src, sha = rec
+    try:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), src), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    if w.lengths is not None or w.varlen_total:
+        return None  # packed sequences: the item count depends on the drawn lengths
+    return per_item * ((w.T + 63) // 64 * w.B * w.H)
 
 
 def kernel_bytes(name, w, N):
@@ -304,7 +332,8 @@ def main():
         ach = kb / avg_s / 1e9
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
-                "traffic": None, "avg_launch_ms": tot / n, "bytes_per_launch": kb}
+                "traffic": measured_traffic(name, w), "avg_launch_ms": tot / n,
+                "bytes_per_launch": kb}
     kern = {k: {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(v[0] for v in per.values())}
             for k, (tot, n) in per.items()}
 
