@@ -175,6 +175,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 8 consecutive columns of the warp's 32 lanes (thread t: lane warp_base + t).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
 // registers -> TMEM, the same shape: thread t writes columns [col, col+16) of lane
 // (warp_base + t).  Complete (for a later tcgen05.ld of the thread) after tmem_st_wait().
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
@@ -294,6 +311,18 @@ __device__ __forceinline__ void tile_load16(const uint8_t* base, int row, int co
             v[8 * h + 2 * j] = __low2float(b);
             v[8 * h + 2 * j + 1] = __high2float(b);
         }
+    }
+}
+// Read 8 consecutive values (col0 multiple of 8) of one tile row.
+__device__ __forceinline__ void tile_load8(const uint8_t* base, int row, int col0, int rows,
+                                           float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(base + sw128_offset(row, col0, rows));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+        v[2 * j] = __low2float(b);
+        v[2 * j + 1] = __high2float(b);
     }
 }
 // Unpack 8 bf16 held in a uint4.

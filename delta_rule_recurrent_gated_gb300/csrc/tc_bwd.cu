@@ -233,16 +233,17 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ============================================================== tc_bwd_chunk
-// 256 threads.  Two accumulator shapes alternate:
+// kChunkThreads threads = kChunkThreads / 128 warp groups of four warps (one warp per
+// TMEM lane quarter).  Two accumulator shapes alternate:
 //  * token-by-token products (M = 64): row i of the accumulator sits in lane
-//    16*(i/16) + i%16 of warp quarter i/16; warps w and w+4 split its columns;
+//    16*(i/16) + i%16 of warp quarter i/16; the warp groups split its columns;
 //  * channel-by-token products (M = D, the transposes of every d-wide result):
 //    channel c sits in lane c (D = 128) or in the M = 64 lane of row c (D = 64);
-//    warps w and w+4 take tokens [0,32) and [32,64).  Everything per element of
+//    the warp groups split the 64 tokens.  Everything per element of
 //    the d-wide results (dv, dq, dk, KDA's dGamma and its reverse cumulative sum)
 //    then runs on full warps, with 32 consecutive channels of one token per
 //    warp store, and the sums over channels are warp transpose-reductions.
-constexpr int kChunkThreads = 256;
+constexpr int kChunkThreads = 512;
 
 template <int D, int VAR>
 struct BChunkSmem {
@@ -262,16 +263,22 @@ struct BChunkSmem {
     static constexpr int kSmall = kX + 8192;
     // small arrays: beta[64], e^{Gamma_last}[2][D] (this item's and the next one's),
     // dgC[D], dGamma per row[64], e^{Gamma} per row[64], e^{-Gamma} per row[64], dbeta
-    // partials of warps 4..7 [64]
-    static constexpr int kBytes = kSmall + (64 * 5 + D * 3) * 4 + 1024;
+    // partials of the other warp groups [3][64]
+    static constexpr int kBytes = kSmall + (64 * 7 + D * 3) * 4 + 1024;
 };
 
-// Sum over the 32 lanes of v[lane][k] for every k: on return lane L holds the
-// sum for k = L.  Five exchange rounds, 31 shuffles, fixed order.
-__device__ __forceinline__ float warp_transpose_sum(float (&v)[32]) {
+// Sum over the 32 lanes of v[lane][k] for every k < N (N = 16 or 32): on return lane
+// L holds the sum for k = L % N.  31 shuffles, fixed order.
+template <int N>
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[N]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
+    for (int s = 16; s >= N; s >>= 1) {  // fold lanes that share k % N
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], s);
+    }
+#pragma unroll
+    for (int s = N / 2; s >= 1; s >>= 1) {
         const bool up = (lane & s) != 0;
 #pragma unroll
         for (int k = 0; k < s; ++k) {
@@ -290,7 +297,7 @@ struct BoolTag {
 
 // A [64][D] output block staged in shared memory in the output's own element type,
 // tokens [0,32) in one buffer and [32,64) in another (a token's D values contiguous);
-// `sb` points at this thread's channel in the row of the first token of its half.
+// `sb` points at this thread's channel in the row of its first token.
 template <int D, bool F32>
 __device__ __forceinline__ void stage_put(uint8_t* sb, int k, float x) {
     if (F32)
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     float* rowsum = dgC_s + D;    // GDN: dGamma per row
     float* Erow = rowsum + 64;    // GDN: e^{Gamma} per row
     float* Eirow = Erow + 64;     // GDN: e^{-Gamma} per row
-    float* part = Eirow + 64;     // dbeta partials of warps 4..7
+    float* part = Eirow + 64;     // [3][64] dbeta partials of warp groups 1..
     __shared__ uint64_t bar_st, bar_tok, bar_mma;
     __shared__ uint32_t tmem_base;
 
@@ -359,7 +366,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     // one result from its product to its last reader.
     constexpr uint32_t C0 = 0, C1 = 64, C2 = 128, C3 = 192, C4 = 256, C_dQ = 320, C6 = 384,
                        C_dKC = 448;
-    const int tid = threadIdx.x, warp = tid >> 5, half = warp >> 2, lane = tid & 31;
+    constexpr int kG = kChunkThreads / 128, kTok = 64 / kG;  // warp groups, tokens per group
+    constexpr int kIssuer = kChunkThreads - 32;  // lane 0 of the last warp: the next item's copies
+    const int tid = threadIdx.x, warp = tid >> 5, grp = warp >> 2, lane = tid & 31;
     const int nitems = p.num_chunks * p.H;  // work item = (chunk, head), item = chunk * H + h
     const float sc = p.scale;
     const bool f32out = p.grad_dtype == DR_F32;
@@ -386,9 +395,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     const uint32_t tl = warp_lane_base(tm);
     const int r = m64_row();                            // row of an M = 64 accumulator, or -1
     const int cl = D == 128 ? (tid & 127) : r;          // channel of an M = D accumulator, or -1
-    const int t0 = 32 * half;                           // first token of this thread's column half
+    const int t0 = kTok * grp;                          // first token of this thread's group
     // Element (t0 + k, cl) of a [64][D] SW128 token tile sits at xo[k % 8] + 128 k: the
-    // swizzle depends on the row only through k % 8 because t0 is a multiple of 8.
+    // swizzle depends on the row only through k % 8 because t0 is a multiple of 16.
     uint32_t xo[8];
     {
         const int c = cl < 0 ? 0 : cl;
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
     // e^{Gamma} and e^{-Gamma} of token t0 + k for this thread's channel
     const float* gam_t = Gam + t0 * S::kGS + (cl < 0 ? 0 : cl);
-    // 16 consecutive per-token values starting at token t0 + k0 (k0 multiple of 4)
+    // 16 (8) consecutive per-token values starting at token t0 + k0 (k0 multiple of 4)
     auto load16 = [&](const float* src, int k0, float (&v)[16]) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -419,32 +428,43 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             v[4 * q + 3] = x.w;
         }
     };
-    // e^{Gamma} and e^{-Gamma} of tokens t0 + 16 b .. + 15 for this thread's channel
-    auto decay16 = [&](int b, float (&e)[16], float (&ei)[16], bool from_tmem = false) {
+    auto load8 = [&](const float* src, int k0, float (&v)[8]) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float4 x = *reinterpret_cast<const float4*>(src + t0 + k0 + 4 * q);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+        }
+    };
+    // e^{Gamma} and e^{-Gamma} of tokens t0 + 8 b .. + 7 for this thread's channel
+    auto decay8 = [&](int b, float (&e)[8], float (&ei)[8], bool from_tmem) {
         if (VAR == DR_KDA) {
             if (from_tmem) {
-                tmem_ld16(tl + C3 + t0 + 16 * b, e);  // copied there by the dq stage
+                tmem_ld8(tl + C3 + t0 + 8 * b, e);  // copied there by the dq stage
                 tmem_ld_wait();
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) e[j] = gam_t[(16 * b + j) * S::kGS];  // e^Gamma, from the decay pass
+                for (int j = 0; j < 8; ++j) e[j] = gam_t[(8 * b + j) * S::kGS];  // from the decay pass
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ei[j] = fast_rcp(e[j]);
+            for (int j = 0; j < 8; ++j) ei[j] = fast_rcp(e[j]);
         } else if (VAR == DR_GDN) {
-            load16(Erow, 16 * b, e);
-            load16(Eirow, 16 * b, ei);
+            load8(Erow, 8 * b, e);
+            load8(Eirow, 8 * b, ei);
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) e[j] = ei[j] = 1.f;
+            for (int j = 0; j < 8; ++j) e[j] = ei[j] = 1.f;
         }
     };
-    // staging base of this thread: its half's buffer, its channel
+    // staging address of (token t0, this thread's channel): tokens [0,32) in lo, [32,64) in hi
     auto stage_base = [&](uint8_t* lo, uint8_t* hi, bool f32) -> uint8_t* {
-        return (half ? hi : lo) + (cl < 0 ? 0 : cl) * (f32 ? 4 : 2);
+        const int esz = f32 ? 4 : 2;
+        return (t0 >= 32 ? hi : lo) + (t0 & 31) * D * esz + (cl < 0 ? 0 : cl) * esz;
     };
     // dGamma of this thread's channel and tokens (KDA), or its share of each token's
-    // dGamma (GDN), is accumulated in TMEM columns C1 + t0 .. + 31 from E4 on
+    // dGamma (GDN), is accumulated in TMEM columns C1 + t0 .. + kTok - 1 from E4 on
     float fsum = 0.f;  // sum over this thread's tokens of dKC * KC
 
     constexpr uint32_t kDD = D * D * 2;
@@ -641,8 +661,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         // while M0 runs: dgC[c] = sum_v dS[c, v] S[c, v] (eight channels by a block of
         // value rows per thread, partials added in a fixed order after the wait)
-        {
-            constexpr int kOct = D / 8, kGroups = kChunkThreads / kOct, kRows = D / kGroups;
+        if (tid < 256) {  // the first eight warps
+            constexpr int kOct = D / 8, kGroups = 256 / kOct, kRows = D / kGroups;
             const int c8 = (tid % kOct) * 8, g = tid / kOct;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -678,7 +698,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             *reinterpret_cast<uint4*>(Kbs + sw128_offset(w / (D / 8), (w % (D / 8)) * 8, 64)) = kbr[n];
         }
 #pragma unroll 1
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTok / 16; ++b) {
             float a[16], c_[16];
             tmem_ld16(tl + C0 + t0 + 16 * b, a);
             tmem_ld16(tl + C1 + t0 + 16 * b, c_);
@@ -704,7 +724,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_after();
         // E2: Aqk = tril(Qb Kr^T) ; P = (dO v^T - dQt Kb^T) diag(beta)
 #pragma unroll 1
-        for (int cb = half; cb < 4; cb += 2) {
+        for (int cb = grp; cb < 4; cb += kG) {
             float a[16], p1[16], p2[16];
             tmem_ld16(tl + C3 + cb * 16, a);
             tmem_ld16(tl + C4 + cb * 16, p1);
@@ -738,7 +758,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cb = half; cb < 4; cb += 2) {
+        for (int cb = grp; cb < 4; cb += kG) {
             float a[16];
             tmem_ld16(tl + C0 + cb * 16, a);
             tmem_ld_wait();
@@ -749,7 +769,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             }
         }
 #pragma unroll 1
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTok / 16; ++b) {
             float a[16], u[16];
             tmem_ld16(tl + C1 + t0 + 16 * b, a);
             tmem_ld16(tl + C2 + t0 + 16 * b, u);
@@ -797,8 +817,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) xr[k] = (uint32_t)(((((rc >> 3) & 7) ^ k) << 4) + (rc & 7) * 2);
 #pragma unroll 1
-            for (int n = 0; n < 2; ++n) {
-                const int cb = half + 2 * n;
+            for (int n = 0; n < 4 / kG; ++n) {
+                const int cb = grp + kG * n;
                 float a[16], b[16];
                 tmem_ld16(tl + C0 + cb * 16, a);
                 tmem_ld16(tl + C1 + cb * 16, b);
@@ -833,7 +853,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         auto dv_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
 #pragma unroll 1
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < kTok / 16; ++b) {
                 uint8_t* sb = stage_base(Vs, dOs, F32) + 16 * b * D * (F32 ? 4 : 2);
                 float a[16];
                 tmem_ld16(tl + C3 + t0 + 16 * b, a);
@@ -859,7 +879,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cb = half; cb < 4; cb += 2) {
+        for (int cb = grp; cb < 4; cb += kG) {
             float a[16];
             tmem_ld16(tl + C0 + cb * 16, a);
             tmem_ld_wait();
@@ -881,33 +901,34 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         auto dq_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
             const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+            uint8_t* sb0 = stage_base(dUts, dWys, F32);
 #pragma unroll 1
-            for (int b = 0; b < 2; ++b) {
-                uint8_t* sb = stage_base(dUts, dWys, F32) + 16 * b * D * (F32 ? 4 : 2);
-                float dq_[16], dkc[16], dqt[16], g[16];
-                tmem_ld16(tl + C_dQ + t0 + 16 * b, dq_);
-                tmem_ld16(tl + C_dKC + t0 + 16 * b, dkc);
+            for (int b = 0; b < kTok / 8; ++b) {
+                uint8_t* sb = sb0 + 8 * b * D * (F32 ? 4 : 2);
+                float dq_[8], dkc[8], g[8], e8[8], ei8[8];
+                tmem_ld8(tl + C_dQ + t0 + 8 * b, dq_);
+                tmem_ld8(tl + C_dKC + t0 + 8 * b, dkc);
                 tmem_ld_wait();
+                decay8(b, e8, ei8, false);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) g[j] = 0.f;
-                float e16[16], ei16[16];
-                decay16(b, e16, ei16);
+                for (int j = 0; j < 8; ++j) g[j] = 0.f;
                 if (cl >= 0) {
-                    tile_load16(dQs, cl, t0 + 16 * b, D, dqt);
-                    const uint8_t* qrow = Qs + 16 * b * 128;
-                    const uint8_t* krow = Ks + 16 * b * 128;
+                    float dqt[8];
+                    tile_load8(dQs, cl, t0 + 8 * b, D, dqt);
+                    const uint8_t* qrow = Qs + 8 * b * 128;
+                    const uint8_t* krow = Ks + 8 * b * 128;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const float qb = tok(qrow, j), kr = tok(krow, j);
                         const float dQb = fmaf(sc, dqt[j], dq_[j]);
                         const float f = dkc[j] * (kr * gc);
                         g[j] = dQb * qb - f;
                         fsum += f;
-                        stage_put<D, F32>(sb, j, dQb * e16[j]);
+                        stage_put<D, F32>(sb, j, dQb * e8[j]);
                     }
                 }
-                tmem_st16(tl + C1 + t0 + 16 * b, g);
-                if (VAR == DR_KDA) tmem_st16(tl + C3 + t0 + 16 * b, e16);  // for the dk stage
+                tmem_st8(tl + C1 + t0 + 8 * b, g);
+                if (VAR == DR_KDA) tmem_st8(tl + C3 + t0 + 8 * b, e8);  // for the dk stage
             }
             tmem_st_wait();
         };
@@ -920,7 +941,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_after();
         // E6: dA = -T^T X (strictly lower), the A part of dbeta, dG = diag(beta) dA
 #pragma unroll 1
-        for (int cb = half; cb < 4; cb += 2) {
+        for (int cb = grp; cb < 4; cb += kG) {
             float a[16], gm[16];
             tmem_ld16(tl + C0 + cb * 16, a);
             tmem_ld16(tl + C6 + cb * 16, gm);
@@ -936,7 +957,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tile_store16(B8b, r, cb * 16, 64, a);
             }
         }
-        if (half == 1 && r >= 0) part[r] = dbeta_acc;
+        if (grp > 0 && r >= 0) part[(grp - 1) * 64 + r] = dbeta_acc;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -951,8 +972,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             mma_commit(&bar_mma);
         }
         // while M6 runs: dbeta and the staged dq go out
-        if (half == 0 && r >= 0 && r < len)
-            p.dbeta[(size_t)(row0 + r) * p.H + h] = dbeta_acc + part[r];
+        if (grp == 0 && r >= 0 && r < len) {
+            float db = dbeta_acc;
+            for (int q = 1; q < kG; ++q) db += part[(q - 1) * 64 + r];
+            p.dbeta[(size_t)(row0 + r) * p.H + h] = db;
+        }
         if (f32out)
             stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
         else
@@ -961,8 +985,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        // the next item's state side goes into what this item no longer reads
-        if (tid == 0 && next < nitems) issue_state(next, !odd);
+        // the next item's state side goes into what this item no longer reads (issued by
+        // the last warp, which has the least to do in the final epilogue)
+        if (tid == kIssuer && next < nitems) issue_state(next, !odd);
         n_st += next < nitems;
 
         // E7: dk = (dKb' + beta dbK) e^{Gamma} + (dKr' + dKC e^{Gamma_last}) e^{-Gamma}, staged
@@ -970,32 +995,32 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         auto dk_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
             const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+            uint8_t* sb0 = stage_base(Vs, dOs, F32);
 #pragma unroll 1
-            for (int b = 0; b < 2; ++b) {
-                uint8_t* sb = stage_base(Vs, dOs, F32) + 16 * b * D * (F32 ? 4 : 2);
-                float dbk[16], dkb[16], dkr[16], dkc[16], g[16];
-                tmem_ld16(tl + C4 + t0 + 16 * b, dbk);
-                tmem_ld16(tl + C6 + t0 + 16 * b, dkb);
-                tmem_ld16(tl + C2 + t0 + 16 * b, dkr);
-                tmem_ld16(tl + C_dKC + t0 + 16 * b, dkc);
-                tmem_ld16(tl + C1 + t0 + 16 * b, g);
+            for (int b = 0; b < kTok / 8; ++b) {
+                uint8_t* sb = sb0 + 8 * b * D * (F32 ? 4 : 2);
+                float dbk[8], dkb[8], dkr[8], dkc[8], g[8], e8[8], ei8[8];
+                tmem_ld8(tl + C4 + t0 + 8 * b, dbk);
+                tmem_ld8(tl + C6 + t0 + 8 * b, dkb);
+                tmem_ld8(tl + C2 + t0 + 8 * b, dkr);
+                tmem_ld8(tl + C_dKC + t0 + 8 * b, dkc);
+                tmem_ld8(tl + C1 + t0 + 8 * b, g);
                 tmem_ld_wait();
-                float e16[16], ei16[16];
-                decay16(b, e16, ei16, true);
+                decay8(b, e8, ei8, true);
                 if (cl >= 0) {
-                    float bt[16];
-                    load16(beta_s, 16 * b, bt);
-                    const uint8_t* kbrow = Kbs + 16 * b * 128;
-                    const uint8_t* krow = Ks + 16 * b * 128;
+                    float bt[8];
+                    load8(beta_s, 8 * b, bt);
+                    const uint8_t* kbrow = Kbs + 8 * b * 128;
+                    const uint8_t* krow = Ks + 8 * b * 128;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const float kb = tok(kbrow, j), kr = tok(krow, j);
                         const float dKb = fmaf(bt[j], dbk[j], dkb[j]);
                         g[j] += dKb * kb - dkr[j] * kr;
-                        stage_put<D, F32>(sb, j, dKb * e16[j] + fmaf(dkc[j], gc, dkr[j]) * ei16[j]);
+                        stage_put<D, F32>(sb, j, dKb * e8[j] + fmaf(dkc[j], gc, dkr[j]) * ei8[j]);
                     }
                 }
-                tmem_st16(tl + C1 + t0 + 16 * b, g);
+                tmem_st8(tl + C1 + t0 + 8 * b, g);
             }
             tmem_st_wait();
         };
@@ -1012,47 +1037,42 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         fence_async_smem();
         __syncthreads();
         if (next < nitems) {
-            if (tid == 0) issue_tok(next, !odd);
+            if (tid == kIssuer) issue_tok(next, !odd);
             load_scalars(next);
             ++n_tok;
         }
 
         // E8: dg_i = (dgC e^{Gamma_last} + sum_rows dKC KC) + sum_{j >= i} dGamma_j
-        float dG[32];
+        float dG[kTok];
         if (VAR != DR_DELTANET) {
-            float g0[16], g1[16];
             tc_fence_after();
-            tmem_ld16(tl + C1 + t0, g0);
-            tmem_ld16(tl + C1 + t0 + 16, g1);
-            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                dG[j] = g0[j];
-                dG[16 + j] = g1[j];
+            for (int b = 0; b < kTok / 16; ++b) {
+                float g16[16];
+                tmem_ld16(tl + C1 + t0 + 16 * b, g16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dG[16 * b + j] = g16[j];
             }
         }
         if (VAR == DR_KDA) {
-            // the two token halves of a channel exchange their totals
-            float* sg1 = Xs;        // [D] sum of dGamma over tokens [32, 64)
-            float* f0 = Xs + D;     // [D] sum of dKC KC over tokens [0, 32)
-            float* f1 = Xs + 2 * D; // [D] ... over tokens [32, 64)
+            // the token groups of a channel exchange their totals
+            float* sgq = Xs;           // [kG][D] sum of dGamma over each group's tokens
+            float* fq = Xs + kG * D;   // [kG][D] sum of dKC KC over each group's tokens
             float sg = 0.f;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) sg += dG[k];
+            for (int k = 0; k < kTok; ++k) sg += dG[k];
             if (cl >= 0) {
-                if (half == 1) {
-                    sg1[cl] = sg;
-                    f1[cl] = fsum;
-                } else {
-                    f0[cl] = fsum;
-                }
+                sgq[grp * D + cl] = sg;
+                fq[grp * D + cl] = fsum;
             }
             __syncthreads();
             if (cl >= 0) {
-                float run = dgC_s[cl] * gC_s[cl] + f0[cl] + f1[cl];
-                if (half == 0) run += sg1[cl];
+                float run = dgC_s[cl] * gC_s[cl];
+                for (int q = 0; q < kG; ++q) run += fq[q * D + cl];
+                for (int q = grp + 1; q < kG; ++q) run += sgq[q * D + cl];
 #pragma unroll
-                for (int k = 31; k >= 0; --k) {
+                for (int k = kTok - 1; k >= 0; --k) {
                     const int i = t0 + k;
                     run += dG[k];
                     if (i < len) p.dg[((size_t)(row0 + i) * p.H + h) * D + cl] = run;
@@ -1060,9 +1080,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             }
         } else if (VAR == DR_GDN) {
             float* red = Xs;          // [4 channel quarters][64 rows]
-            float* fw = Xs + 256;     // [8 warps]
-            const float rs = warp_transpose_sum(dG);  // row t0 + lane, this warp's channels
-            red[(warp & 3) * 64 + t0 + lane] = rs;
+            float* fw = Xs + 256;     // [kChunkThreads / 32 warps]
+            const float rs = warp_transpose_sum<kTok>(dG);  // row t0 + lane % kTok, this warp's channels
+            if (lane < kTok) red[(warp & 3) * 64 + t0 + lane] = rs;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) fsum += __shfl_xor_sync(0xffffffffu, fsum, o);
             if (lane == 0) fw[warp] = fsum;
