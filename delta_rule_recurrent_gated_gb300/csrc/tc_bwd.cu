@@ -167,14 +167,19 @@ __global__ void __launch_bounds__(128, 1)
         ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
-        for (int g = 0; g < 4; ++g) {
-            float acc[16];
+        for (int g = 0; g < 4; g += 2) {  // two loads in flight per wait
+            float acc[16], acc2[16];
             tmem_ld16(tl + g * 16, acc);
+            tmem_ld16(tl + (g + 1) * 16, acc2);
             tmem_ld_wait();
             if (r >= 0) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = -acc[j];
+                for (int j = 0; j < 16; ++j) {
+                    acc[j] = -acc[j];
+                    acc2[j] = -acc2[j];
+                }
                 tile_store16(dUs, r, g * 16, BV, acc);
+                tile_store16(dUs, r, (g + 1) * 16, BV, acc2);
             }
         }
         fence_async_smem();
@@ -198,17 +203,23 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
         const float* gCs = reinterpret_cast<const float*>(st + S::kG);
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb) {
-            float acc[16];
+        for (int cb = 0; cb < D / 16; cb += 2) {  // two loads in flight per wait
+            float acc[16], acc2[16];
             tmem_ld16(tl + 64 + cb * 16, acc);
+            tmem_ld16(tl + 64 + (cb + 1) * 16, acc2);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int c = cb * 16 + j;
                 W[c] = fmaf(W[c], gCs[c], acc[j]);
                 acc[j] = W[c];
+                W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                acc2[j] = W[c + 16];
             }
-            if (r >= 0) tile_store16(Ws, r, cb * 16, BV, acc);
+            if (r >= 0) {
+                tile_store16(Ws, r, cb * 16, BV, acc);
+                tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
+            }
         }
         fence_async_smem();
         tc_fence_before();

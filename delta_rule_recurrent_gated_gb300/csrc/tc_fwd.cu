@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(128, 1)
 
         {
             uint8_t* wy_img = L.Wy + rec * kTile;
-            __nv_bfloat16* utT = reinterpret_cast<__nv_bfloat16*>(L.UtT + rec * kTile);
+            uint8_t* utT = L.UtT + rec * kTile;  // [D][64] SW128 tile image of Ut^T
             for (int cb = 0; cb < D / 16; ++cb) {
                 float w16[16], u16[16];
                 tmem_ld16(tl + cb * 16, w16);
@@ -414,7 +414,8 @@ __global__ void __launch_bounds__(128, 1)
                     tile_store16(Ks, r, cb * 16, 64, u16);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        utT[(cb * 16 + j) * 64 + r] = __float2bfloat16_rn(u16[j]);
+                        *reinterpret_cast<__nv_bfloat16*>(utT + sw128_offset(cb * 16 + j, r, D)) =
+                            __float2bfloat16_rn(u16[j]);
                 }
             }
         }
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(128, 1)
 
         {
             uint8_t* qt_img = L.Qt + rec * kTile;
-            __nv_bfloat16* otT = reinterpret_cast<__nv_bfloat16*>(L.OtT + rec * kTile);
+            uint8_t* otT = L.OtT + rec * kTile;  // [D][64] SW128 tile image of Ot^T
             const float sc = p.scale;
             for (int cb = 0; cb < D / 16; ++cb) {
                 float w16[16], u16[16], qb[16];
@@ -450,7 +451,8 @@ __global__ void __launch_bounds__(128, 1)
                     tile_store16(qt_img, r, cb * 16, 64, qb);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        otT[(cb * 16 + j) * 64 + r] = __float2bfloat16_rn(sc * u16[j]);
+                        *reinterpret_cast<__nv_bfloat16*>(otT + sw128_offset(cb * 16 + j, r, D)) =
+                            __float2bfloat16_rn(sc * u16[j]);
                 }
             }
         }
@@ -600,15 +602,19 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
                 tmem_ld16(tl + (g + 1) * 16, acc2);
                 tmem_ld_wait();
                 if (r >= 0) {
+                    // row r of the swizzled Ut^T rows: 16-byte chunk q sits at q ^ (r % 8)
                     float ut[16];
-                    const uint4* up = reinterpret_cast<const uint4*>(st + S::kUt + r * 128 + g * 32);
-                    unpack8(up[0], ut);
-                    unpack8(up[1], ut + 8);
+                    const uint8_t* urow = st + S::kUt + r * 128;
+                    auto uchunk = [&](int q) {
+                        return *reinterpret_cast<const uint4*>(urow + (((2 * g + q) ^ (r & 7)) << 4));
+                    };
+                    unpack8(uchunk(0), ut);
+                    unpack8(uchunk(1), ut + 8);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] = ut[j] - acc[j];
                     tile_store16(Us, r, g * 16, BV, acc);
-                    unpack8(up[2], ut);
-                    unpack8(up[3], ut + 8);
+                    unpack8(uchunk(2), ut);
+                    unpack8(uchunk(3), ut + 8);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc2[j] = ut[j] - acc2[j];
                     tile_store16(Us, r, (g + 1) * 16, BV, acc2);
@@ -660,10 +666,10 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
                 tmem_ld16(tl + 64 + g * 16, oacc);
                 tmem_ld_wait();
                 if (r >= 0) {
-                    float ot[16];
-                    const uint4* op = reinterpret_cast<const uint4*>(st + S::kOt + r * 128 + g * 32);
-                    unpack8(op[0], ot);
-                    unpack8(op[1], ot + 8);
+                    float ot[16];  // swizzled like the Ut^T rows
+                    const uint8_t* orow = st + S::kOt + r * 128;
+                    unpack8(*reinterpret_cast<const uint4*>(orow + (((2 * g) ^ (r & 7)) << 4)), ot);
+                    unpack8(*reinterpret_cast<const uint4*>(orow + (((2 * g + 1) ^ (r & 7)) << 4)), ot + 8);
                     const int jmax = min(16, len - g * 16);
                     if (p.out_dtype == DR_F32) {
                         float* dst = static_cast<float*>(p.o) + base + (size_t)g * 16 * stride;

@@ -5,7 +5,7 @@
 // tc.cuh) so a kernel fetches one with a single untiled bulk copy.
 //   Wy, Qt, KC        : [64 tokens][D] tile images             (64*D*2 bytes)
 //   U, dU             : [D value channels][64 tokens] tile images of U^T and -dU^T
-//   UtT, OtT          : [D][64] plain bf16, transposed         (D*64*2 bytes)
+//   UtT, OtT          : [D][64] tile images of Ut^T and Ot^T   (D*64*2 bytes)
 //   T                 : [64][64] tile image of the UT inverse  (8 KB)
 //   S, dS             : [D rows = value channel][D cols = key channel] tile images
 //                       (W layout) of the state at the chunk start / of dL/d(state
