@@ -89,6 +89,50 @@ def kernel_bytes(name, w, N):
     return 0
 
 
+DECODE_B, DECODE_H, DECODE_D = 256, 16, 128
+
+
+def decode_bench(dev, stream, max_over_ranks, barrier, steps=20, warmup=3):
+    """The recurrent step (dr_decode) at serving batch: GDN, 256 sequences x 16 heads,
+    d = 128, one bf16 token per sequence per call, state [256, 16, 128, 128] fp32
+    (256 MiB, larger than L2) updated in place.  HBM-bound on the state: the roofline
+    bytes of a call are one read and one write of the state plus the token rows."""
+    import torch
+    from delta_rule_recurrent_gated_gb300 import binding
+    B, H, D = DECODE_B, DECODE_H, DECODE_D
+    gen = torch.Generator().manual_seed(0)
+    q = torch.nn.functional.normalize(torch.randn(B, 1, H, D, generator=gen), dim=-1)
+    k = torch.nn.functional.normalize(torch.randn(B, 1, H, D, generator=gen), dim=-1)
+    v = torch.randn(B, 1, H, D, generator=gen)
+    beta = torch.sigmoid(torch.randn(B, 1, H, generator=gen))
+    g = -torch.nn.functional.softplus(torch.randn(B, 1, H, generator=gen)) * 0.1
+    state = torch.randn(B, H, D, D, generator=gen) * 0.02
+    q, k, v = (t.to(torch.bfloat16).to(dev) for t in (q, k, v))
+    beta, g, state = beta.to(dev), g.to(dev), state.to(dev)
+    dec = binding.Decoder("gdn", B, 1, H, D, D, io="bf16", out="bf16", device=dev)
+    o = torch.empty(B, 1, H, D, dtype=torch.bfloat16, device=dev)
+    for _ in range(warmup):
+        dec.step(q, k, v, beta, g, state, o=o)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        dec.step(q, k, v, beta, g, state, o=o)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    nbytes = 2 * B * H * D * D * 4 + B * H * (4 * D * 2 + 8)
+    hbm, _, peak_src = measured_peaks()
+    ach = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"gdn_decode_b{B}_h{H}_d{D}_1tok", "value": B / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_call": ms, "steps": steps, "warmup": warmup,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "frac": ach / hbm, "bytes_per_call": nbytes,
+                         "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -233,6 +277,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the recurrent-step (dr_decode) measurement")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -410,6 +456,8 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "pipelining": "2 buffer sets; inputs in on one copy stream, results out on another"}
 
+    dec = None if args.no_decode else decode_bench(dev, stream, max_over_ranks, barrier)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -433,6 +481,7 @@ def main():
         "kernels": kern,
         "cpu_baseline": base,
         "e2e": e2e,
+        "decode": dec,
         "gpu_launches": len(launches),
         "clocks": clk,
     }

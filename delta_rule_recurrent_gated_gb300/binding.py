@@ -67,6 +67,8 @@ def load(path: str = LIB_PATH):
     lib.dr_error_string.restype = ctypes.c_char_p
     lib.dr_fwd_noalloc.argtypes = [D] + [P] * 8 + [P]
     lib.dr_fwd_noalloc.restype = I
+    lib.dr_decode.argtypes = [D] + [P] * 7 + [P]
+    lib.dr_decode.restype = I
     lib.dr_trace_enable.argtypes = [I]
     lib.dr_trace_enable.restype = I
     lib.dr_trace_count.argtypes = []
@@ -117,6 +119,10 @@ def dr_bwd(desc, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, 
            stream) -> int:
     return load().dr_bwd(ctypes.byref(desc), q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta,
                          dg, dh0, ws, ws_bytes, stream)
+
+
+def dr_decode(desc, q, k, v, beta, g, state, o, stream) -> int:
+    return load().dr_decode(ctypes.byref(desc), q, k, v, beta, g, state, o, stream)
 
 
 def check_status(ws, stream) -> int:
@@ -234,3 +240,34 @@ class Problem:
 
     def status(self) -> int:
         return check_status(self.ws.data_ptr(), self._stream())
+
+
+class Decoder:
+    """Descriptor for the recurrent (token-by-token) step: `step` enqueues dr_decode
+    on the current torch stream and updates `state` ([B, H, dk, dv] fp32) in place."""
+
+    def __init__(self, variant, B, T, H, dk, dv, io="bf16", out="f32", scale=1.0,
+                 device="cuda"):
+        import torch
+        self.device = torch.device(device)
+        d = DrDesc()
+        d.B, d.T, d.H, d.d_k, d.d_v, d.chunk = B, T, H, dk, dv, 1
+        d.variant = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+        code = {"bf16": DR_BF16, "f32": DR_F32}
+        d.io_dtype, d.out_dtype, d.grad_dtype = code[io], code[out], code[out]
+        d.scale = float(scale)
+        d.flags = 0
+        d.num_seqs = B
+        d.cu_seqlens = d.chunk_table = d.chunk_offsets = None
+        d.num_chunks = 0
+        self.desc = d
+        self.out_dtype = torch.bfloat16 if out == "bf16" else torch.float32
+
+    def step(self, q, k, v, beta, g, state, o=None):
+        import torch
+        d = self.desc
+        if o is None:
+            o = torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.out_dtype, device=self.device)
+        _check(dr_decode(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state), _ptr(o),
+                         torch.cuda.current_stream(self.device).cuda_stream), "dr_decode")
+        return o

@@ -1,0 +1,120 @@
+// decode.cu -- the recurrent step of the delta rule, token by token, on a state
+// that stays resident in fp32 (inference: one or a few new tokens per sequence).
+//
+// Per (sequence n, head h), for each token t of the call in order, on
+// S = W^T in [d_k][d_v] (the layout of h0 / hT):
+//   S~ = D_t S                         (decay rows: DeltaNet none, GDN e^{g_t},
+//                                       KDA e^{g_t[c]} on key channel c)
+//   r  = v_t - S~^T k_t                (the residual the write corrects)
+//   S  = S~ + beta_t k_t r^T           (delta-rule write)
+//   o_t = scale S^T q_t                (read after the write)
+// which is "The Delta Rule and its gated forms" recurrence step read directly,
+// without chunking.
+//
+// One CTA per (sequence, head, 32 value columns): warp w owns key rows
+// [w*R, (w+1)*R) of those columns, lane j column v0 + j, so every state row is
+// read and written as 32 consecutive floats.  The two sums over key channels
+// per token (S~^T k and S^T q) are per-thread partials over R rows, combined
+// across the eight warps through shared memory in a fixed order.
+#include "common.cuh"
+#include "trace.cuh"
+
+namespace dr {
+namespace {
+
+constexpr int kDecodeThreads = 256;  // eight warps
+
+template <int DK>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_kernel(const Params p, float* __restrict__ state) {
+    constexpr int R = DK / 8;  // key rows per warp
+    const int nh = blockIdx.x, n = nh / p.H, h = nh % p.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ncol = min(32, p.dv);
+    const int v = blockIdx.y * ncol + lane;
+    const bool col = lane < ncol;
+    __shared__ float qs[DK], ks[DK], as[DK], vs[32];
+    __shared__ float red[8][33];
+    __shared__ float bsh;
+
+    float* Sg = state + ((size_t)n * p.H + h) * DK * p.dv;
+    float S[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) S[i] = col ? Sg[(size_t)(warp * R + i) * p.dv + v] : 0.f;
+
+    for (int t = 0; t < p.T; ++t) {
+        const size_t tok = (size_t)n * p.T + t;
+        const size_t rk = (tok * p.H + h) * DK, rv = (tok * p.H + h) * p.dv;
+        for (int c = threadIdx.x; c < DK; c += kDecodeThreads) {
+            qs[c] = ld_any(p.q, rk + c, p.io_dtype);
+            ks[c] = ld_any(p.k, rk + c, p.io_dtype);
+            float a = 1.f;
+            if (p.variant == DR_GDN) a = expf(p.g[tok * p.H + h]);
+            else if (p.variant == DR_KDA) a = expf(p.g[rk + c]);
+            as[c] = a;
+        }
+        if (warp == 0) {
+            vs[lane] = col ? ld_any(p.v, rv + v, p.io_dtype) : 0.f;
+            if (lane == 0) bsh = p.beta[tok * p.H + h];
+        }
+        __syncthreads();
+        // decay, then this thread's part of (S~^T k)[v]
+        float pk = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int c = warp * R + i;
+            S[i] *= as[c];
+            pk = fmaf(S[i], ks[c], pk);
+        }
+        red[warp][lane] = pk;
+        __syncthreads();
+        float sk = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sk += red[w][lane];
+        const float br = bsh * (vs[lane] - sk);  // beta * r[v]
+        float pq = 0.f;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int c = warp * R + i;
+            S[i] = fmaf(ks[c], br, S[i]);
+            pq = fmaf(S[i], qs[c], pq);
+        }
+        __syncthreads();  // every warp has read red[] and the token's inputs
+        red[warp][lane] = pq;
+        __syncthreads();
+        if (warp == 0 && col) {
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) o += red[w][lane];
+            st_any(p.o, rv + v, p.out_dtype, p.scale * o);
+        }
+        __syncthreads();  // red[] and the inputs are rewritten by the next token
+    }
+    if (col) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) Sg[(size_t)(warp * R + i) * p.dv + v] = S[i];
+    }
+}
+
+template <int DK>
+cudaError_t launch(const Params& p, float* state, cudaStream_t st) {
+    const int ncol = p.dv < 32 ? p.dv : 32;
+    TraceScope ts("decode", st);
+    decode_kernel<DK><<<dim3(p.B * p.H, p.dv / ncol), kDecodeThreads, 0, st>>>(p, state);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// d_k in {16, 32, 64, 128}; d_v in {16, 32, 64, 128}; checked by the caller.
+cudaError_t decode(const Params& p, float* state, cudaStream_t st) {
+    if (p.B == 0 || p.T == 0) return cudaSuccess;
+    switch (p.dk) {
+        case 16: return launch<16>(p, state, st);
+        case 32: return launch<32>(p, state, st);
+        case 64: return launch<64>(p, state, st);
+        default: return launch<128>(p, state, st);
+    }
+}
+
+}  // namespace dr

@@ -18,6 +18,7 @@ cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse);
 cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st);
 int simt_noalloc_max_units();
 cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st);
+cudaError_t decode(const Params& p, float* state, cudaStream_t st);
 }  // namespace dr
 
 using dr::Params;
@@ -198,6 +199,34 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
     }
     if (path == Path::kSimt) return cuda_status(dr::simt_bwd(p, st));
     return cuda_status(dr::tc_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
+}
+
+int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
+              const float* beta, const float* g, float* state, void* o, void* stream) {
+    if (!desc) return DR_ERR_INVALID_ARG;
+    const dr_desc& d = *desc;
+    if (d.B < 0 || d.T < 0 || d.H < 1 || d.d_k < 1 || d.d_v < 1 || d.chunk < 1)
+        return DR_ERR_INVALID_ARG;
+    if (d.variant < DR_DELTANET || d.variant > DR_KDA) return DR_ERR_INVALID_ARG;
+    for (int t : {d.io_dtype, d.out_dtype})
+        if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
+    if (!std::isfinite(d.scale)) return DR_ERR_INVALID_ARG;
+    if (d.cu_seqlens || d.chunk_table || d.chunk_offsets || d.num_seqs != d.B)
+        return DR_ERR_INVALID_ARG;
+    if ((long long)d.B * d.T * d.H * (d.d_k > d.d_v ? d.d_k : d.d_v) >= (1ll << 40))
+        return DR_ERR_INVALID_ARG;
+    auto size_ok = [](int x) { return x == 16 || x == 32 || x == 64 || x == 128; };
+    if (!size_ok(d.d_k) || !size_ok(d.d_v)) return DR_ERR_UNSUPPORTED;
+    if (d.B > 0 && !state) return DR_ERR_INVALID_ARG;
+    const long long tokens = (long long)d.B * d.T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
+    if (tokens > 0 && ((d.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, beta, g, state, o};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    Params p = make_params(desc);
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.o = o;
+    return cuda_status(dr::decode(p, state, static_cast<cudaStream_t>(stream)));
 }
 
 int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void* v,

@@ -159,6 +159,29 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
                    const float* beta, const float* g, const float* h0, void* o, float* hT,
                    void* stream);
 
+/*
+ * Recurrent step for inference (decode): the delta-rule recurrence applied
+ * token by token, without chunks, to a state that the caller keeps between
+ * calls ("The Delta Rule and its gated forms", the per-token update with the
+ * decay applied before the residual and the read after the write).
+ *   For every sequence n < desc->B, head h and token t < desc->T in order:
+ *     S~ = D_t S;  r = v_t - S~^T k_t;  S = S~ + beta_t k_t r^T;  o_t = scale S^T q_t
+ *   with S = W^T and D_t = I (DeltaNet), e^{g_t} I (GDN) or diag(e^{g_t}) (KDA).
+ * state: [B][H][d_k][d_v] fp32 (the layout of h0 / hT), read at entry and
+ *   overwritten with the state after the last token; device memory owned by
+ *   the caller, never NULL.
+ * q, k: [B][T][H][d_k]; v, o: [B][T][H][d_v] in io_dtype / out_dtype;
+ *   beta [B][T][H] fp32; g as for dr_fwd (NULL for DeltaNet).  Dense batches
+ *   only (cu_seqlens NULL); desc->chunk is ignored (any value >= 1).
+ * Supported: d_k, d_v in {16, 32, 64, 128}, io bf16 or fp32.  No workspace,
+ *   nothing allocated, no device synchronisation; stream-ordered on `stream`.
+ * Errors: DR_ERR_INVALID_ARG (bad desc, NULL state or input, packed layout),
+ *   DR_ERR_UNSUPPORTED (sizes), DR_ERR_ALIGNMENT (pointers not 16-byte
+ *   aligned), DR_ERR_CUDA (launch failure).  Nothing is launched on error.
+ */
+int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
+              const float* beta, const float* g, float* state, void* o, void* stream);
+
 /* Synchronise `stream` and report any device-side error recorded in the
    workspace by the last call that used it (DR_OK or DR_ERR_TIMEOUT), or
    DR_ERR_CUDA when the stream itself failed. */

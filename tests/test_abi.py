@@ -161,3 +161,18 @@ def test_plan_varlen_errors(lib):
     tab = np.zeros(4, dtype=np.int32)
     assert lib.dr_plan_varlen(ok.ctypes.data, 1, 64, tab.ctypes.data, None, 2, ctypes.byref(n)) == B.DR_ERR_INVALID_ARG
     assert n.value == 4
+
+
+def test_decode_rejects_bad_arguments_before_launch(lib):
+    """dr_decode validates on the host: NULL state, packed layout, sizes outside
+    {16, 32, 64, 128}, misaligned pointers."""
+    d = desc(T=1)
+    p16 = 16
+    call = lambda dd, state=p16, q=p16: lib.dr_decode(ctypes.byref(dd), q, p16, p16, p16, p16,
+                                                        state, p16, None)
+    assert call(d, state=None) == B.DR_ERR_INVALID_ARG
+    assert call(desc(T=1, d_k=96)) == B.DR_ERR_UNSUPPORTED
+    assert call(desc(T=1, num_seqs=3)) == B.DR_ERR_INVALID_ARG
+    assert call(d, q=18) == B.DR_ERR_ALIGNMENT
+    dn = desc(T=1, variant=B.DR_DELTANET)
+    assert call(dn) == B.DR_ERR_INVALID_ARG  # a gate pointer for DeltaNet
