@@ -60,9 +60,9 @@ def _load():
             P = ctypes.c_void_p
             I = ctypes.c_int
             common = [I, I, I, I, I, I, ctypes.c_double, P, I, P, I]
-            lib.dro_forward.argtypes = common + [P] * 8 + [I]
+            lib.dro_forward.argtypes = common + [P] * 9 + [I]
             lib.dro_forward.restype = I
-            lib.dro_backward.argtypes = common + [P] * 14 + [I]
+            lib.dro_backward.argtypes = common + [P] * 15 + [I]
             lib.dro_backward.restype = I
             lib.dro_max_threads.argtypes = []
             lib.dro_max_threads.restype = I
@@ -102,8 +102,9 @@ def _dims(q, v, cu_seqlens):
 
 
 def forward(variant, q, k, v, beta, g=None, h0=None, scale=1.0, cu_seqlens=None,
-            units=None, nthreads=0):
-    """Run the recurrence forward.  Returns (o, hT) as fp64 numpy arrays.
+            units=None, nthreads=0, want_u=False):
+    """Run the recurrence forward.  Returns (o, hT) as fp64 numpy arrays, or
+    (o, hT, u) with ``want_u``: the write u_t = beta_t r_t, [B,T,H,dv].
 
     Shapes: q, k [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H]; g [B,T,H] (GDN) or
     [B,T,H,dk] (KDA) holding log(alpha); h0 [N,H,dk,dv] or None (zero state).
@@ -117,21 +118,23 @@ def forward(variant, q, k, v, beta, g=None, h0=None, scale=1.0, cu_seqlens=None,
     B, T, H, dk, dv, N = _dims(q, v, cu)
     o = np.zeros((B, T, H, dv))
     hT = np.zeros((N, H, dk, dv))
+    u = np.zeros((B, T, H, dv)) if want_u else None
     rc = _load().dro_forward(B, T, H, dk, dv, vid, float(scale), _ptr(cu), N,
                              _ptr(un), 0 if un is None else len(un),
                              _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
-                             _ptr(o), _ptr(hT), int(nthreads))
+                             _ptr(o), _ptr(hT), _ptr(u), int(nthreads))
     if rc != 0:
         raise ValueError("oracle forward: bad shape or arguments")
-    return o, hT
+    return (o, hT, u) if want_u else (o, hT)
 
 
 def backward(variant, q, k, v, beta, g, h0, dO, dhT=None, scale=1.0,
-             cu_seqlens=None, units=None, nthreads=0):
-    """Reverse-time gradients.  Returns dict dq, dk, dv, dbeta, dg (None for
-    DeltaNet), dh0 (fp64 numpy)."""
+             cu_seqlens=None, units=None, nthreads=0, dU=None):
+    """Reverse-time gradients of L = sum(dO*o) + sum(dhT*hT) (+ sum(dU*u) when dU,
+    the gradient of the emitted write u, is given).  Returns dict dq, dk, dv,
+    dbeta, dg (None for DeltaNet), dh0 (fp64 numpy)."""
     vid = VARIANTS[variant] if isinstance(variant, str) else int(variant)
-    q, k, v, beta, g, h0, dO, dhT = map(_f64, (q, k, v, beta, g, h0, dO, dhT))
+    q, k, v, beta, g, h0, dO, dhT, dU = map(_f64, (q, k, v, beta, g, h0, dO, dhT, dU))
     cu = _i32(cu_seqlens)
     un = _i32(units)
     B, T, H, dk, dv, N = _dims(q, v, cu)
@@ -144,7 +147,7 @@ def backward(variant, q, k, v, beta, g, h0, dO, dhT=None, scale=1.0,
     rc = _load().dro_backward(B, T, H, dk, dv, vid, float(scale), _ptr(cu), N,
                               _ptr(un), 0 if un is None else len(un),
                               _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
-                              _ptr(dO), _ptr(dhT), _ptr(dq), _ptr(dk_), _ptr(dv_),
+                              _ptr(dO), _ptr(dhT), _ptr(dU), _ptr(dq), _ptr(dk_), _ptr(dv_),
                               _ptr(dbeta), _ptr(dg), _ptr(dh0), int(nthreads))
     if rc != 0:
         raise ValueError("oracle backward: bad shape or arguments")

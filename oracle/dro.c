@@ -22,6 +22,11 @@
  *   written       W_t  = Wd_t + beta_t r_t k_t^T    (write strength beta_t)
  *   read          o_t  = scale * W_t q_t            (read after the write)
  *
+ * Optionally the forward also returns the write u_t = beta_t r_t, the delta-rule
+ * write error scaled by its write strength (section "Metodologia y Marco de
+ * Trabajo", item 3, "Enrutamiento entre Capas", CLER: the write error of one
+ * layer is forwarded to the next), and the backward then accepts dL/du_t.
+ *
  * The gate enters as g = log(alpha) (fp64 here), so a_t = exp(g_t).
  * The write strength beta_t, the read o = W q and the read-after-write order
  * are the standard delta-rule reading of that notation; the pages name a
@@ -32,7 +37,8 @@
  * down to 1).  With G = dL/dW_t (d_v x d_k), initialised to dL/dW_L:
  *
  *   G   += scale * dO_t q_t^T          dq_t = scale * W_t^T dO_t
- *   dr   = beta_t G k_t                dbeta_t = r_t . (G k_t)      dv_t = dr
+ *   dr   = beta_t (G k_t + du_t)       dbeta_t = r_t . (G k_t + du_t)   dv_t = dr
+ *          (du_t = dL/du_t of the emitted write, zero when it is not used)
  *   dk_t = beta_t G^T r_t - Wd_t^T dr
  *   dWd  = G - dr k_t^T
  *   dg_t[c] = a_t[c] * sum_i dWd[i][c] * W_{t-1}[i][c]   (KDA, per channel;
@@ -161,7 +167,7 @@ static int check_shape(const shape_t *s)
 
 static void fwd_unit(const shape_t *s, int u, const double *q, const double *k,
                      const double *v, const double *beta, const double *g,
-                     const double *h0, double *o, double *hT)
+                     const double *h0, double *o, double *hT, double *uw)
 {
     const int dk = s->dk, dv = s->dv, H = s->H;
     const int n = u / H, hd = u % H;
@@ -179,6 +185,10 @@ static void fwd_unit(const shape_t *s, int u, const double *q, const double *k,
         const double *vt = v + (row * H + hd) * dv;
         decay_of(s, g, row, hd, a);
         step(s, W, a, kt, vt, beta[row * H + hd], r);
+        if (uw) {
+            double *ut = uw + (row * H + hd) * dv;
+            for (i = 0; i < dv; ++i) ut[i] = beta[row * H + hd] * r[i];
+        }
         if (o) {
             double *ot = o + (row * H + hd) * dv;
             for (i = 0; i < dv; ++i) {
@@ -198,8 +208,8 @@ static void fwd_unit(const shape_t *s, int u, const double *q, const double *k,
 static void bwd_unit(const shape_t *s, int u, const double *q, const double *k,
                      const double *v, const double *beta, const double *g,
                      const double *h0, const double *dO, const double *dhT,
-                     double *dq, double *dkk, double *dvv, double *dbeta, double *dg,
-                     double *dh0)
+                     const double *dU, double *dq, double *dkk, double *dvv, double *dbeta,
+                     double *dg, double *dh0)
 {
     const int dk = s->dk, dv = s->dv, H = s->H;
     const int n = u / H, hd = u % H;
@@ -285,10 +295,11 @@ static void bwd_unit(const shape_t *s, int u, const double *q, const double *k,
                     acc += (Wt[(int64_t)i * dk + c] + bt * r[i] * kt[c]) * dot[i];
                 dq[(row * H + hd) * dk + c] = s->scale * acc;
             }
-            /* the write and the residual */
+            /* the write and the residual (plus the gradient of the emitted write) */
             for (i = 0; i < dv; ++i) {
                 double acc = 0.0;
                 for (c = 0; c < dk; ++c) acc += G[(int64_t)i * dk + c] * kt[c];
+                if (dU) acc += dU[(row * H + hd) * dv + i];
                 Gk[i] = acc;
                 dr[i] = bt * acc;
                 db += r[i] * acc;
@@ -343,7 +354,8 @@ static void set_threads(int nthreads)
 int dro_forward(int B, int T, int H, int dk, int dv, int variant, double scale,
                 const int32_t *cu_seqlens, int N, const int32_t *units, int n_units,
                 const double *q, const double *k, const double *v, const double *beta,
-                const double *g, const double *h0, double *o, double *hT, int nthreads)
+                const double *g, const double *h0, double *o, double *hT, double *u,
+                int nthreads)
 {
     shape_t s = {B, T, H, dk, dv, variant, scale, cu_seqlens, N};
     int64_t j, nu;
@@ -353,8 +365,8 @@ int dro_forward(int B, int T, int H, int dk, int dv, int variant, double scale,
     set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (j = 0; j < nu; ++j) {
-        const int u = units ? units[j] : (int)j;
-        fwd_unit(&s, u, q, k, v, beta, g, h0, o, hT);
+        const int un = units ? units[j] : (int)j;
+        fwd_unit(&s, un, q, k, v, beta, g, h0, o, hT, u);
     }
     return 0;
 }
@@ -363,8 +375,8 @@ int dro_backward(int B, int T, int H, int dk, int dv, int variant, double scale,
                  const int32_t *cu_seqlens, int N, const int32_t *units, int n_units,
                  const double *q, const double *k, const double *v, const double *beta,
                  const double *g, const double *h0, const double *dO, const double *dhT,
-                 double *dq, double *dk_out, double *dv_out, double *dbeta, double *dg,
-                 double *dh0, int nthreads)
+                 const double *dU, double *dq, double *dk_out, double *dv_out, double *dbeta,
+                 double *dg, double *dh0, int nthreads)
 {
     shape_t s = {B, T, H, dk, dv, variant, scale, cu_seqlens, N};
     int64_t j, nu;
@@ -375,7 +387,7 @@ int dro_backward(int B, int T, int H, int dk, int dv, int variant, double scale,
 #pragma omp parallel for schedule(dynamic, 1)
     for (j = 0; j < nu; ++j) {
         const int u = units ? units[j] : (int)j;
-        bwd_unit(&s, u, q, k, v, beta, g, h0, dO, dhT, dq, dk_out, dv_out, dbeta, dg, dh0);
+        bwd_unit(&s, u, q, k, v, beta, g, h0, dO, dhT, dU, dq, dk_out, dv_out, dbeta, dg, dh0);
     }
     return 0;
 }

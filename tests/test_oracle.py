@@ -79,23 +79,25 @@ def unrolled(variant, q, k, v, beta, g, S0, scale):
     U = np.linalg.solve(M, np.diag(beta) @ (v - Kb @ S0))
     O = scale * (Qb @ S0 + np.tril(Qb @ Kr.T) @ U)
     ST = np.exp(G[-1])[:, None] * S0 + (k * np.exp(G[-1] - G)).T @ U
-    return O, ST
+    return O, ST, U
 
 
 @pytest.mark.parametrize("variant", ["deltanet", "gdn", "kda"])
 @pytest.mark.parametrize("scale", [1.0, 0.7])
 def test_forward_matches_unrolled_solve(variant, scale):
     x = rand_inputs(variant, B=2, T=13, H=2, dk=5, dv=4)
-    o, hT = oracle.forward(variant, x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
-                           scale=scale)
+    o, hT, u = oracle.forward(variant, x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                              scale=scale, want_u=True)
     for b in range(2):
         for h in range(2):
             g = gate_per_channel(variant, None if x["g"] is None else x["g"][b, :, h],
                                  5)
-            O, ST = unrolled(variant, x["q"][b, :, h], x["k"][b, :, h], x["v"][b, :, h],
-                             x["beta"][b, :, h], g, x["h0"][b, h], scale)
+            O, ST, U = unrolled(variant, x["q"][b, :, h], x["k"][b, :, h], x["v"][b, :, h],
+                                x["beta"][b, :, h], g, x["h0"][b, h], scale)
             np.testing.assert_allclose(o[b, :, h], O, rtol=0, atol=1e-12)
             np.testing.assert_allclose(hT[b, h], ST, rtol=0, atol=1e-12)
+            # the emitted write u_t = beta_t r_t is the unknown of the unrolled system
+            np.testing.assert_allclose(u[b, :, h], U, rtol=0, atol=1e-12)
 
 
 def loss_of(variant, x, scale=1.0, **kw):
@@ -130,6 +132,60 @@ def test_backward_matches_central_differences(variant):
         an = grads[gname]
         err = np.max(np.abs(an - fd)) / max(1.0, np.max(np.abs(fd)))
         assert err < 1e-6, f"{variant} {gname}: relative error {err}"
+
+
+def loss_with_write(variant, x, scale):
+    o, hT, u = oracle.forward(variant, x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                              scale=scale, want_u=True)
+    return float(np.sum(o * x["dO"]) + np.sum(hT * x["dhT"]) + np.sum(u * x["dU"]))
+
+
+@pytest.mark.parametrize("variant", ["deltanet", "gdn", "kda"])
+def test_write_gradient_matches_central_differences(variant):
+    """L = sum(dO o) + sum(dhT hT) + sum(dU u) with u the emitted write beta r."""
+    scale = 0.8
+    x = rand_inputs(variant, B=1, T=8, H=2, dk=3, dv=2, seed=17)
+    x["dU"] = np.random.default_rng(18).standard_normal(x["v"].shape)
+    grads = oracle.backward(variant, x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                            x["dO"], x["dhT"], scale=scale, dU=x["dU"])
+    names = [("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("h0", "dh0")]
+    if variant != "deltanet":
+        names.append(("g", "dg"))
+    h = 1e-6
+    for name, gname in names:
+        base = x[name]
+        fd = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp = dict(x)
+            xp[name] = base.copy()
+            xp[name][idx] += h
+            lp = loss_with_write(variant, xp, scale)
+            xp[name][idx] -= 2 * h
+            lm = loss_with_write(variant, xp, scale)
+            fd[idx] = (lp - lm) / (2 * h)
+        an = grads[gname]
+        err = np.max(np.abs(an - fd)) / max(1.0, np.max(np.abs(fd)))
+        assert err < 1e-6, f"{variant} {gname}: relative error {err}"
+
+
+def test_write_gradient_closed_form_last_token():
+    """With only dU in the loss, the last token's value reaches nothing but its own
+    write u_T = beta_T (v_T - Wd_T k_T): dv_T = beta_T dU_T exactly, and dbeta_T =
+    r_T . dU_T = u_T . dU_T / beta_T."""
+    x = rand_inputs("kda", B=2, T=6, H=2, dk=4, dv=3, seed=19)
+    dU = np.random.default_rng(20).standard_normal(x["v"].shape)
+    zero = np.zeros_like(x["dO"])
+    _, _, u = oracle.forward("kda", x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                             want_u=True)
+    gr = oracle.backward("kda", x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"], zero,
+                         None, dU=dU)
+    b = x["beta"][:, -1, :, None]
+    np.testing.assert_allclose(gr["dv"][:, -1], b * dU[:, -1], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(gr["dbeta"][:, -1],
+                               np.sum(u[:, -1] * dU[:, -1], axis=-1) / x["beta"][:, -1],
+                               rtol=1e-12, atol=1e-13)
 
 
 def test_backward_matches_symbolic_gradient():
