@@ -277,6 +277,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-write", action="store_true",
+                    help="skip the step that emits the write u and takes its gradient")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the recurrent-step (dr_decode) measurement")
     ap.add_argument("--no-e2e", action="store_true")
@@ -458,6 +460,37 @@ def main():
 
     dec = None if args.no_decode else decode_bench(dev, stream, max_over_ranks, barrier)
 
+    # the same step emitting every token's write u = beta r (dr_fwd_u) and taking a
+    # gradient for it (dr_bwd_u), device-resident like the headline value
+    wr = None
+    if not args.no_write:
+        u = torch.empty_like(o)
+        dU = torch.randn(t["v"].shape, generator=torch.Generator().manual_seed(1)).to(
+            t["v"].dtype).to(dev)
+
+        def step_w(src):
+            prob.forward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], o=o,
+                         hT=hT, u=u)
+            prob.backward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"],
+                          src["dO"], src["dhT"], reuse_fwd=True, out=grads, dU=dU)
+
+        for _ in range(args.warmup):
+            step_w(t)
+        torch.cuda.synchronize(dev)
+        barrier()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for _ in range(args.steps):
+            step_w(t)
+        w1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        assert prob.status() == binding.DR_OK
+        w_ms = max_over_ranks(w0.elapsed_time(w1) / args.steps)
+        wr = {"value": tokens / (w_ms / 1e3), "unit": "tokens/s", "ms_per_step": w_ms,
+              "ms_over_plain_step": w_ms - ms,
+              "extra_bytes_per_step": 2 * u.numel() * u.element_size()}
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -482,6 +515,7 @@ def main():
         "cpu_baseline": base,
         "e2e": e2e,
         "decode": dec,
+        "emit_write": wr,
         "gpu_launches": len(launches),
         "clocks": clk,
     }

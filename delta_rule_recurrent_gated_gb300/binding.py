@@ -61,6 +61,10 @@ def load(path: str = LIB_PATH):
     lib.dr_fwd.restype = I
     lib.dr_bwd.argtypes = [D] + [P] * 14 + [P, S, P]
     lib.dr_bwd.restype = I
+    lib.dr_fwd_u.argtypes = [D] + [P] * 9 + [P, S, P]
+    lib.dr_fwd_u.restype = I
+    lib.dr_bwd_u.argtypes = [D] + [P] * 15 + [P, S, P]
+    lib.dr_bwd_u.restype = I
     lib.dr_check_status.argtypes = [P, P]
     lib.dr_check_status.restype = I
     lib.dr_error_string.argtypes = [I]
@@ -113,6 +117,17 @@ def plan_varlen(cu_seqlens_host, chunk: int):
 
 def dr_fwd(desc, q, k, v, beta, g, h0, o, hT, ws, ws_bytes, stream) -> int:
     return load().dr_fwd(ctypes.byref(desc), q, k, v, beta, g, h0, o, hT, ws, ws_bytes, stream)
+
+
+def dr_fwd_u(desc, q, k, v, beta, g, h0, o, hT, u, ws, ws_bytes, stream) -> int:
+    return load().dr_fwd_u(ctypes.byref(desc), q, k, v, beta, g, h0, o, hT, u, ws, ws_bytes,
+                           stream)
+
+
+def dr_bwd_u(desc, q, k, v, beta, g, h0, dO, dhT, dU, dq, dk, dv, dbeta, dg, dh0, ws, ws_bytes,
+             stream) -> int:
+    return load().dr_bwd_u(ctypes.byref(desc), q, k, v, beta, g, h0, dO, dhT, dU, dq, dk, dv,
+                           dbeta, dg, dh0, ws, ws_bytes, stream)
 
 
 def dr_bwd(desc, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, ws_bytes,
@@ -204,18 +219,25 @@ class Problem:
         import torch
         return torch.cuda.current_stream(self.device).cuda_stream
 
-    def forward(self, q, k, v, beta, g=None, h0=None, o=None, hT=None, want_hT=True):
+    def forward(self, q, k, v, beta, g=None, h0=None, o=None, hT=None, want_hT=True, u=None):
+        """o, hT; with `u` (a [B,T,H,dv] tensor of the output dtype) also the write
+        beta r of every token (dr_fwd_u)."""
         import torch
         d = self.desc
         if o is None:
             o = torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.out_dtype, device=self.device)
         if hT is None and want_hT:
             hT = torch.empty(self.N, d.H, d.d_k, d.d_v, dtype=torch.float32, device=self.device)
-        _check(dr_fwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(o),
-                      _ptr(hT), self.ws.data_ptr(), self.ws.numel(), self._stream()), "dr_fwd")
+        if u is None:
+            _check(dr_fwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(o),
+                          _ptr(hT), self.ws.data_ptr(), self.ws.numel(), self._stream()), "dr_fwd")
+        else:
+            _check(dr_fwd_u(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(o),
+                            _ptr(hT), _ptr(u), self.ws.data_ptr(), self.ws.numel(),
+                            self._stream()), "dr_fwd_u")
         return o, hT
 
-    def backward(self, q, k, v, beta, g, h0, dO, dhT=None, reuse_fwd=False, out=None):
+    def backward(self, q, k, v, beta, g, h0, dO, dhT=None, reuse_fwd=False, out=None, dU=None):
         import torch
         d = self.desc
         if out is None:
@@ -230,10 +252,18 @@ class Problem:
             }
         d.flags = DR_FLAG_REUSE_FWD if reuse_fwd else 0
         try:
-            _check(dr_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0), _ptr(dO),
-                          _ptr(dhT), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
-                          _ptr(out["dbeta"]), _ptr(out["dg"]), _ptr(out["dh0"]),
-                          self.ws.data_ptr(), self.ws.numel(), self._stream()), "dr_bwd")
+            if dU is None:
+                _check(dr_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                              _ptr(dO), _ptr(dhT), _ptr(out["dq"]), _ptr(out["dk"]),
+                              _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dg"]),
+                              _ptr(out["dh0"]), self.ws.data_ptr(), self.ws.numel(),
+                              self._stream()), "dr_bwd")
+            else:
+                _check(dr_bwd_u(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                                _ptr(dO), _ptr(dhT), _ptr(dU), _ptr(out["dq"]), _ptr(out["dk"]),
+                                _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dg"]),
+                                _ptr(out["dh0"]), self.ws.data_ptr(), self.ws.numel(),
+                                self._stream()), "dr_bwd_u")
         finally:
             d.flags = 0
         return out

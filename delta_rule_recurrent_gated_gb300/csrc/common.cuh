@@ -32,8 +32,10 @@ struct Params {
     const float *beta, *g, *h0;
     void* o;
     float* hT;
+    void* u;                  // optional: the write u = beta r, [.., H, dv] in out_dtype
     const void* dO;
     const float* dhT;
+    const void* dU;           // optional: dL/du of that write, [.., H, dv] in io_dtype
     void *dq, *dk_, *dv_;
     float *dbeta, *dg, *dh0;
     int* err;                 // device error word

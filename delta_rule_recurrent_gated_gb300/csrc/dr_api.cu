@@ -140,9 +140,13 @@ int dr_plan_varlen(const int32_t* cu, int num_seqs, int chunk, int32_t* table, i
     return DR_OK;
 }
 
-int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
-           const float* g, const float* h0, void* o, float* hT, void* ws, size_t ws_size,
-           void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+             const float* g, const float* h0, void* o, float* hT, void* u, void* ws,
+             size_t ws_size, void* stream) {
     Path path;
     int rc = check_desc(desc, &path);
     if (rc != DR_OK) return rc;
@@ -150,13 +154,14 @@ int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
     const long long tokens = (long long)p.B * p.T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
     if (tokens > 0 && ((p.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, beta, g, h0, o, hT, ws};
+    const void* ptrs[] = {q, k, v, beta, g, h0, o, hT, u, ws};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
     const size_t need = ws_bytes(p, path);
     if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.hT = hT;
+    p.u = u;
     p.ws = static_cast<uint8_t*>(ws);
     p.err = static_cast<int*>(ws);
     if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
@@ -168,10 +173,10 @@ int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
     return cuda_status(dr::tc_fwd(p, st, true));
 }
 
-int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
-           const float* g, const float* h0, const void* dO, const float* dhT, void* dq, void* dk,
-           void* dv, float* dbeta, float* dg, float* dh0, void* ws, size_t ws_size,
-           void* stream) {
+int bwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+             const float* g, const float* h0, const void* dO, const float* dhT, const void* dU,
+             void* dq, void* dk, void* dv, float* dbeta, float* dg, float* dh0, void* ws,
+             size_t ws_size, void* stream) {
     Path path;
     int rc = check_desc(desc, &path);
     if (rc != DR_OK) return rc;
@@ -181,14 +186,14 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
         return DR_ERR_INVALID_ARG;
     if (tokens > 0 && ((p.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;
     if (tokens > 0 && ((p.variant == DR_DELTANET) != (dg == nullptr))) return DR_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws};
+    const void* ptrs[] = {q, k, v, beta, g, h0, dO, dhT, dU, dq, dk, dv, dbeta, dg, dh0, ws};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
     const size_t need = ws_bytes(p, path);
     if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0;
-    p.dO = dO; p.dhT = dhT; p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dbeta = dbeta; p.dg = dg;
+    p.dO = dO; p.dhT = dhT; p.dU = dU; p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.dbeta = dbeta; p.dg = dg;
     p.dh0 = dh0;
     p.ws = static_cast<uint8_t*>(ws);
     p.err = static_cast<int*>(ws);
@@ -199,6 +204,38 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, con
     }
     if (path == Path::kSimt) return cuda_status(dr::simt_bwd(p, st));
     return cuda_status(dr::tc_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+           const float* g, const float* h0, void* o, float* hT, void* ws, size_t ws_size,
+           void* stream) {
+    return fwd_impl(desc, q, k, v, beta, g, h0, o, hT, nullptr, ws, ws_size, stream);
+}
+
+int dr_fwd_u(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+             const float* g, const float* h0, void* o, float* hT, void* u, void* ws,
+             size_t ws_size, void* stream) {
+    return fwd_impl(desc, q, k, v, beta, g, h0, o, hT, u, ws, ws_size, stream);
+}
+
+int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+           const float* g, const float* h0, const void* dO, const float* dhT, void* dq, void* dk,
+           void* dv, float* dbeta, float* dg, float* dh0, void* ws, size_t ws_size,
+           void* stream) {
+    return bwd_impl(desc, q, k, v, beta, g, h0, dO, dhT, nullptr, dq, dk, dv, dbeta, dg, dh0, ws,
+                    ws_size, stream);
+}
+
+int dr_bwd_u(const dr_desc* desc, const void* q, const void* k, const void* v, const float* beta,
+             const float* g, const float* h0, const void* dO, const float* dhT, const void* dU,
+             void* dq, void* dk, void* dv, float* dbeta, float* dg, float* dh0, void* ws,
+             size_t ws_size, void* stream) {
+    return bwd_impl(desc, q, k, v, beta, g, h0, dO, dhT, dU, dq, dk, dv, dbeta, dg, dh0, ws,
+                    ws_size, stream);
 }
 
 int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,

@@ -157,9 +157,12 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scr
         chunk_prep(p, s, h, row0, L);
         chunk_scan(p, s, L, S);
         const float* O = s(bO);
+        const float* U = s(bU);
         for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
             const int i = idx / p.dv, j = idx % p.dv;
-            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * p.dv + j, p.out_dtype, O[idx]);
+            const size_t e = ((size_t)(row0 + i) * p.H + h) * p.dv + j;
+            st_any(p.o, e, p.out_dtype, O[idx]);
+            if (p.u) st_any(p.u, e, p.out_dtype, U[idx]);  // the write beta r
         }
         __syncthreads();
     }
@@ -209,6 +212,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         float* dU = s(bdU); float* dSp = s(bdSp);
         // dU = KC dS;  dS_prev = diag(gL) dS + Qt^T dO - Wy^T dU
         mm(dU, dv, s(bKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
+        if (p.dU) {  // plus the gradient of the emitted write
+            for (int idx = tid; idx < L * dv; idx += nt) {
+                const int i = idx / dv, j = idx % dv;
+                dU[idx] += ld_any(p.dU, ((size_t)(row0 + i) * p.H + h) * dv + j, p.io_dtype);
+            }
+            __syncthreads();
+        }
         for (int idx = tid; idx < dk * dv; idx += nt) dSp[idx] = gL[idx / dv] * dS[idx];
         __syncthreads();
         mm(dSp, dv, s(bQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
@@ -384,9 +394,12 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_noalloc_kernel(Params p, fl
         chunk_prep(p, s, h, row0, L);
         chunk_scan(p, s, L, S);
         const float* O = s(bO);
+        const float* U = s(bU);
         for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
             const int i = idx / p.dv, j = idx % p.dv;
-            st_any(p.o, ((size_t)(row0 + i) * p.H + h) * p.dv + j, p.out_dtype, O[idx]);
+            const size_t e = ((size_t)(row0 + i) * p.H + h) * p.dv + j;
+            st_any(p.o, e, p.out_dtype, O[idx]);
+            if (p.u) st_any(p.u, e, p.out_dtype, U[idx]);  // the write beta r
         }
         __syncthreads();
     }

@@ -61,10 +61,11 @@ struct BScanSmem {
     static constexpr int kW = 0;                 // [BV][D]  dS^T slice (bf16 operand)
     static constexpr int kdU = BV * D * 2;       // [BV][64] -dU^T operand
     static constexpr int kStage0 = kdU + BV * 128;
-    // stage layout: KC, Qt, Wy [64][D] tiles; dO [64 tokens][BV] tile; gC [D] fp32
+    // stage layout: KC, Qt, Wy [64][D] tiles; dO [64 tokens][BV] tile; gC [D] fp32;
+    // rows [v0, v0+BV) of the -dU^T image of the emitted write's gradient (dr_bwd_u)
     static constexpr int kKC = 0, kQt = kTile, kWy = 2 * kTile, kdO = 3 * kTile,
-                         kG = kdO + BV * 128;
-    static constexpr int kStageBytes = (kG + D * 4 + 1023) / 1024 * 1024;
+                         kG = kdO + BV * 128, kdUx = kG + D * 4;
+    static constexpr int kStageBytes = (kdUx + BV * 128 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
     static constexpr uint32_t kStageTx = 3 * kTile + BV * 128 + D * 4;
 };
@@ -114,7 +115,8 @@ __global__ void __launch_bounds__(128, 1)
         uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
         const int row0 = srow + ci * 64;
-        mbar_arrive_expect_tx(&bar_ld[s], S::kStageTx);
+        mbar_arrive_expect_tx(&bar_ld[s], S::kStageTx + (p.dU ? BV * 128 : 0));
+        if (p.dU) bulk_g2s(st + S::kdUx, L.dUx + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
         bulk_g2s(st + S::kKC, L.KC + rec * kTile, kTile, &bar_ld[s]);
         bulk_g2s(st + S::kQt, L.Qt + rec * kTile, kTile, &bar_ld[s]);
         bulk_g2s(st + S::kWy, L.Wy + rec * kTile, kTile, &bar_ld[s]);
@@ -177,6 +179,22 @@ __global__ void __launch_bounds__(128, 1)
                 for (int j = 0; j < 16; ++j) {
                     acc[j] = -acc[j];
                     acc2[j] = -acc2[j];
+                }
+                if (p.dU) {  // plus the packed -dU^T of the emitted write: row r, swizzled chunks
+                    const uint8_t* xrow = st + S::kdUx + r * 128;
+                    float x[16];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((2 * g + q) ^ (r & 7)) << 4)), x + 8 * q);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] += x[j];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((2 * g + 2 + q) ^ (r & 7)) << 4)), x + 8 * q);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc2[j] += x[j];
                 }
                 tile_store16(dUs, r, g * 16, BV, acc);
                 tile_store16(dUs, r, (g + 1) * 16, BV, acc2);
@@ -1134,6 +1152,29 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
+// -dU^T of the emitted write's gradient as [D][64] tile images per (chunk, head), the
+// form the backward scan adds to its own -dU^T tile (tokens past the end of a
+// sequence are zero).  Thread (value channel v, 8 tokens) packs one 16-byte chunk.
+template <int D>
+__global__ void __launch_bounds__(256) pack_dux_kernel(const Params p, const TcLayout L) {
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    int seq, row0, len;
+    chunk_info(p, chunk, seq, row0, len);
+    uint8_t* img = L.dUx + ((size_t)chunk * p.H + h) * (64 * D * 2);
+    for (int w = threadIdx.x; w < D * 8; w += blockDim.x) {
+        const int v = w % D, j = w / D;
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int i = 8 * j + t;
+            x[t] = i < len ? -ld_any(p.dU, ((size_t)(row0 + i) * p.H + h) * D + v, p.io_dtype) : 0.f;
+        }
+        *reinterpret_cast<uint4*>(img + sw128_offset(v, 8 * j, D)) =
+            make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                       pack_bf16(x[6], x[7]));
+    }
+}
+
 template <int D>
 cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
     if (!reuse) {
@@ -1148,6 +1189,12 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         return cudaErrorInvalidValue;
     if (p.variant == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows) : !make_token_map(&mg, p.q, D, p.H, rows))
         return cudaErrorInvalidValue;
+    if (p.dU && p.num_chunks > 0) {
+        TraceScope ts("pack_dux", st);
+        pack_dux_kernel<D><<<dim3(p.num_chunks, p.H), 256, 0, st>>>(p, L);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     {
         auto launch_scan = [&](auto kernel, int bv, int smem, bool& attr) -> cudaError_t {
             if (!attr) {

@@ -732,6 +732,39 @@ cudaError_t set_smem(K kernel, int bytes) {
 }  // namespace
 
 // [rows, H, D] bf16 tensor, box = 64 channels x 1 head x 64 rows, 128B swizzle
+// The write u = U (token-major, out_dtype) from the U^T tile images the forward scan
+// leaves in the workspace: a [D][64] image goes through shared memory, then thread
+// (token i, channels 8c .. 8c+7) writes one 8-channel piece of row i.
+template <int D>
+__global__ void __launch_bounds__(256) unpack_u_kernel(const Params p, const TcLayout L) {
+    __shared__ __align__(16) uint8_t img[64 * D * 2];
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    int seq, row0, len;
+    chunk_info(p, chunk, seq, row0, len);
+    const uint4* src = reinterpret_cast<const uint4*>(L.U + ((size_t)chunk * p.H + h) * (64 * D * 2));
+    for (int w = threadIdx.x; w < 64 * D * 2 / 16; w += blockDim.x)
+        reinterpret_cast<uint4*>(img)[w] = src[w];
+    __syncthreads();
+    for (int w = threadIdx.x; w < 64 * (D / 8); w += blockDim.x) {
+        const int i = w % 64, c8 = (w / 64) * 8;
+        if (i >= len) continue;
+        float x[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            x[t] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(img + sw128_offset(c8 + t, i, D)));
+        const size_t e = ((size_t)(row0 + i) * p.H + h) * D + c8;
+        if (p.out_dtype == DR_F32) {
+            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.u) + e);
+            d[0] = make_float4(x[0], x[1], x[2], x[3]);
+            d[1] = make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.u) + e) =
+                make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                           pack_bf16(x[6], x[7]));
+        }
+    }
+}
+
 bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows) {
     auto enc = encode_fn();
     if (!enc) return false;
@@ -816,9 +849,15 @@ cudaError_t tc_fwd_d(const Params& p, cudaStream_t st, bool write_o) {
     // one 128-row value tile per (sequence, head) when that already fills the SMs; two
     // 64-row tiles otherwise (more CTAs for few, long sequences)
     if constexpr (D == 128) {
-        if (p.N * p.H >= 120) return launch_scan_fwd<D, 128>(p, L, st, write_o);
+        if (p.N * p.H >= 120) e = launch_scan_fwd<D, 128>(p, L, st, write_o);
+        else e = launch_scan_fwd<D, 64>(p, L, st, write_o);
+    } else {
+        e = launch_scan_fwd<D, 64>(p, L, st, write_o);
     }
-    return launch_scan_fwd<D, 64>(p, L, st, write_o);
+    if (e != cudaSuccess || !p.u || p.num_chunks == 0) return e;
+    TraceScope ts("unpack_u", st);
+    unpack_u_kernel<D><<<dim3(p.num_chunks, p.H), 256, 0, st>>>(p, L);
+    return cudaGetLastError();
 }
 
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o) {

@@ -11,6 +11,8 @@
 //                       (W layout) of the state at the chunk start / of dL/d(state
 //                       at the chunk end)                       (D*D*2 bytes)
 //   gC                : [D] fp32, e^{Gamma} at the chunk's last token
+//   dUx               : [D][64] tile image of -dU^T for the gradient of the emitted
+//                       write (dr_bwd_u), packed before the backward scan
 #pragma once
 #include <cstdint>
 
@@ -19,7 +21,7 @@
 namespace dr {
 
 struct TcLayout {
-    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS;
+    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS, *dUx;
     float* gC;
 };
 
@@ -34,7 +36,7 @@ struct TcSizes {
 
 __host__ inline size_t tc_layout_bytes(size_t recs, int D) {
     TcSizes s(D);
-    return tc_align(recs * s.kd) * 7 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
+    return tc_align(recs * s.kd) * 8 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
            tc_align(recs * s.g);
 }
 
@@ -53,6 +55,7 @@ __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
     L.T = take(recs * s.cc);
     L.S = take(recs * s.dd);
     L.dS = take(recs * s.dd);
+    L.dUx = take(recs * s.kd);
     L.gC = reinterpret_cast<float*>(take(recs * s.g));
     return L;
 }

@@ -132,6 +132,28 @@ int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
            float* dh0, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The write of every token, for routing it to another layer ("Linear Attention
+ * Architectures: Mechanisms, Trade-offs, and Cross-Layer Routing", section
+ * "Metodologia y Marco de Trabajo", item 3, CLER: the delta-rule write error of a
+ * layer is forwarded to the next one).
+ * dr_fwd_u is dr_fwd that also writes u_t = beta_t r_t, r_t = v_t - (decayed W) k_t
+ * (the write the recurrence adds to the memory), to u: [B][T][H][d_v] in out_dtype
+ * (packed layout as o), or nothing when u is NULL.
+ * dr_bwd_u is dr_bwd for L = sum(dO * o) + sum(dhT * hT) + sum(dU * u): dU has the
+ * layout of u in io_dtype; NULL means zero (dr_bwd).  With DR_FLAG_REUSE_FWD the
+ * workspace may come from dr_fwd or dr_fwd_u.
+ * Same supported set, ownership and errors as dr_fwd / dr_bwd (u and dU 16-byte
+ * aligned).
+ */
+int dr_fwd_u(const dr_desc* desc, const void* q, const void* k, const void* v,
+             const float* beta, const float* g, const float* h0, void* o, float* hT,
+             void* u, void* workspace, size_t workspace_bytes, void* stream);
+int dr_bwd_u(const dr_desc* desc, const void* q, const void* k, const void* v,
+             const float* beta, const float* g, const float* h0, const void* dO,
+             const float* dhT, const void* dU, void* dq, void* dk, void* dv, float* dbeta,
+             float* dg, float* dh0, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Forward for callers that cannot allocate device memory.  The paper has no
  * counterpart; this is an interface convenience of the library.
  *
