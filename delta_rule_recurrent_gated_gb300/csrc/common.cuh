@@ -1,6 +1,7 @@
 // common.cuh -- shared device helpers and the launch-parameter block of the
 // kernels of libdr.so.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -96,6 +97,20 @@ __device__ __forceinline__ void st_any(void* p, size_t i, int dtype, float x) {
 }  // namespace dr
 
 namespace dr {
+// Raise a kernel's dynamic shared-memory limit once per device: `done` keeps one bit per
+// device ordinal (< 64) on which the attribute is set; safe for concurrent callers.
+template <typename K>
+inline cudaError_t set_smem_once(K kernel, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // Store 16 consecutive values of one row (elem multiple of 16, base 16-byte
 // aligned) as fp32 or bf16 with 16-byte vector stores.
 __device__ __forceinline__ void store_row16(void* base, size_t elem, int dtype, const float (&v)[16]) {

@@ -41,10 +41,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ void record_timeout(const Params& p) {
     if (threadIdx.x == 0) atomicExch(p.err, kErrTimeout);
 }
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
 __device__ __forceinline__ void zero_pad_rows(uint8_t* tile, int D, int len) {
     const int pad = 64 - len;
     const int n = (D / 64) * pad * 8;
@@ -1196,17 +1192,17 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         if (e != cudaSuccess) return e;
     }
     {
-        auto launch_scan = [&](auto kernel, int bv, int smem, bool& attr) -> cudaError_t {
-            if (!attr) {
-                cudaError_t e = set_smem(kernel, smem);
+        auto launch_scan = [&](auto kernel, int bv, int smem,
+                               std::atomic<unsigned long long>& attr) -> cudaError_t {
+            {
+                const cudaError_t e = set_smem_once(kernel, smem, attr);
                 if (e != cudaSuccess) return e;
-                attr = true;
             }
             TraceScope ts("tc_scan_bwd", st);
             kernel<<<dim3(p.N * p.H, D / bv), 128, smem, st>>>(mdo, p, L);
             return cudaGetLastError();
         };
-        static bool s64 = false, s128 = false;
+        static std::atomic<unsigned long long> s64{0}, s128{0};
         cudaError_t e;
         if (D == 128 && p.N * p.H >= 120)
             e = launch_scan(tc_scan_bwd_kernel<D, (D == 128 ? 128 : 64)>, D == 128 ? 128 : 64,
@@ -1216,20 +1212,17 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         if (e != cudaSuccess) return e;
     }
     if (p.num_chunks == 0) return cudaSuccess;
-    auto chunk_launch = [&](auto kernel, int smem, bool& attr) -> cudaError_t {
-        if (!attr) {
-            cudaError_t e = set_smem(kernel, smem);
+    auto chunk_launch = [&](auto kernel, int smem, std::atomic<unsigned long long>& attr) -> cudaError_t {
+        {
+            const cudaError_t e = set_smem_once(kernel, smem, attr);
             if (e != cudaSuccess) return e;
-            attr = true;
         }
-        // persistent: one CTA per SM, each taking work items (chunk, head) in a stride
-        static int nsm = 0;
-        if (nsm == 0) {
-            int dev = 0;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-            if (nsm <= 0) nsm = 1;
-        }
+        // persistent: one CTA per SM of the current device, each taking work items
+        // (chunk, head) in a stride
+        int dev = 0, nsm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (nsm <= 0) nsm = 1;
         const long long items = (long long)p.num_chunks * p.H;
         const int grid = (int)(items < nsm ? items : nsm);
         {
@@ -1238,7 +1231,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         }
         return cudaGetLastError();
     };
-    static bool a0 = false, a1 = false, a2 = false;
+    static std::atomic<unsigned long long> a0{0}, a1{0}, a2{0};
     switch (p.variant) {
         case DR_DELTANET:
             return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET>, BChunkSmem<D, DR_DELTANET>::kBytes, a0);

@@ -724,10 +724,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
 
 }  // namespace
 
@@ -809,11 +805,10 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
         !make_token_map(&mv, p.v, D, p.H, rows))
         return cudaErrorInvalidValue;
     constexpr int smem = PrepSmem<D>::kBytes;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = set_smem(tc_prep_kernel<D, VAR>, smem);
+    static std::atomic<unsigned long long> attr{0};
+    {
+        const cudaError_t e = set_smem_once(tc_prep_kernel<D, VAR>, smem, attr);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     if (p.num_chunks == 0) return cudaSuccess;
     TraceScope ts("tc_prep", st);
@@ -824,11 +819,10 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
 template <int D, int BV>
 cudaError_t launch_scan_fwd(const Params& p, const TcLayout& L, cudaStream_t st, bool write_o) {
     constexpr int smem = ScanSmem<D, BV>::kBytes;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = set_smem(tc_scan_fwd_kernel<D, BV>, smem);
+    static std::atomic<unsigned long long> attr{0};
+    {
+        const cudaError_t e = set_smem_once(tc_scan_fwd_kernel<D, BV>, smem, attr);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     if (p.N * p.H == 0) return cudaSuccess;
     TraceScope ts("tc_scan_fwd", st);
