@@ -388,12 +388,13 @@ __global__ void __launch_bounds__(128, 1)
         fence_async_smem();
         __syncthreads();
 
-        // Wy = T (beta Kb) -> cols [0,D);  Ut = T (beta v) -> cols [D,2D)
+        // Wy = T (beta Kb) -> cols [0,D);  Ut^T = (beta v)^T T^T -> cols [128,192) (M = D:
+        // the rows are value channels, so its image and operand tile are written 16 bytes wide)
         if (tid == 0) {
             tc_fence_after();
             const Tile tT{smem_u32(Ts), 64}, tY{smem_u32(Ys), 64}, tV{smem_u32(Vs), 64};
             mma_tiles(tm + 0, tT, false, tY, true, 64, D, 64, false);
-            mma_tiles(tm + D, tT, false, tV, true, 64, D, 64, false);
+            mma_tiles(tm + 128, tV, true, tT, false, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
@@ -404,18 +405,23 @@ __global__ void __launch_bounds__(128, 1)
             uint8_t* wy_img = L.Wy + rec * kTile;
             uint8_t* utT = L.UtT + rec * kTile;  // [D][64] SW128 tile image of Ut^T
             for (int cb = 0; cb < D / 16; ++cb) {
-                float w16[16], u16[16];
+                float w16[16];
                 tmem_ld16(tl + cb * 16, w16);
-                tmem_ld16(tl + D + cb * 16, u16);
                 tmem_ld_wait();
                 if (r >= 0) {
                     tile_store16(Xs, r, cb * 16, 64, w16);
                     tile_store16(wy_img, r, cb * 16, 64, w16);
-                    tile_store16(Ks, r, cb * 16, 64, u16);
+                }
+            }
+            const int cv = D == 128 ? tid : r;  // value channel of the M = D accumulator
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        *reinterpret_cast<__nv_bfloat16*>(utT + sw128_offset(cb * 16 + j, r, D)) =
-                            __float2bfloat16_rn(u16[j]);
+            for (int b = 0; b < 4; ++b) {
+                float u16[16];
+                tmem_ld16(tl + 128 + b * 16, u16);
+                tmem_ld_wait();
+                if (cv >= 0) {
+                    tile_store16(Ks, cv, b * 16, D, u16);  // Ut^T operand tile [D][64] (Kr is consumed)
+                    tile_store16(utT, cv, b * 16, D, u16);
                 }
             }
         }
@@ -423,12 +429,12 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_before();
         __syncthreads();
 
-        // Aqk Wy -> cols [0,D);  Aqk Ut -> cols [D,2D)
+        // Aqk Wy -> cols [0,D);  Ot^T / scale = Ut^T Aqk^T -> cols [128,192) (M = D)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), 64};
+            const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), D};
             mma_tiles(tm + 0, tA, false, tW, true, 64, D, 64, false);
-            mma_tiles(tm + D, tA, false, tU, true, 64, D, 64, false);
+            mma_tiles(tm + 128, tU, false, tA, false, D, 64, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
@@ -440,19 +446,26 @@ __global__ void __launch_bounds__(128, 1)
             uint8_t* otT = L.OtT + rec * kTile;  // [D][64] SW128 tile image of Ot^T
             const float sc = p.scale;
             for (int cb = 0; cb < D / 16; ++cb) {
-                float w16[16], u16[16], qb[16];
+                float w16[16], qb[16];
                 tmem_ld16(tl + cb * 16, w16);
-                tmem_ld16(tl + D + cb * 16, u16);
                 tmem_ld_wait();
                 if (r >= 0) {
                     tile_load16(Qs, r, cb * 16, 64, qb);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) qb[j] = sc * (qb[j] - w16[j]);
                     tile_store16(qt_img, r, cb * 16, 64, qb);
+                }
+            }
+            const int cv = D == 128 ? tid : r;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        *reinterpret_cast<__nv_bfloat16*>(otT + sw128_offset(cb * 16 + j, r, D)) =
-                            __float2bfloat16_rn(sc * u16[j]);
+            for (int b = 0; b < 4; ++b) {
+                float o16[16];
+                tmem_ld16(tl + 128 + b * 16, o16);
+                tmem_ld_wait();
+                if (cv >= 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) o16[j] *= sc;
+                    tile_store16(otT, cv, b * 16, D, o16);
                 }
             }
         }
