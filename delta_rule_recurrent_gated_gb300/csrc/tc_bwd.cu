@@ -29,7 +29,7 @@ namespace dr {
 using namespace tc;
 
 bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
-bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
+bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows, int box_rows);
 TcLayout tc_layout(const Params& p);
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
 
@@ -1183,7 +1183,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
     if (!make_token_map(&mq, p.q, D, p.H, rows) || !make_token_map(&mk, p.k, D, p.H, rows) ||
         !make_token_map(&mv, p.v, D, p.H, rows) || !make_token_map(&mdo, p.dO, D, p.H, rows))
         return cudaErrorInvalidValue;
-    if (p.variant == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows) : !make_token_map(&mg, p.q, D, p.H, rows))
+    if (p.variant == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows, 64) : !make_token_map(&mg, p.q, D, p.H, rows))
         return cudaErrorInvalidValue;
     if (p.dU && p.num_chunks > 0) {
         TraceScope ts("pack_dux", st);

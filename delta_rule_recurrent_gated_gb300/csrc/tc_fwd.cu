@@ -66,7 +66,8 @@ struct PrepSmem {
 template <int D, int VAR>
 __global__ void __launch_bounds__(128, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                   const __grid_constant__ CUtensorMap mv, const Params p, const TcLayout L) {
+                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
+                   const Params p, const TcLayout L) {
     using S = PrepSmem<D>;
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(128, 1)
         prefetch_tmap(&mq);
         prefetch_tmap(&mk);
         prefetch_tmap(&mv);
+        if (VAR == DR_KDA) prefetch_tmap(&mg);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -109,15 +111,19 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t tl = warp_lane_base(tm);
     const int r = m64_row();
     bool ok = true;
+    bool ld_phase2 = false;  // KDA: the second gate copy was issued
 
     do {
         if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_ld, 3 * kTile);
+            // KDA: the gates of the first 32 tokens come with q, k, v (the second 32 later,
+            // into the same staging buffer)
+            mbar_arrive_expect_tx(&bar_ld, 3 * kTile + (VAR == DR_KDA ? 32 * D * 4 : 0));
             for (int kb = 0; kb < D / 64; ++kb) {
                 tma_load_3d(Qs + kb * 8192, &mq, &bar_ld, kb * 64, h, row0);
                 tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
                 tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
             }
+            if (VAR == DR_KDA) tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
         }
         if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
@@ -196,31 +202,28 @@ __global__ void __launch_bounds__(128, 1)
                 *reinterpret_cast<uint4*>(kc_img + off) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
             }
         } else
-        // decay, per key channel (KDA): the cumulative log-decay (thread c holds its channel's
-        // gates in registers), staged 32 rows at a time in the still-unused Aqk / T
-        // buffers, then an elementwise pass eight channels wide
+        // decay, per key channel (KDA): the gates arrive 32 tokens at a time in the
+        // still-unused Aqk / T tiles; thread c carries its channel's cumulative log-decay
+        // through both halves in place, then an elementwise pass eight channels wide.  KC =
+        // Kr e^{Gamma_last} is written once the last token's Gamma is known.
         {
             float* Gb = reinterpret_cast<float*>(Aqs);  // [32][D] fp32
-            float gl[64];
             float G = 0.f;
-            if (tid < D) {
-                float GL = 0.f;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    gl[i] = (VAR != DR_DELTANET && i < len) ? gate_at<VAR>(p, row0 + i, h, tid) : 0.f;
-                    GL += gl[i];
-                }
-                const float eGL = VAR != DR_DELTANET ? expf(GL) : 1.f;
-                L.gC[rec * D + tid] = eGL;
-                GLs[tid] = eGL;  // e^{Gamma_last} per channel
-            }
-            uint8_t* kc_img = L.KC + rec * kTile;
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
+                if (half == 1) {
+                    if (tid == 0) {
+                        mbar_arrive_expect_tx(&bar_ld, 32 * D * 4);
+                        tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0 + 32);
+                    }
+                    ok = mbar_wait(&bar_ld, 1, kWaitLimitNs);
+                    ld_phase2 = true;
+                    if (__syncthreads_or(!ok)) break;
+                }
                 if (tid < D) {
-#pragma unroll
+#pragma unroll 8
                     for (int ii = 0; ii < 32; ++ii) {
-                        G += gl[32 * half + ii];
+                        if (32 * half + ii < len) G += Gb[ii * D + tid];
                         Gb[ii * D + tid] = G;
                     }
                 }
@@ -228,32 +231,23 @@ __global__ void __launch_bounds__(128, 1)
                 for (int w = tid; w < 32 * (D / 8); w += 128) {
                     const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
                     const uint32_t off = sw128_offset(i, c8, 64);
-                    float q8[8], k8[8], v8[8];
+                    float q8[8], k8[8], v8[8], G8[8];
                     unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
                     unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
                     unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
                     const float b = beta_s[i];
-                    float G8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L8[8];
-                    if (VAR != DR_DELTANET) {
-                        const float4* gp = reinterpret_cast<const float4*>(&Gb[ii * D + c8]);
-                        const float4* lp = reinterpret_cast<const float4*>(&GLs[c8]);
-                        const float4 g0 = gp[0], g1 = gp[1], l0 = lp[0], l1 = lp[1];
-                        G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
-                        G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
-                        L8[0] = l0.x; L8[1] = l0.y; L8[2] = l0.z; L8[3] = l0.w;
-                        L8[4] = l1.x; L8[5] = l1.y; L8[6] = l1.z; L8[7] = l1.w;
-                    }
-                    uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
+                    const float4* gp = reinterpret_cast<const float4*>(&Gb[ii * D + c8]);
+                    const float4 g0 = gp[0], g1 = gp[1];
+                    G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
+                    G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
+                    uint32_t wq[4], wr[4], wb[4], wy[4], wv[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        float e[2] = {1.f, 1.f}, ei[2] = {1.f, 1.f}, ec[2] = {1.f, 1.f};
-                        if (VAR != DR_DELTANET) {
+                        float e[2], ei[2];
 #pragma unroll
-                            for (int t = 0; t < 2; ++t) {
-                                e[t] = __expf(G8[2 * j + t]);
-                                ei[t] = fast_rcp(e[t]);
-                                ec[t] = L8[2 * j + t] * ei[t];
-                            }
+                        for (int t = 0; t < 2; ++t) {
+                            e[t] = __expf(G8[2 * j + t]);
+                            ei[t] = fast_rcp(e[t]);
                         }
                         const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
                         wq[j] = pack_bf16(q8[2 * j] * e[0], q8[2 * j + 1] * e[1]);
@@ -261,16 +255,37 @@ __global__ void __launch_bounds__(128, 1)
                         wb[j] = pack_bf16(k0 * e[0], k1 * e[1]);
                         wy[j] = pack_bf16(b * k0 * e[0], b * k1 * e[1]);
                         wv[j] = pack_bf16(b * v8[2 * j], b * v8[2 * j + 1]);
-                        wc[j] = pack_bf16(k0 * ec[0], k1 * ec[1]);
                     }
                     *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                     *reinterpret_cast<uint4*>(Ks + off) = make_uint4(wr[0], wr[1], wr[2], wr[3]);
                     *reinterpret_cast<uint4*>(Xs + off) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
                     *reinterpret_cast<uint4*>(Ys + off) = make_uint4(wy[0], wy[1], wy[2], wy[3]);
                     *reinterpret_cast<uint4*>(Vs + off) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                    *reinterpret_cast<uint4*>(kc_img + off) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
                 }
+                fence_async_smem();  // the staging buffer is refilled by the next copy
                 __syncthreads();
+            }
+            if (!ok) break;
+            if (tid < D) {
+                const float eGL = expf(G);  // e^{Gamma_last} per channel
+                L.gC[rec * D + tid] = eGL;
+                GLs[tid] = eGL;
+            }
+            __syncthreads();
+            uint8_t* kc_img = L.KC + rec * kTile;
+            for (int w = tid; w < 64 * (D / 8); w += 128) {
+                const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
+                const uint32_t off = sw128_offset(i, c8, 64);
+                float kr8[8];
+                unpack8(*reinterpret_cast<const uint4*>(Ks + off), kr8);
+                const float4* lp = reinterpret_cast<const float4*>(&GLs[c8]);
+                const float4 l0 = lp[0], l1 = lp[1];
+                const float L8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                uint32_t wc[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    wc[j] = pack_bf16(kr8[2 * j] * L8[2 * j], kr8[2 * j + 1] * L8[2 * j + 1]);
+                *reinterpret_cast<uint4*>(kc_img + off) = make_uint4(wc[0], wc[1], wc[2], wc[3]);
             }
         }
         fence_async_smem();
@@ -474,6 +489,7 @@ __global__ void __launch_bounds__(128, 1)
     if (!ok) {
         record_timeout(p);
         mbar_wait(&bar_ld, 0, kWaitLimitNs);  // let an outstanding copy land before exit
+        if (ld_phase2) mbar_wait(&bar_ld, 1, kWaitLimitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -787,14 +803,14 @@ bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 per-key-channel gates [rows][H][D]: one box is the D gates of 64 tokens of one
-// head, dense (no swizzle) in shared memory
-bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows) {
+// fp32 per-key-channel gates [rows][H][D]: one box is the D gates of box_rows tokens of
+// one head, dense (no swizzle) in shared memory
+bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows, int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
-    cuuint32_t box[3] = {(cuuint32_t)D, 1, 64};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -812,10 +828,12 @@ size_t tc_workspace_bytes(const Params& p) { return tc_layout_bytes(tc_records(p
 
 template <int D, int VAR>
 cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mg;
     const long long rows = (long long)p.B * p.T;
     if (!make_token_map(&mq, p.q, D, p.H, rows) || !make_token_map(&mk, p.k, D, p.H, rows) ||
         !make_token_map(&mv, p.v, D, p.H, rows))
+        return cudaErrorInvalidValue;
+    if (VAR == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows, 32) : !make_token_map(&mg, p.q, D, p.H, rows))
         return cudaErrorInvalidValue;
     constexpr int smem = PrepSmem<D>::kBytes;
     static std::atomic<unsigned long long> attr{0};
@@ -825,7 +843,7 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
     }
     if (p.num_chunks == 0) return cudaSuccess;
     TraceScope ts("tc_prep", st);
-    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, p, L);
+    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mg, p, L);
     return cudaGetLastError();
 }
 
