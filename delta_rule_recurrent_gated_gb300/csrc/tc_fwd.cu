@@ -520,6 +520,14 @@ constexpr int kScanFwdThreads = 256;
 __device__ __forceinline__ void state_warps_sync() {
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
+// barrier 2 (160 threads): the state warps wait, the first output warp arrives once the
+// chunk-start state image has been read out of the state tile
+__device__ __forceinline__ void state_image_sync() {
+    asm volatile("bar.sync 2, 160;" ::: "memory");
+}
+__device__ __forceinline__ void state_image_arrive() {
+    asm volatile("bar.arrive 2, 160;" ::: "memory");
+}
 
 template <int D, int BV>
 __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const Params p, const TcLayout L,
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Ws = sm + S::kW;
     uint8_t* Us = sm + S::kUs;
-    __shared__ uint64_t bar_ld[2], bar_mma;
+    __shared__ uint64_t bar_ld[2], bar_mma, bar_o;
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
 
@@ -545,6 +553,7 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         mbar_init(&bar_ld[0], 1);
         mbar_init(&bar_ld[1], 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_o, 1);
         fence_barrier_init();
         s_fail = 0;
     }
@@ -560,9 +569,12 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
     const int r = (BV == 128) ? (tid & 127) : m64_row();  // value row (or -1)
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
-    int issued[2] = {0, 0}, waited[2] = {0, 0};   // bulk-load phases per stage (thread 0)
+    // Thread kIss (lane 0 of the first output warp, idle until the products land) issues
+    // the copies: the chunk-start state image and the next chunk's tiles.
+    constexpr int kIss = 128;
+    int issued[2] = {0, 0};   // bulk-load phases per stage (thread kIss)
 
-    auto load_chunk = [&](int ci) {  // thread 0: fetch chunk ci into stage ci & 1
+    auto load_chunk = [&](int ci) {  // thread kIss: fetch chunk ci into stage ci & 1
         const int s = ci & 1;
         uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
@@ -575,7 +587,7 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
     };
-    if (tid == 0 && nc > 0) load_chunk(0);
+    if (tid == kIss && nc > 0) load_chunk(0);
 
     float W[D];  // W[v, :] = S[:, v], fp32 (state warps)
 #pragma unroll
@@ -599,16 +611,8 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         const uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
         const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
-        if (tid == 0) {
-            if (ci + 1 < nc) load_chunk(ci + 1);  // stage s^1 was released at the end of ci-1
-            // the chunk-start state rows [v0, v0+BV) of the W-layout state image
-            uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
-            for (int kb = 0; kb < D / 64; ++kb)
-                bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
-            bulk_commit();
-        }
+        if (tid == 0) bulk_wait_read();  // the previous chunk's U^T image has left Us
         ok = mbar_wait(&bar_ld[s], (ci >> 1) & 1, kWaitLimitNs);
-        if (tid == 0) ++waited[s];
         if (__syncthreads_or(!ok)) break;
 
         // W Wy^T -> cols [0,64) ;  W Qt^T -> cols [64,128)
@@ -616,14 +620,31 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
             tc_fence_after();
             const Tile tW{smem_u32(Ws), BV}, tWy{smem_u32(st + S::kWy), 64}, tQt{smem_u32(st + S::kQt), 64};
             mma_tiles(tm + 0, tW, false, tWy, false, BV, 64, D, false);
+            mma_commit(&bar_mma);  // the state chain waits for W Wy^T only
             mma_tiles(tm + 64, tW, false, tQt, false, BV, 64, D, false);
-            mma_commit(&bar_mma);
+            mma_commit(&bar_o);
         }
-        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-        tc_fence_after();
+        if (tid == kIss) {
+            // the chunk-start state rows [v0, v0+BV) of the W-layout state image, then the
+            // next chunk's tiles (stage s^1 was released at the end of ci-1); Ws may be
+            // rewritten once the image has left it
+            uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
+            for (int kb = 0; kb < D / 64; ++kb)
+                bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
+            bulk_commit();
+            if (ci + 1 < nc) load_chunk(ci + 1);
+            bulk_wait_read();
+        }
+        if (warp == kIss / 32) {
+            __syncwarp();
+            state_image_arrive();
+        }
 
         if (state_warp) {
+            // no block-wide barrier here: the state chain does not wait for the issuing
+            // thread; a failed wait is reported through s_fail at the end of the chunk
+            if (!mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
+            tc_fence_after();
             // U = Ut - W Wy^T
             for (int g = 0; g < 4; g += 2) {
                 float acc[16], acc2[16];
@@ -662,8 +683,7 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
                 bulk_commit();
             }
             const bool ok2 = mbar_wait(&bar_mma, 1, kWaitLimitNs);
-            if (tid == 0) bulk_wait_read();  // Ws and Us are rewritten below / next chunk
-            state_warps_sync();
+            state_image_sync();  // the state image has left Ws, rewritten below
             tc_fence_after();
             if (!ok2) s_fail = 1;
             const float* gCs = reinterpret_cast<const float*>(st + S::kG);
@@ -688,6 +708,8 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
             }
         } else if (write_o) {
             // O = Ot + W Qt^T for rows r, while the state chain proceeds
+            if (!mbar_wait(&bar_o, ci & 1, kWaitLimitNs)) s_fail = 1;
+            tc_fence_after();
             const size_t stride = (size_t)p.H * D;
             const size_t base = ((size_t)row0 * p.H + h) * D + v;
             for (int g = 0; g < 4; ++g) {
@@ -729,11 +751,11 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         }
     } else {
         record_timeout(p);
-        if (tid == 0)
+        if (tid == kIss)  // the latest copy issued into each stage has landed before exit
             for (int s = 0; s < 2; ++s)
-                if (issued[s] > waited[s]) mbar_wait(&bar_ld[s], waited[s] & 1, kWaitLimitNs);
+                if (issued[s] > 0) mbar_wait(&bar_ld[s], (issued[s] - 1) & 1, kWaitLimitNs);
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0 || tid == kIss) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
