@@ -111,25 +111,4 @@ inline cudaError_t set_smem_once(K kernel, int bytes, std::atomic<unsigned long 
     return e;
 }
 
-// Store 16 consecutive values of one row (elem multiple of 16, base 16-byte
-// aligned) as fp32 or bf16 with 16-byte vector stores.
-__device__ __forceinline__ void store_row16(void* base, size_t elem, int dtype, const float (&v)[16]) {
-    if (dtype == DR_F32) {
-        float4* d = reinterpret_cast<float4*>(static_cast<float*>(base) + elem);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    } else {
-        uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + elem);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * h + 2 * j], v[8 * h + 2 * j + 1]);
-                w[j] = *reinterpret_cast<uint32_t*>(&b);
-            }
-            d[h] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
 }  // namespace dr
