@@ -147,6 +147,38 @@ def make(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
             "dhT": dhT, "cu_seqlens": cu, "N": N}
 
 
+def make_raw(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
+    """Inputs before the input preparation, for the library's input-preparation
+    mode: q, k ~ N(0, 1) rows (not normalised) in the io dtype; beta logits
+    b ~ N(0, 1); gate arguments x ~ N(0, 1) - 2.5, so that -softplus(x) falls
+    in the same range as the prepared gates above (about -0.08 typical).  v, h0,
+    dO, dhT as in ``make``.  Same draw order and generator as ``make``.
+    """
+    gen = torch.Generator().manual_seed(seed)
+    dt = io_dtype(w)
+    cu = cu_seqlens_of(w, seed)
+    N = w.B if cu is None else int(cu.numel() - 1)
+    q = torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32).to(dt)
+    k = torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32).to(dt)
+    v = torch.randn(w.B, w.T, w.H, w.dv, generator=gen, dtype=torch.float32).to(dt)
+    beta = torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)
+    g = None
+    if w.variant == "gdn":
+        g = torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32) - 2.5
+    elif w.variant == "kda":
+        g = torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32) - 2.5
+    h0 = None
+    if w.h0:
+        h0 = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02
+    dO = dhT = None
+    if need_grad_inputs:
+        dO = torch.randn(w.B, w.T, w.H, w.dv, generator=gen, dtype=torch.float32).to(dt)
+        if w.dhT:
+            dhT = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02
+    return {"q": q, "k": k, "v": v, "beta": beta, "g": g, "h0": h0, "dO": dO,
+            "dhT": dhT, "cu_seqlens": cu, "N": N}
+
+
 def small(variant: str, B=2, T=200, H=3, dk=64, dv=64, chunk=64, io="bf16", h0=True,
           dhT=True, lengths=None) -> Workload:
     """A small workload of the same distributions (several chunks, ragged tail)."""
@@ -156,5 +188,5 @@ def small(variant: str, B=2, T=200, H=3, dk=64, dv=64, chunk=64, io="bf16", h0=T
                     h0=h0, dhT=dhT, lengths=None if lengths is None else tuple(lengths))
 
 
-__all__ = ["Workload", "WORKLOADS", "get", "make", "small", "ragged_lengths",
+__all__ = ["Workload", "WORKLOADS", "get", "make", "make_raw", "small", "ragged_lengths",
            "cu_seqlens_of", "num_seqs", "io_dtype", "replace", "field"]
