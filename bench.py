@@ -201,6 +201,71 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def prepare_bytes(w, N):
+    """Algorithmic HBM bytes of each input-preparation kernel per launch.
+    prepare_rows: read raw q, k, write the normalised copies; chain_rows: read raw
+    q, k and the prepared-tensor gradients, write the raw gradients in place;
+    prepare_gates / chain_gates: beta and gate values, 4 B each, read once and
+    written once (chain: the raw logit read too)."""
+    th = w.B * w.T * w.H
+    es = 2 if w.io == "bf16" else 4
+    ng = 0 if w.variant == "deltanet" else (th if w.variant == "gdn" else th * w.dk)
+    return {"prepare_rows": 4 * th * w.dk * es,
+            "prepare_gates": 8 * (th + ng),
+            "chain_rows": 6 * th * w.dk * es,
+            "chain_gates": 12 * (th + ng)}
+
+
+def prepare_bench(args, w, rank, world, dev, stream, plain_ms, o, hT, grads, max_over_ranks,
+                  barrier):
+    import torch
+    from delta_rule_recurrent_gated_gb300 import binding, inputs
+    xr = inputs.make_raw(w, seed=rank)
+    tr = {n: (v.to(dev) if torch.is_tensor(v) and n != "cu_seqlens" else v) for n, v in xr.items()}
+    prob = binding.Problem(w.variant, w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io,
+                           out="bf16", grad="bf16", scale=w.scale,
+                           cu_seqlens=xr["cu_seqlens"], device=dev, prepare=True)
+
+    def step_p(src):
+        prob.forward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], o=o, hT=hT)
+        prob.backward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], src["dO"],
+                      src["dhT"], reuse_fwd=True, out=grads)
+
+    for _ in range(args.warmup):
+        step_p(tr)
+    torch.cuda.synchronize(dev)
+    binding.trace_enable(12 * args.steps + 12)
+    barrier()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        step_p(tr)
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    st = prob.status()
+    assert st == binding.DR_OK, binding.error_string(st)
+    launches = binding.trace_read()
+    binding.trace_enable(0)
+    p_ms = max_over_ranks(p0.elapsed_time(p1) / args.steps)
+    hbm, _, _ = measured_peaks()
+    byts = prepare_bytes(w, inputs.num_seqs(w))
+    kern = {}
+    for nm, kms in launches:
+        if nm in byts:
+            tot, n = kern.get(nm, (0.0, 0))
+            kern[nm] = (tot + kms, n + 1)
+    kern = {nm: {"launches": n, "ms_per_launch": tot / n, "bytes_per_launch": byts[nm],
+                 "achieved_gbs": byts[nm] / (tot / n / 1e3) / 1e9,
+                 "frac_of_measured_hbm": byts[nm] / (tot / n / 1e3) / 1e9 / hbm}
+            for nm, (tot, n) in kern.items()}
+    del prob
+    torch.cuda.empty_cache()
+    return {"value": w.tokens * world / (p_ms / 1e3), "unit": "tokens/s", "ms_per_step": p_ms,
+            "ms_over_plain_step": p_ms - plain_ms, "kernels": kern,
+            "inputs": "raw q, k ~ N(0,1), beta logits ~ N(0,1), gate arguments ~ N(0,1) - 2.5"}
+
+
 def cpu_baseline(w, x, budget_s=12.0):
     """Time the fp64 oracle (forward + backward, as it stands) on whole
     (sequence, head) units of the workload on the host cores, and scale the
@@ -282,6 +347,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the recurrent-step (dr_decode) measurement")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prepare", action="store_true",
+                    help="skip the step with input preparation (DR_FLAG_PREPARE_INPUTS)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -491,6 +558,14 @@ def main():
               "ms_over_plain_step": w_ms - ms,
               "extra_bytes_per_step": 2 * u.numel() * u.element_size()}
 
+    # the same step on raw inputs (q, k unnormalised, beta logits, gate arguments) with
+    # the library preparing them (DR_FLAG_PREPARE_INPUTS): its cost over the plain step,
+    # and each preparation kernel against the HBM roofline
+    pr = None
+    if not args.no_prepare:
+        pr = prepare_bench(args, w, rank, world, dev, stream, ms, o, hT, grads, max_over_ranks,
+                           barrier)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -516,6 +591,7 @@ def main():
         "e2e": e2e,
         "decode": dec,
         "emit_write": wr,
+        "prepare_inputs": pr,
         "gpu_launches": len(launches),
         "clocks": clk,
     }

@@ -19,6 +19,7 @@ DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_WORKSPACE, DR_ERR_ALIGNMEN
 DR_DELTANET, DR_GDN, DR_KDA = 0, 1, 2
 DR_BF16, DR_F32 = 0, 1
 DR_FLAG_REUSE_FWD = 1
+DR_FLAG_PREPARE_INPUTS = 2
 VARIANTS = {"deltanet": DR_DELTANET, "gdn": DR_GDN, "kda": DR_KDA}
 
 
@@ -174,11 +175,13 @@ class Problem:
     """Descriptor + device-side chunk plan + workspace for one problem shape.
 
     Build once per shape; `forward` / `backward` then enqueue the library calls
-    on the current torch stream.
+    on the current torch stream.  With ``prepare`` the calls take raw q, k, beta
+    logits and gate arguments (DR_FLAG_PREPARE_INPUTS) and the gradients are with
+    respect to those.
     """
 
     def __init__(self, variant, B, T, H, dk, dv, chunk=64, io="bf16", out="f32",
-                 grad="f32", scale=1.0, cu_seqlens=None, device="cuda"):
+                 grad="f32", scale=1.0, cu_seqlens=None, device="cuda", prepare=False):
         import torch
         self.device = torch.device(device)
         d = DrDesc()
@@ -187,7 +190,8 @@ class Problem:
         code = {"bf16": DR_BF16, "f32": DR_F32}
         d.io_dtype, d.out_dtype, d.grad_dtype = code[io], code[out], code[grad]
         d.scale = float(scale)
-        d.flags = 0
+        self.base_flags = DR_FLAG_PREPARE_INPUTS if prepare else 0
+        d.flags = self.base_flags
         self._keep = []
         if cu_seqlens is not None:
             cu_host = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
@@ -250,7 +254,7 @@ class Problem:
                 "dh0": torch.empty(self.N, d.H, d.d_k, d.d_v, dtype=torch.float32,
                                    device=self.device),
             }
-        d.flags = DR_FLAG_REUSE_FWD if reuse_fwd else 0
+        d.flags = self.base_flags | (DR_FLAG_REUSE_FWD if reuse_fwd else 0)
         try:
             if dU is None:
                 _check(dr_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
@@ -265,7 +269,7 @@ class Problem:
                                 _ptr(out["dh0"]), self.ws.data_ptr(), self.ws.numel(),
                                 self._stream()), "dr_bwd_u")
         finally:
-            d.flags = 0
+            d.flags = self.base_flags
         return out
 
     def status(self) -> int:
@@ -277,7 +281,7 @@ class Decoder:
     on the current torch stream and updates `state` ([B, H, dk, dv] fp32) in place."""
 
     def __init__(self, variant, B, T, H, dk, dv, io="bf16", out="f32", scale=1.0,
-                 device="cuda"):
+                 device="cuda", prepare=False):
         import torch
         self.device = torch.device(device)
         d = DrDesc()
@@ -286,7 +290,7 @@ class Decoder:
         code = {"bf16": DR_BF16, "f32": DR_F32}
         d.io_dtype, d.out_dtype, d.grad_dtype = code[io], code[out], code[out]
         d.scale = float(scale)
-        d.flags = 0
+        d.flags = DR_FLAG_PREPARE_INPUTS if prepare else 0
         d.num_seqs = B
         d.cu_seqlens = d.chunk_table = d.chunk_offsets = None
         d.num_chunks = 0

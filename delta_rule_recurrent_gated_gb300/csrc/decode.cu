@@ -16,6 +16,11 @@
 // read and written as 32 consecutive floats.  The two sums over key channels
 // per token (S~^T k and S^T q) are per-thread partials over R rows, combined
 // across the eight warps through shared memory in a fixed order.
+//
+// With input preparation (PREP) the token's q and k are L2-normalised in shared
+// memory (q * rsqrt(sum q^2 + 1e-6)), beta = sigmoid(b) and the gate
+// log alpha = -softplus(x) are formed as they are read: the same maps as the
+// chunked path's preparation kernels, applied here without a pass over HBM.
 #include "common.cuh"
 #include "trace.cuh"
 
@@ -24,7 +29,11 @@ namespace {
 
 constexpr int kDecodeThreads = 256;  // eight warps
 
-template <int DK>
+__device__ __forceinline__ float neg_softplus(float x) {
+    return -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+}
+
+template <int DK, bool PREP>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(const Params p, float* __restrict__ state) {
     constexpr int R = DK / 8;  // key rows per warp
@@ -35,7 +44,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const bool col = lane < ncol;
     __shared__ float qs[DK], ks[DK], as[DK], vs[32];
     __shared__ float red[8][33];
-    __shared__ float bsh;
+    __shared__ float bsh, nrm_q, nrm_k;
 
     float* Sg = state + ((size_t)n * p.H + h) * DK * p.dv;
     float S[R];
@@ -48,16 +57,34 @@ __global__ void __launch_bounds__(kDecodeThreads)
         for (int c = threadIdx.x; c < DK; c += kDecodeThreads) {
             qs[c] = ld_any(p.q, rk + c, p.io_dtype);
             ks[c] = ld_any(p.k, rk + c, p.io_dtype);
-            float a = 1.f;
-            if (p.variant == DR_GDN) a = expf(p.g[tok * p.H + h]);
-            else if (p.variant == DR_KDA) a = expf(p.g[rk + c]);
-            as[c] = a;
+            float lg = 0.f;
+            if (p.variant == DR_GDN) lg = p.g[tok * p.H + h];
+            else if (p.variant == DR_KDA) lg = p.g[rk + c];
+            if (PREP && p.variant != DR_DELTANET) lg = neg_softplus(lg);
+            as[c] = p.variant == DR_DELTANET ? 1.f : expf(lg);
         }
         if (warp == 0) {
             vs[lane] = col ? ld_any(p.v, rv + v, p.io_dtype) : 0.f;
-            if (lane == 0) bsh = p.beta[tok * p.H + h];
+            if (lane == 0) {
+                const float b = p.beta[tok * p.H + h];
+                bsh = PREP ? 1.f / (1.f + expf(-b)) : b;
+            }
         }
         __syncthreads();
+        if (PREP) {
+            // warp 0 sums q^2, warp 1 k^2; every warp then reads both scales
+            if (warp < 2) {
+                const float* x = warp == 0 ? qs : ks;
+                float ss = 0.f;
+                for (int c = lane; c < DK; c += 32) ss = fmaf(x[c], x[c], ss);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                if (lane == 0) (warp == 0 ? nrm_q : nrm_k) = rsqrtf(ss + 1e-6f);
+            }
+            __syncthreads();
+        }
+        // the norms enter as scales: S~^T k_hat = nrm_k (S~^T k), S^T q_hat = nrm_q (S^T q)
+        const float scq = PREP ? nrm_q : 1.f, sck = PREP ? nrm_k : 1.f;
         // decay, then this thread's part of (S~^T k)[v]
         float pk = 0.f;
 #pragma unroll
@@ -71,12 +98,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
         float sk = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) sk += red[w][lane];
-        const float br = bsh * (vs[lane] - sk);  // beta * r[v]
+        const float br = bsh * (vs[lane] - sck * sk);  // beta * r[v]
+        const float brk = br * sck;                    // k_hat[c] = sck * ks[c]
         float pq = 0.f;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const int c = warp * R + i;
-            S[i] = fmaf(ks[c], br, S[i]);
+            S[i] = fmaf(ks[c], brk, S[i]);
             pq = fmaf(S[i], qs[c], pq);
         }
         __syncthreads();  // every warp has read red[] and the token's inputs
@@ -86,7 +114,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             float o = 0.f;
 #pragma unroll
             for (int w = 0; w < 8; ++w) o += red[w][lane];
-            st_any(p.o, rv + v, p.out_dtype, p.scale * o);
+            st_any(p.o, rv + v, p.out_dtype, p.scale * scq * o);
         }
         __syncthreads();  // red[] and the inputs are rewritten by the next token
     }
@@ -97,23 +125,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
 }
 
 template <int DK>
-cudaError_t launch(const Params& p, float* state, cudaStream_t st) {
+cudaError_t launch(const Params& p, float* state, cudaStream_t st, bool prepare) {
     const int ncol = p.dv < 32 ? p.dv : 32;
+    const dim3 grid(p.B * p.H, p.dv / ncol);
     TraceScope ts("decode", st);
-    decode_kernel<DK><<<dim3(p.B * p.H, p.dv / ncol), kDecodeThreads, 0, st>>>(p, state);
+    if (prepare) decode_kernel<DK, true><<<grid, kDecodeThreads, 0, st>>>(p, state);
+    else decode_kernel<DK, false><<<grid, kDecodeThreads, 0, st>>>(p, state);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 // d_k in {16, 32, 64, 128}; d_v in {16, 32, 64, 128}; checked by the caller.
-cudaError_t decode(const Params& p, float* state, cudaStream_t st) {
+cudaError_t decode(const Params& p, float* state, cudaStream_t st, bool prepare) {
     if (p.B == 0 || p.T == 0) return cudaSuccess;
     switch (p.dk) {
-        case 16: return launch<16>(p, state, st);
-        case 32: return launch<32>(p, state, st);
-        case 64: return launch<64>(p, state, st);
-        default: return launch<128>(p, state, st);
+        case 16: return launch<16>(p, state, st, prepare);
+        case 32: return launch<32>(p, state, st, prepare);
+        case 64: return launch<64>(p, state, st, prepare);
+        default: return launch<128>(p, state, st, prepare);
     }
 }
 

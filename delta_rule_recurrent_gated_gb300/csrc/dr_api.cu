@@ -18,7 +18,11 @@ cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse);
 cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st);
 int simt_noalloc_max_units();
 cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st);
-cudaError_t decode(const Params& p, float* state, cudaStream_t st);
+cudaError_t decode(const Params& p, float* state, cudaStream_t st, bool prepare);
+size_t prepare_bytes(const Params& p);
+cudaError_t prepare_inputs(Params& p, uint8_t* area, cudaStream_t st);
+void use_prepared(Params& p, uint8_t* area);
+cudaError_t chain_prepared_grads(const Params& p, cudaStream_t st);
 }  // namespace dr
 
 using dr::Params;
@@ -40,7 +44,7 @@ int check_desc(const dr_desc* d, Path* path) {
     for (int t : {d->io_dtype, d->out_dtype, d->grad_dtype})
         if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
     if (!std::isfinite(d->scale)) return DR_ERR_INVALID_ARG;
-    if (d->flags & ~DR_FLAG_REUSE_FWD) return DR_ERR_INVALID_ARG;
+    if (d->flags & ~(DR_FLAG_REUSE_FWD | DR_FLAG_PREPARE_INPUTS)) return DR_ERR_INVALID_ARG;
     if ((long long)d->B * d->T * d->H * (d->d_k > d->d_v ? d->d_k : d->d_v) >= (1ll << 40))
         return DR_ERR_INVALID_ARG;
     if (d->cu_seqlens) {
@@ -81,10 +85,20 @@ Params make_params(const dr_desc* d) {
     return p;
 }
 
-size_t ws_bytes(const Params& p, Path path) {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The path's own workspace: header, then the path's residuals and scratch.
+size_t path_ws_bytes(const Params& p, Path path) {
     if (path == Path::kSimt)
         return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
     return kHeader + dr::tc_workspace_bytes(p);
+}
+
+// With DR_FLAG_PREPARE_INPUTS the prepared q, k, beta, g follow the path's area.
+size_t ws_bytes(const Params& p, Path path, int flags) {
+    const size_t base = path_ws_bytes(p, path);
+    if (!(flags & DR_FLAG_PREPARE_INPUTS)) return base;
+    return align256(base) + dr::prepare_bytes(p);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? DR_OK : DR_ERR_CUDA; }
@@ -112,7 +126,7 @@ const char* dr_error_string(int code) {
 size_t dr_workspace_bytes(const dr_desc* desc) {
     Path path;
     if (check_desc(desc, &path) != DR_OK) return 0;
-    return ws_bytes(make_params(desc), path);
+    return ws_bytes(make_params(desc), path, desc->flags);
 }
 
 int dr_plan_varlen(const int32_t* cu, int num_seqs, int chunk, int32_t* table, int32_t* offsets,
@@ -157,7 +171,7 @@ int fwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
     const void* ptrs[] = {q, k, v, beta, g, h0, o, hT, u, ws};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
-    const size_t need = ws_bytes(p, path);
+    const size_t need = ws_bytes(p, path, desc->flags);
     if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.hT = hT;
@@ -168,6 +182,10 @@ int fwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
     if (tokens == 0) {
         if (hT) return cuda_status(dr::state_passthrough(h0, hT, (size_t)p.N * p.H * p.dk * p.dv, st));
         return DR_OK;
+    }
+    if (desc->flags & DR_FLAG_PREPARE_INPUTS) {
+        cudaError_t e = dr::prepare_inputs(p, p.ws + align256(path_ws_bytes(p, path)), st);
+        if (e != cudaSuccess) return DR_ERR_CUDA;
     }
     if (path == Path::kSimt) return cuda_status(dr::simt_fwd(p, st));
     return cuda_status(dr::tc_fwd(p, st, true));
@@ -189,7 +207,7 @@ int bwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
     const void* ptrs[] = {q, k, v, beta, g, h0, dO, dhT, dU, dq, dk, dv, dbeta, dg, dh0, ws};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
-    const size_t need = ws_bytes(p, path);
+    const size_t need = ws_bytes(p, path, desc->flags);
     if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0;
@@ -202,8 +220,25 @@ int bwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
         if (dh0) return cuda_status(dr::state_passthrough(dhT, dh0, (size_t)p.N * p.H * p.dk * p.dv, st));
         return DR_OK;
     }
-    if (path == Path::kSimt) return cuda_status(dr::simt_bwd(p, st));
-    return cuda_status(dr::tc_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
+    const bool prepare = (desc->flags & DR_FLAG_PREPARE_INPUTS) != 0;
+    const bool reuse = (desc->flags & DR_FLAG_REUSE_FWD) != 0;
+    Params raw = p;
+    if (prepare) {
+        // the path runs on the prepared tensors, then its gradients are chained back
+        // to the raw ones in place; with DR_FLAG_REUSE_FWD the forward's prepared
+        // tensors are still in the workspace
+        uint8_t* area = p.ws + align256(path_ws_bytes(p, path));
+        if (reuse) {
+            dr::use_prepared(p, area);
+        } else {
+            cudaError_t e = dr::prepare_inputs(p, area, st);
+            if (e != cudaSuccess) return DR_ERR_CUDA;
+        }
+    }
+    cudaError_t e = path == Path::kSimt ? dr::simt_bwd(p, st) : dr::tc_bwd(p, st, reuse);
+    if (e != cudaSuccess) return DR_ERR_CUDA;
+    if (prepare) return cuda_status(dr::chain_prepared_grads(raw, st));
+    return DR_OK;
 }
 
 }  // namespace
@@ -248,6 +283,7 @@ int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
     for (int t : {d.io_dtype, d.out_dtype})
         if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
     if (!std::isfinite(d.scale)) return DR_ERR_INVALID_ARG;
+    if (d.flags & ~(DR_FLAG_REUSE_FWD | DR_FLAG_PREPARE_INPUTS)) return DR_ERR_INVALID_ARG;
     if (d.cu_seqlens || d.chunk_table || d.chunk_offsets || d.num_seqs != d.B)
         return DR_ERR_INVALID_ARG;
     if ((long long)d.B * d.T * d.H * (d.d_k > d.d_v ? d.d_k : d.d_v) >= (1ll << 40))
@@ -263,7 +299,8 @@ int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
     Params p = make_params(desc);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.o = o;
-    return cuda_status(dr::decode(p, state, static_cast<cudaStream_t>(stream)));
+    return cuda_status(dr::decode(p, state, static_cast<cudaStream_t>(stream),
+                                  (d.flags & DR_FLAG_PREPARE_INPUTS) != 0));
 }
 
 int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void* v,
@@ -272,7 +309,7 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
     Path path;
     int rc = check_desc(desc, &path);
     if (rc != DR_OK) return rc;
-    if (path != Path::kSimt) return DR_ERR_UNSUPPORTED;
+    if (path != Path::kSimt || (desc->flags & DR_FLAG_PREPARE_INPUTS)) return DR_ERR_UNSUPPORTED;
     Params p = make_params(desc);
     const long long tokens = (long long)p.B * p.T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;

@@ -66,6 +66,25 @@ enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
 #define DR_FLAG_REUSE_FWD 1  /* dr_bwd: the workspace still holds the residuals
                                 written by dr_fwd for the same desc and inputs;
                                 skip their recomputation */
+/*
+ * DR_FLAG_PREPARE_INPUTS: q, k, beta and g arrive as the projections produce them,
+ * and the library applies the input maps of these layers itself.  The pages give
+ * the recurrence on prepared inputs only (q, k unit-norm keys, beta in [0, 1],
+ * g = log alpha <= 0); the maps below are the standard ones the workloads use to
+ * produce them (q, k L2-normalised per head, beta through a sigmoid, log alpha
+ * through -softplus), with eps = 1e-6 guarding the zero vector:
+ *   q_hat = q * rsqrt(sum_c q_c^2 + 1e-6)   per (token, head); the same for k
+ *   beta  = sigmoid(b)                       b: the beta argument, a logit
+ *   g     = -softplus(x) = -log(1 + e^x)     x: the g argument (GDN, KDA)
+ * dr_fwd / dr_fwd_u write q_hat, k_hat (io_dtype, fp32 arithmetic), beta and g (fp32)
+ * into the workspace (dr_workspace_bytes counts them) and run on those.  dr_bwd /
+ * dr_bwd_u take the same raw tensors and return gradients with respect to them
+ * (dq, dk, dbeta, dg chained through the three maps); with DR_FLAG_REUSE_FWD they
+ * also reuse the prepared tensors the forward left in the workspace instead of
+ * preparing again (the same raw inputs must be passed).  dr_decode applies the maps in
+ * its own kernel.  dr_fwd_noalloc does not take the flag (DR_ERR_UNSUPPORTED).
+ */
+#define DR_FLAG_PREPARE_INPUTS 2
 
 /*
  * Problem descriptor.  Supported set:
@@ -124,7 +143,8 @@ int dr_fwd(const dr_desc* desc, const void* q, const void* k, const void* v,
  * v, beta, g (the log-gate) and h0.  dhT NULL means a zero final-state
  * gradient; dh0 may be NULL when not needed; dg must be NULL for DeltaNet and
  * non-NULL otherwise.  Gradients are with respect to the tensors as passed
- * (q, k already normalised, beta after its sigmoid, g = log alpha).
+ * (q, k already normalised, beta after its sigmoid, g = log alpha; with
+ * DR_FLAG_PREPARE_INPUTS the raw tensors before those maps).
  */
 int dr_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
            const float* beta, const float* g, const float* h0, const void* dO,
@@ -195,6 +215,8 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
  * q, k: [B][T][H][d_k]; v, o: [B][T][H][d_v] in io_dtype / out_dtype;
  *   beta [B][T][H] fp32; g as for dr_fwd (NULL for DeltaNet).  Dense batches
  *   only (cu_seqlens NULL); desc->chunk is ignored (any value >= 1).
+ * desc->flags: DR_FLAG_PREPARE_INPUTS (q, k normalised, beta and g mapped inside
+ *   the kernel, as for dr_fwd); DR_FLAG_REUSE_FWD is ignored.
  * Supported: d_k, d_v in {16, 32, 64, 128}, io bf16 or fp32.  No workspace,
  *   nothing allocated, no device synchronisation; stream-ordered on `stream`.
  * Errors: DR_ERR_INVALID_ARG (bad desc, NULL state or input, packed layout),

@@ -176,3 +176,30 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     assert call(d, q=18) == B.DR_ERR_ALIGNMENT
     dn = desc(T=1, variant=B.DR_DELTANET)
     assert call(dn) == B.DR_ERR_INVALID_ARG  # a gate pointer for DeltaNet
+
+
+def test_prepare_flag_host_rules(lib):
+    """DR_FLAG_PREPARE_INPUTS: accepted by dr_workspace_bytes with room for the
+    prepared tensors (two q/k-sized buffers in the io dtype plus fp32 beta and
+    gate), refused by dr_fwd_noalloc; an unknown flag bit stays an error."""
+    n = B.DR_FLAG_PREPARE_INPUTS
+    for kw, gate_per_token in ((dict(), 1), (dict(variant=B.DR_KDA), 128),
+                               (dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16,
+                                     variant=B.DR_DELTANET), 0)):
+        base = B.workspace_bytes(desc(**kw))
+        prep = B.workspace_bytes(desc(flags=n, **kw))
+        d = desc(**kw)
+        th = d.B * d.T * d.H
+        esize = 2 if d.io_dtype == B.DR_BF16 else 4
+        need = 2 * th * d.d_k * esize + th * 4 + th * (d.d_k if gate_per_token == 128 else
+                                                       gate_per_token) * 4
+        assert need <= prep - base <= need + 4 * 256 + 255
+    assert call_fwd(desc(flags=n | 4)) == B.DR_ERR_INVALID_ARG
+    d = desc(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16, flags=n)
+    assert lib.dr_fwd_noalloc(ctypes.byref(d), 16, 16, 16, 16, 16, None, 16, None,
+                              None) == B.DR_ERR_UNSUPPORTED
+    # a workspace sized without the flag is too small with it
+    small = B.workspace_bytes(desc())
+    assert call_fwd(desc(flags=n), ws_bytes=small) == B.DR_ERR_WORKSPACE
+    dd = desc(T=1, flags=8)
+    assert lib.dr_decode(ctypes.byref(dd), 16, 16, 16, 16, 16, 16, 16, None) == B.DR_ERR_INVALID_ARG
