@@ -133,6 +133,72 @@ def decode_bench(dev, stream, max_over_ranks, barrier, steps=20, warmup=3):
                          "peak_source": f"{peak_src} hbm_gbs (copy, burst)"}}
 
 
+def gdn2_flops_per_chunk(C, d):
+    """FLOPs of one (chunk, head) of the Gated DeltaNet-2 forward + backward as the
+    CUDA-core kernels execute them (dense products, triangular ones counted in full):
+    the chunk-local products (11 of C x C x d), the inverse (C^3 / 3) and the state
+    products (4 of C x d x d) run once in the forward and twice in the backward
+    (chunk-start states, then the reverse pass); the backward adds 20 C x C x d, 8 C x d x d
+    and 2 C x C x C products."""
+    one = 22 * C * C * d + C ** 3 / 3 + 8 * C * d * d
+    return 3 * one + 40 * C * C * d + 16 * C * d * d + 4 * C ** 3
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    """fp32 FMA peak: 152 SMs x 128 fp32 lanes x 2 flops x the SM clock under load."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def gdn2_bench(dev, stream, max_over_ranks, barrier, sm_mhz, steps=3, warmup=3):
+    """Gated DeltaNet-2 forward + backward (dr_gdn2_fwd / dr_gdn2_bwd) on its workload,
+    device-resident inputs, CUDA events on the launching stream."""
+    import torch
+    from delta_rule_recurrent_gated_gb300 import binding, inputs
+    w = inputs.get("gdn2_b4_t2048_h8_d64")
+    x = inputs.make_gdn2(w, seed=0)
+    t = {n: (v.to(dev) if torch.is_tensor(v) and n != "cu_seqlens" else v) for n, v in x.items()}
+    prob = binding.Gdn2Problem(w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io, out="bf16",
+                               grad="bf16", scale=w.scale, device=dev)
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def step():
+        prob.forward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"], o=o, hT=hT)
+        prob.backward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"], t["dO"],
+                      t["dhT"])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    binding.trace_enable(2 * steps + 2)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    assert prob.status() == binding.DR_OK
+    launches = binding.trace_read()
+    binding.trace_enable(0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    chunks = w.B * w.H * ((w.T + w.chunk - 1) // w.chunk)
+    flops = chunks * gdn2_flops_per_chunk(w.chunk, w.dk)
+    peak = fp32_alu_peak_tflops(sm_mhz)
+    ach = flops / (ms / 1e3) / 1e12
+    kern = {}
+    for nm, kms in launches:
+        tot, n = kern.get(nm, (0.0, 0))
+        kern[nm] = (tot + kms, n + 1)
+    return {"workload": w.name, "value": w.tokens / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps, "warmup": warmup, "dtype": "f32 (bf16 io)",
+            "kernels": {nm: {"launches": n, "ms_per_launch": tot / n} for nm, (tot, n) in kern.items()},
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                         "frac": ach / peak, "flops_per_step": flops,
+                         "peak_source": f"fp32 FMA: 152 SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -347,6 +413,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the recurrent-step (dr_decode) measurement")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-gdn2", action="store_true",
+                    help="skip the Gated DeltaNet-2 measurement")
     ap.add_argument("--no-prepare", action="store_true",
                     help="skip the step with input preparation (DR_FLAG_PREPARE_INPUTS)")
     args = ap.parse_args()
@@ -561,6 +629,11 @@ def main():
     # the same step on raw inputs (q, k unnormalised, beta logits, gate arguments) with
     # the library preparing them (DR_FLAG_PREPARE_INPUTS): its cost over the plain step,
     # and each preparation kernel against the HBM roofline
+    g2 = None
+    if not args.no_gdn2:
+        sm = (clk or {}).get("sm_mhz") or 2070.0
+        g2 = gdn2_bench(dev, stream, max_over_ranks, barrier, sm)
+
     pr = None
     if not args.no_prepare:
         pr = prepare_bench(args, w, rank, world, dev, stream, ms, o, hT, grads, max_over_ranks,
@@ -592,6 +665,7 @@ def main():
         "decode": dec,
         "emit_write": wr,
         "prepare_inputs": pr,
+        "gdn2": g2,
         "gpu_launches": len(launches),
         "clocks": clk,
     }

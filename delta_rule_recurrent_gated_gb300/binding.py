@@ -16,11 +16,11 @@ LIB_PATH = os.path.join(HERE, "libdr.so")
 
 DR_OK, DR_ERR_INVALID_ARG, DR_ERR_UNSUPPORTED, DR_ERR_WORKSPACE, DR_ERR_ALIGNMENT, \
     DR_ERR_CUDA, DR_ERR_TIMEOUT, DR_ERR_SCRATCH_LIMIT = range(8)
-DR_DELTANET, DR_GDN, DR_KDA = 0, 1, 2
+DR_DELTANET, DR_GDN, DR_KDA, DR_GDN2 = 0, 1, 2, 3
 DR_BF16, DR_F32 = 0, 1
 DR_FLAG_REUSE_FWD = 1
 DR_FLAG_PREPARE_INPUTS = 2
-VARIANTS = {"deltanet": DR_DELTANET, "gdn": DR_GDN, "kda": DR_KDA}
+VARIANTS = {"deltanet": DR_DELTANET, "gdn": DR_GDN, "kda": DR_KDA, "gdn2": DR_GDN2}
 
 
 class DrDesc(ctypes.Structure):
@@ -74,6 +74,10 @@ def load(path: str = LIB_PATH):
     lib.dr_fwd_noalloc.restype = I
     lib.dr_decode.argtypes = [D] + [P] * 7 + [P]
     lib.dr_decode.restype = I
+    lib.dr_gdn2_fwd.argtypes = [D] + [P] * 9 + [P, S, P]
+    lib.dr_gdn2_fwd.restype = I
+    lib.dr_gdn2_bwd.argtypes = [D] + [P] * 16 + [P, S, P]
+    lib.dr_gdn2_bwd.restype = I
     lib.dr_trace_enable.argtypes = [I]
     lib.dr_trace_enable.restype = I
     lib.dr_trace_count.argtypes = []
@@ -139,6 +143,17 @@ def dr_bwd(desc, q, k, v, beta, g, h0, dO, dhT, dq, dk, dv, dbeta, dg, dh0, ws, 
 
 def dr_decode(desc, q, k, v, beta, g, state, o, stream) -> int:
     return load().dr_decode(ctypes.byref(desc), q, k, v, beta, g, state, o, stream)
+
+
+def dr_gdn2_fwd(desc, q, k, v, erase, write, g, h0, o, hT, ws, ws_bytes, stream) -> int:
+    return load().dr_gdn2_fwd(ctypes.byref(desc), q, k, v, erase, write, g, h0, o, hT, ws,
+                              ws_bytes, stream)
+
+
+def dr_gdn2_bwd(desc, q, k, v, erase, write, g, h0, dO, dhT, dq, dk, dv, derase, dwrite, dg, dh0,
+                ws, ws_bytes, stream) -> int:
+    return load().dr_gdn2_bwd(ctypes.byref(desc), q, k, v, erase, write, g, h0, dO, dhT, dq, dk,
+                              dv, derase, dwrite, dg, dh0, ws, ws_bytes, stream)
 
 
 def check_status(ws, stream) -> int:
@@ -305,3 +320,46 @@ class Decoder:
         _check(dr_decode(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state), _ptr(o),
                          torch.cuda.current_stream(self.device).cuda_stream), "dr_decode")
         return o
+
+
+class Gdn2Problem(Problem):
+    """Gated DeltaNet-2 (dr_gdn2_fwd / dr_gdn2_bwd): the erase gate [B,T,H,dk] and the
+    write gate [B,T,H,dv] take the place of beta."""
+
+    def __init__(self, B, T, H, dk, dv, chunk=64, io="bf16", out="f32", grad="f32",
+                 scale=1.0, cu_seqlens=None, device="cuda"):
+        super().__init__("gdn2", B, T, H, dk, dv, chunk=chunk, io=io, out=out, grad=grad,
+                         scale=scale, cu_seqlens=cu_seqlens, device=device)
+
+    def forward(self, q, k, v, erase, write, g, h0=None, o=None, hT=None, want_hT=True):
+        import torch
+        d = self.desc
+        if o is None:
+            o = torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.out_dtype, device=self.device)
+        if hT is None and want_hT:
+            hT = torch.empty(self.N, d.H, d.d_k, d.d_v, dtype=torch.float32, device=self.device)
+        _check(dr_gdn2_fwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(g),
+                           _ptr(h0), _ptr(o), _ptr(hT), self.ws.data_ptr(), self.ws.numel(),
+                           self._stream()), "dr_gdn2_fwd")
+        return o, hT
+
+    def backward(self, q, k, v, erase, write, g, h0, dO, dhT=None, out=None):
+        import torch
+        d = self.desc
+        if out is None:
+            f32 = dict(dtype=torch.float32, device=self.device)
+            out = {
+                "dq": torch.empty(d.B, d.T, d.H, d.d_k, dtype=self.grad_dtype, device=self.device),
+                "dk": torch.empty(d.B, d.T, d.H, d.d_k, dtype=self.grad_dtype, device=self.device),
+                "dv": torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.grad_dtype, device=self.device),
+                "derase": torch.empty(d.B, d.T, d.H, d.d_k, **f32),
+                "dwrite": torch.empty(d.B, d.T, d.H, d.d_v, **f32),
+                "dg": torch.empty(d.B, d.T, d.H, **f32),
+                "dh0": torch.empty(self.N, d.H, d.d_k, d.d_v, **f32),
+            }
+        _check(dr_gdn2_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(g),
+                           _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(out["dq"]), _ptr(out["dk"]),
+                           _ptr(out["dv"]), _ptr(out["derase"]), _ptr(out["dwrite"]),
+                           _ptr(out["dg"]), _ptr(out["dh0"]), self.ws.data_ptr(), self.ws.numel(),
+                           self._stream()), "dr_gdn2_bwd")
+        return out

@@ -31,6 +31,7 @@ struct Params {
     const int32_t* coff;      // [N+1] first chunk of each sequence or null
     const void *q, *k, *v;
     const float *beta, *g, *h0;
+    const float *erase, *write;  // Gated DeltaNet-2 gates: [.., H, dk] and [.., H, dv]
     void* o;
     float* hT;
     void* u;                  // optional: the write u = beta r, [.., H, dv] in out_dtype
@@ -39,6 +40,7 @@ struct Params {
     const void* dU;           // optional: dL/du of that write, [.., H, dv] in io_dtype
     void *dq, *dk_, *dv_;
     float *dbeta, *dg, *dh0;
+    float *derase, *dwrite;      // their gradients (Gated DeltaNet-2)
     int* err;                 // device error word
     uint8_t* ws;              // workspace base
 };

@@ -23,6 +23,9 @@ size_t prepare_bytes(const Params& p);
 cudaError_t prepare_inputs(Params& p, uint8_t* area, cudaStream_t st);
 void use_prepared(Params& p, uint8_t* area);
 cudaError_t chain_prepared_grads(const Params& p, cudaStream_t st);
+size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv);
+cudaError_t gdn2_fwd(const Params& p, cudaStream_t st);
+cudaError_t gdn2_bwd(const Params& p, cudaStream_t st);
 }  // namespace dr
 
 using dr::Params;
@@ -33,14 +36,14 @@ constexpr size_t kHeader = 256;  // error word + padding at the start of the wor
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-enum class Path { kNone, kTensor, kSimt };
+enum class Path { kNone, kTensor, kSimt, kGdn2 };
 
 // Structural validity (DR_ERR_INVALID_ARG) and support (DR_ERR_UNSUPPORTED).
 int check_desc(const dr_desc* d, Path* path) {
     if (!d) return DR_ERR_INVALID_ARG;
     if (d->B < 0 || d->T < 0 || d->H < 1 || d->d_k < 1 || d->d_v < 1 || d->chunk < 1)
         return DR_ERR_INVALID_ARG;
-    if (d->variant < DR_DELTANET || d->variant > DR_KDA) return DR_ERR_INVALID_ARG;
+    if (d->variant < DR_DELTANET || d->variant > DR_GDN2) return DR_ERR_INVALID_ARG;
     for (int t : {d->io_dtype, d->out_dtype, d->grad_dtype})
         if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
     if (!std::isfinite(d->scale)) return DR_ERR_INVALID_ARG;
@@ -56,12 +59,17 @@ int check_desc(const dr_desc* d, Path* path) {
         if (d->chunk_table || d->chunk_offsets) return DR_ERR_INVALID_ARG;
     }
     *path = Path::kNone;
+    auto small = [](int x) { return x == 16 || x == 32 || x == 64; };
+    if (d->variant == DR_GDN2) {
+        if (d->flags & DR_FLAG_PREPARE_INPUTS) return DR_ERR_UNSUPPORTED;
+        if (small(d->d_k) && small(d->d_v) && small(d->chunk)) *path = Path::kGdn2;
+        return *path == Path::kNone ? DR_ERR_UNSUPPORTED : DR_OK;
+    }
     if (d->io_dtype == DR_BF16) {
         if (d->d_k == d->d_v && (d->d_k == 64 || d->d_k == 128) && d->chunk == 64)
             *path = Path::kTensor;
     } else {
-        auto ok = [](int x) { return x == 16 || x == 32 || x == 64; };
-        if (ok(d->d_k) && ok(d->d_v) && ok(d->chunk)) *path = Path::kSimt;
+        if (small(d->d_k) && small(d->d_v) && small(d->chunk)) *path = Path::kSimt;
     }
     return *path == Path::kNone ? DR_ERR_UNSUPPORTED : DR_OK;
 }
@@ -89,6 +97,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // The path's own workspace: header, then the path's residuals and scratch.
 size_t path_ws_bytes(const Params& p, Path path) {
+    if (path == Path::kGdn2)
+        return kHeader + dr::gdn2_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
     if (path == Path::kSimt)
         return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
     return kHeader + dr::tc_workspace_bytes(p);
@@ -164,6 +174,7 @@ int fwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
     Path path;
     int rc = check_desc(desc, &path);
     if (rc != DR_OK) return rc;
+    if (path == Path::kGdn2) return DR_ERR_INVALID_ARG;  // its gates go through dr_gdn2_fwd
     Params p = make_params(desc);
     const long long tokens = (long long)p.B * p.T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
@@ -198,6 +209,7 @@ int bwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
     Path path;
     int rc = check_desc(desc, &path);
     if (rc != DR_OK) return rc;
+    if (path == Path::kGdn2) return DR_ERR_INVALID_ARG;  // its gates go through dr_gdn2_bwd
     Params p = make_params(desc);
     const long long tokens = (long long)p.B * p.T;
     if (tokens > 0 && (!q || !k || !v || !beta || !dO || !dq || !dk || !dv || !dbeta))
@@ -325,6 +337,67 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
         return DR_OK;
     }
     return cuda_status(dr::simt_fwd_noalloc(p, st));
+}
+
+int dr_gdn2_fwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+                const float* erase, const float* write, const float* g, const float* h0, void* o,
+                float* hT, void* ws, size_t ws_size, void* stream) {
+    Path path;
+    int rc = check_desc(desc, &path);
+    if (rc != DR_OK) return rc;
+    if (path != Path::kGdn2) return DR_ERR_INVALID_ARG;
+    Params p = make_params(desc);
+    const long long tokens = (long long)p.B * p.T;
+    if (tokens > 0 && (!q || !k || !v || !erase || !write || !g || !o)) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, erase, write, g, h0, o, hT, ws};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    const size_t need = ws_bytes(p, path, desc->flags);
+    if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.q = q; p.k = k; p.v = v; p.erase = erase; p.write = write; p.g = g; p.h0 = h0;
+    p.o = o; p.hT = hT;
+    p.ws = static_cast<uint8_t*>(ws);
+    p.err = static_cast<int*>(ws);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
+    if (tokens == 0) {
+        if (hT) return cuda_status(dr::state_passthrough(h0, hT, (size_t)p.N * p.H * p.dk * p.dv, st));
+        return DR_OK;
+    }
+    return cuda_status(dr::gdn2_fwd(p, st));
+}
+
+int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+                const float* erase, const float* write, const float* g, const float* h0,
+                const void* dO, const float* dhT, void* dq, void* dk, void* dv, float* derase,
+                float* dwrite, float* dg, float* dh0, void* ws, size_t ws_size, void* stream) {
+    Path path;
+    int rc = check_desc(desc, &path);
+    if (rc != DR_OK) return rc;
+    if (path != Path::kGdn2) return DR_ERR_INVALID_ARG;
+    Params p = make_params(desc);
+    const long long tokens = (long long)p.B * p.T;
+    if (tokens > 0 && (!q || !k || !v || !erase || !write || !g || !dO || !dq || !dk || !dv ||
+                       !derase || !dwrite || !dg))
+        return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, erase, write, g, h0, dO, dhT, dq, dk, dv, derase, dwrite, dg,
+                          dh0, ws};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    const size_t need = ws_bytes(p, path, desc->flags);
+    if (!ws || ws_size < need) return DR_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    p.q = q; p.k = k; p.v = v; p.erase = erase; p.write = write; p.g = g; p.h0 = h0;
+    p.dO = dO; p.dhT = dhT; p.dq = dq; p.dk_ = dk; p.dv_ = dv; p.derase = derase;
+    p.dwrite = dwrite; p.dg = dg; p.dh0 = dh0;
+    p.ws = static_cast<uint8_t*>(ws);
+    p.err = static_cast<int*>(ws);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
+    if (tokens == 0) {
+        if (dh0) return cuda_status(dr::state_passthrough(dhT, dh0, (size_t)p.N * p.H * p.dk * p.dv, st));
+        return DR_OK;
+    }
+    return cuda_status(dr::gdn2_bwd(p, st));
 }
 
 int dr_check_status(const void* ws, void* stream) {

@@ -219,11 +219,11 @@ __global__ void __launch_bounds__(kThreads)
     if (ng) map_range<CHAIN ? 3 : 1>(x, g_out, ng, tid, nthreads);
 }
 
+// One block per slice of the work: blocks that finish make room for new ones, so loads
+// of new blocks overlap the stores of finishing ones (the loops above still stride the
+// grid, should the work ever exceed the grid limit).
 int stream_grid(long long blocks_needed) {
-    int dev = 0, sms = 152;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long cap = (long long)sms * 8;  // eight resident 256-thread blocks per SM
+    const long long cap = 0x7fffffffll;
     return (int)(blocks_needed < 1 ? 1 : (blocks_needed < cap ? blocks_needed : cap));
 }
 

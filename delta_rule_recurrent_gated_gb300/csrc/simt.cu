@@ -19,34 +19,13 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "simt_util.cuh"
 #include "trace.cuh"
 
 namespace dr {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBuf = 64 * 64;  // floats per scratch matrix (C, d_k, d_v <= 64)
-
-// C[m x n] = alpha * op(A) op(B) (+ C when acc).  op(A) is m x k.
-__device__ void mm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* Bm,
-                   int ldb, bool tb, int m, int n, int k, float alpha, bool acc) {
-    for (int idx = threadIdx.x; idx < m * n; idx += blockDim.x) {
-        const int i = idx / n, j = idx % n;
-        float s = 0.f;
-        for (int p = 0; p < k; ++p) {
-            const float a = ta ? A[p * lda + i] : A[i * lda + p];
-            const float b = tb ? Bm[j * ldb + p] : Bm[p * ldb + j];
-            s = fmaf(a, b, s);
-        }
-        Cm[i * ldc + j] = acc ? Cm[i * ldc + j] + alpha * s : alpha * s;
-    }
-    __syncthreads();
-}
-
-struct Scratch {
-    float* base;
-    __device__ float* operator()(int i) const { return base + (size_t)i * kBuf; }
-};
+constexpr int kThreads = kSimtThreads;
 
 enum {
     bS, bQ, bK, bV, bGam, bKb, bKr, bQb, bKC, bA, bT, bbK, bbV, bWy, bUt, bAqk, bQt, bOt, bU,
@@ -137,12 +116,6 @@ __device__ void chunk_scan(const Params& p, const Scratch& s, int L, float* S) {
     for (int idx = tid; idx < dk * dv; idx += nt) S[idx] *= gL[idx / dv];
     __syncthreads();
     mm(S, dv, s(bKC), dk, true, U, dv, false, dk, dv, L, 1.f, true);
-}
-
-__device__ void load_state(float* S, const float* h, int n, int hd, int H, int dk, int dv) {
-    for (int idx = threadIdx.x; idx < dk * dv; idx += blockDim.x)
-        S[idx] = h ? h[((size_t)n * H + hd) * dk * dv + idx] : 0.f;
-    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scratch) {

@@ -1,0 +1,328 @@
+// simt_gdn2.cu -- Gated DeltaNet-2 (separate per-channel erase and write gates) on the
+// fp32 CUDA-core chunkwise path.
+//
+// Recurrence ("Linear Attention Architectures: Mechanisms, Trade-offs, and Cross-Layer
+// Routing", section "Metodologia y Marco de Trabajo", item 1, the Gated DeltaNet-2
+// bullet, which gives it in words: erase gates choose which key channels are removed,
+// write gates which value channels are stored; read with the scalar decay of the Gated
+// DeltaNet bullet), on the state S = W^T (d_k x d_v), per token:
+//   Sd = alpha S;  p = Sd^T k;  S = Sd - b p^T + k vw^T;  o = scale S^T q
+// with b = erase . k and vw = write . v (Gated DeltaNet when erase = write = beta).
+//
+// Chunkwise form over L <= C tokens from the chunk-start state S0 (Gamma = within-chunk
+// cumulative log-decay, one scalar per token; the rows of P are the predictions p):
+//   Kb = e^G K, Kr = e^-G K, Br = e^-G B, Qb = e^G Q, KC = e^{G_L - G} K, BC = e^{G_L - G} B
+//   T  = (I + strict_lower(Kb Br^T))^{-1},   Mk = strict_lower(Kb Kr^T)
+//   Wy = T Kb,  X = Mk Vw,  Pt = T X              so that  P = Pt + Wy S0
+//   Aqk = tril(Qb Kr^T), Aqb = tril(Qb Br^T)
+//   Qt = scale (Qb - Aqb Wy),  Ot = scale (Aqk Vw - Aqb Pt)   so that  O = Ot + Qt S0
+//   S_L = e^{G_L} S0 + KC^T Vw - BC^T P
+// (the predictions satisfy (I + strict_lower(Kb Br^T)) P = Kb S0 + Mk Vw: each p_t sees
+// the decayed start state and every earlier write and erase of the chunk).  The
+// backward is the chain rule through exactly these steps.  One CTA per (sequence,
+// head) walks its chunks; matrices live in a per-CTA scratch slice of the workspace.
+#include "common.cuh"
+#include "simt_util.cuh"
+#include "trace.cuh"
+
+namespace dr {
+namespace {
+
+constexpr int kThreads2 = 512;  // one CTA per (sequence, head): few CTAs, so wide ones
+
+enum {
+    gS, gQ, gK, gV, gE, gWg, gVw, gB, gGam, gKb, gKr, gBr, gQb, gKC, gBC, gA, gMk, gT, gWy, gX,
+    gPt, gAqk, gAqb, gQt, gOt, gP, gO, gTmp,
+    // backward only
+    gS0, gdS, gdSp, gdO, gdP, gdQt, gdWy, gdPt, gdX, gdMk, gdKC, gdBC, gdVw, gdAqk, gdAqb, gdQb,
+    gdKb, gdKr, gdBr, gdT, gdA, gdGam, gdVec,
+    kNumBufs2
+};
+
+__device__ void mask(float* M, int L, bool keep_diag) {
+    for (int idx = threadIdx.x; idx < L * L; idx += blockDim.x) {
+        const int i = idx / L, j = idx % L;
+        if (keep_diag ? j > i : j >= i) M[idx] = 0.f;
+    }
+    __syncthreads();
+}
+
+// Load one chunk and evaluate everything that does not depend on the state.
+// gGam holds Gamma_i at [i] and e^{Gamma_L} at [C].
+__device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, int L) {
+    const int dk = p.dk, dv = p.dv, H = p.H, tid = threadIdx.x, nt = blockDim.x;
+    const float sc = p.scale;
+    float* q = s(gQ); float* k = s(gK); float* v = s(gV); float* e = s(gE); float* w = s(gWg);
+    float* gm = s(gGam);
+    for (int idx = tid; idx < L * dk; idx += nt) {
+        const size_t a = ((size_t)(row0 + idx / dk) * H + h) * dk + idx % dk;
+        q[idx] = ld_any(p.q, a, p.io_dtype);
+        k[idx] = ld_any(p.k, a, p.io_dtype);
+        e[idx] = p.erase[a];
+    }
+    for (int idx = tid; idx < L * dv; idx += nt) {
+        const size_t a = ((size_t)(row0 + idx / dv) * H + h) * dv + idx % dv;
+        v[idx] = ld_any(p.v, a, p.io_dtype);
+        w[idx] = p.write[a];
+    }
+    if (tid == 0) {
+        float acc = 0.f;
+        for (int i = 0; i < L; ++i) {
+            acc += p.g[(size_t)(row0 + i) * H + h];
+            gm[i] = acc;
+        }
+        gm[p.C] = expf(acc);
+    }
+    __syncthreads();
+    float* Bm = s(gB); float* Vw = s(gVw); float* Kb = s(gKb); float* Kr = s(gKr);
+    float* Br = s(gBr); float* Qb = s(gQb); float* KC = s(gKC); float* BC = s(gBC);
+    const float GL = gm[L - 1];
+    for (int idx = tid; idx < L * dk; idx += nt) {
+        const float G = gm[idx / dk];
+        const float eG = expf(G), enG = expf(-G), eC = expf(GL - G);
+        const float b = e[idx] * k[idx];
+        Bm[idx] = b;
+        Kb[idx] = k[idx] * eG;
+        Kr[idx] = k[idx] * enG;
+        Br[idx] = b * enG;
+        Qb[idx] = q[idx] * eG;
+        KC[idx] = k[idx] * eC;
+        BC[idx] = b * eC;
+    }
+    for (int idx = tid; idx < L * dv; idx += nt) Vw[idx] = w[idx] * v[idx];
+    __syncthreads();
+    float* A = s(gA); float* T = s(gT); float* Mk = s(gMk);
+    mm2(A, L, Kb, dk, false, Br, dk, true, L, L, dk, 1.f, false);
+    mask(A, L, false);
+    mm2(Mk, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    mask(Mk, L, false);
+    // T = (I + A)^{-1}, forward substitution by rows
+    for (int i = 0; i < L; ++i) {
+        for (int n = tid; n < L; n += nt) {
+            float x = (n == i) ? 1.f : 0.f;
+            if (n < i)
+                for (int j = n; j < i; ++j) x -= A[i * L + j] * T[j * L + n];
+            T[i * L + n] = x;
+        }
+        __syncthreads();
+    }
+    float* Wy = s(gWy); float* X = s(gX); float* Pt = s(gPt); float* Aqk = s(gAqk);
+    float* Aqb = s(gAqb); float* Qt = s(gQt); float* Ot = s(gOt);
+    mm2(Wy, dk, T, L, false, Kb, dk, false, L, dk, L, 1.f, false);
+    mm2(X, dv, Mk, L, false, Vw, dv, false, L, dv, L, 1.f, false);
+    mm2(Pt, dv, T, L, false, X, dv, false, L, dv, L, 1.f, false);
+    mm2(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    mask(Aqk, L, true);
+    mm2(Aqb, L, Qb, dk, false, Br, dk, true, L, L, dk, 1.f, false);
+    mask(Aqb, L, true);
+    mm2(Qt, dk, Aqb, L, false, Wy, dk, false, L, dk, L, -sc, false);
+    for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += sc * Qb[idx];
+    mm2(Ot, dv, Aqk, L, false, Vw, dv, false, L, dv, L, sc, false);
+    mm2(Ot, dv, Aqb, L, false, Pt, dv, false, L, dv, L, -sc, true);
+}
+
+// P = Pt + Wy S; O = Ot + Qt S; S <- e^{Gamma_L} S + KC^T Vw - BC^T P
+__device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S) {
+    const int dk = p.dk, dv = p.dv, tid = threadIdx.x, nt = blockDim.x;
+    float* P = s(gP); float* O = s(gO);
+    for (int idx = tid; idx < L * dv; idx += nt) { P[idx] = s(gPt)[idx]; O[idx] = s(gOt)[idx]; }
+    __syncthreads();
+    mm2(P, dv, s(gWy), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    mm2(O, dv, s(gQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    const float gL = s(gGam)[p.C];
+    for (int idx = tid; idx < dk * dv; idx += nt) S[idx] *= gL;
+    __syncthreads();
+    mm2(S, dv, s(gKC), dk, true, s(gVw), dv, false, dk, dv, L, 1.f, true);
+    mm2(S, dv, s(gBC), dk, true, P, dv, false, dk, dv, L, -1.f, true);
+}
+
+__global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
+    const Scratch s{scratch + (size_t)u * kNumBufs2 * kBuf};
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+    float* S = s(gS);
+    load_state(S, p.h0, n, h, p.H, p.dk, p.dv);
+    for (int c = 0; c < nc; ++c) {
+        const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
+        chunk_prep2(p, s, h, row0, L);
+        chunk_scan2(p, s, L, S);
+        const float* O = s(gO);
+        for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
+            const size_t a = ((size_t)(row0 + idx / p.dv) * p.H + h) * p.dv + idx % p.dv;
+            st_any(p.o, a, p.out_dtype, O[idx]);
+        }
+        __syncthreads();
+    }
+    if (p.hT)
+        for (int idx = threadIdx.x; idx < p.dk * p.dv; idx += blockDim.x)
+            p.hT[((size_t)n * p.H + h) * p.dk * p.dv + idx] = S[idx];
+}
+
+__global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* scratch,
+                                                                float* states) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
+    const int dk = p.dk, dv = p.dv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
+    const float sc = p.scale;
+    const Scratch s{scratch + (size_t)u * kNumBufs2 * kBuf};
+    int c0, nc, srow, slen;
+    seq_chunks(p, n, c0, nc, srow, slen);
+    const size_t SS = (size_t)dk * dv;
+    // pass 1: the state at the start of every chunk
+    float* S = s(gS);
+    load_state(S, p.h0, n, h, p.H, dk, dv);
+    for (int c = 0; c < nc; ++c) {
+        const int row0 = srow + c * C, L = min(C, slen - c * C);
+        float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
+        for (int idx = tid; idx < dk * dv; idx += nt) dst[idx] = S[idx];
+        __syncthreads();
+        chunk_prep2(p, s, h, row0, L);
+        chunk_scan2(p, s, L, S);
+    }
+    // pass 2: reverse over chunks with dS = dL/dS_end
+    float* dS = s(gdS);
+    load_state(dS, p.dhT, n, h, p.H, dk, dv);
+    for (int c = nc - 1; c >= 0; --c) {
+        const int row0 = srow + c * C, L = min(C, slen - c * C);
+        float* S0 = s(gS0);
+        const float* src = states + ((size_t)(c0 + c) * p.H + h) * SS;
+        for (int idx = tid; idx < dk * dv; idx += nt) { S0[idx] = src[idx]; S[idx] = src[idx]; }
+        __syncthreads();
+        chunk_prep2(p, s, h, row0, L);
+        chunk_scan2(p, s, L, S);  // recomputes P (S is scratch here)
+        float* dO = s(gdO);
+        for (int idx = tid; idx < L * dv; idx += nt)
+            dO[idx] = ld_any(p.dO, ((size_t)(row0 + idx / dv) * p.H + h) * dv + idx % dv,
+                             p.io_dtype);
+        __syncthreads();
+        const float gL = s(gGam)[C];
+        float* dP = s(gdP); float* dSp = s(gdSp); float* dQt = s(gdQt); float* dWy = s(gdWy);
+        float* dPt = s(gdPt); float* dKC = s(gdKC); float* dBC = s(gdBC); float* dVw = s(gdVw);
+        float* dVec = s(gdVec);
+        // state update S_L = gL S0 + KC^T Vw - BC^T P and the reads O = Ot + Qt S0
+        mm2(dP, dv, s(gBC), dk, false, dS, dv, false, L, dv, dk, -1.f, false);
+        for (int idx = tid; idx < dk * dv; idx += nt) dSp[idx] = gL * dS[idx];
+        for (int c2 = tid; c2 < dk; c2 += nt) {
+            float acc = 0.f;
+            for (int j = 0; j < dv; ++j) acc += dS[c2 * dv + j] * S0[c2 * dv + j];
+            dVec[c2] = acc;  // d e^{Gamma_L}, per key row
+        }
+        __syncthreads();
+        mm2(dSp, dv, s(gQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
+        mm2(dSp, dv, s(gWy), dk, true, dP, dv, false, dk, dv, L, 1.f, true);
+        mm2(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm2(dWy, dk, dP, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm2(dKC, dk, s(gVw), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
+        mm2(dBC, dk, s(gP), dv, false, dS, dv, true, L, dk, dv, -1.f, false);
+        mm2(dVw, dv, s(gKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
+        for (int idx = tid; idx < L * dv; idx += nt) dPt[idx] = dP[idx];
+        __syncthreads();
+        // Qt = sc (Qb - Aqb Wy), Ot = sc (Aqk Vw - Aqb Pt)
+        float* dAqk = s(gdAqk); float* dAqb = s(gdAqb); float* dQb = s(gdQb);
+        mm2(dAqb, L, dQt, dk, false, s(gWy), dk, true, L, L, dk, -sc, false);
+        mm2(dAqb, L, dO, dv, false, s(gPt), dv, true, L, L, dv, -sc, true);
+        mask(dAqb, L, true);
+        mm2(dAqk, L, dO, dv, false, s(gVw), dv, true, L, L, dv, sc, false);
+        mask(dAqk, L, true);
+        mm2(dWy, dk, s(gAqb), L, true, dQt, dk, false, L, dk, L, -sc, true);
+        mm2(dVw, dv, s(gAqk), L, true, dO, dv, false, L, dv, L, sc, true);
+        mm2(dPt, dv, s(gAqb), L, true, dO, dv, false, L, dv, L, -sc, true);
+        for (int idx = tid; idx < L * dk; idx += nt) dQb[idx] = sc * dQt[idx];
+        __syncthreads();
+        // Wy = T Kb, Pt = T X, X = Mk Vw
+        float* dT = s(gdT); float* dKb = s(gdKb); float* dX = s(gdX); float* dMk = s(gdMk);
+        mm2(dT, L, dWy, dk, false, s(gKb), dk, true, L, L, dk, 1.f, false);
+        mm2(dT, L, dPt, dv, false, s(gX), dv, true, L, L, dv, 1.f, true);
+        mm2(dKb, dk, s(gT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
+        mm2(dX, dv, s(gT), L, true, dPt, dv, false, L, dv, L, 1.f, false);
+        mm2(dMk, L, dX, dv, false, s(gVw), dv, true, L, L, dv, 1.f, false);
+        mask(dMk, L, false);
+        mm2(dVw, dv, s(gMk), L, true, dX, dv, false, L, dv, L, 1.f, true);
+        // T = (I + A)^{-1}: dA = -T^T dT T^T (strictly lower); A = Kb Br^T, Mk = Kb Kr^T
+        float* dA = s(gdA); float* tmp = s(gTmp); float* dKr = s(gdKr); float* dBr = s(gdBr);
+        mm2(tmp, L, dT, L, false, s(gT), L, true, L, L, L, 1.f, false);
+        mm2(dA, L, s(gT), L, true, tmp, L, false, L, L, L, -1.f, false);
+        mask(dA, L, false);
+        mm2(dKb, dk, dA, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
+        mm2(dBr, dk, dA, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
+        mm2(dKb, dk, dMk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
+        mm2(dKr, dk, dMk, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
+        // Aqk = tril(Qb Kr^T), Aqb = tril(Qb Br^T)
+        mm2(dQb, dk, dAqk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
+        mm2(dKr, dk, dAqk, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
+        mm2(dQb, dk, dAqb, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
+        mm2(dBr, dk, dAqb, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
+        // decay and gate chain -> dq, dk, derase, dv, dwrite, dGamma
+        const float* gm = s(gGam);
+        float* dGam = s(gdGam);
+        const float* k = s(gK); const float* e = s(gE);
+        for (int idx = tid; idx < L * dk; idx += nt) {
+            const int i = idx / dk;
+            const float G = gm[i], GL = gm[L - 1];
+            const float eG = expf(G), enG = expf(-G), eC = expf(GL - G);
+            const float dB = dBr[idx] * enG + dBC[idx] * eC;
+            const size_t a = ((size_t)(row0 + i) * p.H + h) * dk + idx % dk;
+            st_any(p.dq, a, p.grad_dtype, dQb[idx] * eG);
+            st_any(p.dk_, a, p.grad_dtype,
+                   dKb[idx] * eG + dKr[idx] * enG + dKC[idx] * eC + e[idx] * dB);
+            p.derase[a] = k[idx] * dB;
+            tmp[idx] = dQb[idx] * s(gQb)[idx] + dKb[idx] * s(gKb)[idx] - dKr[idx] * s(gKr)[idx] -
+                       dKC[idx] * s(gKC)[idx] - dBr[idx] * s(gBr)[idx] - dBC[idx] * s(gBC)[idx];
+            dGam[idx] = dKC[idx] * s(gKC)[idx] + dBC[idx] * s(gBC)[idx];  // Gamma_L terms
+        }
+        for (int idx = tid; idx < L * dv; idx += nt) {
+            const size_t a = ((size_t)(row0 + idx / dv) * p.H + h) * dv + idx % dv;
+            st_any(p.dv_, a, p.grad_dtype, s(gWg)[idx] * dVw[idx]);
+            p.dwrite[a] = s(gV)[idx] * dVw[idx];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            // dGamma_i = sum over channels; Gamma_L also collects the KC, BC and e^{Gamma_L}
+            // terms; dg = reverse cumulative sum
+            float tail = 0.f;
+            for (int c2 = 0; c2 < dk; ++c2) tail += dVec[c2];
+            tail *= gL;
+            for (int idx = 0; idx < L * dk; ++idx) tail += dGam[idx];
+            float run = 0.f;
+            for (int i = L - 1; i >= 0; --i) {
+                float di = (i == L - 1) ? tail : 0.f;
+                for (int c2 = 0; c2 < dk; ++c2) di += tmp[i * dk + c2];
+                run += di;
+                p.dg[(size_t)(row0 + i) * p.H + h] = run;
+            }
+        }
+        for (int idx = tid; idx < dk * dv; idx += nt) dS[idx] = dSp[idx];
+        __syncthreads();
+    }
+    if (p.dh0)
+        for (int idx = tid; idx < dk * dv; idx += nt)
+            p.dh0[((size_t)n * p.H + h) * SS + idx] = dS[idx];
+}
+
+}  // namespace
+
+size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv) {
+    return (size_t)units * kNumBufs2 * kBuf * sizeof(float) +
+           (size_t)num_chunks * H * dk * dv * sizeof(float);
+}
+
+cudaError_t gdn2_fwd(const Params& p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    TraceScope ts("gdn2_fwd", st);
+    gdn2_fwd_kernel<<<units, kThreads2, 0, st>>>(p, scratch);
+    return cudaGetLastError();
+}
+
+cudaError_t gdn2_bwd(const Params& p, cudaStream_t st) {
+    const int units = p.N * p.H;
+    if (units == 0) return cudaSuccess;
+    float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    float* states = scratch + (size_t)units * kNumBufs2 * kBuf;
+    TraceScope ts("gdn2_bwd", st);
+    gdn2_bwd_kernel<<<units, kThreads2, 0, st>>>(p, scratch, states);
+    return cudaGetLastError();
+}
+
+}  // namespace dr

@@ -17,7 +17,7 @@ from typing import List, Optional
 
 import torch
 
-VARIANT_IDS = {"deltanet": 0, "gdn": 1, "kda": 2}
+VARIANT_IDS = {"deltanet": 0, "gdn": 1, "kda": 2, "gdn2": 3}
 
 
 @dataclass(frozen=True)
@@ -59,6 +59,8 @@ WORKLOADS = {
 # a two-sequence case of the same layer, for kernel profiling (inputs still exceed L2)
 WORKLOADS["gdn_b2_t4096_h16_d128"] = Workload("gdn_b2_t4096_h16_d128", "gdn", 2, 4096, 16, 128, 128,
                                               h0=True)
+# Gated DeltaNet-2 on the layer shape of the Gated DeltaNet workload above
+WORKLOADS["gdn2_b4_t2048_h8_d64"] = Workload("gdn2_b4_t2048_h8_d64", "gdn2", 4, 2048, 8, 64, 64)
 for _v in ("deltanet", "gdn", "kda"):
     for _T, _B in ((4096, 16), (8192, 8), (16384, 4), (32768, 2)):
         _n = f"sweep_{_v}_b{_B}_t{_T}_h16_d128"
@@ -179,6 +181,40 @@ def make_raw(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
             "dhT": dhT, "cu_seqlens": cu, "N": N}
 
 
+def make_gdn2(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
+    """Inputs of a Gated DeltaNet-2 workload: q, k, v, g, h0, dO, dhT drawn as for Gated
+    DeltaNet in ``make``; the erase gate [B,T,H,dk] and the write gate [B,T,H,dv] are
+    sigmoid(N(0,1)) per channel (in place of beta).  Same generator, in the draw order
+    q, k, v, erase logits, write logits, g logits, h0, dO, dhT."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = io_dtype(w)
+    cu = cu_seqlens_of(w, seed)
+    N = w.B if cu is None else int(cu.numel() - 1)
+
+    def unit_rows(shape):
+        x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+        return x.to(dt)
+
+    q = unit_rows((w.B, w.T, w.H, w.dk))
+    k = unit_rows((w.B, w.T, w.H, w.dk))
+    v = torch.randn(w.B, w.T, w.H, w.dv, generator=gen, dtype=torch.float32).to(dt)
+    erase = torch.sigmoid(torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32))
+    write = torch.sigmoid(torch.randn(w.B, w.T, w.H, w.dv, generator=gen, dtype=torch.float32))
+    g = -torch.nn.functional.softplus(
+        torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)) * 0.1
+    h0 = None
+    if w.h0:
+        h0 = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02
+    dO = dhT = None
+    if need_grad_inputs:
+        dO = torch.randn(w.B, w.T, w.H, w.dv, generator=gen, dtype=torch.float32).to(dt)
+        if w.dhT:
+            dhT = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02
+    return {"q": q, "k": k, "v": v, "erase": erase, "write": write, "g": g, "h0": h0,
+            "dO": dO, "dhT": dhT, "cu_seqlens": cu, "N": N}
+
+
 def small(variant: str, B=2, T=200, H=3, dk=64, dv=64, chunk=64, io="bf16", h0=True,
           dhT=True, lengths=None) -> Workload:
     """A small workload of the same distributions (several chunks, ragged tail)."""
@@ -188,5 +224,5 @@ def small(variant: str, B=2, T=200, H=3, dk=64, dv=64, chunk=64, io="bf16", h0=T
                     h0=h0, dhT=dhT, lengths=None if lengths is None else tuple(lengths))
 
 
-__all__ = ["Workload", "WORKLOADS", "get", "make", "make_raw", "small", "ragged_lengths",
+__all__ = ["Workload", "WORKLOADS", "get", "make", "make_raw", "make_gdn2", "small", "ragged_lengths",
            "cu_seqlens_of", "num_seqs", "io_dtype", "replace", "field"]

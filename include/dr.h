@@ -59,7 +59,7 @@ enum dr_status_code {
     DR_ERR_SCRATCH_LIMIT = 7  /* dr_fwd_noalloc: problem larger than its static scratch */
 };
 
-enum dr_variant { DR_DELTANET = 0, DR_GDN = 1, DR_KDA = 2 };
+enum dr_variant { DR_DELTANET = 0, DR_GDN = 1, DR_KDA = 2, DR_GDN2 = 3 /* dr_gdn2_* only */ };
 enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
 
 /* dr_desc.flags */
@@ -225,6 +225,36 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
  */
 int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
               const float* beta, const float* g, float* state, void* o, void* stream);
+
+/*
+ * Gated DeltaNet-2: separate per-channel erase and write gates ("Linear Attention
+ * Architectures: Mechanisms, Trade-offs, and Cross-Layer Routing", section "Metodologia
+ * y Marco de Trabajo", item 1, the Gated DeltaNet-2 bullet, which describes it in words
+ * only).  The library reads it as Gated DeltaNet's scalar decay followed by an erase
+ * along the gated key channels and a write of the gated value channels:
+ *   Wd_t = alpha_t W_{t-1};  p_t = Wd_t k_t;
+ *   W_t  = Wd_t - p_t (erase_t . k_t)^T + (write_t . v_t) k_t^T;  o_t = scale W_t q_t
+ * ("." elementwise), which is Gated DeltaNet when erase_t = write_t = beta_t.
+ * desc->variant must be DR_GDN2.  Inputs as dr_fwd / dr_bwd with beta replaced by
+ *   erase [B, T, H, d_k] fp32 (gate per key channel, normally in [0, 1]) and
+ *   write [B, T, H, d_v] fp32 (gate per value channel, normally in [0, 1]);
+ *   g [B, T, H] fp32 = log alpha, never NULL.
+ * dr_gdn2_bwd returns dq, dk, dv (grad dtype), derase, dwrite, dg (fp32) and dh0
+ * (optional) for L = sum(dO * o) + sum(dhT * hT).
+ * Supported: d_k, d_v, chunk in {16, 32, 64}; io bf16 or fp32 (fp32 arithmetic on the
+ * CUDA cores for both); dense or packed layout as dr_fwd.  dr_workspace_bytes sizes the
+ * workspace (same value for both calls).  Flags: DR_FLAG_REUSE_FWD is ignored;
+ * DR_FLAG_PREPARE_INPUTS is DR_ERR_UNSUPPORTED.  Errors as dr_fwd / dr_bwd; dr_fwd and
+ * dr_bwd refuse DR_GDN2 with DR_ERR_INVALID_ARG.
+ */
+int dr_gdn2_fwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+                const float* erase, const float* write, const float* g, const float* h0,
+                void* o, float* hT, void* workspace, size_t workspace_bytes, void* stream);
+int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v,
+                const float* erase, const float* write, const float* g, const float* h0,
+                const void* dO, const float* dhT, void* dq, void* dk, void* dv, float* derase,
+                float* dwrite, float* dg, float* dh0, void* workspace, size_t workspace_bytes,
+                void* stream);
 
 /* Synchronise `stream` and report any device-side error recorded in the
    workspace by the last call that used it (DR_OK or DR_ERR_TIMEOUT), or

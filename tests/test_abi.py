@@ -203,3 +203,35 @@ def test_prepare_flag_host_rules(lib):
     assert call_fwd(desc(flags=n), ws_bytes=small) == B.DR_ERR_WORKSPACE
     dd = desc(T=1, flags=8)
     assert lib.dr_decode(ctypes.byref(dd), 16, 16, 16, 16, 16, 16, 16, None) == B.DR_ERR_INVALID_ARG
+
+
+def test_gdn2_host_rules(lib):
+    """Gated DeltaNet-2 has its own entry points: dr_fwd / dr_bwd refuse the variant,
+    dr_gdn2_* refuse the others; sizes outside {16, 32, 64} and the preparation flag
+    are unsupported; its workspace is sized by dr_workspace_bytes."""
+    d2 = dict(variant=B.DR_GDN2, d_k=64, d_v=32, chunk=32)
+    assert B.workspace_bytes(desc(**d2)) > 0
+    assert B.workspace_bytes(desc(variant=B.DR_GDN2)) == 0            # d = 128
+    assert call_fwd(desc(**d2)) == B.DR_ERR_INVALID_ARG
+
+    def fwd2(d, **kw):
+        p = dict(q=16, k=16, v=16, erase=16, write=16, g=16, h0=None, o=16, hT=None)
+        p.update(kw)
+        return B.dr_gdn2_fwd(d, *p.values(), 16, 1 << 40, None)
+    assert fwd2(desc()) == B.DR_ERR_INVALID_ARG                       # variant GDN
+    assert fwd2(desc(variant=B.DR_GDN2)) == B.DR_ERR_UNSUPPORTED
+    assert fwd2(desc(flags=B.DR_FLAG_PREPARE_INPUTS, **d2)) == B.DR_ERR_UNSUPPORTED
+    assert fwd2(desc(**d2), erase=None) == B.DR_ERR_INVALID_ARG
+    assert fwd2(desc(**d2), g=None) == B.DR_ERR_INVALID_ARG
+    assert fwd2(desc(**d2), write=8) == B.DR_ERR_ALIGNMENT
+    assert B.dr_gdn2_fwd(desc(**d2), 16, 16, 16, 16, 16, 16, None, 16, None, 16, 100,
+                         None) == B.DR_ERR_WORKSPACE
+
+    def bwd2(d, **kw):
+        p = dict(q=16, k=16, v=16, erase=16, write=16, g=16, h0=None, dO=16, dhT=None, dq=16,
+                 dk=16, dv=16, derase=16, dwrite=16, dg=16, dh0=None)
+        p.update(kw)
+        return B.dr_gdn2_bwd(d, *p.values(), 16, 1 << 40, None)
+    assert bwd2(desc(**d2), dwrite=None) == B.DR_ERR_INVALID_ARG
+    assert bwd2(desc(**d2), dh0=4) == B.DR_ERR_ALIGNMENT
+    assert bwd2(desc(variant=B.DR_KDA, d_k=64, d_v=64)) == B.DR_ERR_INVALID_ARG
