@@ -331,12 +331,10 @@ __global__ void __launch_bounds__(128, 1)
             float* T11 = reinterpret_cast<float*>(sm + S::kInv);  // [32][32] row-major
             float* T22 = T11 + 1024;                     // [32][32] row-major
             float* Y = T22 + 1024;                       // [32][32] row-major, A21 T11
-            uint8_t* t_img = L.T + rec * 8192;
+            // T goes to the operand tile only; its workspace image is one bulk copy of it
             auto put_t = [&](int i, int n, float x) {
-                const __nv_bfloat16 b = __float2bfloat16_rn(x);
-                const uint32_t off = sw128_offset(i, n, 64);
-                *reinterpret_cast<__nv_bfloat16*>(Ts + off) = b;
-                *reinterpret_cast<__nv_bfloat16*>(t_img + off) = b;
+                *reinterpret_cast<__nv_bfloat16*>(Ts + sw128_offset(i, n, 64)) =
+                    __float2bfloat16_rn(x);
             };
             if (tid < 64) {
                 const int o = tid & 32, n = tid & 31;
@@ -404,8 +402,10 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
 
         // Wy = T (beta Kb) -> cols [0,D);  Ut^T = (beta v)^T T^T -> cols [128,192) (M = D:
-        // the rows are value channels, so its image and operand tile are written 16 bytes wide)
+        // the rows are value channels, so its operand tile is written 16 bytes wide)
         if (tid == 0) {
+            bulk_s2g(L.T + rec * 8192, Ts, 8192);
+            bulk_commit();
             tc_fence_after();
             const Tile tT{smem_u32(Ts), 64}, tY{smem_u32(Ys), 64}, tV{smem_u32(Vs), 64};
             mma_tiles(tm + 0, tT, false, tY, true, 64, D, 64, false);
@@ -416,17 +416,14 @@ __global__ void __launch_bounds__(128, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
+        // Wy and Ut^T into their operand tiles; the workspace images (Wy [64][D], Ut^T
+        // [D][64], SW128 tile images) are bulk copies of those tiles
         {
-            uint8_t* wy_img = L.Wy + rec * kTile;
-            uint8_t* utT = L.UtT + rec * kTile;  // [D][64] SW128 tile image of Ut^T
             for (int cb = 0; cb < D / 16; ++cb) {
                 float w16[16];
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld_wait();
-                if (r >= 0) {
-                    tile_store16(Xs, r, cb * 16, 64, w16);
-                    tile_store16(wy_img, r, cb * 16, 64, w16);
-                }
+                if (r >= 0) tile_store16(Xs, r, cb * 16, 64, w16);
             }
             const int cv = D == 128 ? tid : r;  // value channel of the M = D accumulator
 #pragma unroll
@@ -434,10 +431,7 @@ __global__ void __launch_bounds__(128, 1)
                 float u16[16];
                 tmem_ld16(tl + 128 + b * 16, u16);
                 tmem_ld_wait();
-                if (cv >= 0) {
-                    tile_store16(Ks, cv, b * 16, D, u16);  // Ut^T operand tile [D][64] (Kr is consumed)
-                    tile_store16(utT, cv, b * 16, D, u16);
-                }
+                if (cv >= 0) tile_store16(Ks, cv, b * 16, D, u16);  // Ut^T [D][64] (Kr is consumed)
             }
         }
         fence_async_smem();
@@ -446,6 +440,9 @@ __global__ void __launch_bounds__(128, 1)
 
         // Aqk Wy -> cols [0,D);  Ot^T / scale = Ut^T Aqk^T -> cols [128,192) (M = D)
         if (tid == 0) {
+            bulk_s2g(L.Wy + rec * kTile, Xs, kTile);
+            bulk_s2g(L.UtT + rec * kTile, Ks, kTile);
+            bulk_commit();
             tc_fence_after();
             const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), D};
             mma_tiles(tm + 0, tA, false, tW, true, 64, D, 64, false);
@@ -491,6 +488,7 @@ __global__ void __launch_bounds__(128, 1)
         mbar_wait(&bar_ld, 0, kWaitLimitNs);  // let an outstanding copy land before exit
         if (ld_phase2) mbar_wait(&bar_ld, 1, kWaitLimitNs);
     }
+    if (tid == 0) bulk_wait_all();  // the image copies are complete
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
