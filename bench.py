@@ -170,7 +170,7 @@ def gdn2_bench(dev, stream, max_over_ranks, barrier, sm_mhz, steps=3, warmup=3):
     for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
-    binding.trace_enable(2 * steps + 2)
+    binding.trace_enable(3 * steps + 3)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)

@@ -23,7 +23,7 @@ size_t prepare_bytes(const Params& p);
 cudaError_t prepare_inputs(Params& p, uint8_t* area, cudaStream_t st);
 void use_prepared(Params& p, uint8_t* area);
 cudaError_t chain_prepared_grads(const Params& p, cudaStream_t st);
-size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv);
+size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, long long th);
 cudaError_t gdn2_fwd(const Params& p, cudaStream_t st);
 cudaError_t gdn2_bwd(const Params& p, cudaStream_t st);
 }  // namespace dr
@@ -98,7 +98,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // The path's own workspace: header, then the path's residuals and scratch.
 size_t path_ws_bytes(const Params& p, Path path) {
     if (path == Path::kGdn2)
-        return kHeader + dr::gdn2_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
+        return kHeader + dr::gdn2_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv,
+                                                  (long long)p.B * p.T * p.H);
     if (path == Path::kSimt)
         return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
     return kHeader + dr::tc_workspace_bytes(p);

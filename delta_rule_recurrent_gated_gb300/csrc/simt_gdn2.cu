@@ -19,8 +19,13 @@
 //   S_L = e^{G_L} S0 + KC^T Vw - BC^T P
 // (the predictions satisfy (I + strict_lower(Kb Br^T)) P = Kb S0 + Mk Vw: each p_t sees
 // the decayed start state and every earlier write and erase of the chunk).  The
-// backward is the chain rule through exactly these steps.  One CTA per (sequence,
-// head) walks its chunks; matrices live in a per-CTA scratch slice of the workspace.
+// backward is the chain rule through exactly these steps.  One CTA per (sequence, head,
+// slice of bv value columns) walks its chunks; matrices live in a per-CTA scratch slice
+// of the workspace.  The value columns of the state evolve independently (the key-side
+// matrices T, Wy, Aqk, Aqb, Qt do not depend on v), so a slice recomputes the key side
+// and carries only its columns of S, P and O.  In the backward, the key-side gradients
+// (dq, dk, derase, dg) are sums over the slices of the same formulas: each slice writes
+// its partial sums and a reduction kernel adds them in slice order.
 #include "common.cuh"
 #include "simt_util.cuh"
 #include "trace.cuh"
@@ -49,8 +54,9 @@ __device__ void mask(float* M, int L, bool keep_diag) {
 
 // Load one chunk and evaluate everything that does not depend on the state.
 // gGam holds Gamma_i at [i] and e^{Gamma_L} at [C].
-__device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, int L) {
-    const int dk = p.dk, dv = p.dv, H = p.H, tid = threadIdx.x, nt = blockDim.x;
+__device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, int L, int j0,
+                            int dv) {
+    const int dk = p.dk, H = p.H, tid = threadIdx.x, nt = blockDim.x;
     const float sc = p.scale;
     float* q = s(gQ); float* k = s(gK); float* v = s(gV); float* e = s(gE); float* w = s(gWg);
     float* gm = s(gGam);
@@ -61,7 +67,7 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
         e[idx] = p.erase[a];
     }
     for (int idx = tid; idx < L * dv; idx += nt) {
-        const size_t a = ((size_t)(row0 + idx / dv) * H + h) * dv + idx % dv;
+        const size_t a = ((size_t)(row0 + idx / dv) * H + h) * p.dv + j0 + idx % dv;
         v[idx] = ld_any(p.v, a, p.io_dtype);
         w[idx] = p.write[a];
     }
@@ -122,8 +128,8 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
 }
 
 // P = Pt + Wy S; O = Ot + Qt S; S <- e^{Gamma_L} S + KC^T Vw - BC^T P
-__device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S) {
-    const int dk = p.dk, dv = p.dv, tid = threadIdx.x, nt = blockDim.x;
+__device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S, int dv) {
+    const int dk = p.dk, tid = threadIdx.x, nt = blockDim.x;
     float* P = s(gP); float* O = s(gO);
     for (int idx = tid; idx < L * dv; idx += nt) { P[idx] = s(gPt)[idx]; O[idx] = s(gOt)[idx]; }
     __syncthreads();
@@ -136,63 +142,91 @@ __device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S) 
     mm2(S, dv, s(gBC), dk, true, P, dv, false, dk, dv, L, -1.f, true);
 }
 
-__global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch) {
-    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
-    const Scratch s{scratch + (size_t)u * kNumBufs2 * kBuf};
+// S (d_k x bv, columns j0.. of the [d_k][d_v] state h) into scratch; zero when h is NULL
+__device__ void load_state_cols(float* S, const float* h, int n, int hd, const Params& p, int j0,
+                                int bv) {
+    for (int idx = threadIdx.x; idx < p.dk * bv; idx += blockDim.x)
+        S[idx] = h ? h[(((size_t)n * p.H + hd) * p.dk + idx / bv) * p.dv + j0 + idx % bv] : 0.f;
+    __syncthreads();
+}
+__device__ void store_state_cols(float* h, const float* S, int n, int hd, const Params& p, int j0,
+                                 int bv) {
+    for (int idx = threadIdx.x; idx < p.dk * bv; idx += blockDim.x)
+        h[(((size_t)n * p.H + hd) * p.dk + idx / bv) * p.dv + j0 + idx % bv] = S[idx];
+}
+
+__global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch, int bv) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
+    const Scratch s{scratch + ((size_t)u * gridDim.y + blockIdx.y) * kNumBufs2 * kBuf};
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     float* S = s(gS);
-    load_state(S, p.h0, n, h, p.H, p.dk, p.dv);
+    load_state_cols(S, p.h0, n, h, p, j0, bv);
     for (int c = 0; c < nc; ++c) {
         const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
-        chunk_prep2(p, s, h, row0, L);
-        chunk_scan2(p, s, L, S);
+        chunk_prep2(p, s, h, row0, L, j0, bv);
+        chunk_scan2(p, s, L, S, bv);
         const float* O = s(gO);
-        for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
-            const size_t a = ((size_t)(row0 + idx / p.dv) * p.H + h) * p.dv + idx % p.dv;
+        for (int idx = threadIdx.x; idx < L * bv; idx += blockDim.x) {
+            const size_t a = ((size_t)(row0 + idx / bv) * p.H + h) * p.dv + j0 + idx % bv;
             st_any(p.o, a, p.out_dtype, O[idx]);
         }
         __syncthreads();
     }
-    if (p.hT)
-        for (int idx = threadIdx.x; idx < p.dk * p.dv; idx += blockDim.x)
-            p.hT[((size_t)n * p.H + h) * p.dk * p.dv + idx] = S[idx];
+    if (p.hT) store_state_cols(p.hT, S, n, h, p, j0, bv);
 }
 
+// Key-side gradient partials of one slice: [slice][token·head][d_k] for dq, dk, derase and
+// [slice][token·head] for dg (null when there is one slice: the kernel writes the outputs).
+struct Gdn2Partials {
+    float *q, *k, *e, *g;
+};
+
 __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* scratch,
-                                                                float* states) {
-    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
-    const int dk = p.dk, dv = p.dv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
+                                                                float* states, int bv,
+                                                                Gdn2Partials part) {
+    const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
+    const int dk = p.dk, dv = bv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
     const float sc = p.scale;
-    const Scratch s{scratch + (size_t)u * kNumBufs2 * kBuf};
+    const Scratch s{scratch + ((size_t)u * gridDim.y + blockIdx.y) * kNumBufs2 * kBuf};
+    const size_t th = (size_t)p.B * p.T * p.H;
+    const bool direct = part.q == nullptr;
+    float* pq = direct ? nullptr : part.q + blockIdx.y * th * dk;
+    float* pk = direct ? nullptr : part.k + blockIdx.y * th * dk;
+    float* pe = direct ? nullptr : part.e + blockIdx.y * th * dk;
+    float* pg = direct ? nullptr : part.g + blockIdx.y * th;
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
-    const size_t SS = (size_t)dk * dv;
-    // pass 1: the state at the start of every chunk
+    const size_t SS = (size_t)dk * p.dv;
+    // pass 1: the state at the start of every chunk (this slice's columns)
     float* S = s(gS);
-    load_state(S, p.h0, n, h, p.H, dk, dv);
+    load_state_cols(S, p.h0, n, h, p, j0, bv);
     for (int c = 0; c < nc; ++c) {
         const int row0 = srow + c * C, L = min(C, slen - c * C);
         float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
-        for (int idx = tid; idx < dk * dv; idx += nt) dst[idx] = S[idx];
+        for (int idx = tid; idx < dk * dv; idx += nt) dst[(idx / dv) * p.dv + j0 + idx % dv] = S[idx];
         __syncthreads();
-        chunk_prep2(p, s, h, row0, L);
-        chunk_scan2(p, s, L, S);
+        chunk_prep2(p, s, h, row0, L, j0, bv);
+        chunk_scan2(p, s, L, S, bv);
     }
     // pass 2: reverse over chunks with dS = dL/dS_end
     float* dS = s(gdS);
-    load_state(dS, p.dhT, n, h, p.H, dk, dv);
+    load_state_cols(dS, p.dhT, n, h, p, j0, bv);
     for (int c = nc - 1; c >= 0; --c) {
         const int row0 = srow + c * C, L = min(C, slen - c * C);
         float* S0 = s(gS0);
         const float* src = states + ((size_t)(c0 + c) * p.H + h) * SS;
-        for (int idx = tid; idx < dk * dv; idx += nt) { S0[idx] = src[idx]; S[idx] = src[idx]; }
+        for (int idx = tid; idx < dk * dv; idx += nt) {
+            const float x = src[(idx / dv) * p.dv + j0 + idx % dv];
+            S0[idx] = x;
+            S[idx] = x;
+        }
         __syncthreads();
-        chunk_prep2(p, s, h, row0, L);
-        chunk_scan2(p, s, L, S);  // recomputes P (S is scratch here)
+        chunk_prep2(p, s, h, row0, L, j0, bv);
+        chunk_scan2(p, s, L, S, bv);  // recomputes P (S is scratch here)
         float* dO = s(gdO);
         for (int idx = tid; idx < L * dv; idx += nt)
-            dO[idx] = ld_any(p.dO, ((size_t)(row0 + idx / dv) * p.H + h) * dv + idx % dv,
+            dO[idx] = ld_any(p.dO, ((size_t)(row0 + idx / dv) * p.H + h) * p.dv + j0 + idx % dv,
                              p.io_dtype);
         __syncthreads();
         const float gL = s(gGam)[C];
@@ -262,16 +296,23 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
             const float eG = expf(G), enG = expf(-G), eC = expf(GL - G);
             const float dB = dBr[idx] * enG + dBC[idx] * eC;
             const size_t a = ((size_t)(row0 + i) * p.H + h) * dk + idx % dk;
-            st_any(p.dq, a, p.grad_dtype, dQb[idx] * eG);
-            st_any(p.dk_, a, p.grad_dtype,
-                   dKb[idx] * eG + dKr[idx] * enG + dKC[idx] * eC + e[idx] * dB);
-            p.derase[a] = k[idx] * dB;
+            const float gq = dQb[idx] * eG;
+            const float gk = dKb[idx] * eG + dKr[idx] * enG + dKC[idx] * eC + e[idx] * dB;
+            if (direct) {
+                st_any(p.dq, a, p.grad_dtype, gq);
+                st_any(p.dk_, a, p.grad_dtype, gk);
+                p.derase[a] = k[idx] * dB;
+            } else {
+                pq[a] = gq;
+                pk[a] = gk;
+                pe[a] = k[idx] * dB;
+            }
             tmp[idx] = dQb[idx] * s(gQb)[idx] + dKb[idx] * s(gKb)[idx] - dKr[idx] * s(gKr)[idx] -
                        dKC[idx] * s(gKC)[idx] - dBr[idx] * s(gBr)[idx] - dBC[idx] * s(gBC)[idx];
             dGam[idx] = dKC[idx] * s(gKC)[idx] + dBC[idx] * s(gBC)[idx];  // Gamma_L terms
         }
         for (int idx = tid; idx < L * dv; idx += nt) {
-            const size_t a = ((size_t)(row0 + idx / dv) * p.H + h) * dv + idx % dv;
+            const size_t a = ((size_t)(row0 + idx / dv) * p.H + h) * p.dv + j0 + idx % dv;
             st_any(p.dv_, a, p.grad_dtype, s(gWg)[idx] * dVw[idx]);
             p.dwrite[a] = s(gV)[idx] * dVw[idx];
         }
@@ -288,40 +329,85 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
                 float di = (i == L - 1) ? tail : 0.f;
                 for (int c2 = 0; c2 < dk; ++c2) di += tmp[i * dk + c2];
                 run += di;
-                p.dg[(size_t)(row0 + i) * p.H + h] = run;
+                if (direct) p.dg[(size_t)(row0 + i) * p.H + h] = run;
+                else pg[(size_t)(row0 + i) * p.H + h] = run;
             }
         }
         for (int idx = tid; idx < dk * dv; idx += nt) dS[idx] = dSp[idx];
         __syncthreads();
     }
-    if (p.dh0)
-        for (int idx = tid; idx < dk * dv; idx += nt)
-            p.dh0[((size_t)n * p.H + h) * SS + idx] = dS[idx];
+    if (p.dh0) store_state_cols(p.dh0, dS, n, h, p, j0, bv);
 }
+
+// dq, dk, derase, dg = the slices' partial sums, added in slice order
+__global__ void __launch_bounds__(256) gdn2_reduce_kernel(Params p, Gdn2Partials part, int nsl) {
+    const size_t th = (size_t)p.B * p.T * p.H, n = th * p.dk;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+        float q = 0.f, k = 0.f, e = 0.f;
+        for (int sl = 0; sl < nsl; ++sl) {
+            q += part.q[sl * n + i];
+            k += part.k[sl * n + i];
+            e += part.e[sl * n + i];
+        }
+        st_any(p.dq, i, p.grad_dtype, q);
+        st_any(p.dk_, i, p.grad_dtype, k);
+        p.derase[i] = e;
+        if (i < th) {
+            float g = 0.f;
+            for (int sl = 0; sl < nsl; ++sl) g += part.g[sl * th + i];
+            p.dg[i] = g;
+        }
+    }
+}
+
 
 }  // namespace
 
-size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv) {
-    return (size_t)units * kNumBufs2 * kBuf * sizeof(float) +
-           (size_t)num_chunks * H * dk * dv * sizeof(float);
+// Value-column slices per (sequence, head): 16-column slices while there are fewer units
+// than SMs (more CTAs for the same work), else one slice.
+int gdn2_slices(int units, int dv) { return (units >= 152 || dv < 32) ? 1 : dv / 16; }
+
+size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, long long th) {
+    const int nsl = gdn2_slices(units, dv);
+    return (size_t)units * nsl * kNumBufs2 * kBuf * sizeof(float) +
+           (size_t)num_chunks * H * dk * dv * sizeof(float) +
+           (nsl > 1 ? (size_t)nsl * (size_t)th * (3 * dk + 1) * sizeof(float) : 0);
 }
 
 cudaError_t gdn2_fwd(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
+    const int nsl = gdn2_slices(units, p.dv);
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
     TraceScope ts("gdn2_fwd", st);
-    gdn2_fwd_kernel<<<units, kThreads2, 0, st>>>(p, scratch);
+    gdn2_fwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, p.dv / nsl);
     return cudaGetLastError();
 }
 
 cudaError_t gdn2_bwd(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
+    const int nsl = gdn2_slices(units, p.dv);
+    const size_t th = (size_t)p.B * p.T * p.H;
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
-    float* states = scratch + (size_t)units * kNumBufs2 * kBuf;
-    TraceScope ts("gdn2_bwd", st);
-    gdn2_bwd_kernel<<<units, kThreads2, 0, st>>>(p, scratch, states);
+    float* states = scratch + (size_t)units * nsl * kNumBufs2 * kBuf;
+    Gdn2Partials part{nullptr, nullptr, nullptr, nullptr};
+    if (nsl > 1) {
+        float* base = states + (size_t)p.num_chunks * p.H * p.dk * p.dv;
+        const size_t n = (size_t)nsl * th * p.dk;
+        part = Gdn2Partials{base, base + n, base + 2 * n, base + 3 * n};
+    }
+    {
+        TraceScope ts("gdn2_bwd", st);
+        gdn2_bwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, states, p.dv / nsl, part);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nsl == 1) return e;
+    const size_t n = th * p.dk;
+    const int grid = (int)((n + 255) / 256 < 65536 ? (n + 255) / 256 : 65535);
+    TraceScope ts("gdn2_reduce", st);
+    gdn2_reduce_kernel<<<grid, 256, 0, st>>>(p, part, nsl);
     return cudaGetLastError();
 }
 

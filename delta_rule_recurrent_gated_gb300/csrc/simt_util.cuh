@@ -29,20 +29,66 @@ __device__ void mm(float* Cm, int ldc, const float* A, int lda, bool ta, const f
 
 // The same product with each thread computing a 2 x 2 block of C (one pass over k
 // loads two values of op(A) and two of op(B) for four multiply-adds).  Every output
-// sums its k terms in the same order as mm.  Edges of odd m or n are bounds-checked.
-__device__ void mm2(float* Cm, int ldc, const float* A, int lda, bool ta, const float* Bm,
-                    int ldb, bool tb, int m, int n, int k, float alpha, bool acc) {
+// sums its k terms in the same order as mm.  When the shapes allow (even m and n, k and
+// the leading dimensions multiples of 4), four steps of k are loaded at once: float4
+// along k for an operand read along its rows, float2 across the 2 x 2 pair for one read
+// down its columns; otherwise the scalar loop.  Operands start on 16-byte boundaries.
+template <bool TA, bool TB>
+__device__ __forceinline__ void mm2_body(float* Cm, int ldc, const float* A, int lda,
+                                         const float* Bm, int ldb, int m, int n, int k,
+                                         float alpha, bool acc) {
     const int mh = (m + 1) / 2, nh = (n + 1) / 2;
+    const bool vec = (m % 2 == 0) && (n % 2 == 0) && (k % 4 == 0) && (lda % 4 == 0) &&
+                     (ldb % 4 == 0);
     for (int idx = threadIdx.x; idx < mh * nh; idx += blockDim.x) {
         const int i0 = 2 * (idx / nh), j0 = 2 * (idx % nh);
         const bool i1ok = i0 + 1 < m, j1ok = j0 + 1 < n;
         const int i1 = i1ok ? i0 + 1 : i0, j1 = j1ok ? j0 + 1 : j0;
         float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-        for (int p = 0; p < k; ++p) {
-            const float a0 = ta ? A[p * lda + i0] : A[i0 * lda + p];
-            const float a1 = ta ? A[p * lda + i1] : A[i1 * lda + p];
-            const float b0 = tb ? Bm[j0 * ldb + p] : Bm[p * ldb + j0];
-            const float b1 = tb ? Bm[j1 * ldb + p] : Bm[p * ldb + j1];
+        int p = 0;
+        if (vec) {
+            for (; p < k; p += 4) {
+                float a0[4], a1[4], b0[4], b1[4];
+                if (TA) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 t = *reinterpret_cast<const float2*>(A + (p + q) * lda + i0);
+                        a0[q] = t.x;
+                        a1[q] = t.y;
+                    }
+                } else {
+                    const float4 t0 = *reinterpret_cast<const float4*>(A + i0 * lda + p);
+                    const float4 t1 = *reinterpret_cast<const float4*>(A + i1 * lda + p);
+                    a0[0] = t0.x; a0[1] = t0.y; a0[2] = t0.z; a0[3] = t0.w;
+                    a1[0] = t1.x; a1[1] = t1.y; a1[2] = t1.z; a1[3] = t1.w;
+                }
+                if (TB) {
+                    const float4 t0 = *reinterpret_cast<const float4*>(Bm + j0 * ldb + p);
+                    const float4 t1 = *reinterpret_cast<const float4*>(Bm + j1 * ldb + p);
+                    b0[0] = t0.x; b0[1] = t0.y; b0[2] = t0.z; b0[3] = t0.w;
+                    b1[0] = t1.x; b1[1] = t1.y; b1[2] = t1.z; b1[3] = t1.w;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 t = *reinterpret_cast<const float2*>(Bm + (p + q) * ldb + j0);
+                        b0[q] = t.x;
+                        b1[q] = t.y;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    s00 = fmaf(a0[q], b0[q], s00);
+                    s01 = fmaf(a0[q], b1[q], s01);
+                    s10 = fmaf(a1[q], b0[q], s10);
+                    s11 = fmaf(a1[q], b1[q], s11);
+                }
+            }
+        }
+        for (; p < k; ++p) {
+            const float a0 = TA ? A[p * lda + i0] : A[i0 * lda + p];
+            const float a1 = TA ? A[p * lda + i1] : A[i1 * lda + p];
+            const float b0 = TB ? Bm[j0 * ldb + p] : Bm[p * ldb + j0];
+            const float b1 = TB ? Bm[j1 * ldb + p] : Bm[p * ldb + j1];
             s00 = fmaf(a0, b0, s00);
             s01 = fmaf(a0, b1, s01);
             s10 = fmaf(a1, b0, s10);
@@ -56,6 +102,17 @@ __device__ void mm2(float* Cm, int ldc, const float* A, int lda, bool ta, const 
             c1[j0] = acc ? c1[j0] + alpha * s10 : alpha * s10;
             if (j1ok) c1[j1] = acc ? c1[j1] + alpha * s11 : alpha * s11;
         }
+    }
+}
+
+__device__ void mm2(float* Cm, int ldc, const float* A, int lda, bool ta, const float* Bm,
+                    int ldb, bool tb, int m, int n, int k, float alpha, bool acc) {
+    if (ta) {
+        if (tb) mm2_body<true, true>(Cm, ldc, A, lda, Bm, ldb, m, n, k, alpha, acc);
+        else mm2_body<true, false>(Cm, ldc, A, lda, Bm, ldb, m, n, k, alpha, acc);
+    } else {
+        if (tb) mm2_body<false, true>(Cm, ldc, A, lda, Bm, ldb, m, n, k, alpha, acc);
+        else mm2_body<false, false>(Cm, ldc, A, lda, Bm, ldb, m, n, k, alpha, acc);
     }
     __syncthreads();
 }
