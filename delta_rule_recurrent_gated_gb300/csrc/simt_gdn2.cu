@@ -71,13 +71,26 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
         v[idx] = ld_any(p.v, a, p.io_dtype);
         w[idx] = p.write[a];
     }
-    if (tid == 0) {
-        float acc = 0.f;
-        for (int i = 0; i < L; ++i) {
-            acc += p.g[(size_t)(row0 + i) * H + h];
-            gm[i] = acc;
+    if (tid < 32) {
+        // Gamma: inclusive scan of the chunk's log-decays (L <= 64: two per lane)
+        const int lane = tid;
+        float g0 = lane < L ? p.g[(size_t)(row0 + lane) * H + h] : 0.f;
+        float g1 = lane + 32 < L ? p.g[(size_t)(row0 + lane + 32) * H + h] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t0 = __shfl_up_sync(0xffffffffu, g0, o);
+            const float t1 = __shfl_up_sync(0xffffffffu, g1, o);
+            if (lane >= o) {
+                g0 += t0;
+                g1 += t1;
+            }
         }
-        gm[p.C] = expf(acc);
+        g1 += __shfl_sync(0xffffffffu, g0, 31);
+        if (lane < L) gm[lane] = g0;
+        if (lane + 32 < L) gm[lane + 32] = g1;
+        const float last = L > 32 ? __shfl_sync(0xffffffffu, g1, (L - 33) & 31)
+                                  : __shfl_sync(0xffffffffu, g0, (L - 1) & 31);
+        if (lane == 0) gm[p.C] = expf(last);
     }
     __syncthreads();
     float* Bm = s(gB); float* Vw = s(gVw); float* Kb = s(gKb); float* Kr = s(gKr);
@@ -97,20 +110,57 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
     }
     for (int idx = tid; idx < L * dv; idx += nt) Vw[idx] = w[idx] * v[idx];
     __syncthreads();
-    float* A = s(gA); float* T = s(gT); float* Mk = s(gMk);
-    mm2(A, L, Kb, dk, false, Br, dk, true, L, L, dk, 1.f, false);
-    mask(A, L, false);
+    // A^T (column j of A = strict_lower(Kb Br^T) contiguous): AT[j][i] = Br_j . Kb_i, i > j
+    float* AT = s(gA); float* T = s(gT); float* Mk = s(gMk);
+    mm2(AT, L, Br, dk, false, Kb, dk, true, L, L, dk, 1.f, false);
+    for (int idx = tid; idx < L * L; idx += nt)
+        if (idx % L <= idx / L) AT[idx] = 0.f;
     mm2(Mk, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
     mask(Mk, L, false);
-    // T = (I + A)^{-1}, forward substitution by rows
-    for (int i = 0; i < L; ++i) {
-        for (int n = tid; n < L; n += nt) {
-            float x = (n == i) ? 1.f : 0.f;
-            if (n < i)
-                for (int j = n; j < i; ++j) x -= A[i * L + j] * T[j * L + n];
-            T[i * L + n] = x;
+    // T = (I + A)^{-1} by 2 x 2 blocks of 32: T11 = (I + A11)^{-1} and T22 = (I + A22)^{-1}
+    // side by side (thread n of each half solves column n right-looking: once x_j is final
+    // it is subtracted from every later row, so the dependent chain is one multiply-add
+    // per row), T12 = 0, then T21 = -T22 (A21 T11) with two tiled products
+    if (L == 64) {
+        if (tid < 64) {
+            const int o = tid & 32, n = tid & 31;
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = (i == n) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < 31; ++j) {
+                const float xj = x[j];
+                const float* col = AT + (o + j) * 64 + o;
+#pragma unroll
+                for (int i4 = (j + 1) & ~3; i4 < 32; i4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(col + i4);
+                    if (i4 + 0 > j) x[i4 + 0] = fmaf(-a.x, xj, x[i4 + 0]);
+                    if (i4 + 1 > j) x[i4 + 1] = fmaf(-a.y, xj, x[i4 + 1]);
+                    if (i4 + 2 > j) x[i4 + 2] = fmaf(-a.z, xj, x[i4 + 2]);
+                    if (i4 + 3 > j) x[i4 + 3] = fmaf(-a.w, xj, x[i4 + 3]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                T[(o + i) * 64 + o + n] = x[i];
+                if (o == 0) T[i * 64 + 32 + n] = 0.f;
+            }
         }
         __syncthreads();
+        float* Y = s(gTmp);  // [32][32]: A21 T11, with A21[i][k] = AT[k][32 + i]
+        mm2(Y, 32, AT + 32, 64, true, T, 64, false, 32, 32, 32, 1.f, false);
+        mm2(T + 32 * 64, 64, T + 32 * 64 + 32, 64, false, Y, 32, false, 32, 32, 32, -1.f, false);
+    } else {
+        // a chunk's ragged tail: forward substitution by rows
+        for (int i = 0; i < L; ++i) {
+            for (int n = tid; n < L; n += nt) {
+                float x = (n == i) ? 1.f : 0.f;
+                if (n < i)
+                    for (int j = n; j < i; ++j) x -= AT[j * L + i] * T[j * L + n];
+                T[i * L + n] = x;
+            }
+            __syncthreads();
+        }
     }
     float* Wy = s(gWy); float* X = s(gX); float* Pt = s(gPt); float* Aqk = s(gAqk);
     float* Aqb = s(gAqb); float* Qt = s(gQt); float* Ot = s(gOt);
@@ -317,21 +367,50 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
             p.dwrite[a] = s(gV)[idx] * dVw[idx];
         }
         __syncthreads();
-        if (tid == 0) {
-            // dGamma_i = sum over channels; Gamma_L also collects the KC, BC and e^{Gamma_L}
-            // terms; dg = reverse cumulative sum
-            float tail = 0.f;
-            for (int c2 = 0; c2 < dk; ++c2) tail += dVec[c2];
-            tail *= gL;
-            for (int idx = 0; idx < L * dk; ++idx) tail += dGam[idx];
-            float run = 0.f;
-            for (int i = L - 1; i >= 0; --i) {
-                float di = (i == L - 1) ? tail : 0.f;
-                for (int c2 = 0; c2 < dk; ++c2) di += tmp[i * dk + c2];
-                run += di;
-                if (direct) p.dg[(size_t)(row0 + i) * p.H + h] = run;
-                else pg[(size_t)(row0 + i) * p.H + h] = run;
+        // dGamma_i = sum over channels (tmp); Gamma_L also collects the KC, BC terms (dGam)
+        // and the e^{Gamma_L} one (dVec); dg = reverse cumulative sum.  Row sums by one
+        // thread per token, then warp 0 adds the tail and scans.
+        float* rs = dVec + 64;  // [0, L): per-token sums; [64, 128): per-token tail parts
+        for (int i = tid; i < L; i += nt) {
+            float a = 0.f, b = 0.f;
+            for (int c2 = 0; c2 < dk; ++c2) {
+                a += tmp[i * dk + c2];
+                b += dGam[i * dk + c2];
             }
+            rs[i] = a;
+            rs[64 + i] = b;
+        }
+        __syncthreads();
+        if (tid < 32) {
+            const int lane = tid;
+            float tail = 0.f;
+            for (int c2 = lane; c2 < dk; c2 += 32) tail += dVec[c2];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tail += __shfl_xor_sync(0xffffffffu, tail, o);
+            tail *= gL;
+            float tb = (lane < L ? rs[64 + lane] : 0.f) + (lane + 32 < L ? rs[96 + lane] : 0.f);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tb += __shfl_xor_sync(0xffffffffu, tb, o);
+            tail += tb;
+            // reverse inclusive scan over tokens L-1 .. 0 (two per lane, from the end)
+            float d0 = lane < L ? rs[lane] : 0.f, d1 = lane + 32 < L ? rs[lane + 32] : 0.f;
+            if (lane == ((L - 1) & 31)) {
+                if (L > 32) d1 += tail;
+                else d0 += tail;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t0 = __shfl_down_sync(0xffffffffu, d0, o);
+                const float t1 = __shfl_down_sync(0xffffffffu, d1, o);
+                if (lane + o < 32) {
+                    d0 += t0;
+                    d1 += t1;
+                }
+            }
+            d0 += __shfl_sync(0xffffffffu, d1, 0);
+            float* out = direct ? p.dg : pg;
+            if (lane < L) out[(size_t)(row0 + lane) * p.H + h] = d0;
+            if (lane + 32 < L) out[(size_t)(row0 + lane + 32) * p.H + h] = d1;
         }
         for (int idx = tid; idx < dk * dv; idx += nt) dS[idx] = dSp[idx];
         __syncthreads();

@@ -33,6 +33,8 @@ __device__ void mm(float* Cm, int ldc, const float* A, int lda, bool ta, const f
 // the leading dimensions multiples of 4), four steps of k are loaded at once: float4
 // along k for an operand read along its rows, float2 across the 2 x 2 pair for one read
 // down its columns; otherwise the scalar loop.  Operands start on 16-byte boundaries.
+// A warp covers a patch of 4 x 8 output pairs (rows x columns), so a load of A touches
+// at most 4 rows of it and a load of B at most 8.
 template <bool TA, bool TB>
 __device__ __forceinline__ void mm2_body(float* Cm, int ldc, const float* A, int lda,
                                          const float* Bm, int ldb, int m, int n, int k,
@@ -40,8 +42,12 @@ __device__ __forceinline__ void mm2_body(float* Cm, int ldc, const float* A, int
     const int mh = (m + 1) / 2, nh = (n + 1) / 2;
     const bool vec = (m % 2 == 0) && (n % 2 == 0) && (k % 4 == 0) && (lda % 4 == 0) &&
                      (ldb % 4 == 0);
-    for (int idx = threadIdx.x; idx < mh * nh; idx += blockDim.x) {
-        const int i0 = 2 * (idx / nh), j0 = 2 * (idx % nh);
+    const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int tm = (mh + 3) / 4, tn = (nh + 7) / 8;
+    for (int t = threadIdx.x >> 5; t < tm * tn; t += nwarps) {
+        const int pi = (t / tn) * 4 + (lane & 3), pj = (t % tn) * 8 + (lane >> 2);
+        if (pi >= mh || pj >= nh) continue;
+        const int i0 = 2 * pi, j0 = 2 * pj;
         const bool i1ok = i0 + 1 < m, j1ok = j0 + 1 < n;
         const int i1 = i1ok ? i0 + 1 : i0, j1 = j1ok ? j0 + 1 : j0;
         float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
