@@ -368,14 +368,9 @@ def cpu_baseline(w, x, budget_s=12.0):
                       f"fp64 forward+backward, {secs:.1f} s on {threads} threads"}
 
 
-def dist_setup():
-    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
-            int(os.environ.get("LOCAL_RANK", "0")))
-
-
 def run_reference(args, w):
-    world, rank, _ = dist_setup()
-    if rank != 0:
+    from delta_rule_recurrent_gated_gb300.replicas import Replicas
+    if not Replicas.from_env().is_root:  # the oracle runs once, on rank 0's host cores
         return
     from delta_rule_recurrent_gated_gb300 import inputs
     x = inputs.make(w, seed=0)
@@ -429,15 +424,14 @@ def main():
     import torch
     from delta_rule_recurrent_gated_gb300 import binding
 
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    from delta_rule_recurrent_gated_gb300.replicas import Replicas
+    rep = Replicas.from_env()
+    world, rank = rep.world, rep.rank
+    torch.cuda.set_device(rep.local_rank)
+    dev = torch.device("cuda", rep.local_rank)
+    rep.init("nccl", dev)
 
-    x = inputs.make(w, seed=rank)
+    x = inputs.make(w, seed=rep.seed())
     N = x["N"]
     prob = binding.Problem(w.variant, w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io,
                            out="bf16", grad="bf16", scale=w.scale,
@@ -461,16 +455,10 @@ def main():
 
     stream = torch.cuda.current_stream(dev)
 
-    def barrier():
-        if dist:
-            dist.barrier()
+    barrier = rep.barrier
 
     def max_over_ranks(v):
-        if not dist:
-            return v
-        tt = torch.tensor([v], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
+        return rep.max_over_ranks(v, dev)
 
     for _ in range(args.warmup):
         step(t)
@@ -502,7 +490,7 @@ def main():
         tot, n = per.get(nm, (0.0, 0))
         per[nm] = (tot + kms, n + 1)
 
-    tokens = w.tokens * world
+    tokens = rep.total_units(w.tokens)
     value = tokens / (ms / 1e3)
     hbm, tflops, peak_src = measured_peaks()
     flops, byts = algorithmic(w, N)
@@ -639,9 +627,8 @@ def main():
         pr = prepare_bench(args, w, rank, world, dev, stream, ms, o, hT, grads, max_over_ranks,
                            barrier)
 
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
+    if not rep.is_root:
+        rep.shutdown()
         return
     base = None if args.no_cpu_baseline else cpu_baseline(w, x)
     in_bytes = sum(v.numel() * v.element_size() for n, v in t.items()
@@ -670,8 +657,7 @@ def main():
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    rep.shutdown()
 
 
 if __name__ == "__main__":
