@@ -467,7 +467,7 @@ def main():
 
     # timed region: K steps, per-kernel events recorded on the launching stream
     binding.trace_enable(8 * args.steps + 8)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(rep.local_rank)
     clocks.start()
     time.sleep(0.3)
     barrier()

@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH):
     lib.dr_fwd_noalloc.restype = I
     lib.dr_decode.argtypes = [D] + [P] * 7 + [P]
     lib.dr_decode.restype = I
+    lib.dr_selftest_wait.argtypes = [P, I, ctypes.c_longlong, P]
+    lib.dr_selftest_wait.restype = I
     lib.dr_gdn2_fwd.argtypes = [D] + [P] * 9 + [P, S, P]
     lib.dr_gdn2_fwd.restype = I
     lib.dr_gdn2_bwd.argtypes = [D] + [P] * 16 + [P, S, P]
@@ -154,6 +156,10 @@ def dr_gdn2_bwd(desc, q, k, v, erase, write, g, h0, dO, dhT, dq, dk, dv, derase,
                 ws, ws_bytes, stream) -> int:
     return load().dr_gdn2_bwd(ctypes.byref(desc), q, k, v, erase, write, g, h0, dO, dhT, dq, dk,
                               dv, derase, dwrite, dg, dh0, ws, ws_bytes, stream)
+
+
+def selftest_wait(ws, arrive: bool, limit_ns: int, stream) -> int:
+    return load().dr_selftest_wait(ws, 1 if arrive else 0, int(limit_ns), stream)
 
 
 def check_status(ws, stream) -> int:

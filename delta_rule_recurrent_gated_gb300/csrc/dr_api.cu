@@ -26,6 +26,7 @@ cudaError_t chain_prepared_grads(const Params& p, cudaStream_t st);
 size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, long long th);
 cudaError_t gdn2_fwd(const Params& p, cudaStream_t st);
 cudaError_t gdn2_bwd(const Params& p, cudaStream_t st);
+cudaError_t wait_selftest(int* err, int arrive, unsigned long long limit_ns, cudaStream_t st);
 }  // namespace dr
 
 using dr::Params;
@@ -399,6 +400,14 @@ int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v
         return DR_OK;
     }
     return cuda_status(dr::gdn2_bwd(p, st));
+}
+
+int dr_selftest_wait(void* ws, int arrive, long long limit_ns, void* stream) {
+    if (!ws || !aligned16(ws) || limit_ns < 0 || limit_ns > 100000000ll) return DR_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return DR_ERR_CUDA;
+    return cuda_status(dr::wait_selftest(static_cast<int*>(ws), arrive ? 1 : 0,
+                                         (unsigned long long)limit_ns, st));
 }
 
 int dr_check_status(const void* ws, void* stream) {

@@ -256,6 +256,20 @@ int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v
                 float* dwrite, float* dg, float* dh0, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/*
+ * Self-test of the device failure path (no counterpart on the pages).  Launches one
+ * warp that waits, with the bounded wait every tensor-core kernel uses, on an mbarrier
+ * phase that only completes when `arrive` is non-zero (the warp completes it itself);
+ * a wait that runs out after limit_ns records DR_ERR_TIMEOUT in the workspace error
+ * word, as the kernels do.  The workspace needs only its first 16 bytes (16-byte
+ * aligned, device memory).  limit_ns in [0, 1e8].  Read the outcome with
+ * dr_check_status: DR_ERR_TIMEOUT without `arrive`, DR_OK with it.  Nothing is copied
+ * and no tensor memory is held, so the expired wait leaves nothing in flight.
+ * Errors: DR_ERR_INVALID_ARG (NULL or misaligned workspace, limit out of range),
+ * DR_ERR_CUDA (launch).
+ */
+int dr_selftest_wait(void* workspace, int arrive, long long limit_ns, void* stream);
+
 /* Synchronise `stream` and report any device-side error recorded in the
    workspace by the last call that used it (DR_OK or DR_ERR_TIMEOUT), or
    DR_ERR_CUDA when the stream itself failed. */

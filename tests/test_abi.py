@@ -235,3 +235,10 @@ def test_gdn2_host_rules(lib):
     assert bwd2(desc(**d2), dwrite=None) == B.DR_ERR_INVALID_ARG
     assert bwd2(desc(**d2), dh0=4) == B.DR_ERR_ALIGNMENT
     assert bwd2(desc(variant=B.DR_KDA, d_k=64, d_v=64)) == B.DR_ERR_INVALID_ARG
+
+
+def test_selftest_wait_rejects_bad_arguments_before_launch(lib):
+    assert B.selftest_wait(None, False, 1000, None) == B.DR_ERR_INVALID_ARG
+    assert B.selftest_wait(24, False, 1000, None) == B.DR_ERR_INVALID_ARG      # misaligned
+    assert B.selftest_wait(16, False, -1, None) == B.DR_ERR_INVALID_ARG
+    assert B.selftest_wait(16, True, 10 ** 9, None) == B.DR_ERR_INVALID_ARG   # > 100 ms
