@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH):
     lib.dr_fwd_noalloc.restype = I
     lib.dr_decode.argtypes = [D] + [P] * 7 + [P]
     lib.dr_decode.restype = I
+    lib.dr_gdn2_decode.argtypes = [D] + [P] * 8 + [P]
+    lib.dr_gdn2_decode.restype = I
     lib.dr_selftest_wait.argtypes = [P, I, ctypes.c_longlong, P]
     lib.dr_selftest_wait.restype = I
     lib.dr_gdn2_fwd.argtypes = [D] + [P] * 9 + [P, S, P]
@@ -325,6 +327,18 @@ class Decoder:
             o = torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.out_dtype, device=self.device)
         _check(dr_decode(d, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(state), _ptr(o),
                          torch.cuda.current_stream(self.device).cuda_stream), "dr_decode")
+        return o
+
+    def step_gdn2(self, q, k, v, erase, write, g, state, o=None):
+        """Gated DeltaNet-2 (a Decoder built with variant "gdn2"): dr_gdn2_decode."""
+        import torch
+        d = self.desc
+        if o is None:
+            o = torch.empty(d.B, d.T, d.H, d.d_v, dtype=self.out_dtype, device=self.device)
+        _check(load().dr_gdn2_decode(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(erase),
+                                     _ptr(write), _ptr(g), _ptr(state), _ptr(o),
+                                     torch.cuda.current_stream(self.device).cuda_stream),
+               "dr_gdn2_decode")
         return o
 
 

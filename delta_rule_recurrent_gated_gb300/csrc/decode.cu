@@ -17,6 +17,11 @@
 // per token (S~^T k and S^T q) are per-thread partials over R rows, combined
 // across the eight warps through shared memory in a fixed order.
 //
+// Gated DeltaNet-2 (GDN2): the same step with the erase gate e (per key channel) and
+// the write gate w (per value channel) in place of beta: with p = S~^T k,
+//   S = S~ - (e . k) p^T + k (w . v)^T      (Gated DeltaNet when e = w = beta),
+// the decay the scalar one of Gated DeltaNet.
+//
 // With input preparation (PREP) the token's q and k are L2-normalised in shared
 // memory (q * rsqrt(sum q^2 + 1e-6)), beta = sigmoid(b) and the gate
 // log alpha = -softplus(x) are formed as they are read: the same maps as the
@@ -33,7 +38,7 @@ __device__ __forceinline__ float neg_softplus(float x) {
     return -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
 }
 
-template <int DK, bool PREP>
+template <int DK, bool PREP, bool GDN2>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(const Params p, float* __restrict__ state) {
     constexpr int R = DK / 8;  // key rows per warp
@@ -42,7 +47,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int ncol = min(32, p.dv);
     const int v = blockIdx.y * ncol + lane;
     const bool col = lane < ncol;
-    __shared__ float qs[DK], ks[DK], as[DK], vs[32];
+    __shared__ float qs[DK], ks[DK], as[DK], es[GDN2 ? DK : 1], vs[32], ws[32];
     __shared__ float red[8][33];
     __shared__ float bsh, nrm_q, nrm_k;
 
@@ -58,14 +63,17 @@ __global__ void __launch_bounds__(kDecodeThreads)
             qs[c] = ld_any(p.q, rk + c, p.io_dtype);
             ks[c] = ld_any(p.k, rk + c, p.io_dtype);
             float lg = 0.f;
-            if (p.variant == DR_GDN) lg = p.g[tok * p.H + h];
+            if (p.variant == DR_GDN || GDN2) lg = p.g[tok * p.H + h];
             else if (p.variant == DR_KDA) lg = p.g[rk + c];
+            if constexpr (GDN2) es[c] = p.erase[rk + c];
             if (PREP && p.variant != DR_DELTANET) lg = neg_softplus(lg);
             as[c] = p.variant == DR_DELTANET ? 1.f : expf(lg);
         }
         if (warp == 0) {
             vs[lane] = col ? ld_any(p.v, rv + v, p.io_dtype) : 0.f;
-            if (lane == 0) {
+            if constexpr (GDN2) {
+                ws[lane] = col ? p.write[rv + v] : 0.f;
+            } else if (lane == 0) {
                 const float b = p.beta[tok * p.H + h];
                 bsh = PREP ? 1.f / (1.f + expf(-b)) : b;
             }
@@ -98,14 +106,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
         float sk = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) sk += red[w][lane];
-        const float br = bsh * (vs[lane] - sck * sk);  // beta * r[v]
-        const float brk = br * sck;                    // k_hat[c] = sck * ks[c]
         float pq = 0.f;
+        if constexpr (GDN2) {
+            // S = S~ - (e . k) p^T + k (w . v)^T on column v: p[v] = sk
+            const float wv = ws[lane] * vs[lane];
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const int c = warp * R + i;
-            S[i] = fmaf(ks[c], brk, S[i]);
-            pq = fmaf(S[i], qs[c], pq);
+            for (int i = 0; i < R; ++i) {
+                const int c = warp * R + i;
+                S[i] = fmaf(ks[c], wv, fmaf(-es[c] * ks[c], sk, S[i]));
+                pq = fmaf(S[i], qs[c], pq);
+            }
+        } else {
+            const float br = bsh * (vs[lane] - sck * sk);  // beta * r[v]
+            const float brk = br * sck;                    // k_hat[c] = sck * ks[c]
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int c = warp * R + i;
+                S[i] = fmaf(ks[c], brk, S[i]);
+                pq = fmaf(S[i], qs[c], pq);
+            }
         }
         __syncthreads();  // every warp has read red[] and the token's inputs
         red[warp][lane] = pq;
@@ -129,14 +148,16 @@ cudaError_t launch(const Params& p, float* state, cudaStream_t st, bool prepare)
     const int ncol = p.dv < 32 ? p.dv : 32;
     const dim3 grid(p.B * p.H, p.dv / ncol);
     TraceScope ts("decode", st);
-    if (prepare) decode_kernel<DK, true><<<grid, kDecodeThreads, 0, st>>>(p, state);
-    else decode_kernel<DK, false><<<grid, kDecodeThreads, 0, st>>>(p, state);
+    if (p.variant == DR_GDN2) decode_kernel<DK, false, true><<<grid, kDecodeThreads, 0, st>>>(p, state);
+    else if (prepare) decode_kernel<DK, true, false><<<grid, kDecodeThreads, 0, st>>>(p, state);
+    else decode_kernel<DK, false, false><<<grid, kDecodeThreads, 0, st>>>(p, state);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// d_k in {16, 32, 64, 128}; d_v in {16, 32, 64, 128}; checked by the caller.
+// d_k in {16, 32, 64, 128}; d_v in {16, 32, 64, 128}; checked by the caller.  Gated
+// DeltaNet-2 (p.variant == DR_GDN2) reads p.erase / p.write instead of p.beta.
 cudaError_t decode(const Params& p, float* state, cudaStream_t st, bool prepare) {
     if (p.B == 0 || p.T == 0) return cudaSuccess;
     switch (p.dk) {

@@ -287,13 +287,11 @@ int dr_bwd_u(const dr_desc* desc, const void* q, const void* k, const void* v, c
                     ws_size, stream);
 }
 
-int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
-              const float* beta, const float* g, float* state, void* o, void* stream) {
-    if (!desc) return DR_ERR_INVALID_ARG;
-    const dr_desc& d = *desc;
+namespace {
+// Host checks shared by dr_decode and dr_gdn2_decode (sizes, layout, flags, state).
+int check_decode(const dr_desc& d, const float* state) {
     if (d.B < 0 || d.T < 0 || d.H < 1 || d.d_k < 1 || d.d_v < 1 || d.chunk < 1)
         return DR_ERR_INVALID_ARG;
-    if (d.variant < DR_DELTANET || d.variant > DR_KDA) return DR_ERR_INVALID_ARG;
     for (int t : {d.io_dtype, d.out_dtype})
         if (t != DR_BF16 && t != DR_F32) return DR_ERR_INVALID_ARG;
     if (!std::isfinite(d.scale)) return DR_ERR_INVALID_ARG;
@@ -305,6 +303,36 @@ int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
     auto size_ok = [](int x) { return x == 16 || x == 32 || x == 64 || x == 128; };
     if (!size_ok(d.d_k) || !size_ok(d.d_v)) return DR_ERR_UNSUPPORTED;
     if (d.B > 0 && !state) return DR_ERR_INVALID_ARG;
+    return DR_OK;
+}
+}  // namespace
+
+int dr_gdn2_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
+                   const float* erase, const float* write, const float* g, float* state,
+                   void* o, void* stream) {
+    if (!desc) return DR_ERR_INVALID_ARG;
+    const dr_desc& d = *desc;
+    if (d.variant != DR_GDN2) return DR_ERR_INVALID_ARG;
+    int rc = check_decode(d, state);
+    if (rc != DR_OK) return rc;
+    if (d.flags & DR_FLAG_PREPARE_INPUTS) return DR_ERR_UNSUPPORTED;
+    const long long tokens = (long long)d.B * d.T;
+    if (tokens > 0 && (!q || !k || !v || !erase || !write || !g || !o)) return DR_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, erase, write, g, state, o};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
+    Params p = make_params(desc);
+    p.q = q; p.k = k; p.v = v; p.erase = erase; p.write = write; p.g = g; p.o = o;
+    return cuda_status(dr::decode(p, state, static_cast<cudaStream_t>(stream), false));
+}
+
+int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
+              const float* beta, const float* g, float* state, void* o, void* stream) {
+    if (!desc) return DR_ERR_INVALID_ARG;
+    const dr_desc& d = *desc;
+    if (d.variant < DR_DELTANET || d.variant > DR_KDA) return DR_ERR_INVALID_ARG;
+    int rc = check_decode(d, state);
+    if (rc != DR_OK) return rc;
     const long long tokens = (long long)d.B * d.T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DR_ERR_INVALID_ARG;
     if (tokens > 0 && ((d.variant == DR_DELTANET) != (g == nullptr))) return DR_ERR_INVALID_ARG;

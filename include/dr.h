@@ -257,6 +257,20 @@ int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v
                 void* stream);
 
 /*
+ * Recurrent step of Gated DeltaNet-2 (the update of dr_gdn2_fwd token by token, as
+ * dr_decode for the other variants): for every sequence, head and token in order,
+ *   S~ = e^{g_t} S;  p = S~^T k_t;  S = S~ - (erase_t . k_t) p^T + k_t (write_t . v_t)^T;
+ *   o_t = scale S^T q_t
+ * on the caller's fp32 state [B][H][d_k][d_v], updated in place.  desc->variant must be
+ * DR_GDN2; erase [B][T][H][d_k], write [B][T][H][d_v], g [B][T][H] fp32, none NULL when
+ * there are tokens.  Sizes, dtypes, layout and errors as dr_decode;
+ * DR_FLAG_PREPARE_INPUTS is DR_ERR_UNSUPPORTED.
+ */
+int dr_gdn2_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
+                   const float* erase, const float* write, const float* g, float* state,
+                   void* o, void* stream);
+
+/*
  * Self-test of the device failure path (no counterpart on the pages).  Launches one
  * warp that waits, with the bounded wait every tensor-core kernel uses, on an mbarrier
  * phase that only completes when `arrive` is non-zero (the warp completes it itself);

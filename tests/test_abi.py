@@ -242,3 +242,21 @@ def test_selftest_wait_rejects_bad_arguments_before_launch(lib):
     assert B.selftest_wait(24, False, 1000, None) == B.DR_ERR_INVALID_ARG      # misaligned
     assert B.selftest_wait(16, False, -1, None) == B.DR_ERR_INVALID_ARG
     assert B.selftest_wait(16, True, 10 ** 9, None) == B.DR_ERR_INVALID_ARG   # > 100 ms
+
+
+def test_gdn2_decode_host_rules(lib):
+    p16 = 16
+
+    def call(dd, **kw):
+        a = dict(q=p16, k=p16, v=p16, erase=p16, write=p16, g=p16, state=p16, o=p16)
+        a.update(kw)
+        return lib.dr_gdn2_decode(ctypes.byref(dd), *a.values(), None)
+    d2 = desc(T=1, variant=B.DR_GDN2)
+    assert call(desc(T=1)) == B.DR_ERR_INVALID_ARG                    # not DR_GDN2
+    assert call(d2, erase=None) == B.DR_ERR_INVALID_ARG
+    assert call(d2, state=None) == B.DR_ERR_INVALID_ARG
+    assert call(d2, write=8) == B.DR_ERR_ALIGNMENT
+    assert call(desc(T=1, variant=B.DR_GDN2, d_k=96)) == B.DR_ERR_UNSUPPORTED
+    assert call(desc(T=1, variant=B.DR_GDN2, flags=B.DR_FLAG_PREPARE_INPUTS)) == B.DR_ERR_UNSUPPORTED
+    # dr_decode itself refuses the variant (its beta has no place in it)
+    assert lib.dr_decode(ctypes.byref(d2), p16, p16, p16, p16, p16, p16, p16, None) == B.DR_ERR_INVALID_ARG

@@ -124,3 +124,29 @@ def test_full_size_sampled():
             g = got[name][n, h] if name in ("hT", "dh0") else got[name][n, :, h]
             err = float(np.max(np.abs(g.astype(np.float64) - r)))
             assert err <= tolerance(w, r), f"unit {u} {name}: err {err}"
+
+
+@pytest.mark.parametrize("io,d", [("bf16", 128), ("f32", 64), ("f32", 16)])
+def test_decode_steps_match_the_recurrence(io, d):
+    """dr_gdn2_decode token by token (state carried between calls) and as one
+    multi-token call reproduce the oracle's outputs and final state."""
+    w = inputs.replace(inputs.small("gdn2", B=3, T=9, H=2, dk=d, dv=d, io=io), scale=0.5)
+    x = inputs.make_gdn2(w, seed=46, need_grad_inputs=False)
+    o_ref, h_ref = oracle.forward_gdn2(x["q"], x["k"], x["v"], x["erase"], x["write"], x["g"],
+                                       x["h0"], scale=w.scale)
+    dev = torch.device("cuda:0")
+    for per_token in (True, False):
+        T = 1 if per_token else w.T
+        dec = binding.Decoder("gdn2", w.B, T, w.H, d, d, io=io, out="f32", scale=w.scale,
+                              device=dev)
+        state = x["h0"].to(dev).clone()
+        outs = []
+        for t0 in range(0, w.T, T):
+            sl = slice(t0, t0 + T)
+            args = [x[n][:, sl].contiguous().to(dev) for n in ("q", "k", "v", "erase", "write", "g")]
+            outs.append(dec.step_gdn2(*args, state))
+        torch.cuda.synchronize()
+        o = torch.cat(outs, dim=1).cpu().numpy()
+        for name, got, ref in (("o", o, o_ref), ("state", state.cpu().numpy(), h_ref)):
+            err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+            assert err <= tolerance(w, ref), f"{name} per_token={per_token}: err {err}"
