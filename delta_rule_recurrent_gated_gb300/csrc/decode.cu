@@ -62,12 +62,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
         for (int c = threadIdx.x; c < DK; c += kDecodeThreads) {
             qs[c] = ld_any(p.q, rk + c, p.io_dtype);
             ks[c] = ld_any(p.k, rk + c, p.io_dtype);
-            float lg = 0.f;
-            if (p.variant == DR_GDN || GDN2) lg = p.g[tok * p.H + h];
-            else if (p.variant == DR_KDA) lg = p.g[rk + c];
+            float a = 1.f;
+            if (p.variant == DR_GDN || GDN2) {
+                const float lg = p.g[tok * p.H + h];
+                a = expf(PREP ? neg_softplus(lg) : lg);
+            } else if (p.variant == DR_KDA) {
+                const float lg = p.g[rk + c];
+                a = expf(PREP ? neg_softplus(lg) : lg);
+            }
+            as[c] = a;
             if constexpr (GDN2) es[c] = p.erase[rk + c];
-            if (PREP && p.variant != DR_DELTANET) lg = neg_softplus(lg);
-            as[c] = p.variant == DR_DELTANET ? 1.f : expf(lg);
         }
         if (warp == 0) {
             vs[lane] = col ? ld_any(p.v, rv + v, p.io_dtype) : 0.f;
