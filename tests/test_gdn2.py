@@ -150,3 +150,21 @@ def test_decode_steps_match_the_recurrence(io, d):
         for name, got, ref in (("o", o, o_ref), ("state", state.cpu().numpy(), h_ref)):
             err = float(np.max(np.abs(got.astype(np.float64) - ref)))
             assert err <= tolerance(w, ref), f"{name} per_token={per_token}: err {err}"
+
+
+def test_bf16_gradients_and_rerun_bit_identical():
+    """bf16-written outputs and gradients stay within the bf16 reading of the tolerance
+    (half an ulp of bf16 on top of 2e-2); two runs are bit-identical (the slices' partial
+    gradients are added in a fixed order)."""
+    w = inputs.small("gdn2", B=2, T=130, H=2, dk=64, dv=64, chunk=64, io="bf16")
+    x = inputs.make_gdn2(w, seed=47)
+    a = run_gpu(w, x, out="bf16", grad="bf16")
+    b = run_gpu(w, x, out="bf16", grad="bf16")
+    for n in FIELDS:
+        assert np.array_equal(a[n], b[n]), n
+    ref = run_oracle(w, x)
+    for n in ("o", "dq", "dk", "dv"):
+        r = ref[n]
+        half_ulp = np.abs(r) * 2.0 ** -9
+        err = np.abs(a[n].astype(np.float64) - r)
+        assert np.all(err <= half_ulp + tolerance(w, r)), n

@@ -172,3 +172,17 @@ def test_prepared_full_size_sampled(name):
             tol = tolerance(w, r)
             assert err <= tol, f"{name} seq {n} head {h} {fname}: err {err} > tol {tol}"
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_prepared_bf16_outputs_and_gradients(variant):
+    """bf16-written o and gradients (the bench's precision) in the preparation mode,
+    against the oracle within half a bf16 ulp on top of the tolerance."""
+    w = inputs.small(variant, B=2, T=150, H=2, dk=128, dv=128)
+    x = inputs.make_raw(w, seed=37)
+    got = run_gpu(w, x, prob=problem(w, x, out="bf16", grad="bf16"))
+    ref = oracle_raw(w, x)
+    for n in ("o", "dq", "dk", "dv"):
+        r = ref[n]
+        err = np.abs(got[n].astype(np.float64) - r)
+        assert np.all(err <= np.abs(r) * 2.0 ** -9 + tolerance(w, r)), n
