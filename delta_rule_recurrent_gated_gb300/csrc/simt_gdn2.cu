@@ -112,10 +112,10 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
     __syncthreads();
     // A^T (column j of A = strict_lower(Kb Br^T) contiguous): AT[j][i] = Br_j . Kb_i, i > j
     float* AT = s(gA); float* T = s(gT); float* Mk = s(gMk);
-    mm2(AT, L, Br, dk, false, Kb, dk, true, L, L, dk, 1.f, false);
+    mm4(AT, L, Br, dk, false, Kb, dk, true, L, L, dk, 1.f, false);
     for (int idx = tid; idx < L * L; idx += nt)
         if (idx % L <= idx / L) AT[idx] = 0.f;
-    mm2(Mk, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    mm4(Mk, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
     mask(Mk, L, false);
     // T = (I + A)^{-1} by 2 x 2 blocks of 32: T11 = (I + A11)^{-1} and T22 = (I + A22)^{-1}
     // side by side (thread n of each half solves column n right-looking: once x_j is final
@@ -148,8 +148,8 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
         }
         __syncthreads();
         float* Y = s(gTmp);  // [32][32]: A21 T11, with A21[i][k] = AT[k][32 + i]
-        mm2(Y, 32, AT + 32, 64, true, T, 64, false, 32, 32, 32, 1.f, false);
-        mm2(T + 32 * 64, 64, T + 32 * 64 + 32, 64, false, Y, 32, false, 32, 32, 32, -1.f, false);
+        mm4(Y, 32, AT + 32, 64, true, T, 64, false, 32, 32, 32, 1.f, false);
+        mm4(T + 32 * 64, 64, T + 32 * 64 + 32, 64, false, Y, 32, false, 32, 32, 32, -1.f, false);
     } else {
         // a chunk's ragged tail: forward substitution by rows
         for (int i = 0; i < L; ++i) {
@@ -164,17 +164,17 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
     }
     float* Wy = s(gWy); float* X = s(gX); float* Pt = s(gPt); float* Aqk = s(gAqk);
     float* Aqb = s(gAqb); float* Qt = s(gQt); float* Ot = s(gOt);
-    mm2(Wy, dk, T, L, false, Kb, dk, false, L, dk, L, 1.f, false);
-    mm2(X, dv, Mk, L, false, Vw, dv, false, L, dv, L, 1.f, false);
-    mm2(Pt, dv, T, L, false, X, dv, false, L, dv, L, 1.f, false);
-    mm2(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    mm4(Wy, dk, T, L, false, Kb, dk, false, L, dk, L, 1.f, false);
+    mm4(X, dv, Mk, L, false, Vw, dv, false, L, dv, L, 1.f, false);
+    mm4(Pt, dv, T, L, false, X, dv, false, L, dv, L, 1.f, false);
+    mm4(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
     mask(Aqk, L, true);
-    mm2(Aqb, L, Qb, dk, false, Br, dk, true, L, L, dk, 1.f, false);
+    mm4(Aqb, L, Qb, dk, false, Br, dk, true, L, L, dk, 1.f, false);
     mask(Aqb, L, true);
-    mm2(Qt, dk, Aqb, L, false, Wy, dk, false, L, dk, L, -sc, false);
+    mm4(Qt, dk, Aqb, L, false, Wy, dk, false, L, dk, L, -sc, false);
     for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += sc * Qb[idx];
-    mm2(Ot, dv, Aqk, L, false, Vw, dv, false, L, dv, L, sc, false);
-    mm2(Ot, dv, Aqb, L, false, Pt, dv, false, L, dv, L, -sc, true);
+    mm4(Ot, dv, Aqk, L, false, Vw, dv, false, L, dv, L, sc, false);
+    mm4(Ot, dv, Aqb, L, false, Pt, dv, false, L, dv, L, -sc, true);
 }
 
 // P = Pt + Wy S; O = Ot + Qt S; S <- e^{Gamma_L} S + KC^T Vw - BC^T P
@@ -183,13 +183,13 @@ __device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S, 
     float* P = s(gP); float* O = s(gO);
     for (int idx = tid; idx < L * dv; idx += nt) { P[idx] = s(gPt)[idx]; O[idx] = s(gOt)[idx]; }
     __syncthreads();
-    mm2(P, dv, s(gWy), dk, false, S, dv, false, L, dv, dk, 1.f, true);
-    mm2(O, dv, s(gQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    mm4(P, dv, s(gWy), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    mm4(O, dv, s(gQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
     const float gL = s(gGam)[p.C];
     for (int idx = tid; idx < dk * dv; idx += nt) S[idx] *= gL;
     __syncthreads();
-    mm2(S, dv, s(gKC), dk, true, s(gVw), dv, false, dk, dv, L, 1.f, true);
-    mm2(S, dv, s(gBC), dk, true, P, dv, false, dk, dv, L, -1.f, true);
+    mm4(S, dv, s(gKC), dk, true, s(gVw), dv, false, dk, dv, L, 1.f, true);
+    mm4(S, dv, s(gBC), dk, true, P, dv, false, dk, dv, L, -1.f, true);
 }
 
 // S (d_k x bv, columns j0.. of the [d_k][d_v] state h) into scratch; zero when h is NULL
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
         float* dPt = s(gdPt); float* dKC = s(gdKC); float* dBC = s(gdBC); float* dVw = s(gdVw);
         float* dVec = s(gdVec);
         // state update S_L = gL S0 + KC^T Vw - BC^T P and the reads O = Ot + Qt S0
-        mm2(dP, dv, s(gBC), dk, false, dS, dv, false, L, dv, dk, -1.f, false);
+        mm4(dP, dv, s(gBC), dk, false, dS, dv, false, L, dv, dk, -1.f, false);
         for (int idx = tid; idx < dk * dv; idx += nt) dSp[idx] = gL * dS[idx];
         for (int c2 = tid; c2 < dk; c2 += nt) {
             float acc = 0.f;
@@ -292,50 +292,50 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
             dVec[c2] = acc;  // d e^{Gamma_L}, per key row
         }
         __syncthreads();
-        mm2(dSp, dv, s(gQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
-        mm2(dSp, dv, s(gWy), dk, true, dP, dv, false, dk, dv, L, 1.f, true);
-        mm2(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
-        mm2(dWy, dk, dP, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
-        mm2(dKC, dk, s(gVw), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
-        mm2(dBC, dk, s(gP), dv, false, dS, dv, true, L, dk, dv, -1.f, false);
-        mm2(dVw, dv, s(gKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
+        mm4(dSp, dv, s(gQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
+        mm4(dSp, dv, s(gWy), dk, true, dP, dv, false, dk, dv, L, 1.f, true);
+        mm4(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm4(dWy, dk, dP, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm4(dKC, dk, s(gVw), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
+        mm4(dBC, dk, s(gP), dv, false, dS, dv, true, L, dk, dv, -1.f, false);
+        mm4(dVw, dv, s(gKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
         for (int idx = tid; idx < L * dv; idx += nt) dPt[idx] = dP[idx];
         __syncthreads();
         // Qt = sc (Qb - Aqb Wy), Ot = sc (Aqk Vw - Aqb Pt)
         float* dAqk = s(gdAqk); float* dAqb = s(gdAqb); float* dQb = s(gdQb);
-        mm2(dAqb, L, dQt, dk, false, s(gWy), dk, true, L, L, dk, -sc, false);
-        mm2(dAqb, L, dO, dv, false, s(gPt), dv, true, L, L, dv, -sc, true);
+        mm4(dAqb, L, dQt, dk, false, s(gWy), dk, true, L, L, dk, -sc, false);
+        mm4(dAqb, L, dO, dv, false, s(gPt), dv, true, L, L, dv, -sc, true);
         mask(dAqb, L, true);
-        mm2(dAqk, L, dO, dv, false, s(gVw), dv, true, L, L, dv, sc, false);
+        mm4(dAqk, L, dO, dv, false, s(gVw), dv, true, L, L, dv, sc, false);
         mask(dAqk, L, true);
-        mm2(dWy, dk, s(gAqb), L, true, dQt, dk, false, L, dk, L, -sc, true);
-        mm2(dVw, dv, s(gAqk), L, true, dO, dv, false, L, dv, L, sc, true);
-        mm2(dPt, dv, s(gAqb), L, true, dO, dv, false, L, dv, L, -sc, true);
+        mm4(dWy, dk, s(gAqb), L, true, dQt, dk, false, L, dk, L, -sc, true);
+        mm4(dVw, dv, s(gAqk), L, true, dO, dv, false, L, dv, L, sc, true);
+        mm4(dPt, dv, s(gAqb), L, true, dO, dv, false, L, dv, L, -sc, true);
         for (int idx = tid; idx < L * dk; idx += nt) dQb[idx] = sc * dQt[idx];
         __syncthreads();
         // Wy = T Kb, Pt = T X, X = Mk Vw
         float* dT = s(gdT); float* dKb = s(gdKb); float* dX = s(gdX); float* dMk = s(gdMk);
-        mm2(dT, L, dWy, dk, false, s(gKb), dk, true, L, L, dk, 1.f, false);
-        mm2(dT, L, dPt, dv, false, s(gX), dv, true, L, L, dv, 1.f, true);
-        mm2(dKb, dk, s(gT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
-        mm2(dX, dv, s(gT), L, true, dPt, dv, false, L, dv, L, 1.f, false);
-        mm2(dMk, L, dX, dv, false, s(gVw), dv, true, L, L, dv, 1.f, false);
+        mm4(dT, L, dWy, dk, false, s(gKb), dk, true, L, L, dk, 1.f, false);
+        mm4(dT, L, dPt, dv, false, s(gX), dv, true, L, L, dv, 1.f, true);
+        mm4(dKb, dk, s(gT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
+        mm4(dX, dv, s(gT), L, true, dPt, dv, false, L, dv, L, 1.f, false);
+        mm4(dMk, L, dX, dv, false, s(gVw), dv, true, L, L, dv, 1.f, false);
         mask(dMk, L, false);
-        mm2(dVw, dv, s(gMk), L, true, dX, dv, false, L, dv, L, 1.f, true);
+        mm4(dVw, dv, s(gMk), L, true, dX, dv, false, L, dv, L, 1.f, true);
         // T = (I + A)^{-1}: dA = -T^T dT T^T (strictly lower); A = Kb Br^T, Mk = Kb Kr^T
         float* dA = s(gdA); float* tmp = s(gTmp); float* dKr = s(gdKr); float* dBr = s(gdBr);
-        mm2(tmp, L, dT, L, false, s(gT), L, true, L, L, L, 1.f, false);
-        mm2(dA, L, s(gT), L, true, tmp, L, false, L, L, L, -1.f, false);
+        mm4(tmp, L, dT, L, false, s(gT), L, true, L, L, L, 1.f, false);
+        mm4(dA, L, s(gT), L, true, tmp, L, false, L, L, L, -1.f, false);
         mask(dA, L, false);
-        mm2(dKb, dk, dA, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
-        mm2(dBr, dk, dA, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
-        mm2(dKb, dk, dMk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
-        mm2(dKr, dk, dMk, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
+        mm4(dKb, dk, dA, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
+        mm4(dBr, dk, dA, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
+        mm4(dKb, dk, dMk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
+        mm4(dKr, dk, dMk, L, true, s(gKb), dk, false, L, dk, L, 1.f, false);
         // Aqk = tril(Qb Kr^T), Aqb = tril(Qb Br^T)
-        mm2(dQb, dk, dAqk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
-        mm2(dKr, dk, dAqk, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
-        mm2(dQb, dk, dAqb, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
-        mm2(dBr, dk, dAqb, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
+        mm4(dQb, dk, dAqk, L, false, s(gKr), dk, false, L, dk, L, 1.f, true);
+        mm4(dKr, dk, dAqk, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
+        mm4(dQb, dk, dAqb, L, false, s(gBr), dk, false, L, dk, L, 1.f, true);
+        mm4(dBr, dk, dAqb, L, true, s(gQb), dk, false, L, dk, L, 1.f, true);
         // decay and gate chain -> dq, dk, derase, dv, dwrite, dGamma
         const float* gm = s(gGam);
         float* dGam = s(gdGam);
