@@ -80,7 +80,7 @@ __device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, i
     for (int idx = tid; idx < L * dv; idx += nt) bV[idx] = beta[idx / dv] * v[idx];
     __syncthreads();
     float* A = s(bA); float* T = s(bT);
-    mm(A, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);  // Gram (kept for backward)
+    mm4(A, L, Kb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);  // Gram (kept for backward)
     // T = (I + diag(beta) strict_lower(Gram))^{-1}, forward substitution by rows
     for (int i = 0; i < L; ++i) {
         for (int n = tid; n < L; n += nt) {
@@ -92,16 +92,16 @@ __device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, i
         __syncthreads();
     }
     float* Wy = s(bWy); float* Ut = s(bUt); float* Aqk = s(bAqk);
-    mm(Wy, dk, T, L, false, bK, dk, false, L, dk, L, 1.f, false);
-    mm(Ut, dv, T, L, false, bV, dv, false, L, dv, L, 1.f, false);
-    mm(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
+    mm4(Wy, dk, T, L, false, bK, dk, false, L, dk, L, 1.f, false);
+    mm4(Ut, dv, T, L, false, bV, dv, false, L, dv, L, 1.f, false);
+    mm4(Aqk, L, Qb, dk, false, Kr, dk, true, L, L, dk, 1.f, false);
     for (int idx = tid; idx < L * L; idx += nt)
         if (idx % L > idx / L) Aqk[idx] = 0.f;
     __syncthreads();
     float* Qt = s(bQt); float* Ot = s(bOt);
-    mm(Qt, dk, Aqk, L, false, Wy, dk, false, L, dk, L, -p.scale, false);
+    mm4(Qt, dk, Aqk, L, false, Wy, dk, false, L, dk, L, -p.scale, false);
     for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += p.scale * Qb[idx];
-    mm(Ot, dv, Aqk, L, false, Ut, dv, false, L, dv, L, p.scale, false);
+    mm4(Ot, dv, Aqk, L, false, Ut, dv, false, L, dv, L, p.scale, false);
 }
 
 // U = Ut - Wy S; O = Qt S + Ot; S <- diag(e^{Gamma_L}) S + KC^T U
@@ -110,12 +110,12 @@ __device__ void chunk_scan(const Params& p, const Scratch& s, int L, float* S) {
     float* U = s(bU); float* O = s(bO);
     for (int idx = tid; idx < L * dv; idx += nt) { U[idx] = s(bUt)[idx]; O[idx] = s(bOt)[idx]; }
     __syncthreads();
-    mm(U, dv, s(bWy), dk, false, S, dv, false, L, dv, dk, -1.f, true);
-    mm(O, dv, s(bQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
+    mm4(U, dv, s(bWy), dk, false, S, dv, false, L, dv, dk, -1.f, true);
+    mm4(O, dv, s(bQt), dk, false, S, dv, false, L, dv, dk, 1.f, true);
     const float* gL = s(bVec) + p.C;
     for (int idx = tid; idx < dk * dv; idx += nt) S[idx] *= gL[idx / dv];
     __syncthreads();
-    mm(S, dv, s(bKC), dk, true, U, dv, false, dk, dv, L, 1.f, true);
+    mm4(S, dv, s(bKC), dk, true, U, dv, false, dk, dv, L, 1.f, true);
 }
 
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scratch) {
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         const float* gL = s(bVec) + C;
         float* dU = s(bdU); float* dSp = s(bdSp);
         // dU = KC dS;  dS_prev = diag(gL) dS + Qt^T dO - Wy^T dU
-        mm(dU, dv, s(bKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
+        mm4(dU, dv, s(bKC), dk, false, dS, dv, false, L, dv, dk, 1.f, false);
         if (p.dU) {  // plus the gradient of the emitted write
             for (int idx = tid; idx < L * dv; idx += nt) {
                 const int i = idx / dv, j = idx % dv;
@@ -194,13 +194,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         }
         for (int idx = tid; idx < dk * dv; idx += nt) dSp[idx] = gL[idx / dv] * dS[idx];
         __syncthreads();
-        mm(dSp, dv, s(bQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
-        mm(dSp, dv, s(bWy), dk, true, dU, dv, false, dk, dv, L, -1.f, true);
+        mm4(dSp, dv, s(bQt), dk, true, dO, dv, false, dk, dv, L, 1.f, true);
+        mm4(dSp, dv, s(bWy), dk, true, dU, dv, false, dk, dv, L, -1.f, true);
         // state-side gradients of the chunk
         float* dQt = s(bdQt); float* dWy = s(bdWy); float* dUt = s(bdUt); float* dKC = s(bdKC);
-        mm(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
-        mm(dWy, dk, dU, dv, false, S0, dv, true, L, dk, dv, -1.f, false);
-        mm(dKC, dk, s(bU), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
+        mm4(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
+        mm4(dWy, dk, dU, dv, false, S0, dv, true, L, dk, dv, -1.f, false);
+        mm4(dKC, dk, s(bU), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
         float* dVec = s(bdVec);  // [0, dk): d e^{Gamma_L} ; [C + ...] unused
         for (int c2 = tid; c2 < dk; c2 += nt) {
             float acc = 0.f;
@@ -212,29 +212,29 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         // Qt = scale (Qb - Aqk Wy), Ot = scale Aqk Ut
         const float sc = p.scale;
         float* dAqk = s(bdAqk); float* dQb = s(bdQb);
-        mm(dAqk, L, dQt, dk, false, s(bWy), dk, true, L, L, dk, -sc, false);
-        mm(dAqk, L, dO, dv, false, s(bUt), dv, true, L, L, dv, sc, true);
+        mm4(dAqk, L, dQt, dk, false, s(bWy), dk, true, L, L, dk, -sc, false);
+        mm4(dAqk, L, dO, dv, false, s(bUt), dv, true, L, L, dv, sc, true);
         for (int idx = tid; idx < L * L; idx += nt)
             if (idx % L > idx / L) dAqk[idx] = 0.f;
         __syncthreads();
-        mm(dWy, dk, s(bAqk), L, true, dQt, dk, false, L, dk, L, -sc, true);
-        mm(dUt, dv, s(bAqk), L, true, dO, dv, false, L, dv, L, sc, true);
+        mm4(dWy, dk, s(bAqk), L, true, dQt, dk, false, L, dk, L, -sc, true);
+        mm4(dUt, dv, s(bAqk), L, true, dO, dv, false, L, dv, L, sc, true);
         for (int idx = tid; idx < L * dk; idx += nt) dQb[idx] = sc * dQt[idx];
         __syncthreads();
         // Aqk = tril(Qb Kr^T)
         float* dKr = s(bdKr); float* dKb = s(bdKb);
-        mm(dQb, dk, dAqk, L, false, s(bKr), dk, false, L, dk, L, 1.f, true);
-        mm(dKr, dk, dAqk, L, true, s(bQb), dk, false, L, dk, L, 1.f, false);
+        mm4(dQb, dk, dAqk, L, false, s(bKr), dk, false, L, dk, L, 1.f, true);
+        mm4(dKr, dk, dAqk, L, true, s(bQb), dk, false, L, dk, L, 1.f, false);
         // Wy = T bK, Ut = T bV
         float* dT = s(bdT); float* dbK = s(bdbK); float* dbV = s(bdbV); float* dA = s(bdA);
         float* tmp = s(bTmp);
-        mm(dT, L, dWy, dk, false, s(bbK), dk, true, L, L, dk, 1.f, false);
-        mm(dT, L, dUt, dv, false, s(bbV), dv, true, L, L, dv, 1.f, true);
-        mm(dbK, dk, s(bT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
-        mm(dbV, dv, s(bT), L, true, dUt, dv, false, L, dv, L, 1.f, false);
+        mm4(dT, L, dWy, dk, false, s(bbK), dk, true, L, L, dk, 1.f, false);
+        mm4(dT, L, dUt, dv, false, s(bbV), dv, true, L, L, dv, 1.f, true);
+        mm4(dbK, dk, s(bT), L, true, dWy, dk, false, L, dk, L, 1.f, false);
+        mm4(dbV, dv, s(bT), L, true, dUt, dv, false, L, dv, L, 1.f, false);
         // T = (I + A)^{-1}: dA = -T^T dT T^T, strictly lower
-        mm(tmp, L, dT, L, false, s(bT), L, true, L, L, L, 1.f, false);
-        mm(dA, L, s(bT), L, true, tmp, L, false, L, L, L, -1.f, false);
+        mm4(tmp, L, dT, L, false, s(bT), L, true, L, L, L, 1.f, false);
+        mm4(dA, L, s(bT), L, true, tmp, L, false, L, L, L, -1.f, false);
         for (int idx = tid; idx < L * L; idx += nt)
             if (idx % L >= idx / L) dA[idx] = 0.f;
         __syncthreads();
@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         __syncthreads();
         for (int idx = tid; idx < L * L; idx += nt) dA[idx] *= beta[idx / L];
         __syncthreads();
-        mm(dKb, dk, dA, L, false, s(bKr), dk, false, L, dk, L, 1.f, false);
-        mm(dKr, dk, dA, L, true, s(bKb), dk, false, L, dk, L, 1.f, true);
+        mm4(dKb, dk, dA, L, false, s(bKr), dk, false, L, dk, L, 1.f, false);
+        mm4(dKr, dk, dA, L, true, s(bKb), dk, false, L, dk, L, 1.f, true);
         // decay chain -> dq, dk, dv, dbeta, dGamma
         float* dGam = s(bdGam);
         const float* gm = s(bGam);
