@@ -15,6 +15,11 @@
  *   read      o_t  = scale * W_t q_t
  * The gate enters as its logarithm g = log(alpha) <= 0.  beta_t, the read after
  * the write and `scale` are the standard delta-rule reading of that notation.
+ * Also here: the recurrent step for inference (dr_decode), the emitted write
+ * u = beta r with its gradient (dr_fwd_u / dr_bwd_u), input preparation inside the
+ * library (DR_FLAG_PREPARE_INPUTS), and Gated DeltaNet-2, the fourth variant of the
+ * same section (dr_gdn2_*, separate erase and write gates; its equations are a
+ * reading, stated at its entry points).
  *
  * Memory: the caller allocates every buffer (device memory unless stated) and
  * the workspace; the library never allocates, frees or synchronises inside
