@@ -135,13 +135,13 @@ def decode_bench(dev, stream, max_over_ranks, barrier, steps=20, warmup=3):
 
 def gdn2_flops_per_chunk(C, d):
     """FLOPs of one (chunk, head) of the Gated DeltaNet-2 forward + backward as the
-    CUDA-core kernels execute them (dense products, triangular ones counted in full):
-    the chunk-local products (11 of C x C x d), the inverse (C^3 / 3) and the state
-    products (4 of C x d x d) run once in the forward and twice in the backward
-    (chunk-start states, then the reverse pass); the backward adds 20 C x C x d, 8 C x d x d
-    and 2 C x C x C products."""
+    CUDA-core kernels execute them with DR_FLAG_REUSE_FWD (dense products, triangular
+    ones counted in full): the chunk-local products (11 of C x C x d), the inverse (C^3 / 3)
+    and the state products (4 of C x d x d) run once in the forward and once more in the
+    backward's reverse pass (the chunk-start states come from the forward); the backward
+    adds 20 C x C x d, 8 C x d x d and 2 C x C x C products."""
     one = 22 * C * C * d + C ** 3 / 3 + 8 * C * d * d
-    return 3 * one + 40 * C * C * d + 16 * C * d * d + 4 * C ** 3
+    return 2 * one + 40 * C * C * d + 16 * C * d * d + 4 * C ** 3
 
 
 def fp32_alu_peak_tflops(sm_mhz):
@@ -165,7 +165,7 @@ def gdn2_bench(dev, stream, max_over_ranks, barrier, sm_mhz, steps=3, warmup=3):
     def step():
         prob.forward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"], o=o, hT=hT)
         prob.backward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"], t["dO"],
-                      t["dhT"])
+                      t["dhT"], reuse_fwd=True)
 
     for _ in range(warmup):
         step()

@@ -363,7 +363,7 @@ class Gdn2Problem(Problem):
                            self._stream()), "dr_gdn2_fwd")
         return o, hT
 
-    def backward(self, q, k, v, erase, write, g, h0, dO, dhT=None, out=None):
+    def backward(self, q, k, v, erase, write, g, h0, dO, dhT=None, out=None, reuse_fwd=False):
         import torch
         d = self.desc
         if out is None:
@@ -377,9 +377,13 @@ class Gdn2Problem(Problem):
                 "dg": torch.empty(d.B, d.T, d.H, **f32),
                 "dh0": torch.empty(self.N, d.H, d.d_k, d.d_v, **f32),
             }
-        _check(dr_gdn2_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(g),
-                           _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(out["dq"]), _ptr(out["dk"]),
-                           _ptr(out["dv"]), _ptr(out["derase"]), _ptr(out["dwrite"]),
-                           _ptr(out["dg"]), _ptr(out["dh0"]), self.ws.data_ptr(), self.ws.numel(),
-                           self._stream()), "dr_gdn2_bwd")
+        d.flags = DR_FLAG_REUSE_FWD if reuse_fwd else 0
+        try:
+            _check(dr_gdn2_bwd(d, _ptr(q), _ptr(k), _ptr(v), _ptr(erase), _ptr(write), _ptr(g),
+                               _ptr(h0), _ptr(dO), _ptr(dhT), _ptr(out["dq"]), _ptr(out["dk"]),
+                               _ptr(out["dv"]), _ptr(out["derase"]), _ptr(out["dwrite"]),
+                               _ptr(out["dg"]), _ptr(out["dh0"]), self.ws.data_ptr(),
+                               self.ws.numel(), self._stream()), "dr_gdn2_bwd")
+        finally:
+            d.flags = 0
         return out

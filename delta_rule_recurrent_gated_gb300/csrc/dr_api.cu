@@ -25,7 +25,7 @@ void use_prepared(Params& p, uint8_t* area);
 cudaError_t chain_prepared_grads(const Params& p, cudaStream_t st);
 size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, long long th);
 cudaError_t gdn2_fwd(const Params& p, cudaStream_t st);
-cudaError_t gdn2_bwd(const Params& p, cudaStream_t st);
+cudaError_t gdn2_bwd(const Params& p, cudaStream_t st, bool reuse);
 cudaError_t wait_selftest(int* err, int arrive, unsigned long long limit_ns, cudaStream_t st);
 }  // namespace dr
 
@@ -427,7 +427,7 @@ int dr_gdn2_bwd(const dr_desc* desc, const void* q, const void* k, const void* v
         if (dh0) return cuda_status(dr::state_passthrough(dhT, dh0, (size_t)p.N * p.H * p.dk * p.dv, st));
         return DR_OK;
     }
-    return cuda_status(dr::gdn2_bwd(p, st));
+    return cuda_status(dr::gdn2_bwd(p, st, (desc->flags & DR_FLAG_REUSE_FWD) != 0));
 }
 
 int dr_selftest_wait(void* ws, int arrive, long long limit_ns, void* stream) {

@@ -205,15 +205,22 @@ __device__ void store_state_cols(float* h, const float* S, int n, int hd, const 
         h[(((size_t)n * p.H + hd) * p.dk + idx / bv) * p.dv + j0 + idx % bv] = S[idx];
 }
 
-__global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch, int bv) {
+// The forward also leaves the chunk-start states (this slice's columns) in `states`, where
+// a backward with DR_FLAG_REUSE_FWD reads them instead of recomputing them.
+__global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch, int bv,
+                                                                float* states) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
     const Scratch s{scratch + ((size_t)u * gridDim.y + blockIdx.y) * kNumBufs2 * kBuf};
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     float* S = s(gS);
     load_state_cols(S, p.h0, n, h, p, j0, bv);
+    const size_t SS = (size_t)p.dk * p.dv;
     for (int c = 0; c < nc; ++c) {
         const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
+        float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
+        for (int idx = threadIdx.x; idx < p.dk * bv; idx += blockDim.x)
+            dst[(idx / bv) * p.dv + j0 + idx % bv] = S[idx];
         chunk_prep2(p, s, h, row0, L, j0, bv);
         chunk_scan2(p, s, L, S, bv);
         const float* O = s(gO);
@@ -234,7 +241,7 @@ struct Gdn2Partials {
 
 __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* scratch,
                                                                 float* states, int bv,
-                                                                Gdn2Partials part) {
+                                                                Gdn2Partials part, int reuse) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
     const int dk = p.dk, dv = bv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
     const float sc = p.scale;
@@ -248,10 +255,11 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     const size_t SS = (size_t)dk * p.dv;
-    // pass 1: the state at the start of every chunk (this slice's columns)
+    // pass 1: the state at the start of every chunk (this slice's columns), unless the
+    // forward left them
     float* S = s(gS);
-    load_state_cols(S, p.h0, n, h, p, j0, bv);
-    for (int c = 0; c < nc; ++c) {
+    if (!reuse) load_state_cols(S, p.h0, n, h, p, j0, bv);
+    for (int c = 0; c < nc && !reuse; ++c) {
         const int row0 = srow + c * C, L = min(C, slen - c * C);
         float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
         for (int idx = tid; idx < dk * dv; idx += nt) dst[(idx / dv) * p.dv + j0 + idx % dv] = S[idx];
@@ -459,12 +467,13 @@ cudaError_t gdn2_fwd(const Params& p, cudaStream_t st) {
     if (units == 0) return cudaSuccess;
     const int nsl = gdn2_slices(units, p.dv);
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    float* states = scratch + (size_t)units * nsl * kNumBufs2 * kBuf;
     TraceScope ts("gdn2_fwd", st);
-    gdn2_fwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, p.dv / nsl);
+    gdn2_fwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, p.dv / nsl, states);
     return cudaGetLastError();
 }
 
-cudaError_t gdn2_bwd(const Params& p, cudaStream_t st) {
+cudaError_t gdn2_bwd(const Params& p, cudaStream_t st, bool reuse) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
     const int nsl = gdn2_slices(units, p.dv);
@@ -479,7 +488,8 @@ cudaError_t gdn2_bwd(const Params& p, cudaStream_t st) {
     }
     {
         TraceScope ts("gdn2_bwd", st);
-        gdn2_bwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, states, p.dv / nsl, part);
+        gdn2_bwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, states, p.dv / nsl, part,
+                                                               reuse ? 1 : 0);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nsl == 1) return e;

@@ -248,8 +248,10 @@ int dr_decode(const dr_desc* desc, const void* q, const void* k, const void* v,
  * (optional) for L = sum(dO * o) + sum(dhT * hT).
  * Supported: d_k, d_v, chunk in {16, 32, 64}; io bf16 or fp32 (fp32 arithmetic on the
  * CUDA cores for both); dense or packed layout as dr_fwd.  dr_workspace_bytes sizes the
- * workspace (same value for both calls).  Flags: DR_FLAG_REUSE_FWD is ignored;
- * DR_FLAG_PREPARE_INPUTS is DR_ERR_UNSUPPORTED.  Errors as dr_fwd / dr_bwd; dr_fwd and
+ * workspace (same value for both calls); dr_gdn2_fwd leaves the chunk-start states in
+ * it, and dr_gdn2_bwd with DR_FLAG_REUSE_FWD reads them instead of recomputing them
+ * (the same desc, inputs and workspace as the forward).  DR_FLAG_PREPARE_INPUTS is
+ * DR_ERR_UNSUPPORTED.  Errors as dr_fwd / dr_bwd; dr_fwd and
  * dr_bwd refuse DR_GDN2 with DR_ERR_INVALID_ARG.
  */
 int dr_gdn2_fwd(const dr_desc* desc, const void* q, const void* k, const void* v,

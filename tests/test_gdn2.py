@@ -20,13 +20,13 @@ pytestmark = pytest.mark.gpu
 FIELDS = ("o", "hT", "dq", "dk", "dv", "derase", "dwrite", "dg", "dh0")
 
 
-def run_gpu(w, x, out="f32", grad="f32"):
+def run_gpu(w, x, out="f32", grad="f32", reuse=True):
     prob = binding.Gdn2Problem(w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io, out=out,
                                grad=grad, scale=w.scale, cu_seqlens=x["cu_seqlens"])
     t = {n: (v.cuda() if torch.is_tensor(v) and n != "cu_seqlens" else v) for n, v in x.items()}
     o, hT = prob.forward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"])
     gr = prob.backward(t["q"], t["k"], t["v"], t["erase"], t["write"], t["g"], t["h0"], t["dO"],
-                       t["dhT"])
+                       t["dhT"], reuse_fwd=reuse)
     torch.cuda.synchronize()
     assert prob.status() == binding.DR_OK
     res = {"o": o, "hT": hT, **gr}
@@ -168,3 +168,15 @@ def test_bf16_gradients_and_rerun_bit_identical():
         half_ulp = np.abs(r) * 2.0 ** -9
         err = np.abs(a[n].astype(np.float64) - r)
         assert np.all(err <= half_ulp + tolerance(w, r)), n
+
+
+@pytest.mark.parametrize("d", [64, 16])
+def test_backward_reusing_the_forward_states_is_bit_identical(d):
+    """DR_FLAG_REUSE_FWD: the chunk-start states the forward left give the same bits as
+    the backward's own recomputation (both slice counts: d = 64 four slices, d = 16 one)."""
+    w = inputs.small("gdn2", H=2, dk=d, dv=d, chunk=64, io="bf16", lengths=[100, 0, 64, 131])
+    x = inputs.make_gdn2(w, seed=48)
+    a = run_gpu(w, x, reuse=True)
+    b = run_gpu(w, x, reuse=False)
+    for n in FIELDS:
+        assert np.array_equal(a[n], b[n]), n
