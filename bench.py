@@ -134,14 +134,14 @@ def decode_bench(dev, stream, max_over_ranks, barrier, steps=20, warmup=3):
 
 
 def gdn2_flops_per_chunk(C, d):
-    """FLOPs of one (chunk, head) of the Gated DeltaNet-2 forward + backward as the
-    CUDA-core kernels execute them with DR_FLAG_REUSE_FWD (dense products, triangular
-    ones counted in full): the chunk-local products (11 of C x C x d), the inverse (C^3 / 3)
-    and the state products (4 of C x d x d) run once in the forward and once more in the
-    backward's reverse pass (the chunk-start states come from the forward); the backward
-    adds 20 C x C x d, 8 C x d x d and 2 C x C x C products."""
-    one = 22 * C * C * d + C ** 3 / 3 + 8 * C * d * d
-    return 2 * one + 40 * C * C * d + 16 * C * d * d + 4 * C ** 3
+    """FLOPs of one (chunk, head) of the Gated DeltaNet-2 forward + backward in the
+    chunkwise form as run with DR_FLAG_REUSE_FWD (dense products, triangular ones counted
+    in full, each product once): the forward's chunk-local products (11 of C x C x d), the
+    inverse (C^3 / 3) and the state products (4 of C x d x d); the backward, which reads
+    the forward's per-chunk records, adds 20 C x C x d, 8 C x d x d and 2 C x C x C
+    products."""
+    fwd = 22 * C * C * d + C ** 3 / 3 + 8 * C * d * d
+    return fwd + 40 * C * C * d + 16 * C * d * d + 4 * C ** 3
 
 
 def fp32_alu_peak_tflops(sm_mhz):

@@ -35,14 +35,35 @@ namespace {
 
 constexpr int kThreads2 = 512;  // one CTA per (sequence, head): few CTAs, so wide ones
 
+// Scratch matrices.  The first group is one chunk's: the forward writes it into a
+// record per (chunk, head, slice), where a backward with DR_FLAG_REUSE_FWD finds the
+// chunk's key-side matrices and predictions instead of recomputing them.  The second
+// group (the carried state and the backward's work matrices) is per CTA.
 enum {
-    gS, gQ, gK, gV, gE, gWg, gVw, gB, gGam, gKb, gKr, gBr, gQb, gKC, gBC, gA, gMk, gT, gWy, gX,
+    gQ, gK, gV, gE, gWg, gVw, gB, gGam, gKb, gKr, gBr, gQb, gKC, gBC, gA, gMk, gT, gWy, gX,
     gPt, gAqk, gAqb, gQt, gOt, gP, gO, gTmp,
+    kChunkBufs,
+    gS = kChunkBufs,
     // backward only
     gS0, gdS, gdSp, gdO, gdP, gdQt, gdWy, gdPt, gdX, gdMk, gdKC, gdBC, gdVw, gdAqk, gdAqb, gdQb,
     gdKb, gdKr, gdBr, gdT, gdA, gdGam, gdVec,
     kNumBufs2
 };
+constexpr int kCtaBufs = kNumBufs2 - kChunkBufs;
+
+struct Scratch2 {
+    float* chunk;  // this chunk's record
+    float* cta;    // this CTA's matrices
+    __device__ float* operator()(int i) const {
+        return i < kChunkBufs ? chunk + (size_t)i * kBuf : cta + (size_t)(i - kChunkBufs) * kBuf;
+    }
+};
+
+// record of chunk c (global index) of head h, value slice y (of nsl)
+__device__ __forceinline__ float* chunk_record(float* area, const Params& p, int c, int h, int y,
+                                               int nsl) {
+    return area + (((size_t)c * p.H + h) * nsl + y) * kChunkBufs * kBuf;
+}
 
 __device__ void mask(float* M, int L, bool keep_diag) {
     for (int idx = threadIdx.x; idx < L * L; idx += blockDim.x) {
@@ -54,7 +75,7 @@ __device__ void mask(float* M, int L, bool keep_diag) {
 
 // Load one chunk and evaluate everything that does not depend on the state.
 // gGam holds Gamma_i at [i] and e^{Gamma_L} at [C].
-__device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, int L, int j0,
+__device__ void chunk_prep2(const Params& p, const Scratch2& s, int h, int row0, int L, int j0,
                             int dv) {
     const int dk = p.dk, H = p.H, tid = threadIdx.x, nt = blockDim.x;
     const float sc = p.scale;
@@ -178,7 +199,7 @@ __device__ void chunk_prep2(const Params& p, const Scratch& s, int h, int row0, 
 }
 
 // P = Pt + Wy S; O = Ot + Qt S; S <- e^{Gamma_L} S + KC^T Vw - BC^T P
-__device__ void chunk_scan2(const Params& p, const Scratch& s, int L, float* S, int dv) {
+__device__ void chunk_scan2(const Params& p, const Scratch2& s, int L, float* S, int dv) {
     const int dk = p.dk, tid = threadIdx.x, nt = blockDim.x;
     float* P = s(gP); float* O = s(gO);
     for (int idx = tid; idx < L * dv; idx += nt) { P[idx] = s(gPt)[idx]; O[idx] = s(gOt)[idx]; }
@@ -208,9 +229,9 @@ __device__ void store_state_cols(float* h, const float* S, int n, int hd, const 
 // The forward also leaves the chunk-start states (this slice's columns) in `states`, where
 // a backward with DR_FLAG_REUSE_FWD reads them instead of recomputing them.
 __global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* scratch, int bv,
-                                                                float* states) {
+                                                                float* records, float* states) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
-    const Scratch s{scratch + ((size_t)u * gridDim.y + blockIdx.y) * kNumBufs2 * kBuf};
+    Scratch2 s{nullptr, scratch + ((size_t)u * gridDim.y + blockIdx.y) * kCtaBufs * kBuf};
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     float* S = s(gS);
@@ -221,6 +242,7 @@ __global__ void __launch_bounds__(kThreads2) gdn2_fwd_kernel(Params p, float* sc
         float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
         for (int idx = threadIdx.x; idx < p.dk * bv; idx += blockDim.x)
             dst[(idx / bv) * p.dv + j0 + idx % bv] = S[idx];
+        s.chunk = chunk_record(records, p, c0 + c, h, blockIdx.y, gridDim.y);
         chunk_prep2(p, s, h, row0, L, j0, bv);
         chunk_scan2(p, s, L, S, bv);
         const float* O = s(gO);
@@ -240,12 +262,13 @@ struct Gdn2Partials {
 };
 
 __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* scratch,
-                                                                float* states, int bv,
-                                                                Gdn2Partials part, int reuse) {
+                                                                float* records, float* states,
+                                                                int bv, Gdn2Partials part,
+                                                                int reuse) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H, j0 = blockIdx.y * bv;
     const int dk = p.dk, dv = bv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
     const float sc = p.scale;
-    const Scratch s{scratch + ((size_t)u * gridDim.y + blockIdx.y) * kNumBufs2 * kBuf};
+    Scratch2 s{nullptr, scratch + ((size_t)u * gridDim.y + blockIdx.y) * kCtaBufs * kBuf};
     const size_t th = (size_t)p.B * p.T * p.H;
     const bool direct = part.q == nullptr;
     float* pq = direct ? nullptr : part.q + blockIdx.y * th * dk;
@@ -264,6 +287,7 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
         float* dst = states + ((size_t)(c0 + c) * p.H + h) * SS;
         for (int idx = tid; idx < dk * dv; idx += nt) dst[(idx / dv) * p.dv + j0 + idx % dv] = S[idx];
         __syncthreads();
+        s.chunk = chunk_record(records, p, c0 + c, h, blockIdx.y, gridDim.y);
         chunk_prep2(p, s, h, row0, L, j0, bv);
         chunk_scan2(p, s, L, S, bv);
     }
@@ -280,8 +304,11 @@ __global__ void __launch_bounds__(kThreads2) gdn2_bwd_kernel(Params p, float* sc
             S[idx] = x;
         }
         __syncthreads();
-        chunk_prep2(p, s, h, row0, L, j0, bv);
-        chunk_scan2(p, s, L, S, bv);  // recomputes P (S is scratch here)
+        s.chunk = chunk_record(records, p, c0 + c, h, blockIdx.y, gridDim.y);
+        if (!reuse) {  // else the forward's record of this chunk holds all of it
+            chunk_prep2(p, s, h, row0, L, j0, bv);
+            chunk_scan2(p, s, L, S, bv);  // recomputes P (S is scratch here)
+        }
         float* dO = s(gdO);
         for (int idx = tid; idx < L * dv; idx += nt)
             dO[idx] = ld_any(p.dO, ((size_t)(row0 + idx / dv) * p.H + h) * p.dv + j0 + idx % dv,
@@ -455,9 +482,12 @@ __global__ void __launch_bounds__(256) gdn2_reduce_kernel(Params p, Gdn2Partials
 // than SMs (more CTAs for the same work), else one slice.
 int gdn2_slices(int units, int dv) { return (units >= 152 || dv < 32) ? 1 : dv / 16; }
 
+// Workspace after the header: the CTAs' matrices, the chunk records, the chunk-start
+// states, then (with several slices) the partial key-side gradients.
 size_t gdn2_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, long long th) {
     const int nsl = gdn2_slices(units, dv);
-    return (size_t)units * nsl * kNumBufs2 * kBuf * sizeof(float) +
+    return (size_t)units * nsl * kCtaBufs * kBuf * sizeof(float) +
+           (size_t)num_chunks * H * nsl * kChunkBufs * kBuf * sizeof(float) +
            (size_t)num_chunks * H * dk * dv * sizeof(float) +
            (nsl > 1 ? (size_t)nsl * (size_t)th * (3 * dk + 1) * sizeof(float) : 0);
 }
@@ -467,9 +497,10 @@ cudaError_t gdn2_fwd(const Params& p, cudaStream_t st) {
     if (units == 0) return cudaSuccess;
     const int nsl = gdn2_slices(units, p.dv);
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
-    float* states = scratch + (size_t)units * nsl * kNumBufs2 * kBuf;
+    float* records = scratch + (size_t)units * nsl * kCtaBufs * kBuf;
+    float* states = records + (size_t)p.num_chunks * p.H * nsl * kChunkBufs * kBuf;
     TraceScope ts("gdn2_fwd", st);
-    gdn2_fwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, p.dv / nsl, states);
+    gdn2_fwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, p.dv / nsl, records, states);
     return cudaGetLastError();
 }
 
@@ -479,7 +510,8 @@ cudaError_t gdn2_bwd(const Params& p, cudaStream_t st, bool reuse) {
     const int nsl = gdn2_slices(units, p.dv);
     const size_t th = (size_t)p.B * p.T * p.H;
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
-    float* states = scratch + (size_t)units * nsl * kNumBufs2 * kBuf;
+    float* records = scratch + (size_t)units * nsl * kCtaBufs * kBuf;
+    float* states = records + (size_t)p.num_chunks * p.H * nsl * kChunkBufs * kBuf;
     Gdn2Partials part{nullptr, nullptr, nullptr, nullptr};
     if (nsl > 1) {
         float* base = states + (size_t)p.num_chunks * p.H * p.dk * p.dv;
@@ -488,8 +520,8 @@ cudaError_t gdn2_bwd(const Params& p, cudaStream_t st, bool reuse) {
     }
     {
         TraceScope ts("gdn2_bwd", st);
-        gdn2_bwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, states, p.dv / nsl, part,
-                                                               reuse ? 1 : 0);
+        gdn2_bwd_kernel<<<dim3(units, nsl), kThreads2, 0, st>>>(p, scratch, records, states,
+                                                               p.dv / nsl, part, reuse ? 1 : 0);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nsl == 1) return e;
