@@ -17,7 +17,9 @@ oracle where the two must agree.  The reading itself is not pinned by the pages.
 * closed forms: no erase and no write (the memory only decays); no erase
   (decayed linear attention, a plain sum); erase = write = 1 with unit keys and
   no decay (exact recall of the last value written under a key);
-* packed ragged sequences == separate calls.
+* packed ragged sequences == separate calls;
+* a hand-worked two-token example with different erase and write gates
+  (tests/golden/scalar_gdn2_t2.txt).
 """
 import numpy as np
 import pytest
@@ -173,3 +175,28 @@ def test_packed_equals_separate():
                                      sl(x["write"]), sl(x["g"]), h0[n:n + 1])
         np.testing.assert_allclose(o[:, lo:hi], on, rtol=0, atol=1e-13)
         np.testing.assert_allclose(hT[n:n + 1], hn, rtol=0, atol=1e-13)
+
+
+def test_hand_worked_scalar_example():
+    """tests/golden/scalar_gdn2_t2.txt: two tokens with d_k = d_v = 1 and different erase
+    and write gates, worked by hand (every value an exact binary fraction)."""
+    import os
+    gv = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "scalar_gdn2_t2.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                key, rhs = line.split("=", 1)
+                gv[key.strip()] = [float(x) for x in rhs.split()]
+    sh = (1, 2, 1, 1)
+    q, k, v = (np.array(gv[n]).reshape(sh) for n in ("q", "k", "v"))
+    e, wr = np.array(gv["erase"]).reshape(sh), np.array(gv["write"]).reshape(sh)
+    g = np.log(np.array(gv["alpha"])).reshape(1, 2, 1)
+    h0 = np.array(gv["W0"]).reshape(1, 1, 1, 1)
+    o, hT = oracle.forward_gdn2(q, k, v, e, wr, g, h0)
+    np.testing.assert_allclose(o.ravel(), gv["o"], atol=1e-14)
+    np.testing.assert_allclose(hT.ravel(), gv["WT"], atol=1e-14)
+    gr = oracle.backward_gdn2(q, k, v, e, wr, g, h0, np.ones_like(o), None)
+    for key, name in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("derase", "derase"),
+                      ("dwrite", "dwrite"), ("dg", "dg"), ("dW0", "dh0")):
+        np.testing.assert_allclose(gr[name].ravel(), gv[key], atol=1e-14, err_msg=key)
