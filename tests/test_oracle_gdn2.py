@@ -14,6 +14,7 @@ oracle where the two must agree.  The reading itself is not pinned by the pages.
 * explicit unrolling: one (sequence, head) solved as a dense lower-triangular
   system for the predictions p_t, then the outputs as matrix products (numpy);
 * central finite differences of every input;
+* exact symbolic derivatives (sympy, rational inputs) of the reading's lines;
 * closed forms: no erase and no write (the memory only decays); no erase
   (decayed linear attention, a plain sum); erase = write = 1 with unit keys and
   no decay (exact recall of the last value written under a key);
@@ -200,3 +201,57 @@ def test_hand_worked_scalar_example():
     for key, name in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("derase", "derase"),
                       ("dwrite", "dwrite"), ("dg", "dg"), ("dW0", "dh0")):
         np.testing.assert_allclose(gr[name].ravel(), gv[key], atol=1e-14, err_msg=key)
+
+
+def test_backward_matches_symbolic_gradient():
+    """Exact derivatives by sympy on a tiny case (T=3, d_k=2, d_v=2) with rational
+    inputs: the symbolic forward is built from the lines of the reading (decay,
+    prediction, erase, write, read) and differentiated by sympy itself."""
+    sp = pytest.importorskip("sympy")
+    T, dk, dv = 3, 2, 2
+    rng = np.random.default_rng(13)
+    q64 = lambda a: np.round(a * 64) / 64  # binary fractions: sympy and the oracle agree
+    qn, kn = q64(rng.standard_normal((T, dk))), q64(rng.standard_normal((T, dk)))
+    vn, dOn = q64(rng.standard_normal((T, dv))), q64(rng.standard_normal((T, dv)))
+    en, wn = q64(rng.uniform(0.1, 0.9, (T, dk))), q64(rng.uniform(0.1, 0.9, (T, dv)))
+    gn = q64(-np.abs(rng.standard_normal(T)) * 0.5)
+    s0n = q64(rng.standard_normal((dk, dv)) * 0.5)
+    syms = {}
+
+    def symmat(name, shape):
+        m = sp.Matrix(shape[0], shape[1], lambda i, j: sp.Symbol(f"{name}_{i}_{j}"))
+        syms[name] = m
+        return m
+
+    Q = symmat("q", (T, dk)); K = symmat("k", (T, dk)); V = symmat("v", (T, dv))
+    E = symmat("e", (T, dk)); Wg = symmat("w", (T, dv)); G = symmat("g", (T, 1))
+    S0 = symmat("s", (dk, dv))
+    W = S0.T  # d_v x d_k
+    loss = 0
+    for t in range(T):
+        Wd = sp.exp(G[t, 0]) * W
+        p = Wd * K[t, :].T                                            # prediction
+        b = sp.Matrix(1, dk, lambda _, c: E[t, c] * K[t, c])          # erase key
+        vw = sp.Matrix(dv, 1, lambda j, _: Wg[t, j] * V[t, j])        # gated value
+        W = Wd - p * b + vw * K[t, :]
+        o = W * Q[t, :].T
+        loss += sum(o[j] * sp.Rational(int(round(dOn[t, j] * 64)), 64) for j in range(dv))
+    vals = {}
+    for name, arr in (("q", qn), ("k", kn), ("v", vn), ("e", en), ("w", wn),
+                      ("g", gn[:, None]), ("s", s0n)):
+        m = syms[name]
+        for i in range(m.rows):
+            for j in range(m.cols):
+                vals[m[i, j]] = sp.Rational(int(round(arr[i, j] * 64)), 64)
+    sh = lambda a: a[None, :, None]
+    gr = oracle.backward_gdn2(sh(qn), sh(kn), sh(vn), sh(en), sh(wn), gn[None, :, None],
+                              s0n[None, None], sh(dOn), None)
+    table = (("q", gr["dq"][0, :, 0]), ("k", gr["dk"][0, :, 0]), ("v", gr["dv"][0, :, 0]),
+             ("e", gr["derase"][0, :, 0]), ("w", gr["dwrite"][0, :, 0]),
+             ("g", gr["dg"][0, :, 0][:, None]), ("s", gr["dh0"][0, 0]))
+    for name, got in table:
+        m = syms[name]
+        for i in range(m.rows):
+            for j in range(m.cols):
+                exact = float(sp.diff(loss, m[i, j]).subs(vals).evalf(30))
+                assert abs(got[i, j] - exact) < 1e-12 * max(1.0, abs(exact)), (name, i, j)
