@@ -89,6 +89,35 @@ def kernel_bytes(name, w, N):
     return 0
 
 
+def kernel_algorithmic_bytes(name, w, N):
+    """The part of the whole path's algorithmic bytes (the formula of `algorithmic`) that
+    each kernel of the step owns, per launch: tc_prep reads q, k, v, beta, g; the forward
+    scan writes o (and reads h0, writes hT); the backward scan reads dhT and h0 and writes
+    dh0; tc_bwd_chunk reads q, k, v, dO, beta, g and writes dq, dk, dv, dbeta, dg.  The
+    four add up to `algorithmic`'s bytes."""
+    s = 2 if w.io == "bf16" else 4
+    G = {"deltanet": 0, "gdn": 4, "kda": 4 * w.dk}[w.variant]
+    th = w.B * w.T * w.H
+    st = w.dk * w.dv * 4 * N * w.H if w.h0 else 0
+    if name == "tc_prep":
+        return th * (s * (2 * w.dk + w.dv) + 4 + G)
+    if name == "tc_scan_fwd":
+        return th * s * w.dv + 2 * st
+    if name == "tc_scan_bwd":
+        return 3 * st
+    if name == "tc_bwd_chunk":
+        return th * (s * (4 * w.dk + 3 * w.dv) + 8 + 2 * G)
+    return 0
+
+
+def config_of(w, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": w.name, "variant": w.variant, "global_batch": w.B * world,
+            "seq_len": w.T, "heads": w.H, "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
 DECODE_B, DECODE_H, DECODE_D = 256, 16, 128
 
 
@@ -332,67 +361,150 @@ def prepare_bench(args, w, rank, world, dev, stream, plain_ms, o, hT, grads, max
             "inputs": "raw q, k ~ N(0,1), beta logits ~ N(0,1), gate arguments ~ N(0,1) - 2.5"}
 
 
-def cpu_baseline(w, x, budget_s=12.0):
-    """Time the fp64 oracle (forward + backward, as it stands) on whole
-    (sequence, head) units of the workload on the host cores, and scale the
-    result to tokens/s of the layer (a token carries H heads)."""
+def oracle_step(w, x, units):
+    """One timed pass of the fp64 oracle (forward + backward, as it stands) over the given
+    (sequence, head) units of the workload; returns (seconds, token-equivalents), a token
+    of the layer carrying H heads."""
     import numpy as np
     import oracle
-    threads = oracle.max_threads()
-    N = x["N"]
-    total_units = N * w.H
     a = dict(q=x["q"], k=x["k"], v=x["v"], beta=x["beta"], g=x["g"], h0=x["h0"],
-             cu_seqlens=x["cu_seqlens"])
-
-    def run(units):
-        oracle.forward(w.variant, units=units, **a)
-        oracle.backward(w.variant, dO=x["dO"], dhT=x["dhT"], units=units, **a)
-
-    n1 = min(total_units, threads)
+             cu_seqlens=x["cu_seqlens"], scale=w.scale)
+    u = np.asarray(units, dtype=np.int32)
     t0 = time.perf_counter()
-    run(np.arange(n1, dtype=np.int32))
-    dt1 = max(time.perf_counter() - t0, 1e-3)
-    batches = max(0, min(int(budget_s / dt1) - 1, total_units // max(n1, 1) - 1))
-    n2 = batches * n1
-    dt2 = 0.0
-    if n2 > 0:
-        t0 = time.perf_counter()
-        run(np.arange(n1, n1 + n2, dtype=np.int32))
-        dt2 = time.perf_counter() - t0
-    units = n1 + n2
-    secs = dt1 + dt2
+    oracle.forward(w.variant, units=u, **a)
+    oracle.backward(w.variant, dO=x["dO"], dhT=x["dhT"], units=u, **a)
+    secs = time.perf_counter() - t0
+    N = x["N"]
     tok_per_unit = w.T if x["cu_seqlens"] is None else w.T / max(N, 1)
-    tokens_per_s = units * tok_per_unit / secs / w.H
-    return {"value": tokens_per_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{units} of {total_units} (sequence, head) units of {w.name}, "
+    return secs, len(u) * tok_per_unit / w.H
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    """Time the fp64 oracle (forward + backward, as it stands) on whole (sequence, head)
+    units of the workload on the host cores, one unit per thread per pass, for about
+    budget_s seconds, and express it as tokens/s of the layer."""
+    import oracle
+    threads = oracle.max_threads()
+    total = x["N"] * w.H
+    secs = toks = 0.0
+    done = 0
+    while done < total and (secs < budget_s or done == 0):
+        n = min(threads, total - done)
+        dt, tk = oracle_step(w, x, range(done, done + n))
+        secs, toks, done = secs + dt, toks + tk, done + n
+    return {"value": toks / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {total} (sequence, head) units of {w.name}, "
                       f"fp64 forward+backward, {secs:.1f} s on {threads} threads"}
 
 
 def run_reference(args, w):
+    """The reference arm: the fp64 oracle as it stands on the host cores.  Each step is
+    one pass over `threads` (sequence, head) units of the workload (a bounded sample,
+    different units every step); ms_per_step is that pass's wall time and value the
+    token-equivalents it processed per second."""
     from delta_rule_recurrent_gated_gb300.replicas import Replicas
     if not Replicas.from_env().is_root:  # the oracle runs once, on rank 0's host cores
         return
+    import oracle
     from delta_rule_recurrent_gated_gb300 import inputs
     x = inputs.make(w, seed=0)
-    vals = []
-    base = None
-    per_step = max(2.0, 90.0 / max(args.steps + args.warmup, 1))
+    threads = oracle.max_threads()
+    total = x["N"] * w.H
+    n = min(threads, total)
+    secs = toks = 0.0
     for i in range(args.warmup + args.steps):
-        base = cpu_baseline(w, x, budget_s=per_step)
+        units = [(i * n + j) % total for j in range(n)]
+        dt, tk = oracle_step(w, x, units)
         if i >= args.warmup:
-            vals.append(base["value"])
-    value = sum(vals) / len(vals)
+            secs, toks = secs + dt, toks + tk
+    value = toks / secs
+    ms = 1e3 * secs / args.steps
+    base = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {total} (sequence, head) units of {w.name} per step "
+                      f"({toks / args.steps:.0f} token-equivalents), fp64 forward+backward "
+                      f"on {threads} threads"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * w.tokens / value, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "variant": w.variant, "global_batch": w.B,
-                       "seq_len": w.T, "heads": w.H, "d_k": w.dk, "d_v": w.dv,
-                       "parallelism": "host cores (OpenMP over sequence x head)"},
-            "cpu_baseline": dict(base, value=value),
+            "config": config_of(w, 1),
+            "cpu_baseline": base,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def time_workload(name, dev, stream, steps, warmup, max_over_ranks, barrier, seed=0):
+    """Forward + backward (dr_fwd, dr_bwd reusing the forward) of a workload on device-
+    resident inputs: ms per step from CUDA events on the launching stream, the path's
+    roofline fraction and the per-kernel device times."""
+    import torch
+    from delta_rule_recurrent_gated_gb300 import binding, inputs
+    w = inputs.get(name)
+    x = inputs.make(w, seed=seed)
+    N = x["N"]
+    t = {n: (v.to(dev) if torch.is_tensor(v) and n != "cu_seqlens" else v) for n, v in x.items()}
+    del x
+    prob = binding.Problem(w.variant, w.B, w.T, w.H, w.dk, w.dv, chunk=w.chunk, io=w.io,
+                           out="bf16", grad="bf16", scale=w.scale, device=dev)
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(N, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def step():
+        prob.forward(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], o=o, hT=hT)
+        prob.backward(t["q"], t["k"], t["v"], t["beta"], t["g"], t["h0"], t["dO"], t["dhT"],
+                      reuse_fwd=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    binding.trace_enable(8 * steps + 8)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    assert prob.status() == binding.DR_OK
+    launches = binding.trace_read()
+    binding.trace_enable(0)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps)
+    hbm, tflops, _ = measured_peaks()
+    flops, byts = algorithmic(w, N)
+    t_roof = max(flops / (tflops * 1e12), byts / (hbm * 1e9))
+    kern = {}
+    for nm, kms in launches:
+        tot, n = kern.get(nm, (0.0, 0))
+        kern[nm] = (tot + kms, n + 1)
+    del prob, t, o, hT
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "value": w.tokens / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps, "warmup": warmup,
+            "roofline_frac": t_roof / (ms / 1e3), "t_roof_ms": t_roof * 1e3,
+            "kernels_ms": {nm: tot / n for nm, (tot, n) in kern.items()}}
+
+
+def sweep_bench(dev, stream, max_over_ranks, barrier, steps=5, warmup=3):
+    """The sequence-length sweep: every variant at T = 4096 .. 32768 with B T = 65536
+    tokens, H = 16, d = 128; tokens/s, the path roofline fraction and the iteration-time
+    ratio t(T) / t(4096)."""
+    out = {}
+    for variant in ("deltanet", "gdn", "kda"):
+        rows = []
+        for T, B in ((4096, 16), (8192, 8), (16384, 4), (32768, 2)):
+            r = time_workload(f"sweep_{variant}_b{B}_t{T}_h16_d128", dev, stream, steps, warmup,
+                              max_over_ranks, barrier)
+            rows.append(r)
+        t0 = rows[0]["ms_per_step"]
+        out[variant] = [{"T": int(r["workload"].split("_t")[1].split("_")[0]),
+                         "ms_per_step": r["ms_per_step"], "tokens_per_s": r["value"],
+                         "roofline_frac": r["roofline_frac"],
+                         "ratio_vs_t4096": r["ms_per_step"] / t0,
+                         "scan_ms": r["kernels_ms"].get("tc_scan_fwd", 0.0)
+                         + r["kernels_ms"].get("tc_scan_bwd", 0.0)} for r in rows]
+    return out
 
 
 def main():
@@ -412,6 +524,10 @@ def main():
                     help="skip the Gated DeltaNet-2 measurement")
     ap.add_argument("--no-prepare", action="store_true",
                     help="skip the step with input preparation (DR_FLAG_PREPARE_INPUTS)")
+    ap.add_argument("--no-kda", action="store_true",
+                    help="skip the KDA step at the headline shape")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sequence-length sweep (all variants, T = 4096 .. 32768)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -495,17 +611,36 @@ def main():
     hbm, tflops, peak_src = measured_peaks()
     flops, byts = algorithmic(w, N)
     t_roof = max(flops / (tflops * 1e12), byts / (hbm * 1e9))
-    roof = None
+    # the roofline of the whole step: its algorithmic bytes (every kernel's inputs and
+    # outputs, no intermediates) over its measured time, against the HBM copy peak; the
+    # FLOP leg is below it at the measured bf16 peak
+    roof = {"bound": "hbm" if byts / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
+            "achieved": byts / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": t_roof / (ms / 1e3), "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
+            "bytes_per_step": byts, "flops_per_step": flops, "t_roof_ms": t_roof * 1e3,
+            "tflops_achieved": flops / (ms / 1e3) / 1e12, "tflops_peak": tflops,
+            "traffic": None}
+    dom = None
     if per:
         name, (tot, n) = max(per.items(), key=lambda kv: kv[1][0])
         avg_s = tot / n / 1e3
-        kb = kernel_bytes(name, w, N)
-        ach = kb / avg_s / 1e9
-        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
-                "traffic": measured_traffic(name, w), "avg_launch_ms": tot / n,
-                "bytes_per_launch": kb}
-    kern = {k: {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(v[0] for v in per.values())}
+        ab = kernel_algorithmic_bytes(name, w, N)
+        db = kernel_bytes(name, w, N)
+        tr = measured_traffic(name, w)
+        dom = {"kernel": name, "avg_launch_ms": tot / n, "launches_per_step": n / args.steps,
+               "algorithmic_bytes_per_launch": ab, "achieved": ab / avg_s / 1e9,
+               "frac": ab / avg_s / 1e9 / hbm, "unit": "GB/s",
+               "traffic": tr,
+               "design_bytes_per_launch": db,
+               "design_bytes_gbs": db / avg_s / 1e9, "design_bytes_frac": db / avg_s / 1e9 / hbm}
+        roof["dominant_kernel"] = dom
+        # DRAM traffic of the whole step, when every kernel of it has a recorded capture
+        trs = [measured_traffic(k, w) for k in per]
+        if all(x is not None for x in trs):
+            roof["traffic"] = sum(x * per[k][1] / args.steps for x, k in zip(trs, per))
+    kern = {k: {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(v[0] for v in per.values()),
+                "algorithmic_bytes_per_launch": kernel_algorithmic_bytes(k, w, N),
+                "design_bytes_per_launch": kernel_bytes(k, w, N)}
             for k, (tot, n) in per.items()}
 
     # end to end through the public API from pinned host buffers, copies inside: every
@@ -627,6 +762,11 @@ def main():
         pr = prepare_bench(args, w, rank, world, dev, stream, ms, o, hT, grads, max_over_ranks,
                            barrier)
 
+    # KDA at the headline shape and the sequence-length sweep (same step, own workloads)
+    kda = None if args.no_kda else time_workload("kda_b8_t4096_h16_d128", dev, stream, args.steps,
+                                                  args.warmup, max_over_ranks, barrier, rep.seed())
+    sweep = None if args.no_sweep else sweep_bench(dev, stream, max_over_ranks, barrier)
+
     if not rep.is_root:
         rep.shutdown()
         return
@@ -638,14 +778,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "variant": w.variant, "global_batch": w.B * world,
-                   "seq_len": w.T, "heads": w.H, "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB per step > 129 MB)"},
+        "config": config_of(w, world),
+        "inputs_mib_per_step": in_bytes / 2**20,
         "roofline": roof,
-        "path_roofline": {"flops_per_step": flops, "bytes_per_step": byts,
-                          "t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3),
-                          "peaks": {"hbm_gbs": hbm, "bf16_tflops": tflops, "source": peak_src}},
         "kernels": kern,
         "cpu_baseline": base,
         "e2e": e2e,
@@ -653,6 +788,8 @@ def main():
         "emit_write": wr,
         "prepare_inputs": pr,
         "gdn2": g2,
+        "kda": kda,
+        "sweep": sweep,
         "gpu_launches": len(launches),
         "clocks": clk,
     }

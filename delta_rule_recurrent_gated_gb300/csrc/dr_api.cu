@@ -9,14 +9,14 @@
 #include "dr.h"
 
 namespace dr {
-size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv);
+size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, int C);
 cudaError_t simt_fwd(const Params& p, cudaStream_t st);
 cudaError_t simt_bwd(const Params& p, cudaStream_t st);
 size_t tc_workspace_bytes(const Params& p);
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
 cudaError_t tc_bwd(const Params& p, cudaStream_t st, bool reuse);
 cudaError_t state_passthrough(const float* src, float* dst, size_t n, cudaStream_t st);
-int simt_noalloc_max_units();
+int simt_noalloc_max_units(int C, int dk, int dv);
 cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st);
 cudaError_t decode(const Params& p, float* state, cudaStream_t st, bool prepare);
 size_t prepare_bytes(const Params& p);
@@ -70,7 +70,8 @@ int check_desc(const dr_desc* d, Path* path) {
         if (d->d_k == d->d_v && (d->d_k == 64 || d->d_k == 128) && d->chunk == 64)
             *path = Path::kTensor;
     } else {
-        if (small(d->d_k) && small(d->d_v) && small(d->chunk)) *path = Path::kSimt;
+        auto dim = [&](int x) { return small(x) || x == 128; };
+        if (dim(d->d_k) && dim(d->d_v) && small(d->chunk)) *path = Path::kSimt;
     }
     return *path == Path::kNone ? DR_ERR_UNSUPPORTED : DR_OK;
 }
@@ -102,7 +103,7 @@ size_t path_ws_bytes(const Params& p, Path path) {
         return kHeader + dr::gdn2_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv,
                                                   (long long)p.B * p.T * p.H);
     if (path == Path::kSimt)
-        return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv);
+        return kHeader + dr::simt_workspace_bytes(p.N * p.H, p.num_chunks, p.H, p.dk, p.dv, p.C);
     return kHeader + dr::tc_workspace_bytes(p);
 }
 
@@ -359,7 +360,7 @@ int dr_fwd_noalloc(const dr_desc* desc, const void* q, const void* k, const void
     const void* ptrs[] = {q, k, v, beta, g, h0, o, hT};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DR_ERR_ALIGNMENT;
-    if ((long long)p.N * p.H > dr::simt_noalloc_max_units()) return DR_ERR_SCRATCH_LIMIT;
+    if ((long long)p.N * p.H > dr::simt_noalloc_max_units(p.C, p.dk, p.dv)) return DR_ERR_SCRATCH_LIMIT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.o = o; p.hT = hT;
     if (tokens == 0) {

@@ -118,9 +118,11 @@ __device__ void chunk_scan(const Params& p, const Scratch& s, int L, float* S) {
     mm4(S, dv, s(bKC), dk, true, U, dv, false, dk, dv, L, 1.f, true);
 }
 
-__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scratch) {
+// Forward of one (sequence, head) unit per CTA over the scratch slice s.
+__global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scratch,
+                                                            size_t unit_floats, int buf) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H;
-    const Scratch s{scratch + (size_t)u * kNumBufs * kBuf};
+    const Scratch s{scratch + (size_t)u * unit_floats, buf};
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     float* S = s(bS);
@@ -145,10 +147,10 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Params p, float* scr
 }
 
 __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scratch,
-                                                            float* states) {
+                                                            float* states, int buf) {
     const int u = blockIdx.x, n = u / p.H, h = u % p.H;
     const int dk = p.dk, dv = p.dv, C = p.C, tid = threadIdx.x, nt = blockDim.x;
-    const Scratch s{scratch + (size_t)u * kNumBufs * kBuf};
+    const Scratch s{scratch + (size_t)u * kNumBufs * buf, buf};
     int c0, nc, srow, slen;
     seq_chunks(p, n, c0, nc, srow, slen);
     const size_t SS = (size_t)dk * dv;
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         mm4(dQt, dk, dO, dv, false, S0, dv, true, L, dk, dv, 1.f, false);
         mm4(dWy, dk, dU, dv, false, S0, dv, true, L, dk, dv, -1.f, false);
         mm4(dKC, dk, s(bU), dv, false, dS, dv, true, L, dk, dv, 1.f, false);
-        float* dVec = s(bdVec);  // [0, dk): d e^{Gamma_L} ; [C + ...] unused
+        float* dVec = s(bdVec);  // [0, dk): d e^{Gamma_L}; [128, 128 + C): dbeta
         for (int c2 = tid; c2 < dk; c2 += nt) {
             float acc = 0.f;
             for (int j = 0; j < dv; ++j) acc += dS[c2 * dv + j] * S0[c2 * dv + j];
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
             if (idx % L >= idx / L) dA[idx] = 0.f;
         __syncthreads();
         // A = diag(beta) strict_lower(Kb Kr^T) (Gram kept in bA)
-        float* db = dVec + 64;  // per-token dbeta partials
+        float* db = dVec + 128;  // per-token dbeta partials (after the d_k <= 128 values)
         const float* Gm = s(bA);
         for (int i = tid; i < L; i += nt) {
             float acc = 0.f;
@@ -310,8 +312,15 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
 
 }  // namespace
 
-size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv) {
-    return (size_t)units * kNumBufs * kBuf * sizeof(float) +
+// Floats per scratch matrix: every matrix of a chunk is at most max(C, d_k, d_v)
+// squared (4096 for the sizes up to 64, 16384 at d = 128).
+int simt_buf_floats(int C, int dk, int dv) {
+    const int m = max(64, max(C, max(dk, dv)));
+    return m * m;
+}
+
+size_t simt_workspace_bytes(int units, int num_chunks, int H, int dk, int dv, int C) {
+    return (size_t)units * kNumBufs * simt_buf_floats(C, dk, dv) * sizeof(float) +
            (size_t)num_chunks * H * dk * dv * sizeof(float);
 }
 
@@ -319,18 +328,20 @@ cudaError_t simt_fwd(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
+    const int buf = simt_buf_floats(p.C, p.dk, p.dv);
     TraceScope ts("simt_fwd", st);
-    simt_fwd_kernel<<<units, kThreads, 0, st>>>(p, scratch);
+    simt_fwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, (size_t)kNumBufs * buf, buf);
     return cudaGetLastError();
 }
 
 cudaError_t simt_bwd(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
+    const int buf = simt_buf_floats(p.C, p.dk, p.dv);
     float* scratch = reinterpret_cast<float*>(p.ws + 256);
-    float* states = scratch + (size_t)units * kNumBufs * kBuf;
+    float* states = scratch + (size_t)units * kNumBufs * buf;
     TraceScope ts("simt_bwd", st);
-    simt_bwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, states);
+    simt_bwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, states, buf);
     return cudaGetLastError();
 }
 
@@ -350,40 +361,15 @@ cudaError_t simt_bwd(const Params& p, cudaStream_t st) {
 // and nothing needs clearing.
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;       // 16 MiB per GPU
 constexpr int kNoAllocBufs = bTmp + 1;                          // forward-only buffers
-constexpr size_t kNoAllocUnitFloats = (size_t)kNoAllocBufs * kBuf;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
 
 namespace {
-// The forward kernel of this file with a forward-only per-unit scratch stride.
-__global__ void __launch_bounds__(kThreads) simt_fwd_noalloc_kernel(Params p, float* scratch) {
-    const int u = blockIdx.x, n = u / p.H, h = u % p.H;
-    const Scratch s{scratch + (size_t)u * kNoAllocUnitFloats};
-    int c0, nc, srow, slen;
-    seq_chunks(p, n, c0, nc, srow, slen);
-    float* S = s(bS);
-    load_state(S, p.h0, n, h, p.H, p.dk, p.dv);
-    for (int c = 0; c < nc; ++c) {
-        const int row0 = srow + c * p.C, L = min(p.C, slen - c * p.C);
-        chunk_prep(p, s, h, row0, L);
-        chunk_scan(p, s, L, S);
-        const float* O = s(bO);
-        const float* U = s(bU);
-        for (int idx = threadIdx.x; idx < L * p.dv; idx += blockDim.x) {
-            const int i = idx / p.dv, j = idx % p.dv;
-            const size_t e = ((size_t)(row0 + i) * p.H + h) * p.dv + j;
-            st_any(p.o, e, p.out_dtype, O[idx]);
-            if (p.u) st_any(p.u, e, p.out_dtype, U[idx]);  // the write beta r
-        }
-        __syncthreads();
-    }
-    if (p.hT)
-        for (int idx = threadIdx.x; idx < p.dk * p.dv; idx += blockDim.x)
-            p.hT[((size_t)n * p.H + h) * p.dk * p.dv + idx] = S[idx];
-}
-
 // Device address of g_noalloc_scratch, looked up once per device with that
-// device current.  The host-side name of the array is only a stand-in for the
-// symbol; the kernel must receive this address.
+// device current, and cached by device ordinal for the life of the process
+// (the address belongs to the device's primary context; it is not valid after
+// a cudaDeviceReset of that device, nor in another context made current on
+// it).  The host-side name of the array is only a stand-in for the symbol;
+// the kernel must receive this address.
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kMaxDevices] = {};
@@ -405,17 +391,24 @@ cudaError_t noalloc_scratch(float** out) {
 }
 }  // namespace
 
-// Largest number of (sequence, head) units the static scratch holds.
-int simt_noalloc_max_units() { return (int)(kNoAllocScratchBytes / (kNoAllocUnitFloats * sizeof(float))); }
+// Largest number of (sequence, head) units the static scratch holds for a problem
+// of these sizes (the forward keeps kNoAllocBufs matrices per unit).
+int simt_noalloc_max_units(int C, int dk, int dv) {
+    return (int)(kNoAllocScratchBytes /
+                 ((size_t)kNoAllocBufs * simt_buf_floats(C, dk, dv) * sizeof(float)));
+}
 
+// The forward kernel of this file over the static scratch, with the forward-only
+// per-unit stride.
 cudaError_t simt_fwd_noalloc(const Params& p, cudaStream_t st) {
     const int units = p.N * p.H;
     if (units == 0) return cudaSuccess;
     float* scratch = nullptr;
     cudaError_t e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return e;
+    const int buf = simt_buf_floats(p.C, p.dk, p.dv);
     TraceScope ts("simt_fwd_noalloc", st);
-    simt_fwd_noalloc_kernel<<<units, kThreads, 0, st>>>(p, scratch);
+    simt_fwd_kernel<<<units, kThreads, 0, st>>>(p, scratch, (size_t)kNoAllocBufs * buf, buf);
     return cudaGetLastError();
 }
 

@@ -9,7 +9,7 @@ namespace dr {
 namespace {
 
 constexpr int kSimtThreads = 256;
-constexpr int kBuf = 64 * 64;  // floats per scratch matrix (C, d_k, d_v <= 64)
+constexpr int kBuf = 64 * 64;  // floats per scratch matrix when C, d_k, d_v <= 64
 
 // C[m x n] = alpha * op(A) op(B) (+ C when acc).  op(A) is m x k.
 __device__ void mm(float* Cm, int ldc, const float* A, int lda, bool ta, const float* Bm,
@@ -200,9 +200,11 @@ __device__ void mm4(float* Cm, int ldc, const float* A, int lda, bool ta, const 
     __syncthreads();
 }
 
+// Matrix i of a CTA's scratch slice; `buf` floats per matrix.
 struct Scratch {
     float* base;
-    __device__ float* operator()(int i) const { return base + (size_t)i * kBuf; }
+    int buf;
+    __device__ float* operator()(int i) const { return base + (size_t)i * buf; }
 };
 
 __device__ void load_state(float* S, const float* h, int n, int hd, int H, int dk, int dv) {

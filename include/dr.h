@@ -94,7 +94,7 @@ enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
 /*
  * Problem descriptor.  Supported set:
  *   io bf16: d_k = d_v in {64, 128}, chunk = 64  (tensor-core path)
- *   io fp32: d_k, d_v in {16, 32, 64}, chunk in {16, 32, 64}  (fp32 CUDA-core path)
+ *   io fp32: d_k, d_v in {16, 32, 64, 128}, chunk in {16, 32, 64}  (fp32 CUDA-core path)
  *   any T >= 0 (a partial last chunk is fine), B >= 0, H >= 1.
  */
 typedef struct dr_desc {
@@ -190,11 +190,16 @@ int dr_bwd_u(const dr_desc* desc, const void* q, const void* k, const void* v,
  * inputs), but takes no workspace: its scratch is a 16 MiB array that the
  * library keeps in the global memory of every GPU that loads it, for the life
  * of the process.  It allocates nothing itself.
- *   - Size limit: N * H (sequences times heads) must not exceed 46; larger
+ *   - Size limit: N * H (sequences times heads) must not exceed 46 when d_k,
+ *     d_v and chunk are at most 64, or 11 when d_k or d_v is 128; larger
  *     problems return DR_ERR_SCRATCH_LIMIT and launch nothing.
  *   - The first call on each device looks up the array's device address with
  *     that device current (a runtime symbol query); make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device.  The address is cached per
+ *     device ordinal for the rest of the process: it belongs to the device's
+ *     primary context (the one the CUDA runtime uses), is not valid after a
+ *     cudaDeviceReset of that device, and must not be used from another
+ *     context made current on it.
  *   - Every call shares the one array: calls whose kernels can overlap on the
  *     GPU (other streams, other host threads) race on it and must be
  *     serialised by the caller.  Contents left by an earlier call are never

@@ -3,15 +3,26 @@ and the fp64 oracle on the same seeded inputs, and compare element by element.
 
 Tolerance (written here, used by every parity test):
   * fp32 inputs: max |gpu - oracle| <= 1e-4 on every output and gradient.
-  * bf16 inputs (fp32 accumulation, fp32-written outputs):
-        max |gpu - oracle| <= 2e-2 * max(1, max |oracle|)   per tensor,
-    i.e. 2e-2 absolute for tensors whose entries stay within +-1 and 2e-2
-    relative to the tensor's largest entry beyond that.  bf16 operands carry
-    a relative rounding of 2^-9 into every tensor-core product, so the error of
-    a large-magnitude gradient scales with its magnitude; the absolute error is
-    reported alongside in the failure message.
+  * bf16 inputs (fp32 accumulation, fp32-written outputs), per tensor:
+        max |gpu - oracle| <= max(2e-2, 1e-2 * max |oracle|)
+    i.e. the stated 2e-2 absolute for every tensor whose entries stay within +-2
+    (o, hT, dh0 and dv of every workload here), and 1e-2 of the tensor's
+    largest entry beyond that.  The bf16 path rounds every intermediate operand
+    of its tensor-core products (decayed keys and queries, the UT inverse, the
+    WY factors, the state, the writes and their gradients) to bf16, a relative
+    2^-9 each; the gradients dq, dk, dbeta, dg reach 10-90 at T = 4096 and
+    their measured full-size error is 3-7e-3 of the tensor's largest entry
+    (0.06-0.08 absolute for Gated DeltaNet and KDA, up to 0.46 for DeltaNet,
+    whose gradients grow largest).  The relative term is about 1.5x that
+    measured error: loose enough for rounding, tight enough that a dropped
+    term or a wrong index (errors of the size of the values) fails.
+Every comparison is recorded (absolute error, largest reference entry, bound)
+and summarised at the end of the run.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -20,6 +31,39 @@ import oracle
 from delta_rule_recurrent_gated_gb300 import binding, inputs
 
 FIELDS = ("o", "hT", "dq", "dk", "dv", "dbeta", "dg", "dh0")
+
+F32_ABS = 1e-4
+BF16_ABS = 2e-2
+BF16_REL = 1e-2
+
+# (test, workload, tensor, max abs error, max |reference|, bound) of every comparison
+RECORDS: list = []
+
+
+def record(w, name: str, err: float, ref_max: float, tol: float):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    RECORDS.append((test, w.name, w.io, name, float(err), float(ref_max), float(tol)))
+
+
+def summary_lines():
+    """Worst absolute error per (workload, tensor) over the recorded comparisons."""
+    worst = {}
+    for test, wname, io, name, err, rmax, tol in RECORDS:
+        key = (wname, io)
+        d = worst.setdefault(key, {})
+        if name not in d or err / tol > d[name][0] / d[name][2]:
+            d[name] = (err, rmax, tol)
+    out = []
+    for (wname, io), d in sorted(worst.items()):
+        parts = [f"{n} {e:.1e}/{t:.1e} (|ref| {r:.2g})" for n, (e, r, t) in d.items()]
+        out.append(f"{wname} [{io}]: " + "; ".join(parts))
+    log = os.environ.get("DR_PARITY_LOG")
+    if log:
+        with open(log, "w") as f:
+            for r in RECORDS:
+                f.write(json.dumps(dict(zip(("test", "workload", "io", "tensor", "max_abs_err",
+                                             "max_abs_ref", "bound"), r))) + "\n")
+    return out
 
 
 def to_dev(x, dev):
@@ -59,8 +103,17 @@ def run_oracle(w: inputs.Workload, x: dict, units=None, backward=True):
 
 def tolerance(w: inputs.Workload, ref: np.ndarray) -> float:
     if w.io == "f32":
-        return 1e-4
-    return 2e-2 * max(1.0, float(np.max(np.abs(ref))) if ref.size else 1.0)
+        return F32_ABS
+    return max(BF16_ABS, BF16_REL * (float(np.max(np.abs(ref))) if ref.size else 0.0))
+
+
+def check(w, name: str, got: np.ndarray, ref: np.ndarray):
+    """Max-abs error of one tensor against its bound, recorded; returns (err, tol)."""
+    assert np.all(np.isfinite(got)), f"{w.name} {name}: non-finite values"
+    err = float(np.max(np.abs(got.astype(np.float64) - ref))) if ref.size else 0.0
+    tol = tolerance(w, ref)
+    record(w, name, err, float(np.max(np.abs(ref))) if ref.size else 0.0, tol)
+    return err, tol
 
 
 def unit_mask(w, x, units, name, shape):
@@ -91,10 +144,8 @@ def compare(w, x, got: dict, ref: dict, units=None, fields=FIELDS):
         if units is not None:
             m = unit_mask(w, x, units, n, r.shape)
             r, g = r[m], g[m]
-        assert np.all(np.isfinite(g)), f"{n}: non-finite values"
-        err = float(np.max(np.abs(g.astype(np.float64) - r))) if r.size else 0.0
-        tol = tolerance(w, r)
-        report[n] = (err, tol)
+        err, tol = check(w, n, g, r)
+        report[n] = (err, tol, err / max(float(np.max(np.abs(r))) if r.size else 0.0, 1e-30))
     bad = {n: v for n, v in report.items() if not v[0] <= v[1]}
-    assert not bad, f"{w.name}: over tolerance (err, tol): {bad}; all: {report}"
+    assert not bad, f"{w.name}: over tolerance (abs err, bound, rel err): {bad}; all: {report}"
     return report

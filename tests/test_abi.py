@@ -70,7 +70,11 @@ def test_workspace_bytes(lib):
     assert B.workspace_bytes(desc(H=0)) == 0
     assert B.workspace_bytes(desc(d_k=96, d_v=96)) == 0          # unsupported
     assert B.workspace_bytes(desc(chunk=32)) == 0                 # bf16 path needs chunk 64
-    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=128, d_v=128, chunk=64)) == 0
+    # the fp32 CUDA-core path takes d_k, d_v up to 128 (chunk at most 64)
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=128, d_v=128, chunk=64)) > 0
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=128, d_v=16, chunk=16)) > 0
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=96, d_v=96, chunk=64)) == 0
+    assert B.workspace_bytes(desc(io_dtype=B.DR_F32, d_k=128, d_v=128, chunk=128)) == 0
 
 
 def call_fwd(d, ptrs=None, ws=None, ws_bytes=1 << 40):

@@ -68,3 +68,25 @@ def test_prepare_bytes(bench):
     assert b["prepare_rows"] == 4 * th * 128 * 2      # read q, k; write q_hat, k_hat
     assert b["chain_rows"] == 6 * th * 128 * 2        # read q, k, dq_hat, dk_hat; write dq, dk
     assert b["prepare_gates"] == 8 * (th + th * 128)  # beta and the per-channel gate, in and out
+
+
+@pytest.mark.parametrize("name", ["gdn_h0_b8_t4096_h16_d128", "kda_b8_t4096_h16_d128",
+                                  "sweep_deltanet_b16_t4096_h16_d128", "gdn_b4_t2048_h8_d64"])
+def test_kernel_shares_add_up_to_the_path_bytes(bench, name):
+    """Each kernel's share of the algorithmic bytes (what bench.py divides by the
+    kernel's own time) sums to the whole path's algorithmic bytes."""
+    w = inputs.get(name)
+    N = w.B
+    _, byts = bench.algorithmic(w, N)
+    parts = sum(bench.kernel_algorithmic_bytes(k, w, N)
+                for k in ("tc_prep", "tc_scan_fwd", "tc_scan_bwd", "tc_bwd_chunk"))
+    assert parts == byts
+    # tc_bwd_chunk of the headline: q, k, v, dO in; dq, dk, dv out (bf16); beta, g, dbeta, dg
+    if name == "gdn_h0_b8_t4096_h16_d128":
+        assert bench.kernel_algorithmic_bytes("tc_bwd_chunk", w, N) == 8 * 4096 * 16 * 1808
+
+
+def test_both_arms_share_the_config(bench):
+    w = inputs.get("gdn_h0_b8_t4096_h16_d128")
+    c = bench.config_of(w, 1)
+    assert c["chunk"] == 64 and c["seq_len"] == 4096 and c["heads"] == 16 and c["d_k"] == 128

@@ -11,7 +11,7 @@ import torch
 import oracle
 from delta_rule_recurrent_gated_gb300 import binding, inputs
 
-from parity import tolerance
+from parity import check
 
 pytestmark = pytest.mark.gpu
 
@@ -24,9 +24,7 @@ def _oracle(w, x):
 
 
 def _check(w, name, got, ref):
-    assert np.all(np.isfinite(got)), name
-    err = float(np.max(np.abs(got.astype(np.float64) - ref))) if ref.size else 0.0
-    tol = tolerance(w, ref)
+    err, tol = check(w, name, got, ref)
     assert err <= tol, f"{w.name} {name}: err {err} > tol {tol}"
 
 

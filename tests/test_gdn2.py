@@ -13,7 +13,7 @@ import torch
 import oracle
 from delta_rule_recurrent_gated_gb300 import binding, inputs
 
-from parity import tolerance
+from parity import check, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -48,10 +48,9 @@ def compare(w, got, ref):
     for n in FIELDS:
         r, g = ref[n], got[n]
         assert r.shape == g.shape, (n, r.shape, g.shape)
-        assert np.all(np.isfinite(g)), n
-        err = float(np.max(np.abs(g.astype(np.float64) - r))) if r.size else 0.0
-        if not err <= tolerance(w, r):
-            bad[n] = (err, tolerance(w, r))
+        err, tol = check(w, n, g, r)
+        if not err <= tol:
+            bad[n] = (err, tol)
     assert not bad, f"{w.name}: over tolerance {bad}"
 
 
@@ -122,8 +121,8 @@ def test_full_size_sampled():
         for name in FIELDS:
             r = ref[name][n, h] if name in ("hT", "dh0") else ref[name][n, :, h]
             g = got[name][n, h] if name in ("hT", "dh0") else got[name][n, :, h]
-            err = float(np.max(np.abs(g.astype(np.float64) - r)))
-            assert err <= tolerance(w, r), f"unit {u} {name}: err {err}"
+            err, tol = check(w, name, g, r)
+            assert err <= tol, f"unit {u} {name}: err {err}"
 
 
 @pytest.mark.parametrize("io,d", [("bf16", 128), ("f32", 64), ("f32", 16)])
@@ -148,8 +147,8 @@ def test_decode_steps_match_the_recurrence(io, d):
         torch.cuda.synchronize()
         o = torch.cat(outs, dim=1).cpu().numpy()
         for name, got, ref in (("o", o, o_ref), ("state", state.cpu().numpy(), h_ref)):
-            err = float(np.max(np.abs(got.astype(np.float64) - ref)))
-            assert err <= tolerance(w, ref), f"{name} per_token={per_token}: err {err}"
+            err, tol = check(w, name, got, ref)
+            assert err <= tol, f"{name} per_token={per_token}: err {err}"
 
 
 def test_bf16_gradients_and_rerun_bit_identical():

@@ -10,7 +10,7 @@ import torch
 import oracle
 from delta_rule_recurrent_gated_gb300 import binding, inputs
 
-from parity import tolerance
+from parity import check
 
 pytestmark = pytest.mark.gpu
 
@@ -46,10 +46,7 @@ def _compare(w, got, ref):
     for name, r in ref.items():
         if r is None:
             continue
-        gg = got[name]
-        assert np.all(np.isfinite(gg)), name
-        err = float(np.max(np.abs(gg.astype(np.float64) - r))) if r.size else 0.0
-        tol = tolerance(w, r)
+        err, tol = check(w, name, got[name], r)
         assert err <= tol, f"{w.name} {name}: err {err} > tol {tol}"
 
 

@@ -13,7 +13,7 @@ import torch
 from oracle import prepare as prep
 from delta_rule_recurrent_gated_gb300 import binding, inputs
 
-from parity import compare, run_gpu, tolerance
+from parity import check, compare, run_gpu, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -126,9 +126,8 @@ def test_prepared_decode_matches_the_recurrence(variant, io, d):
     torch.cuda.synchronize()
     o = torch.cat(outs, dim=1).cpu().numpy()
     for name, got, ref in (("o", o, o_ref), ("state", state.cpu().numpy(), h_ref)):
-        assert np.all(np.isfinite(got)), name
-        err = float(np.max(np.abs(got.astype(np.float64) - ref)))
-        assert err <= tolerance(w, ref), f"{w.name} {name}: err {err}"
+        err, tol = check(w, name, got, ref)
+        assert err <= tol, f"{w.name} {name}: err {err}"
 
 
 def _oracle_unit(w, x, n, h):
@@ -167,9 +166,7 @@ def test_prepared_full_size_sampled(name):
                 gg = got[fname][n:n + 1, h:h + 1]
             else:
                 gg = got[fname][rows, toks, h:h + 1]
-            assert np.all(np.isfinite(gg)), fname
-            err = float(np.max(np.abs(gg.astype(np.float64) - r)))
-            tol = tolerance(w, r)
+            err, tol = check(w, fname, gg, r)
             assert err <= tol, f"{name} seq {n} head {h} {fname}: err {err} > tol {tol}"
     torch.cuda.empty_cache()
 
