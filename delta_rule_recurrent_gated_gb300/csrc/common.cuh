@@ -43,7 +43,23 @@ struct Params {
     float *derase, *dwrite;      // their gradients (Gated DeltaNet-2)
     int* err;                 // device error word
     uint8_t* ws;              // workspace base
+    int prepare;              // tensor-core path: q, k, beta, g are raw (DR_FLAG_PREPARE_INPUTS)
 };
+
+// Input preparation of DR_FLAG_PREPARE_INPUTS, as the tensor-core kernels apply it on
+// the fly: q_hat = q rsqrt(sum q^2 + eps), beta = sigmoid(b), g = -softplus(x).
+constexpr float kPrepEps = 1e-6f;
+__device__ __forceinline__ float prep_sigmoid(float b) { return 1.f / (1.f + expf(-b)); }
+__device__ __forceinline__ float prep_neg_softplus(float x) {
+    return -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+}
+// Sum of x over an aligned group of N consecutive lanes (N a power of two, full warp).
+template <int N>
+__device__ __forceinline__ float lane_group_sum(float x) {
+#pragma unroll
+    for (int o = N / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
 
 // (sequence, first row, length) of global chunk `c`
 __device__ __forceinline__ void chunk_info(const Params& p, int c, int& seq, int& row0, int& len) {

@@ -107,10 +107,11 @@ size_t path_ws_bytes(const Params& p, Path path) {
     return kHeader + dr::tc_workspace_bytes(p);
 }
 
-// With DR_FLAG_PREPARE_INPUTS the prepared q, k, beta, g follow the path's area.
+// With DR_FLAG_PREPARE_INPUTS on the fp32 CUDA-core path the prepared q, k, beta, g
+// follow the path's area; the tensor-core kernels prepare their inputs on the fly.
 size_t ws_bytes(const Params& p, Path path, int flags) {
     const size_t base = path_ws_bytes(p, path);
-    if (!(flags & DR_FLAG_PREPARE_INPUTS)) return base;
+    if (!(flags & DR_FLAG_PREPARE_INPUTS) || path == Path::kTensor) return base;
     return align256(base) + dr::prepare_bytes(p);
 }
 
@@ -198,8 +199,12 @@ int fwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
         return DR_OK;
     }
     if (desc->flags & DR_FLAG_PREPARE_INPUTS) {
-        cudaError_t e = dr::prepare_inputs(p, p.ws + align256(path_ws_bytes(p, path)), st);
-        if (e != cudaSuccess) return DR_ERR_CUDA;
+        if (path == Path::kTensor) {
+            p.prepare = 1;  // the tensor-core kernels normalise and map on the fly
+        } else {
+            cudaError_t e = dr::prepare_inputs(p, p.ws + align256(path_ws_bytes(p, path)), st);
+            if (e != cudaSuccess) return DR_ERR_CUDA;
+        }
     }
     if (path == Path::kSimt) return cuda_status(dr::simt_fwd(p, st));
     return cuda_status(dr::tc_fwd(p, st, true));
@@ -235,8 +240,14 @@ int bwd_impl(const dr_desc* desc, const void* q, const void* k, const void* v, c
         if (dh0) return cuda_status(dr::state_passthrough(dhT, dh0, (size_t)p.N * p.H * p.dk * p.dv, st));
         return DR_OK;
     }
-    const bool prepare = (desc->flags & DR_FLAG_PREPARE_INPUTS) != 0;
     const bool reuse = (desc->flags & DR_FLAG_REUSE_FWD) != 0;
+    if ((desc->flags & DR_FLAG_PREPARE_INPUTS) && path == Path::kTensor) {
+        // the tensor-core kernels normalise and map the raw inputs on the fly and chain
+        // their gradients back to them before writing
+        p.prepare = 1;
+        return cuda_status(dr::tc_bwd(p, st, reuse));
+    }
+    const bool prepare = (desc->flags & DR_FLAG_PREPARE_INPUTS) != 0;
     Params raw = p;
     if (prepare) {
         // the path runs on the prepared tensors, then its gradients are chained back

@@ -14,6 +14,13 @@
 // then the decay: dq = dQb e^{Gamma}, dk = dKb e^{Gamma} + dKr e^{-Gamma} + dKC e^{Gamma_last-Gamma},
 // dGamma = dQb Qb + dKb Kb - dKr Kr - dKC KC (+ sum_i dKC KC + dgC e^{Gamma_last} at the
 // last token), dg = reverse cumulative sum of dGamma within the chunk.
+// As in the forward, the Gram-type operands take their exponents relative to Gamma_r
+// (the cumulative log-decay at the chunk's 32nd token): Qb' = q e^{Gamma - Gamma_r},
+// Kb' = k e^{Gamma - Gamma_r}, Kr' = k e^{Gamma_r - Gamma}.  The products with the
+// absolute Kb (dQt Kb^T, Kb dWy^T) use Kb' against dQt and dWy scaled by e^{Gamma_r} per
+// key channel, so every formula above holds with e^{Gamma} replaced by e^{Gamma -
+// Gamma_r}, e^{Gamma_last} by e^{Gamma_last - Gamma_r} (in dk and KC) and dQt, dWy, dbK by
+// their scaled forms; L does not depend on Gamma_r, so dg needs no term for it.
 //
 // Kernels: tc_scan_bwd (reverse over chunks, one CTA per (sequence, head, value
 // tile), dS kept in fp32 registers) and tc_bwd_chunk (chunk-parallel: first the
@@ -287,9 +294,11 @@ struct BChunkSmem {
     static constexpr int kX = kGam + (VAR == DR_KDA ? 64 * kGS * 4 : 0);  // fp32 scratch, 8 KB
     static constexpr int kSmall = kX + 8192;
     // small arrays: beta[64], e^{Gamma_last}[2][D] (this item's and the next one's),
-    // dgC[D], dGamma per row[64], e^{Gamma} per row[64], e^{-Gamma} per row[64], dbeta
-    // partials of the other warp groups [3][64]
-    static constexpr int kBytes = kSmall + (64 * 7 + D * 3) * 4 + 1024;
+    // dgC[D], dGamma per row[64], e^{Gamma - Gamma_r} per row[64], e^{Gamma_r - Gamma} per
+    // row[64], dbeta partials of the other warp groups [3][64], e^{Gamma_r}[D],
+    // e^{Gamma_last - Gamma_r}[D], and with input preparation the inverse norms of the q and
+    // k rows [2][64], GDN's sigmoid of the raw gate arguments [64]
+    static constexpr int kBytes = kSmall + (64 * 10 + D * 5) * 4 + 1024;
 };
 
 // Sum over the 32 lanes of v[lane][k] for every k < N (N = 16 or 32): on return lane
@@ -344,6 +353,72 @@ __device__ __forceinline__ void stage_copy_out(void* out, const uint8_t* lo, con
     }
 }
 
+// The same copy-out for the gradient of a normalised input (DR_FLAG_PREPARE_INPUTS): the
+// staged rows hold dL/dx_hat of x_hat = x rsqrt(sum x^2 + eps); each row is chained to
+// dL/dx = r (dx_hat - x_hat (x_hat . dx_hat)), r = rinv[row], from the raw bf16 row x.
+// The kChunks threads of a row are consecutive lanes of one warp and sum the dot product
+// by shuffles, so every thread runs every pass (rows past `len` are not written).
+template <int D, bool F32>
+__device__ __forceinline__ void stage_copy_out_prep(void* out, const uint8_t* lo, const uint8_t* hi,
+                                                    const Params& p, int row0, int len, int h,
+                                                    const __nv_bfloat16* __restrict__ raw,
+                                                    const float* rinv) {
+    constexpr int kRow = D * (F32 ? 4 : 2), kChunks = kRow / 16, E = F32 ? 4 : 8;
+    constexpr int kPass = 64 * kChunks / kChunkThreads;
+    static_assert(kPass * kChunkThreads == 64 * kChunks && kChunks <= 32, "whole warps per pass");
+    // every raw row piece is loaded before the first store (they may not be reordered past it)
+    float x[kPass][E];
+#pragma unroll
+    for (int ps = 0; ps < kPass; ++ps) {
+        const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
+        const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
+        if (i >= len) {
+#pragma unroll
+            for (int j = 0; j < E; ++j) x[ps][j] = 0.f;
+        } else if constexpr (F32) {
+            const uint2 u = *reinterpret_cast<const uint2*>(raw + e0);
+            const uint32_t wv[2] = {u.x, u.y};
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
+                x[ps][2 * j] = __low2float(b);
+                x[ps][2 * j + 1] = __high2float(b);
+            }
+        } else {
+            unpack8(*reinterpret_cast<const uint4*>(raw + e0), x[ps]);
+        }
+    }
+#pragma unroll
+    for (int ps = 0; ps < kPass; ++ps) {
+        const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
+        const uint8_t* src = (i < 32 ? lo + i * kRow : hi + (i - 32) * kRow) + c * 16;
+        const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
+        float d[E];
+        if constexpr (F32) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        } else {
+            unpack8(*reinterpret_cast<const uint4*>(src), d);
+        }
+        float xd = 0.f;
+#pragma unroll
+        for (int j = 0; j < E; ++j) xd = fmaf(x[ps][j], d[j], xd);
+        xd = lane_group_sum<kChunks>(xd);
+        const float r = rinv[i], f = r * r * xd;  // (x_hat . dx_hat) / |x|
+#pragma unroll
+        for (int j = 0; j < E; ++j) d[j] = r * (d[j] - x[ps][j] * f);
+        if (i < len) {
+            uint8_t* dst = static_cast<uint8_t*>(out) + e0 * (F32 ? 4 : 2);
+            if constexpr (F32) {
+                *reinterpret_cast<float4*>(dst) = make_float4(d[0], d[1], d[2], d[3]);
+            } else {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]),
+                                                            pack_bf16(d[4], d[5]), pack_bf16(d[6], d[7]));
+            }
+        }
+    }
+}
+
 // Buffer roles of one work item.  Even items: q in P0, U^T in P4 (then dQt^T), dS in
 // P5..P6 (then Kb in P5, dWy^T in P6), -dU^T in P7.  Odd items: q in P5, U^T in P0 (then
 // Kb), dS in P6..P7 (then dQt^T in P6, dWy^T in P7), -dU^T in P4.  What an even item
@@ -358,7 +433,7 @@ __device__ __forceinline__ ChunkRoles chunk_roles(uint8_t* sm, int kTile, bool o
     return ChunkRoles{P(0), P(4), P(4), P(5), P(5), P(6), P(7)};
 }
 
-template <int D, int VAR>
+template <int D, int VAR, bool PREP>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -381,9 +456,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     float* gC_b = beta_s + 64;    // [2][D]
     float* dgC_s = gC_b + 2 * D;
     float* rowsum = dgC_s + D;    // GDN: dGamma per row
-    float* Erow = rowsum + 64;    // GDN: e^{Gamma} per row
-    float* Eirow = Erow + 64;     // GDN: e^{-Gamma} per row
+    float* Erow = rowsum + 64;    // GDN: e^{Gamma - Gamma_r} per row
+    float* Eirow = Erow + 64;     // GDN: e^{Gamma_r - Gamma} per row
     float* part = Eirow + 64;     // [3][64] dbeta partials of warp groups 1..
+    float* eref = part + 3 * 64;  // [D] e^{Gamma_r} per key channel
+    float* gcr = eref + D;        // [D] e^{Gamma_last - Gamma_r} per key channel
+    float* rq_s = gcr + D;        // [64] rsqrt(sum q^2 + eps) per token (input preparation)
+    float* rk_s = rq_s + 64;      // [64] the same for k
+    float* sgx = rk_s + 64;       // GDN, input preparation: sigmoid(x) per token
     __shared__ uint64_t bar_st, bar_tok, bar_mma;
     __shared__ uint32_t tmem_base;
 
@@ -526,18 +606,27 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     };
     // per-token scalars of an item, read into registers ahead of time: beta (threads
     // 64..127) and GDN's log-decays (two per lane of warp 1)
-    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f;
+    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f, sx0 = 0.f, sx1 = 0.f;
     auto load_scalars = [&](int itm) {
         const int c = itm / p.H, hh = itm % p.H;
         int sq, r0, ln;
         chunk_info(p, c, sq, r0, ln);
         beta_ld = (tid >= 64 && tid < 128 && tid - 64 < ln) ? p.beta[(size_t)(r0 + tid - 64) * p.H + hh] : 0.f;
+        if (PREP && tid >= 64 && tid < 128 && tid - 64 < ln) beta_ld = prep_sigmoid(beta_ld);
         if (VAR == DR_GDN && warp == 1) {
             gl0 = 2 * lane < ln ? p.g[(size_t)(r0 + 2 * lane) * p.H + hh] : 0.f;
             gl1 = 2 * lane + 1 < ln ? p.g[(size_t)(r0 + 2 * lane + 1) * p.H + hh] : 0.f;
+            if (PREP) {
+                sx0 = prep_sigmoid(gl0);
+                sx1 = prep_sigmoid(gl1);
+                gl0 = 2 * lane < ln ? prep_neg_softplus(gl0) : 0.f;
+                gl1 = 2 * lane + 1 < ln ? prep_neg_softplus(gl1) : 0.f;
+            }
         }
     };
     uint32_t n_st = 0, n_tok = 0;  // copy groups issued on bar_st / bar_tok
+    if (VAR == DR_DELTANET)  // no decay: the reference factors are 1 for every item
+        for (int c = tid; c < D; c += kChunkThreads) eref[c] = gcr[c] = 1.f;
     if ((int)blockIdx.x < nitems) {
         load_scalars(blockIdx.x);
         if (tid == 0) {
@@ -583,7 +672,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const int c = tid % D, pt = tid / D;
             float v[kR];
 #pragma unroll
-            for (int t = 0; t < kR; ++t) v[t] = Gam[(pt * kR + t) * S::kGS + c];
+            for (int t = 0; t < kR; ++t) {
+                v[t] = Gam[(pt * kR + t) * S::kGS + c];
+                if (PREP) v[t] = prep_neg_softplus(v[t]);  // rows past the end are not added
+            }
             float G = 0.f;
 #pragma unroll
             for (int t = 0; t < kR; ++t) {
@@ -601,11 +693,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
-                const float e0 = __expf(x - gl1), e1 = __expf(x);
-                Erow[2 * lane] = e0;
-                Erow[2 * lane + 1] = e1;
-                Eirow[2 * lane] = fast_rcp(e0);
-                Eirow[2 * lane + 1] = fast_rcp(e1);
+                const float G_r = __shfl_sync(0xffffffffu, x, 15);  // Gamma at token 31
+                const float GL = __shfl_sync(0xffffffffu, x, 31);
+                const float x0 = x - gl1;
+                Erow[2 * lane] = __expf(x0 - G_r);
+                Erow[2 * lane + 1] = __expf(x - G_r);
+                Eirow[2 * lane] = __expf(G_r - x0);
+                Eirow[2 * lane + 1] = __expf(G_r - x);
+                const float er = expf(G_r), lr = expf(GL - G_r);
+                for (int c = lane; c < D; c += 32) {
+                    eref[c] = er;
+                    gcr[c] = lr;
+                }
+                if (PREP) {
+                    sgx[2 * lane] = sx0;
+                    sgx[2 * lane + 1] = sx1;
+                }
             }
         }
         __syncthreads();
@@ -619,7 +722,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
             const uint32_t off = sw128_offset(i, c8, 64);
             const uint4 kv = *reinterpret_cast<const uint4*>(Ks + off);
-            if (VAR == DR_DELTANET) {
+            if (VAR == DR_DELTANET && !PREP) {
                 kbr[n] = kv;
                 continue;
             }
@@ -627,22 +730,58 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             float q8[8], k8[8], e8[8], i8[8];
             unpack8(qv, q8);
             unpack8(kv, k8);
-            if (VAR == DR_KDA) {
+            if (PREP) {  // L2-normalise the raw rows; keep the inverse norms for the chain
+                float sq = 0.f, sk = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    sq = fmaf(q8[j], q8[j], sq);
+                    sk = fmaf(k8[j], k8[j], sk);
+                }
+                const float rq = rsqrtf(lane_group_sum<D / 8>(sq) + kPrepEps);
+                const float rk = rsqrtf(lane_group_sum<D / 8>(sk) + kPrepEps);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    q8[j] *= rq;
+                    k8[j] *= rk;
+                }
+                if (c8 == 0) {
+                    rq_s[i] = rq;
+                    rk_s[i] = rk;
+                }
+            }
+            if (VAR == DR_DELTANET) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e8[j] = i8[j] = 1.f;
+            } else if (VAR == DR_KDA) {
                 float4* gp = reinterpret_cast<float4*>(&Gam[i * S::kGS + c8]);
                 const float4 g0 = gp[0], g1 = gp[1];
                 float G8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                for (int q = 0; q < i / kR; ++q) {  // totals of the row blocks above
+                float R8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // Gamma_r
+                float L8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // Gamma_last
+                for (int q = 0; q < kP; ++q) {  // totals of the row blocks
                     const float4* tp = reinterpret_cast<const float4*>(tot + q * D + c8);
                     const float4 t0v = tp[0], t1v = tp[1];
-                    G8[0] += t0v.x, G8[1] += t0v.y, G8[2] += t0v.z, G8[3] += t0v.w;
-                    G8[4] += t1v.x, G8[5] += t1v.y, G8[6] += t1v.z, G8[7] += t1v.w;
+                    const float T8[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (q < i / kR) G8[j] += T8[j];   // the blocks above this row
+                        if (q < 32 / kR) R8[j] += T8[j];  // the first 32 rows
+                        L8[j] += T8[j];
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    e8[j] = __expf(G8[j]);
+                    e8[j] = __expf(G8[j] - R8[j]);
                     i8[j] = fast_rcp(e8[j]);
                 }
-                gp[0] = make_float4(e8[0], e8[1], e8[2], e8[3]);  // e^Gamma from here on
+                if (i == 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        eref[c8 + j] = expf(R8[j]);
+                        gcr[c8 + j] = expf(L8[j] - R8[j]);
+                    }
+                }
+                gp[0] = make_float4(e8[0], e8[1], e8[2], e8[3]);  // e^{Gamma - Gamma_r} from here on
                 gp[1] = make_float4(e8[4], e8[5], e8[6], e8[7]);
             } else {
                 const float e = Erow[i], ei = Eirow[i];
@@ -715,8 +854,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int q = 0; q < 128 / (D / 8); ++q) a += Xs[q * D + c];
             dgC_s[c] = a;
         }
-        // E0: Kb into its tile; dQt^T -> its tile (U^T is consumed), -dWyA^T -> the dWy
-        // tile (dS is consumed)
+        // E0: Kb' into its tile; dQt^T -> its tile (U^T is consumed), -dWyA^T -> the dWy
+        // tile (dS is consumed), both scaled by e^{Gamma_r} of their key channel
 #pragma unroll
         for (int n = 0; n < kPer; ++n) {
             const int w = tid + n * kChunkThreads;
@@ -729,6 +868,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tmem_ld16(tl + C1 + t0 + 16 * b, c_);
             tmem_ld_wait();
             if (cl >= 0) {
+                if (VAR != DR_DELTANET) {
+                    const float er = eref[cl];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        a[j] *= er;
+                        c_[j] *= er;
+                    }
+                }
                 tile_store16(dQs, cl, t0 + 16 * b, D, a);
                 tile_store16(dWys, cl, t0 + 16 * b, D, c_);
             }
@@ -925,7 +1072,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // sequence have zero q and k rows, so they add nothing to dGamma.
         auto dq_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
-            const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+            const float gc = cl >= 0 ? gcr[cl] : 0.f;  // e^{Gamma_last - Gamma_r}
             uint8_t* sb0 = stage_base(dUts, dWys, F32);
 #pragma unroll 1
             for (int b = 0; b < kTok / 8; ++b) {
@@ -975,8 +1122,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 const float br = beta_s[r];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float dA = (cb * 16 + j < r) ? -a[j] : 0.f;
-                    dbeta_acc = fmaf(dA, gm[j], dbeta_acc);
+                    const bool low = cb * 16 + j < r;  // the Gram above the diagonal may be inf
+                    const float dA = low ? -a[j] : 0.f;
+                    if (low) dbeta_acc = fmaf(dA, gm[j], dbeta_acc);
                     a[j] = br * dA;  // dG
                 }
                 tile_store16(B8b, r, cb * 16, 64, a);
@@ -1000,9 +1148,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         if (grp == 0 && r >= 0 && r < len) {
             float db = dbeta_acc;
             for (int q = 1; q < kG; ++q) db += part[(q - 1) * 64 + r];
+            if (PREP) db *= beta_s[r] * (1.f - beta_s[r]);  // through beta = sigmoid(b)
             p.dbeta[(size_t)(row0 + r) * p.H + h] = db;
         }
-        if (f32out)
+        if (PREP) {
+            const __nv_bfloat16* rawq = static_cast<const __nv_bfloat16*>(p.q);
+            if (f32out)
+                stage_copy_out_prep<D, true>(p.dq, dUts, dWys, p, row0, len, h, rawq, rq_s);
+            else
+                stage_copy_out_prep<D, false>(p.dq, dUts, dWys, p, row0, len, h, rawq, rq_s);
+        } else if (f32out)
             stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
         else
             stage_copy_out<D, false>(p.dq, dUts, dWys, p, row0, len, h);
@@ -1019,7 +1174,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // in the v / dO tiles (consumed), and the dKb Kb - dKr Kr part of dGamma
         auto dk_stage = [&](auto f32) {
             constexpr bool F32 = decltype(f32)::value;
-            const float gc = cl >= 0 ? gC_s[cl] : 0.f;
+            const float gc = cl >= 0 ? gcr[cl] : 0.f;  // e^{Gamma_last - Gamma_r}
             uint8_t* sb0 = stage_base(Vs, dOs, F32);
 #pragma unroll 1
             for (int b = 0; b < kTok / 8; ++b) {
@@ -1054,7 +1209,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         else
             dk_stage(BoolTag<false>{});
         __syncthreads();
-        if (f32out)
+        if (PREP) {
+            const __nv_bfloat16* rawk = static_cast<const __nv_bfloat16*>(p.k);
+            if (f32out)
+                stage_copy_out_prep<D, true>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s);
+            else
+                stage_copy_out_prep<D, false>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s);
+        } else if (f32out)
             stage_copy_out<D, true>(p.dk_, Vs, dOs, p, row0, len, h);
         else
             stage_copy_out<D, false>(p.dk_, Vs, dOs, p, row0, len, h);
@@ -1097,10 +1258,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 for (int q = 0; q < kG; ++q) run += fq[q * D + cl];
                 for (int q = grp + 1; q < kG; ++q) run += sgq[q * D + cl];
 #pragma unroll
+                float sx[PREP ? kTok : 1];  // sigmoid of the raw gate arguments
+                if (PREP) {
+#pragma unroll
+                    for (int k = 0; k < kTok; ++k) {
+                        const int i = t0 + k;
+                        sx[k] = i < len ? __ldg(p.g + ((size_t)(row0 + i) * p.H + h) * D + cl) : 0.f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kTok; ++k) sx[k] = prep_sigmoid(sx[k]);
+                }
+#pragma unroll
                 for (int k = kTok - 1; k >= 0; --k) {
                     const int i = t0 + k;
                     run += dG[k];
-                    if (i < len) p.dg[((size_t)(row0 + i) * p.H + h) * D + cl] = run;
+                    // through g = -softplus(x): dx = -dg sigmoid(x)
+                    if (i < len) p.dg[((size_t)(row0 + i) * p.H + h) * D + cl] = PREP ? -run * sx[PREP ? k : 0] : run;
                 }
             }
         } else if (VAR == DR_GDN) {
@@ -1130,8 +1303,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                     const float y = __shfl_down_sync(0xffffffffu, x, o);
                     if (lane + o < 32) x += y;
                 }
-                if (2 * lane < len) p.dg[(size_t)(row0 + 2 * lane) * p.H + h] = e + x;
-                if (2 * lane + 1 < len) p.dg[(size_t)(row0 + 2 * lane + 1) * p.H + h] = e + x - a0;
+                const size_t g0 = (size_t)(row0 + 2 * lane) * p.H + h, g1 = g0 + p.H;
+                // through g = -softplus(x): dx = -dg sigmoid(x), sigmoid(x) kept by the scan
+                if (2 * lane < len) p.dg[g0] = PREP ? -(e + x) * sgx[2 * lane] : e + x;
+                if (2 * lane + 1 < len) p.dg[g1] = PREP ? -(e + x - a0) * sgx[2 * lane + 1] : e + x - a0;
             }
         }
         tc_fence_before();
@@ -1231,14 +1406,20 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         }
         return cudaGetLastError();
     };
-    static std::atomic<unsigned long long> a0{0}, a1{0}, a2{0};
-    switch (p.variant) {
-        case DR_DELTANET:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET>, BChunkSmem<D, DR_DELTANET>::kBytes, a0);
-        case DR_GDN:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN>, BChunkSmem<D, DR_GDN>::kBytes, a1);
+    static std::atomic<unsigned long long> a0{0}, a1{0}, a2{0}, a3{0}, a4{0}, a5{0};
+    switch (p.variant * 2 + (p.prepare ? 1 : 0)) {
+        case 2 * DR_DELTANET:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET, false>, BChunkSmem<D, DR_DELTANET>::kBytes, a0);
+        case 2 * DR_DELTANET + 1:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET, true>, BChunkSmem<D, DR_DELTANET>::kBytes, a3);
+        case 2 * DR_GDN:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN, false>, BChunkSmem<D, DR_GDN>::kBytes, a1);
+        case 2 * DR_GDN + 1:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN, true>, BChunkSmem<D, DR_GDN>::kBytes, a4);
+        case 2 * DR_KDA:
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA, false>, BChunkSmem<D, DR_KDA>::kBytes, a2);
         default:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA>, BChunkSmem<D, DR_KDA>::kBytes, a2);
+            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA, true>, BChunkSmem<D, DR_KDA>::kBytes, a5);
     }
 }
 

@@ -9,6 +9,13 @@
 //   T  = (I + diag(beta) strict_lower(Kb Kr^T))^{-1}          (the UT inverse)
 //   Wy = T diag(beta) Kb,  Ut = T diag(beta) v,  Aqk = tril(Qb Kr^T)
 //   Qt = scale (Qb - Aqk Wy),  Ot = scale Aqk Ut
+// The two Gram-type products (Kb Kr^T, Qb Kr^T) only need the decay between two
+// tokens, e^{Gamma_i - Gamma_j}, so their operands take the exponents relative to
+// Gamma_r, the cumulative log-decay at the chunk's 32nd token: Kb' = k e^{Gamma -
+// Gamma_r}, Kr' = k e^{Gamma_r - Gamma}, Qb' = q e^{Gamma - Gamma_r}.  Each factor
+// then spans only the decay of one half-chunk (its exponent stays within the fp32
+// range while each 32-token half decays by less than e^{-87}); Wy and Qt use the
+// absolute e^{Gamma} <= 1.
 // and, from the state S at the chunk start (W = S^T),
 //   U = Ut - Wy S  (the writes beta r),  O = Qt S + Ot,
 //   S_next = diag(e^{Gamma_last}) S + KC^T U.
@@ -59,11 +66,31 @@ struct PrepSmem {
     // fp32 blocks of the inverse (12 KB): the consumed Kr tile when it is large enough
     static constexpr int kInv = (D == 128) ? kK : kT + 8192 + 16384;
     static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384 + 12288;
-    static constexpr int kGL = kBeta + 256;              // [D] fp32 Gamma at the last token
-    static constexpr int kBytes = kGL + D * 4 + 1024;    // + alignment slack
+    static constexpr int kGL = kBeta + 256;              // [D] fp32 e^{Gamma_last - Gamma_r}
+    static constexpr int kRf = kGL + D * 4;              // [D] fp32 e^{Gamma_r}; then Gamma_r (KDA)
+    static constexpr int kBytes = kRf + 2 * D * 4 + 1024;  // + alignment slack
 };
 
-template <int D, int VAR>
+// q8, k8: eight channels of one token row, whose D / 8 lanes are consecutive in the warp;
+// scaled in place to the L2-normalised row (DR_FLAG_PREPARE_INPUTS).
+template <int D>
+__device__ __forceinline__ void normalize_row8(float (&q8)[8], float (&k8)[8]) {
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        sq = fmaf(q8[j], q8[j], sq);
+        sk = fmaf(k8[j], k8[j], sk);
+    }
+    const float rq = rsqrtf(lane_group_sum<D / 8>(sq) + kPrepEps);
+    const float rk = rsqrtf(lane_group_sum<D / 8>(sk) + kPrepEps);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        q8[j] *= rq;
+        k8[j] *= rk;
+    }
+}
+
+template <int D, int VAR, bool PREP>
 __global__ void __launch_bounds__(128, 1)
     tc_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mg,
@@ -82,6 +109,8 @@ __global__ void __launch_bounds__(128, 1)
     float* Af = reinterpret_cast<float*>(sm + S::kAf);
     float* beta_s = reinterpret_cast<float*>(sm + S::kBeta);
     float* GLs = reinterpret_cast<float*>(sm + S::kGL);
+    float* Rf = reinterpret_cast<float*>(sm + S::kRf);   // e^{Gamma_r} per key channel
+    float* Gr = Rf + D;                                  // KDA: Gamma_r per key channel
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base;
 
@@ -125,7 +154,10 @@ __global__ void __launch_bounds__(128, 1)
             }
             if (VAR == DR_KDA) tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
         }
-        if (tid < 64) beta_s[tid] = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
+        if (tid < 64) {
+            const float b = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
+            beta_s[tid] = tid < len ? (PREP ? prep_sigmoid(b) : b) : 0.f;
+        }
         ok = mbar_wait(&bar_ld, 0, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
 
@@ -143,16 +175,20 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
 
         // decay, per token (DeltaNet, GDN): warp 0 scans the 64 log-decays, two per lane, and
-        // keeps e^{Gamma}, e^{-Gamma} and e^{Gamma_last - Gamma} per token in the still-unused
-        // Aqk tile; then an elementwise pass eight channels wide
+        // keeps e^{Gamma - Gamma_r}, e^{Gamma_r - Gamma}, e^{Gamma_last - Gamma} and e^{Gamma}
+        // per token in the still-unused Aqk tile; then an elementwise pass eight channels wide
         if (VAR != DR_KDA) {
-            float* Er = reinterpret_cast<float*>(Aqs);  // [3][64]
+            float* Er = reinterpret_cast<float*>(Aqs);  // [4][64]
             if (warp == 0) {
                 const int lane = tid & 31;
                 float a0 = 0.f, a1 = 0.f;
                 if (VAR == DR_GDN) {
                     a0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
                     a1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+                    if (PREP) {
+                        a0 = 2 * lane < len ? prep_neg_softplus(a0) : 0.f;
+                        a1 = 2 * lane + 1 < len ? prep_neg_softplus(a1) : 0.f;
+                    }
                 }
                 float x = a0 + a1;
 #pragma unroll
@@ -161,17 +197,22 @@ __global__ void __launch_bounds__(128, 1)
                     if (lane >= o) x += y;
                 }
                 const float GL = __shfl_sync(0xffffffffu, x, 31);
-                const float eGL = VAR != DR_DELTANET ? expf(GL) : 1.f;
-                const float e0 = VAR != DR_DELTANET ? __expf(x - a1) : 1.f;
-                const float e1 = VAR != DR_DELTANET ? __expf(x) : 1.f;
-                const float i0 = fast_rcp(e0), i1 = fast_rcp(e1);
-                Er[2 * lane] = e0;
-                Er[2 * lane + 1] = e1;
-                Er[64 + 2 * lane] = i0;
-                Er[64 + 2 * lane + 1] = i1;
-                Er[128 + 2 * lane] = eGL * i0;
-                Er[128 + 2 * lane + 1] = eGL * i1;
-                for (int c = lane; c < D; c += 32) L.gC[rec * D + c] = eGL;  // e^{Gamma_last}
+                const float G_r = __shfl_sync(0xffffffffu, x, 15);  // Gamma at token 31
+                const bool dec = VAR != DR_DELTANET;
+                const float x0 = x - a1;
+                Er[2 * lane] = dec ? __expf(x0 - G_r) : 1.f;
+                Er[2 * lane + 1] = dec ? __expf(x - G_r) : 1.f;
+                Er[64 + 2 * lane] = dec ? __expf(G_r - x0) : 1.f;
+                Er[64 + 2 * lane + 1] = dec ? __expf(G_r - x) : 1.f;
+                Er[128 + 2 * lane] = dec ? __expf(GL - x0) : 1.f;
+                Er[128 + 2 * lane + 1] = dec ? __expf(GL - x) : 1.f;
+                Er[192 + 2 * lane] = dec ? __expf(x0) : 1.f;
+                Er[192 + 2 * lane + 1] = dec ? __expf(x) : 1.f;
+                const float eGL = dec ? expf(GL) : 1.f, eGr = dec ? expf(G_r) : 1.f;
+                for (int c = lane; c < D; c += 32) {
+                    L.gC[rec * D + c] = eGL;  // e^{Gamma_last}
+                    Rf[c] = eGr;
+                }
             }
             __syncthreads();
             uint8_t* kc_img = L.KC + rec * kTile;
@@ -182,7 +223,9 @@ __global__ void __launch_bounds__(128, 1)
                 unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
                 unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
                 unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
-                const float b = beta_s[i], e = Er[i], ei = Er[64 + i], ec = Er[128 + i];
+                if (PREP) normalize_row8<D>(q8, k8);
+                const float b = beta_s[i], e = Er[i], ei = Er[64 + i], ec = Er[128 + i],
+                            ea = Er[192 + i];
                 uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -190,7 +233,7 @@ __global__ void __launch_bounds__(128, 1)
                     wq[j] = pack_bf16(q8[2 * j] * e, q8[2 * j + 1] * e);
                     wr[j] = pack_bf16(k0 * ei, k1 * ei);
                     wb[j] = pack_bf16(k0 * e, k1 * e);
-                    wy[j] = pack_bf16(b * k0 * e, b * k1 * e);
+                    wy[j] = pack_bf16(b * k0 * ea, b * k1 * ea);
                     wv[j] = pack_bf16(b * v8[2 * j], b * v8[2 * j + 1]);
                     wc[j] = pack_bf16(k0 * ec, k1 * ec);
                 }
@@ -204,8 +247,9 @@ __global__ void __launch_bounds__(128, 1)
         } else
         // decay, per key channel (KDA): the gates arrive 32 tokens at a time in the
         // still-unused Aqk / T tiles; thread c carries its channel's cumulative log-decay
-        // through both halves in place, then an elementwise pass eight channels wide.  KC =
-        // Kr e^{Gamma_last} is written once the last token's Gamma is known.
+        // through both halves in place (Gamma_r is its value after the first half), then an
+        // elementwise pass eight channels wide.  KC = Kr' e^{Gamma_last - Gamma_r} is written
+        // once the last token's Gamma is known.
         {
             float* Gb = reinterpret_cast<float*>(Aqs);  // [32][D] fp32
             float G = 0.f;
@@ -223,37 +267,52 @@ __global__ void __launch_bounds__(128, 1)
                 if (tid < D) {
 #pragma unroll 8
                     for (int ii = 0; ii < 32; ++ii) {
-                        if (32 * half + ii < len) G += Gb[ii * D + tid];
+                        if (32 * half + ii < len)
+                            G += PREP ? prep_neg_softplus(Gb[ii * D + tid]) : Gb[ii * D + tid];
                         Gb[ii * D + tid] = G;
+                    }
+                    if (half == 0) {
+                        Gr[tid] = G;
+                        Rf[tid] = expf(G);
                     }
                 }
                 __syncthreads();
                 for (int w = tid; w < 32 * (D / 8); w += 128) {
                     const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
                     const uint32_t off = sw128_offset(i, c8, 64);
-                    float q8[8], k8[8], v8[8], G8[8];
+                    float q8[8], k8[8], v8[8], G8[8], R8[8], E8[8];
                     unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
                     unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
                     unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
+                    if (PREP) normalize_row8<D>(q8, k8);
                     const float b = beta_s[i];
                     const float4* gp = reinterpret_cast<const float4*>(&Gb[ii * D + c8]);
                     const float4 g0 = gp[0], g1 = gp[1];
                     G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
                     G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
+                    const float4* rp = reinterpret_cast<const float4*>(&Gr[c8]);
+                    const float4 r0 = rp[0], r1 = rp[1];
+                    R8[0] = r0.x; R8[1] = r0.y; R8[2] = r0.z; R8[3] = r0.w;
+                    R8[4] = r1.x; R8[5] = r1.y; R8[6] = r1.z; R8[7] = r1.w;
+                    const float4* ep = reinterpret_cast<const float4*>(&Rf[c8]);
+                    const float4 f0 = ep[0], f1 = ep[1];
+                    E8[0] = f0.x; E8[1] = f0.y; E8[2] = f0.z; E8[3] = f0.w;
+                    E8[4] = f1.x; E8[5] = f1.y; E8[6] = f1.z; E8[7] = f1.w;
                     uint32_t wq[4], wr[4], wb[4], wy[4], wv[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        float e[2], ei[2];
+                        float e[2], ei[2], ea[2];
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            e[t] = __expf(G8[2 * j + t]);
+                            e[t] = __expf(G8[2 * j + t] - R8[2 * j + t]);  // e^{Gamma - Gamma_r}
                             ei[t] = fast_rcp(e[t]);
+                            ea[t] = e[t] * E8[2 * j + t];                   // e^{Gamma}
                         }
                         const float k0 = k8[2 * j], k1 = k8[2 * j + 1];
                         wq[j] = pack_bf16(q8[2 * j] * e[0], q8[2 * j + 1] * e[1]);
                         wr[j] = pack_bf16(k0 * ei[0], k1 * ei[1]);
                         wb[j] = pack_bf16(k0 * e[0], k1 * e[1]);
-                        wy[j] = pack_bf16(b * k0 * e[0], b * k1 * e[1]);
+                        wy[j] = pack_bf16(b * k0 * ea[0], b * k1 * ea[1]);
                         wv[j] = pack_bf16(b * v8[2 * j], b * v8[2 * j + 1]);
                     }
                     *reinterpret_cast<uint4*>(Qs + off) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
@@ -267,9 +326,8 @@ __global__ void __launch_bounds__(128, 1)
             }
             if (!ok) break;
             if (tid < D) {
-                const float eGL = expf(G);  // e^{Gamma_last} per channel
-                L.gC[rec * D + tid] = eGL;
-                GLs[tid] = eGL;
+                L.gC[rec * D + tid] = expf(G);   // e^{Gamma_last} per channel
+                GLs[tid] = expf(G - Gr[tid]);    // e^{Gamma_last - Gamma_r}
             }
             __syncthreads();
             uint8_t* kc_img = L.KC + rec * kTile;
@@ -462,9 +520,9 @@ __global__ void __launch_bounds__(128, 1)
                 tmem_ld16(tl + cb * 16, w16);
                 tmem_ld_wait();
                 if (r >= 0) {
-                    tile_load16(Qs, r, cb * 16, 64, qb);
+                    tile_load16(Qs, r, cb * 16, 64, qb);  // Qb' = q e^{Gamma - Gamma_r}
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) qb[j] = sc * (qb[j] - w16[j]);
+                    for (int j = 0; j < 16; ++j) qb[j] = sc * (qb[j] * Rf[cb * 16 + j] - w16[j]);
                     tile_store16(qt_img, r, cb * 16, 64, qb);
                 }
             }
@@ -846,7 +904,7 @@ TcLayout tc_layout(const Params& p) {
 
 size_t tc_workspace_bytes(const Params& p) { return tc_layout_bytes(tc_records(p), p.dk); }
 
-template <int D, int VAR>
+template <int D, int VAR, bool PREP>
 cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mg;
     const long long rows = (long long)p.B * p.T;
@@ -858,12 +916,12 @@ cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {
     constexpr int smem = PrepSmem<D>::kBytes;
     static std::atomic<unsigned long long> attr{0};
     {
-        const cudaError_t e = set_smem_once(tc_prep_kernel<D, VAR>, smem, attr);
+        const cudaError_t e = set_smem_once(tc_prep_kernel<D, VAR, PREP>, smem, attr);
         if (e != cudaSuccess) return e;
     }
     if (p.num_chunks == 0) return cudaSuccess;
     TraceScope ts("tc_prep", st);
-    tc_prep_kernel<D, VAR><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mg, p, L);
+    tc_prep_kernel<D, VAR, PREP><<<dim3(p.num_chunks, p.H), 128, smem, st>>>(mq, mk, mv, mg, p, L);
     return cudaGetLastError();
 }
 
@@ -885,10 +943,13 @@ template <int D>
 cudaError_t tc_fwd_d(const Params& p, cudaStream_t st, bool write_o) {
     const TcLayout L = tc_layout(p);
     cudaError_t e;
-    switch (p.variant) {
-        case DR_DELTANET: e = launch_prep<D, DR_DELTANET>(p, L, st); break;
-        case DR_GDN: e = launch_prep<D, DR_GDN>(p, L, st); break;
-        default: e = launch_prep<D, DR_KDA>(p, L, st); break;
+    switch (p.variant * 2 + (p.prepare ? 1 : 0)) {
+        case 2 * DR_DELTANET: e = launch_prep<D, DR_DELTANET, false>(p, L, st); break;
+        case 2 * DR_DELTANET + 1: e = launch_prep<D, DR_DELTANET, true>(p, L, st); break;
+        case 2 * DR_GDN: e = launch_prep<D, DR_GDN, false>(p, L, st); break;
+        case 2 * DR_GDN + 1: e = launch_prep<D, DR_GDN, true>(p, L, st); break;
+        case 2 * DR_KDA: e = launch_prep<D, DR_KDA, false>(p, L, st); break;
+        default: e = launch_prep<D, DR_KDA, true>(p, L, st); break;
     }
     if (e != cudaSuccess) return e;
     // one 128-row value tile per (sequence, head) when that already fills the SMs; two

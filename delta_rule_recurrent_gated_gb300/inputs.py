@@ -4,7 +4,8 @@ This module is shared by the tests, the benchmark and the oracle checks.  It
 holds no arithmetic of the method itself: it only draws random tensors and
 applies the input preparation a model layer performs before calling the mixer
 (L2 normalisation of q and k per head, beta = sigmoid(.), log-gate
-g = -softplus(.) * 0.1), then rounds to the io dtype.
+g = -softplus(.) * gate_scale, 0.1 for the specified workloads), then rounds to
+the io dtype.
 
 Everything is drawn on the CPU from one ``torch.Generator`` seeded with
 ``seed`` in a fixed order: q, k, v, beta logits, gate logits, h0, dO, dhT.
@@ -38,6 +39,7 @@ class Workload:
     varlen_hi: int = 4096
     lengths: Optional[tuple] = None   # explicit packed lengths (overrides the draw)
     scale: float = 1.0
+    gate_scale: float = 0.1  # prepared log-gates g = -softplus(N(0,1)) * gate_scale
 
     @property
     def tokens(self) -> int:
@@ -133,10 +135,10 @@ def make(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
     g = None
     if w.variant == "gdn":
         g = -torch.nn.functional.softplus(
-            torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)) * 0.1
+            torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)) * w.gate_scale
     elif w.variant == "kda":
         g = -torch.nn.functional.softplus(
-            torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32)) * 0.1
+            torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32)) * w.gate_scale
     h0 = None
     if w.h0:
         h0 = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02
@@ -152,9 +154,10 @@ def make(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
 def make_raw(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
     """Inputs before the input preparation, for the library's input-preparation
     mode: q, k ~ N(0, 1) rows (not normalised) in the io dtype; beta logits
-    b ~ N(0, 1); gate arguments x ~ N(0, 1) - 2.5, so that -softplus(x) falls
-    in the same range as the prepared gates above (about -0.08 typical).  v, h0,
-    dO, dhT as in ``make``.  Same draw order and generator as ``make``.
+    b ~ N(0, 1); gate arguments x ~ N(0, 1), so that the gate the library forms,
+    -softplus(x), is about -0.8 per token (a 64-token chunk decays by about e^-50
+    per key channel).  v, h0, dO, dhT as in ``make``.  Same draw order and
+    generator as ``make``.
     """
     gen = torch.Generator().manual_seed(seed)
     dt = io_dtype(w)
@@ -166,9 +169,9 @@ def make_raw(w: Workload, seed: int = 0, need_grad_inputs: bool = True) -> dict:
     beta = torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)
     g = None
     if w.variant == "gdn":
-        g = torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32) - 2.5
+        g = torch.randn(w.B, w.T, w.H, generator=gen, dtype=torch.float32)
     elif w.variant == "kda":
-        g = torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32) - 2.5
+        g = torch.randn(w.B, w.T, w.H, w.dk, generator=gen, dtype=torch.float32)
     h0 = None
     if w.h0:
         h0 = torch.randn(N, w.H, w.dk, w.dv, generator=gen, dtype=torch.float32) * 0.02

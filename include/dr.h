@@ -81,13 +81,15 @@ enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
  *   q_hat = q * rsqrt(sum_c q_c^2 + 1e-6)   per (token, head); the same for k
  *   beta  = sigmoid(b)                       b: the beta argument, a logit
  *   g     = -softplus(x) = -log(1 + e^x)     x: the g argument (GDN, KDA)
- * dr_fwd / dr_fwd_u write q_hat, k_hat (io_dtype, fp32 arithmetic), beta and g (fp32)
- * into the workspace (dr_workspace_bytes counts them) and run on those.  dr_bwd /
- * dr_bwd_u take the same raw tensors and return gradients with respect to them
- * (dq, dk, dbeta, dg chained through the three maps); with DR_FLAG_REUSE_FWD they
- * also reuse the prepared tensors the forward left in the workspace instead of
- * preparing again (the same raw inputs must be passed).  dr_decode applies the maps in
- * its own kernel.  dr_fwd_noalloc does not take the flag (DR_ERR_UNSUPPORTED).
+ * dr_bwd / dr_bwd_u take the same raw tensors and return gradients with respect to
+ * them (dq, dk, dbeta, dg chained through the three maps).  On the bf16 tensor-core
+ * path the kernels apply the maps on the fly, in fp32, to the raw tiles they load
+ * (forward and backward alike; the prepared values are never stored) and chain the
+ * gradients before writing them.  On the fp32 CUDA-core path dr_fwd / dr_fwd_u write
+ * q_hat, k_hat (io_dtype), beta and g (fp32) into the workspace (dr_workspace_bytes
+ * counts them) and run on those; with DR_FLAG_REUSE_FWD the backward reuses them (the
+ * same raw inputs must be passed).  dr_decode applies the maps in its own kernel.
+ * dr_fwd_noalloc does not take the flag (DR_ERR_UNSUPPORTED).
  */
 #define DR_FLAG_PREPARE_INPUTS 2
 

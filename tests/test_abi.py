@@ -183,11 +183,17 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
 
 
 def test_prepare_flag_host_rules(lib):
-    """DR_FLAG_PREPARE_INPUTS: accepted by dr_workspace_bytes with room for the
-    prepared tensors (two q/k-sized buffers in the io dtype plus fp32 beta and
-    gate), refused by dr_fwd_noalloc; an unknown flag bit stays an error."""
+    """DR_FLAG_PREPARE_INPUTS: accepted by dr_workspace_bytes; the bf16 tensor-core
+    path prepares on the fly and needs no more workspace, the fp32 CUDA-core path
+    adds room for the prepared tensors (two q/k-sized buffers in the io dtype plus
+    fp32 beta and gate); refused by dr_fwd_noalloc; an unknown flag bit stays an
+    error."""
     n = B.DR_FLAG_PREPARE_INPUTS
-    for kw, gate_per_token in ((dict(), 1), (dict(variant=B.DR_KDA), 128),
+    for kw in (dict(), dict(variant=B.DR_KDA)):
+        assert B.workspace_bytes(desc(flags=n, **kw)) == B.workspace_bytes(desc(**kw)) > 0
+    for kw, gate_per_token in ((dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16), 1),
+                               (dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16,
+                                     variant=B.DR_KDA), 128),
                                (dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16,
                                      variant=B.DR_DELTANET), 0)):
         base = B.workspace_bytes(desc(**kw))
@@ -197,14 +203,16 @@ def test_prepare_flag_host_rules(lib):
         esize = 2 if d.io_dtype == B.DR_BF16 else 4
         need = 2 * th * d.d_k * esize + th * 4 + th * (d.d_k if gate_per_token == 128 else
                                                        gate_per_token) * 4
+        assert esize == 4
         assert need <= prep - base <= need + 4 * 256 + 255
     assert call_fwd(desc(flags=n | 4)) == B.DR_ERR_INVALID_ARG
     d = desc(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16, flags=n)
     assert lib.dr_fwd_noalloc(ctypes.byref(d), 16, 16, 16, 16, 16, None, 16, None,
                               None) == B.DR_ERR_UNSUPPORTED
-    # a workspace sized without the flag is too small with it
-    small = B.workspace_bytes(desc())
-    assert call_fwd(desc(flags=n), ws_bytes=small) == B.DR_ERR_WORKSPACE
+    # on the fp32 path a workspace sized without the flag is too small with it
+    f32 = dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16)
+    small = B.workspace_bytes(desc(**f32))
+    assert call_fwd(desc(flags=n, **f32), ws_bytes=small) == B.DR_ERR_WORKSPACE
     dd = desc(T=1, flags=8)
     assert lib.dr_decode(ctypes.byref(dd), 16, 16, 16, 16, 16, 16, 16, None) == B.DR_ERR_INVALID_ARG
 

@@ -2,7 +2,8 @@
 independently: the whole path's FLOPs and bytes per token and head at d = 128
 (693,589 FLOPs; DeltaNet 2,828 B, Gated DeltaNet 2,840 B, KDA 4,364 B), the
 design bytes of each kernel launch, the fp32 peak from unit counts and clock, and
-the Gated DeltaNet-2 FLOP count restated from its product list."""
+the Gated DeltaNet-2 FLOP count restated from its product list, and each kernel's
+share of the path's bytes."""
 import importlib.util
 import os
 
@@ -59,15 +60,6 @@ def test_fp32_peak_and_gdn2_flops(bench):
     fwd = 2 * (11 * C * C * d) + C ** 3 / 3 + 2 * (4 * C * d * d)
     bwd = 2 * (20 * C * C * d) + 2 * (8 * C * d * d) + 2 * (2 * C ** 3)
     assert bench.gdn2_flops_per_chunk(C, d) == pytest.approx(fwd + bwd)
-
-
-def test_prepare_bytes(bench):
-    w = inputs.get("kda_b8_t4096_h16_d128")
-    th = 8 * 4096 * 16
-    b = bench.prepare_bytes(w, 8)
-    assert b["prepare_rows"] == 4 * th * 128 * 2      # read q, k; write q_hat, k_hat
-    assert b["chain_rows"] == 6 * th * 128 * 2        # read q, k, dq_hat, dk_hat; write dq, dk
-    assert b["prepare_gates"] == 8 * (th + th * 128)  # beta and the per-channel gate, in and out
 
 
 @pytest.mark.parametrize("name", ["gdn_h0_b8_t4096_h16_d128", "kda_b8_t4096_h16_d128",
