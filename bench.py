@@ -500,6 +500,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the recurrent-step (dr_decode) measurement")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="copy streams per direction in the end-to-end measurement")
     ap.add_argument("--no-gdn2", action="store_true",
                     help="skip the Gated DeltaNet-2 measurement")
     ap.add_argument("--no-prepare", action="store_true",
@@ -648,33 +650,50 @@ def main():
                      for os_ in out_sets]
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
         d2h = sum(v.numel() * v.element_size() for v in outs_host[0])
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ncs = max(1, args.copy_streams)
+
+        def spread(sizes):
+            """Tensor indices per copy stream, balancing bytes (largest first)."""
+            parts, load = [[] for _ in range(ncs)], [0] * ncs
+            for i in sorted(range(len(sizes)), key=lambda i: -sizes[i]):
+                j = load.index(min(load))
+                parts[j].append(i)
+                load[j] += sizes[i]
+            return parts
+
+        in_parts = spread([host_in[n].numel() * host_in[n].element_size() for n in names])
+        out_parts = spread([v.numel() * v.element_size() for v in outs_host[0]])
+        s_in = [torch.cuda.Stream(dev) for _ in range(ncs)]
+        s_out = [torch.cuda.Stream(dev) for _ in range(ncs)]
+        ev_in = [[torch.cuda.Event() for _ in range(ncs)] for _ in range(2)]
         ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [[torch.cuda.Event() for _ in range(ncs)] for _ in range(2)]
         used = [False, False]
 
         def e2e_step(i):
             bi = i % 2
             src, (oo, hh, gg) = dev_in[bi], out_sets[bi]
-            with torch.cuda.stream(s_in):
+            for j in range(ncs):
+                with torch.cuda.stream(s_in[j]):
+                    if used[bi]:
+                        s_in[j].wait_event(ev_comp[bi])  # step i-2 has read this input set
+                    for ti in in_parts[j]:
+                        src[names[ti]].copy_(host_in[names[ti]], non_blocking=True)
+                    ev_in[bi][j].record(s_in[j])
+                stream.wait_event(ev_in[bi][j])
                 if used[bi]:
-                    s_in.wait_event(ev_comp[bi])  # step i-2 has read this input set
-                for n in names:
-                    src[n].copy_(host_in[n], non_blocking=True)
-                ev_in[bi].record(s_in)
-            stream.wait_event(ev_in[bi])
-            if used[bi]:
-                stream.wait_event(ev_out[bi])  # step i-2's results have left this output set
+                    stream.wait_event(ev_out[bi][j])  # step i-2's results have left this set
             prob.forward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], o=oo, hT=hh)
             prob.backward(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"], src["dO"],
                           src["dhT"], reuse_fwd=True, out=gg)
             ev_comp[bi].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[bi])
-                for hv, dv_ in zip(outs_host[bi], flat(out_sets[bi])):
-                    hv.copy_(dv_, non_blocking=True)
-                ev_out[bi].record(s_out)
+            dsts, srcs = outs_host[bi], flat(out_sets[bi])
+            for j in range(ncs):
+                with torch.cuda.stream(s_out[j]):
+                    s_out[j].wait_event(ev_comp[bi])
+                    for ti in out_parts[j]:
+                        dsts[ti].copy_(srcs[ti], non_blocking=True)
+                    ev_out[bi][j].record(s_out[j])
             used[bi] = True
 
         for i in range(2):
@@ -683,18 +702,22 @@ def main():
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        s_in.wait_event(e0)
+        for j in range(ncs):
+            s_in[j].wait_event(e0)
         for i in range(args.steps):
             e2e_step(i)
         for bi in range(2):
-            stream.wait_event(ev_out[bi])
+            for j in range(ncs):
+                stream.wait_event(ev_out[bi][j])
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
         e2e = {"value": tokens / (e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "pipelining": "2 buffer sets; inputs in on one copy stream, results out on another"}
+               "h2d_gbs": h2d / (e_ms / 1e3) / 1e9, "d2h_gbs": d2h / (e_ms / 1e3) / 1e9,
+               "pipelining": f"2 buffer sets; inputs in on {ncs} copy streams, results out on "
+                             f"{ncs} others, tensors spread over them by size"}
 
     dec = None if args.no_decode else decode_bench(dev, stream, max_over_ranks, barrier)
 

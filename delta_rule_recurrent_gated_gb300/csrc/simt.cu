@@ -9,6 +9,9 @@
 // "Metodologia y Marco de Trabajo", item 1):
 //   Gamma = within-chunk cumulative sum of the log-decay (per key channel)
 //   Kb = k e^{Gamma}, Kr = k e^{-Gamma}, Qb = q e^{Gamma}, KC = k e^{Gamma_L - Gamma}
+// (in the two Gram-type products, Kb Kr^T and Qb Kr^T, the factors are taken relative to
+// Gamma_r, the cumulative log-decay at the chunk's middle token, so that neither overflows
+// while each half of the chunk decays by less than e^-87; Wy and Qt use e^{Gamma} <= 1)
 //   T  = (I + diag(beta) strict_lower(Kb Kr^T))^{-1}
 //   Wy = T diag(beta) Kb,  Ut = T diag(beta) v,  Aqk = tril(Qb Kr^T)
 //   Qt = scale (Qb - Aqk Wy),  Ot = scale Aqk Ut
@@ -41,7 +44,7 @@ enum {
 __device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, int L) {
     const int dk = p.dk, dv = p.dv, H = p.H, tid = threadIdx.x, nt = blockDim.x;
     float* q = s(bQ); float* k = s(bK); float* v = s(bV); float* gm = s(bGam);
-    float* beta = s(bVec);  // [0, C): beta;  [C, C + dk): e^{Gamma_L}
+    float* beta = s(bVec);  // [0, C): beta;  [C, C + dk): e^{Gamma_L};  [C + dk, C + 2 dk): Gamma_r
     for (int idx = tid; idx < L * dk; idx += nt) {
         const int i = idx / dk, c = idx % dk;
         const size_t e = ((size_t)(row0 + i) * H + h) * dk + c;
@@ -68,14 +71,17 @@ __device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, i
     __syncthreads();
     float* Kb = s(bKb); float* Kr = s(bKr); float* Qb = s(bQb); float* KC = s(bKC);
     float* bK = s(bbK); float* bV = s(bbV);
+    float* Gr = beta + p.C + dk;
+    for (int c = tid; c < dk; c += nt) Gr[c] = gm[((L - 1) / 2) * dk + c];
+    __syncthreads();
     for (int idx = tid; idx < L * dk; idx += nt) {
         const int i = idx / dk, c = idx % dk;
-        const float G = gm[idx], GL = gm[(L - 1) * dk + c];
-        Kb[idx] = k[idx] * expf(G);
-        Kr[idx] = k[idx] * expf(-G);
-        Qb[idx] = q[idx] * expf(G);
+        const float G = gm[idx], GL = gm[(L - 1) * dk + c], R = Gr[c];
+        Kb[idx] = k[idx] * expf(G - R);   // Kb' (Gram)
+        Kr[idx] = k[idx] * expf(R - G);   // Kr' (both Gram-type products)
+        Qb[idx] = q[idx] * expf(G - R);   // Qb' (Aqk)
         KC[idx] = k[idx] * expf(GL - G);
-        bK[idx] = beta[i] * Kb[idx];
+        bK[idx] = beta[i] * k[idx] * expf(G);  // beta Kb with the absolute factor (Wy)
     }
     for (int idx = tid; idx < L * dv; idx += nt) bV[idx] = beta[idx / dv] * v[idx];
     __syncthreads();
@@ -100,7 +106,7 @@ __device__ void chunk_prep(const Params& p, const Scratch& s, int h, int row0, i
     __syncthreads();
     float* Qt = s(bQt); float* Ot = s(bOt);
     mm4(Qt, dk, Aqk, L, false, Wy, dk, false, L, dk, L, -p.scale, false);
-    for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += p.scale * Qb[idx];
+    for (int idx = tid; idx < L * dk; idx += nt) Qt[idx] += p.scale * q[idx] * expf(gm[idx]);
     mm4(Ot, dv, Aqk, L, false, Ut, dv, false, L, dv, L, p.scale, false);
 }
 
@@ -221,11 +227,10 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         __syncthreads();
         mm4(dWy, dk, s(bAqk), L, true, dQt, dk, false, L, dk, L, -sc, true);
         mm4(dUt, dv, s(bAqk), L, true, dO, dv, false, L, dv, L, sc, true);
-        for (int idx = tid; idx < L * dk; idx += nt) dQb[idx] = sc * dQt[idx];
         __syncthreads();
         // Aqk = tril(Qb Kr^T)
         float* dKr = s(bdKr); float* dKb = s(bdKb);
-        mm4(dQb, dk, dAqk, L, false, s(bKr), dk, false, L, dk, L, 1.f, true);
+        mm4(dQb, dk, dAqk, L, false, s(bKr), dk, false, L, dk, L, 1.f, false);  // of Qb' 
         mm4(dKr, dk, dAqk, L, true, s(bQb), dk, false, L, dk, L, 1.f, false);
         // Wy = T bK, Ut = T bV
         float* dT = s(bdT); float* dbK = s(bdbK); float* dbV = s(bdbV); float* dA = s(bdA);
@@ -246,7 +251,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         for (int i = tid; i < L; i += nt) {
             float acc = 0.f;
             for (int j = 0; j < i; ++j) acc += dA[i * L + j] * Gm[i * L + j];
-            for (int c2 = 0; c2 < dk; ++c2) acc += dbK[i * dk + c2] * s(bKb)[i * dk + c2];
+            for (int c2 = 0; c2 < dk; ++c2)  // beta Kb with the absolute factor
+                acc += dbK[i * dk + c2] * s(bK)[i * dk + c2] * expf(s(bGam)[i * dk + c2]);
             for (int j = 0; j < dv; ++j) acc += dbV[i * dv + j] * s(bV)[i * dv + j];
             db[i] = acc;
         }
@@ -260,13 +266,17 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_kernel(Params p, float* scr
         const float* gm = s(bGam);
         for (int idx = tid; idx < L * dk; idx += nt) {
             const int i = idx / dk, c2 = idx % dk;
-            dKb[idx] += beta[i] * dbK[idx];
-            const float G = gm[idx], GL = gm[(L - 1) * dk + c2];
-            const float eG = expf(G), enG = expf(-G), eC = expf(GL - G);
+            // dKb, dKr, dQb hold the gradients of Kb', Kr', Qb'; sc dQt and beta dbK those of
+            // the absolute Qb and Kb
+            const float G = gm[idx], GL = gm[(L - 1) * dk + c2], R = s(bVec)[C + dk + c2];
+            const float eG = expf(G), er = expf(G - R), eri = expf(R - G), eC = expf(GL - G);
+            const float dQa = sc * s(bdQt)[idx], dKa = beta[i] * dbK[idx];
+            const float qa = s(bQ)[idx] * eG, ka = s(bK)[idx] * eG;
             const size_t e = ((size_t)(row0 + i) * p.H + h) * dk + c2;
-            st_any(p.dq, e, p.grad_dtype, dQb[idx] * eG);
-            st_any(p.dk_, e, p.grad_dtype, dKb[idx] * eG + dKr[idx] * enG + dKC[idx] * eC);
-            dGam[idx] = dQb[idx] * s(bQb)[idx] + dKb[idx] * s(bKb)[idx] -
+            st_any(p.dq, e, p.grad_dtype, dQa * eG + dQb[idx] * er);
+            st_any(p.dk_, e, p.grad_dtype,
+                   dKa * eG + dKb[idx] * er + dKr[idx] * eri + dKC[idx] * eC);
+            dGam[idx] = dQa * qa + dQb[idx] * s(bQb)[idx] + dKa * ka + dKb[idx] * s(bKb)[idx] -
                         dKr[idx] * s(bKr)[idx] - dKC[idx] * s(bKC)[idx];
         }
         for (int idx = tid; idx < L * dv; idx += nt) {

@@ -127,6 +127,13 @@ __global__ void __launch_bounds__(128, 1)
             tma_load_3d(st + S::kdO + kb * 8192, &mdo, &bar_ld[s], v0 + kb * 64, h, row0);
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
+        if (ci > 0) {  // the chunk before it into L2, one step ahead of its copy
+            const size_t rp = rec - p.H;
+            bulk_prefetch_l2(L.KC + rp * kTile, kTile);
+            bulk_prefetch_l2(L.Qt + rp * kTile, kTile);
+            bulk_prefetch_l2(L.Wy + rp * kTile, kTile);
+            for (int kb = 0; kb < BV / 64; ++kb) tma_prefetch_3d(&mdo, v0 + kb * 64, h, row0 - 64);
+        }
     };
     if (tid == 0 && nc > 0) load_iter(0);
 
@@ -388,32 +395,38 @@ __device__ __forceinline__ void stage_copy_out_prep(void* out, const uint8_t* lo
             unpack8(*reinterpret_cast<const uint4*>(raw + e0), x[ps]);
         }
     }
+    float d[kPass][E], xd[kPass];
 #pragma unroll
     for (int ps = 0; ps < kPass; ++ps) {
         const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
         const uint8_t* src = (i < 32 ? lo + i * kRow : hi + (i - 32) * kRow) + c * 16;
-        const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
-        float d[E];
         if constexpr (F32) {
             const float4 v = *reinterpret_cast<const float4*>(src);
-            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+            d[ps][0] = v.x; d[ps][1] = v.y; d[ps][2] = v.z; d[ps][3] = v.w;
         } else {
-            unpack8(*reinterpret_cast<const uint4*>(src), d);
+            unpack8(*reinterpret_cast<const uint4*>(src), d[ps]);
         }
-        float xd = 0.f;
+        xd[ps] = 0.f;
 #pragma unroll
-        for (int j = 0; j < E; ++j) xd = fmaf(x[ps][j], d[j], xd);
-        xd = lane_group_sum<kChunks>(xd);
-        const float r = rinv[i], f = r * r * xd;  // (x_hat . dx_hat) / |x|
+        for (int j = 0; j < E; ++j) xd[ps] = fmaf(x[ps][j], d[ps][j], xd[ps]);
+    }
 #pragma unroll
-        for (int j = 0; j < E; ++j) d[j] = r * (d[j] - x[ps][j] * f);
+    for (int ps = 0; ps < kPass; ++ps) xd[ps] = lane_group_sum<kChunks>(xd[ps]);
+#pragma unroll
+    for (int ps = 0; ps < kPass; ++ps) {
+        const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
+        const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
+        const float r = rinv[i], f = r * r * xd[ps];  // (x_hat . dx_hat) / |x|
+#pragma unroll
+        for (int j = 0; j < E; ++j) d[ps][j] = r * (d[ps][j] - x[ps][j] * f);
         if (i < len) {
             uint8_t* dst = static_cast<uint8_t*>(out) + e0 * (F32 ? 4 : 2);
             if constexpr (F32) {
-                *reinterpret_cast<float4*>(dst) = make_float4(d[0], d[1], d[2], d[3]);
+                *reinterpret_cast<float4*>(dst) = make_float4(d[ps][0], d[ps][1], d[ps][2], d[ps][3]);
             } else {
-                *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(d[0], d[1]), pack_bf16(d[2], d[3]),
-                                                            pack_bf16(d[4], d[5]), pack_bf16(d[6], d[7]));
+                *reinterpret_cast<uint4*>(dst) =
+                    make_uint4(pack_bf16(d[ps][0], d[ps][1]), pack_bf16(d[ps][2], d[ps][3]),
+                               pack_bf16(d[ps][4], d[ps][5]), pack_bf16(d[ps][6], d[ps][7]));
             }
         }
     }
@@ -605,23 +618,18 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
     };
     // per-token scalars of an item, read into registers ahead of time: beta (threads
-    // 64..127) and GDN's log-decays (two per lane of warp 1)
-    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f, sx0 = 0.f, sx1 = 0.f;
+    // 64..127) and GDN's log-decays (two per lane of warp 1); with input preparation
+    // the raw values, mapped only when the item starts (so no thread waits on the loads
+    // before then)
+    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f;
     auto load_scalars = [&](int itm) {
         const int c = itm / p.H, hh = itm % p.H;
         int sq, r0, ln;
         chunk_info(p, c, sq, r0, ln);
         beta_ld = (tid >= 64 && tid < 128 && tid - 64 < ln) ? p.beta[(size_t)(r0 + tid - 64) * p.H + hh] : 0.f;
-        if (PREP && tid >= 64 && tid < 128 && tid - 64 < ln) beta_ld = prep_sigmoid(beta_ld);
         if (VAR == DR_GDN && warp == 1) {
             gl0 = 2 * lane < ln ? p.g[(size_t)(r0 + 2 * lane) * p.H + hh] : 0.f;
             gl1 = 2 * lane + 1 < ln ? p.g[(size_t)(r0 + 2 * lane + 1) * p.H + hh] : 0.f;
-            if (PREP) {
-                sx0 = prep_sigmoid(gl0);
-                sx1 = prep_sigmoid(gl1);
-                gl0 = 2 * lane < ln ? prep_neg_softplus(gl0) : 0.f;
-                gl1 = 2 * lane + 1 < ln ? prep_neg_softplus(gl1) : 0.f;
-            }
         }
     };
     uint32_t n_st = 0, n_tok = 0;  // copy groups issued on bar_st / bar_tok
@@ -654,7 +662,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         uint8_t* dUts = R.dUt;  // -dU^T -> dUt^T
         float* gC_s = gC_b + (odd ? D : 0);
         fsum = 0.f;
-        if (tid >= 64 && tid < 128) beta_s[tid - 64] = beta_ld;
+        if (tid >= 64 && tid < 128)  // with input preparation beta = sigmoid(b)
+            beta_s[tid - 64] = PREP ? (tid - 64 < len ? prep_sigmoid(beta_ld) : 0.f) : beta_ld;
+        if (tid == kIssuer && next < nitems) {
+            // the next item's q, k, v, dO boxes into L2 now; their loads into shared memory
+            // can only be issued once this item's last stage has read those buffers
+            const int nc = next / p.H, nh = next % p.H;
+            int nsq, nr0, nln;
+            chunk_info(p, nc, nsq, nr0, nln);
+            for (int kb = 0; kb < D / 64; ++kb) {
+                tma_prefetch_3d(&mq, kb * 64, nh, nr0);
+                tma_prefetch_3d(&mk, kb * 64, nh, nr0);
+                tma_prefetch_3d(&mv, kb * 64, nh, nr0);
+                tma_prefetch_3d(&mdo, kb * 64, nh, nr0);
+            }
+            if (VAR == DR_KDA) tma_prefetch_3d(&mg, 0, nh, nr0);  // its gates (one box)
+        }
         ok = mbar_wait(&bar_tok, ph, kWaitLimitNs);
         if (VAR == DR_KDA) ok = ok && mbar_wait(&bar_st, ph, kWaitLimitNs);  // the gates
         if (__syncthreads_or(!ok)) break;
@@ -687,6 +710,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tot[pt * D + c] = G;
         } else if (VAR == DR_GDN) {
             if (warp == 1) {
+                if (PREP) {  // g = -softplus(x); sigmoid(x) is kept for the chain of dg
+                    sgx[2 * lane] = prep_sigmoid(gl0);
+                    sgx[2 * lane + 1] = prep_sigmoid(gl1);
+                    gl0 = 2 * lane < len ? prep_neg_softplus(gl0) : 0.f;
+                    gl1 = 2 * lane + 1 < len ? prep_neg_softplus(gl1) : 0.f;
+                }
                 float x = gl0 + gl1;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -705,10 +734,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                     eref[c] = er;
                     gcr[c] = lr;
                 }
-                if (PREP) {
-                    sgx[2 * lane] = sx0;
-                    sgx[2 * lane + 1] = sx1;
-                }
             }
         }
         __syncthreads();
@@ -716,37 +741,61 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // until the state-side products have read dS out of the Kb tile
         constexpr int kPer = 64 * (D / 8) / kChunkThreads;
         uint4 kbr[kPer];
+        // the rows of every pass are loaded first (the stores below may not pass them), and
+        // with input preparation their norms reduced together
+        uint4 qv_[kPer], kv_[kPer];
+        float rq_[kPer], rk_[kPer];
+#pragma unroll
+        for (int n = 0; n < kPer; ++n) {
+            const int w = tid + n * kChunkThreads;
+            const uint32_t off = sw128_offset(w / (D / 8), (w % (D / 8)) * 8, 64);
+            kv_[n] = *reinterpret_cast<const uint4*>(Ks + off);
+            qv_[n] = *reinterpret_cast<const uint4*>(Qs + off);
+        }
+        if (PREP) {  // L2 norms of the raw rows; the inverse norms are kept for the chain
+#pragma unroll
+            for (int n = 0; n < kPer; ++n) {
+                float q8[8], k8[8], a = 0.f, b = 0.f;
+                unpack8(qv_[n], q8);
+                unpack8(kv_[n], k8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    a = fmaf(q8[j], q8[j], a);
+                    b = fmaf(k8[j], k8[j], b);
+                }
+                rq_[n] = a;
+                rk_[n] = b;
+            }
+#pragma unroll
+            for (int n = 0; n < kPer; ++n) {
+                rq_[n] = rsqrtf(lane_group_sum<D / 8>(rq_[n]) + kPrepEps);
+                rk_[n] = rsqrtf(lane_group_sum<D / 8>(rk_[n]) + kPrepEps);
+                const int w = tid + n * kChunkThreads;
+                if (w % (D / 8) == 0) {
+                    rq_s[w / (D / 8)] = rq_[n];
+                    rk_s[w / (D / 8)] = rk_[n];
+                }
+            }
+        }
 #pragma unroll
         for (int n = 0; n < kPer; ++n) {
             const int w = tid + n * kChunkThreads;
             const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
             const uint32_t off = sw128_offset(i, c8, 64);
-            const uint4 kv = *reinterpret_cast<const uint4*>(Ks + off);
+            const uint4 kv = kv_[n];
             if (VAR == DR_DELTANET && !PREP) {
                 kbr[n] = kv;
                 continue;
             }
-            const uint4 qv = *reinterpret_cast<const uint4*>(Qs + off);
+            const uint4 qv = qv_[n];
             float q8[8], k8[8], e8[8], i8[8];
             unpack8(qv, q8);
             unpack8(kv, k8);
-            if (PREP) {  // L2-normalise the raw rows; keep the inverse norms for the chain
-                float sq = 0.f, sk = 0.f;
+            if (PREP) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    sq = fmaf(q8[j], q8[j], sq);
-                    sk = fmaf(k8[j], k8[j], sk);
-                }
-                const float rq = rsqrtf(lane_group_sum<D / 8>(sq) + kPrepEps);
-                const float rk = rsqrtf(lane_group_sum<D / 8>(sk) + kPrepEps);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    q8[j] *= rq;
-                    k8[j] *= rk;
-                }
-                if (c8 == 0) {
-                    rq_s[i] = rq;
-                    rk_s[i] = rk;
+                    q8[j] *= rq_[n];
+                    k8[j] *= rk_[n];
                 }
             }
             if (VAR == DR_DELTANET) {

@@ -68,25 +68,46 @@ struct PrepSmem {
     static constexpr int kBeta = (D == 128) ? kT + 8192 : kT + 8192 + 16384 + 12288;
     static constexpr int kGL = kBeta + 256;              // [D] fp32 e^{Gamma_last - Gamma_r}
     static constexpr int kRf = kGL + D * 4;              // [D] fp32 e^{Gamma_r}; then Gamma_r (KDA)
-    static constexpr int kBytes = kRf + 2 * D * 4 + 1024;  // + alignment slack
+    static constexpr int kRn = kRf + 2 * D * 4;          // [2][64] inverse norms of q, k rows
+    static constexpr int kBytes = kRn + 2 * 64 * 4 + 1024;  // + alignment slack
 };
 
-// q8, k8: eight channels of one token row, whose D / 8 lanes are consecutive in the warp;
-// scaled in place to the L2-normalised row (DR_FLAG_PREPARE_INPUTS).
-template <int D>
-__device__ __forceinline__ void normalize_row8(float (&q8)[8], float (&k8)[8]) {
-    float sq = 0.f, sk = 0.f;
+// Inverse L2 norms of the 64 q and k rows of [64][D] SW128 tiles (DR_FLAG_PREPARE_INPUTS):
+// a row's D / 8 threads are consecutive lanes and sum its squares by shuffles; all rows of
+// a thread are loaded before any reduction so that the shuffle chains overlap.
+template <int D, int NT>
+__device__ __forceinline__ void row_inv_norms(const uint8_t* Qs, const uint8_t* Ks, float* rq, float* rk) {
+    constexpr int kIt = 64 * (D / 8) / NT;
+    static_assert(kIt * NT == 64 * (D / 8), "whole warps per pass");
+    float sq[kIt], sk[kIt];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        sq = fmaf(q8[j], q8[j], sq);
-        sk = fmaf(k8[j], k8[j], sk);
+    for (int n = 0; n < kIt; ++n) {
+        const int w = threadIdx.x + n * NT, i = w / (D / 8), c8 = (w % (D / 8)) * 8;
+        const uint32_t off = sw128_offset(i, c8, 64);
+        float q8[8], k8[8];
+        unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
+        unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            a = fmaf(q8[j], q8[j], a);
+            b = fmaf(k8[j], k8[j], b);
+        }
+        sq[n] = a;
+        sk[n] = b;
     }
-    const float rq = rsqrtf(lane_group_sum<D / 8>(sq) + kPrepEps);
-    const float rk = rsqrtf(lane_group_sum<D / 8>(sk) + kPrepEps);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        q8[j] *= rq;
-        k8[j] *= rk;
+    for (int n = 0; n < kIt; ++n) {
+        sq[n] = lane_group_sum<D / 8>(sq[n]);
+        sk[n] = lane_group_sum<D / 8>(sk[n]);
+    }
+#pragma unroll
+    for (int n = 0; n < kIt; ++n) {
+        const int w = threadIdx.x + n * NT;
+        if (w % (D / 8) == 0) {
+            rq[w / (D / 8)] = rsqrtf(sq[n] + kPrepEps);
+            rk[w / (D / 8)] = rsqrtf(sk[n] + kPrepEps);
+        }
     }
 }
 
@@ -111,6 +132,8 @@ __global__ void __launch_bounds__(128, 1)
     float* GLs = reinterpret_cast<float*>(sm + S::kGL);
     float* Rf = reinterpret_cast<float*>(sm + S::kRf);   // e^{Gamma_r} per key channel
     float* Gr = Rf + D;                                  // KDA: Gamma_r per key channel
+    float* RQ = reinterpret_cast<float*>(sm + S::kRn);   // input preparation: 1 / |q row|
+    float* RK = RQ + 64;                                 // and 1 / |k row|
     __shared__ uint64_t bar_ld, bar_mma;
     __shared__ uint32_t tmem_base;
 
@@ -154,6 +177,34 @@ __global__ void __launch_bounds__(128, 1)
             }
             if (VAR == DR_KDA) tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
         }
+        if (tid == 32) {
+            // the tiles of the block one wave later (two blocks per SM) into L2, so that its
+            // own loads find them there
+            uint32_t nsm;
+            asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+            const long long ahead = (long long)blockIdx.y * gridDim.x + blockIdx.x + 2ll * nsm;
+            if (ahead < (long long)gridDim.x * gridDim.y) {
+                const int ac = (int)(ahead % gridDim.x), ah = (int)(ahead / gridDim.x);
+                int asq, ar0, aln;
+                chunk_info(p, ac, asq, ar0, aln);
+                for (int kb = 0; kb < D / 64; ++kb) {
+                    tma_prefetch_3d(&mq, kb * 64, ah, ar0);
+                    tma_prefetch_3d(&mk, kb * 64, ah, ar0);
+                    tma_prefetch_3d(&mv, kb * 64, ah, ar0);
+                }
+                if (VAR == DR_KDA) {
+                    tma_prefetch_3d(&mg, 0, ah, ar0);
+                    tma_prefetch_3d(&mg, 0, ah, ar0 + 32);
+                }
+            }
+        }
+        // GDN's log-decays (two per lane of warp 0) are read while the tiles land
+        float ga0 = 0.f, ga1 = 0.f;
+        if (VAR == DR_GDN && warp == 0) {
+            const int ln2 = 2 * (tid & 31);
+            ga0 = ln2 < len ? p.g[(size_t)(row0 + ln2) * p.H + h] : 0.f;
+            ga1 = ln2 + 1 < len ? p.g[(size_t)(row0 + ln2 + 1) * p.H + h] : 0.f;
+        }
         if (tid < 64) {
             const float b = tid < len ? p.beta[(size_t)(row0 + tid) * p.H + h] : 0.f;
             beta_s[tid] = tid < len ? (PREP ? prep_sigmoid(b) : b) : 0.f;
@@ -173,6 +224,10 @@ __global__ void __launch_bounds__(128, 1)
             }
         }
         __syncthreads();
+        if (PREP) {  // raw q, k rows: their inverse norms, applied in the decay pass
+            row_inv_norms<D, 128>(Qs, Ks, RQ, RK);
+            __syncthreads();
+        }
 
         // decay, per token (DeltaNet, GDN): warp 0 scans the 64 log-decays, two per lane, and
         // keeps e^{Gamma - Gamma_r}, e^{Gamma_r - Gamma}, e^{Gamma_last - Gamma} and e^{Gamma}
@@ -183,8 +238,8 @@ __global__ void __launch_bounds__(128, 1)
                 const int lane = tid & 31;
                 float a0 = 0.f, a1 = 0.f;
                 if (VAR == DR_GDN) {
-                    a0 = 2 * lane < len ? p.g[(size_t)(row0 + 2 * lane) * p.H + h] : 0.f;
-                    a1 = 2 * lane + 1 < len ? p.g[(size_t)(row0 + 2 * lane + 1) * p.H + h] : 0.f;
+                    a0 = ga0;
+                    a1 = ga1;
                     if (PREP) {
                         a0 = 2 * lane < len ? prep_neg_softplus(a0) : 0.f;
                         a1 = 2 * lane + 1 < len ? prep_neg_softplus(a1) : 0.f;
@@ -223,7 +278,14 @@ __global__ void __launch_bounds__(128, 1)
                 unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
                 unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
                 unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
-                if (PREP) normalize_row8<D>(q8, k8);
+                if (PREP) {
+                    const float rq = RQ[i], rk = RK[i];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        q8[j] *= rq;
+                        k8[j] *= rk;
+                    }
+                }
                 const float b = beta_s[i], e = Er[i], ei = Er[64 + i], ec = Er[128 + i],
                             ea = Er[192 + i];
                 uint32_t wq[4], wr[4], wb[4], wy[4], wv[4], wc[4];
@@ -277,14 +339,34 @@ __global__ void __launch_bounds__(128, 1)
                     }
                 }
                 __syncthreads();
-                for (int w = tid; w < 32 * (D / 8); w += 128) {
+                // all passes' q, k, v pieces are loaded before the first store
+                constexpr int kIt = 32 * (D / 8) / 128;
+                uint4 qb_[kIt], kb_[kIt], vb_[kIt];
+#pragma unroll
+                for (int u = 0; u < kIt; ++u) {
+                    const int w = tid + 128 * u;
+                    const uint32_t off = sw128_offset(32 * half + w / (D / 8), (w % (D / 8)) * 8, 64);
+                    qb_[u] = *reinterpret_cast<const uint4*>(Qs + off);
+                    kb_[u] = *reinterpret_cast<const uint4*>(Ks + off);
+                    vb_[u] = *reinterpret_cast<const uint4*>(Vs + off);
+                }
+#pragma unroll
+                for (int u = 0; u < kIt; ++u) {
+                    const int w = tid + 128 * u;
                     const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
                     const uint32_t off = sw128_offset(i, c8, 64);
                     float q8[8], k8[8], v8[8], G8[8], R8[8], E8[8];
-                    unpack8(*reinterpret_cast<const uint4*>(Qs + off), q8);
-                    unpack8(*reinterpret_cast<const uint4*>(Ks + off), k8);
-                    unpack8(*reinterpret_cast<const uint4*>(Vs + off), v8);
-                    if (PREP) normalize_row8<D>(q8, k8);
+                    unpack8(qb_[u], q8);
+                    unpack8(kb_[u], k8);
+                    unpack8(vb_[u], v8);
+                    if (PREP) {
+                        const float rq = RQ[i], rk = RK[i];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            q8[j] *= rq;
+                            k8[j] *= rk;
+                        }
+                    }
                     const float b = beta_s[i];
                     const float4* gp = reinterpret_cast<const float4*>(&Gb[ii * D + c8]);
                     const float4 g0 = gp[0], g1 = gp[1];
@@ -642,6 +724,14 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         bulk_g2s(st + S::kOt, L.OtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
+        if (ci + 1 < nc) {  // the chunk after it into L2, one step ahead of its copy
+            const size_t rn = rec + p.H;
+            bulk_prefetch_l2(L.Wy + rn * kTile, kTile);
+            bulk_prefetch_l2(L.Qt + rn * kTile, kTile);
+            bulk_prefetch_l2(L.KC + rn * kTile, kTile);
+            bulk_prefetch_l2(L.UtT + rn * kTile + (size_t)v0 * 128, BV * 128);
+            bulk_prefetch_l2(L.OtT + rn * kTile + (size_t)v0 * 128, BV * 128);
+        }
     };
     if (tid == kIss && nc > 0) load_chunk(0);
 

@@ -57,3 +57,15 @@ def test_strong_gates_full_size_kda():
     got = run_gpu(w, x, reuse=True)
     check_sampled(w, x, got, pick(w, x, 1, seed=3))
     assert np.all(np.isfinite(got["o"]))
+
+
+@pytest.mark.parametrize("variant", ["kda", "gdn"])
+@pytest.mark.parametrize("chunk,d", [(64, 64), (64, 128), (32, 32)])
+def test_strong_gates_fp32_path(variant, chunk, d):
+    """The fp32 CUDA-core path under the same gates, at its 1e-4 bound."""
+    w = inputs.replace(inputs.small(variant, B=2, T=150, H=2, dk=d, dv=d, chunk=chunk, io="f32"),
+                       gate_scale=2.0)
+    x = inputs.make(w, seed=74)
+    if chunk == 64:
+        assert chunk_log_decay_min(w, x) < -100.0
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
