@@ -127,13 +127,6 @@ __global__ void __launch_bounds__(128, 1)
             tma_load_3d(st + S::kdO + kb * 8192, &mdo, &bar_ld[s], v0 + kb * 64, h, row0);
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
-        if (ci > 0) {  // the chunk before it into L2, one step ahead of its copy
-            const size_t rp = rec - p.H;
-            bulk_prefetch_l2(L.KC + rp * kTile, kTile);
-            bulk_prefetch_l2(L.Qt + rp * kTile, kTile);
-            bulk_prefetch_l2(L.Wy + rp * kTile, kTile);
-            for (int kb = 0; kb < BV / 64; ++kb) tma_prefetch_3d(&mdo, v0 + kb * 64, h, row0 - 64);
-        }
     };
     if (tid == 0 && nc > 0) load_iter(0);
 

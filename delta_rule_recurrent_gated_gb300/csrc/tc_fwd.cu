@@ -177,27 +177,6 @@ __global__ void __launch_bounds__(128, 1)
             }
             if (VAR == DR_KDA) tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
         }
-        if (tid == 32) {
-            // the tiles of the block one wave later (two blocks per SM) into L2, so that its
-            // own loads find them there
-            uint32_t nsm;
-            asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
-            const long long ahead = (long long)blockIdx.y * gridDim.x + blockIdx.x + 2ll * nsm;
-            if (ahead < (long long)gridDim.x * gridDim.y) {
-                const int ac = (int)(ahead % gridDim.x), ah = (int)(ahead / gridDim.x);
-                int asq, ar0, aln;
-                chunk_info(p, ac, asq, ar0, aln);
-                for (int kb = 0; kb < D / 64; ++kb) {
-                    tma_prefetch_3d(&mq, kb * 64, ah, ar0);
-                    tma_prefetch_3d(&mk, kb * 64, ah, ar0);
-                    tma_prefetch_3d(&mv, kb * 64, ah, ar0);
-                }
-                if (VAR == DR_KDA) {
-                    tma_prefetch_3d(&mg, 0, ah, ar0);
-                    tma_prefetch_3d(&mg, 0, ah, ar0 + 32);
-                }
-            }
-        }
         // GDN's log-decays (two per lane of warp 0) are read while the tiles land
         float ga0 = 0.f, ga1 = 0.f;
         if (VAR == DR_GDN && warp == 0) {
