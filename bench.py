@@ -45,11 +45,15 @@ def algorithmic(w, N):
 
 # DRAM bytes (read + write) per work item (chunk x head) from one ncu capture, with the
 # sha256 of the kernel source it was taken on; reported only while the source is unchanged.
-# profiles/tc_bwd_chunk_gdn_b2_t4096_h16_d128.md: 434.9 MB for 2048 items.
+# profiles/dram_traffic_gdn_b2_t4096_h16_d128.md: 2048 records per launch.  Only the
+# chunk-parallel kernels, whose traffic per record does not depend on the batch.
 MEASURED_TRAFFIC = {
-    ("tc_bwd_chunk", "gdn", 128): (434.904832e6 / 2048,
+    ("tc_bwd_chunk", "gdn", 128): ((355029248 + 77033472) / 2048,
                                    "delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-                                   "d76aaac4a0485432c455065f8b5e1f83a59c95fcea762421307397fc73a05cd7"),
+                                   "c8049b033855c9dfbb294e2a156d15a9dea3699c8a14770ef7ccb9e3e3db4257"),
+    ("tc_prep", "gdn", 128): ((102339584 + 129750784) / 2048,
+                              "delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
+                              "5e2d369426e2f0a53e16d1974770e159ddfd736a49091534d55d999e76316ab7"),
 }
 
 
