@@ -354,38 +354,68 @@ __device__ __forceinline__ void stage_copy_out(void* out, const uint8_t* lo, con
 }
 
 // The same copy-out for the gradient of a normalised input (DR_FLAG_PREPARE_INPUTS): the
-// staged rows hold dL/dx_hat of x_hat = x rsqrt(sum x^2 + eps); each row is chained to
-// dL/dx = r (dx_hat - x_hat (x_hat . dx_hat)), r = rinv[row], from the raw bf16 row x.
+// staged rows hold dL/dx_hat of x_hat = x r, r = rsqrt(sum x^2 + eps) = rinv[row]; each row
+// is chained to dL/dx = r (dx_hat - x_hat (x_hat . dx_hat)).  x_hat comes from
+//   SRC 0: the raw bf16 rows x in global memory (read once, before the first store);
+//   SRC 1: the decayed operand tile (x_hat e^{+-(Gamma - Gamma_r)}, bf16) times a per-row
+//          factor rowf[row] that undoes the decay (GDN; DeltaNet with rowf = null);
+//   SRC 2: the decayed tile divided by the per-element factor gam[row][channel] (KDA).
 // The kChunks threads of a row are consecutive lanes of one warp and sum the dot product
 // by shuffles, so every thread runs every pass (rows past `len` are not written).
-template <int D, bool F32>
+template <int D, bool F32, int SRC>
 __device__ __forceinline__ void stage_copy_out_prep(void* out, const uint8_t* lo, const uint8_t* hi,
                                                     const Params& p, int row0, int len, int h,
                                                     const __nv_bfloat16* __restrict__ raw,
-                                                    const float* rinv) {
+                                                    const float* rinv, const uint8_t* tile,
+                                                    const float* rowf, const float* gam) {
     constexpr int kRow = D * (F32 ? 4 : 2), kChunks = kRow / 16, E = F32 ? 4 : 8;
     constexpr int kPass = 64 * kChunks / kChunkThreads;
     static_assert(kPass * kChunkThreads == 64 * kChunks && kChunks <= 32, "whole warps per pass");
-    // every raw row piece is loaded before the first store (they may not be reordered past it)
+    // every row piece is loaded before the first store (they may not be reordered past it)
     float x[kPass][E];
 #pragma unroll
     for (int ps = 0; ps < kPass; ++ps) {
         const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
-        const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
-        if (i >= len) {
+        if (SRC == 0) {
+            const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
+            if (i >= len) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) x[ps][j] = 0.f;
-        } else if constexpr (F32) {
-            const uint2 u = *reinterpret_cast<const uint2*>(raw + e0);
-            const uint32_t wv[2] = {u.x, u.y};
+                for (int j = 0; j < E; ++j) x[ps][j] = 0.f;
+            } else if constexpr (F32) {
+                const uint2 u = *reinterpret_cast<const uint2*>(raw + e0);
+                const uint32_t wv[2] = {u.x, u.y};
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
-                x[ps][2 * j] = __low2float(b);
-                x[ps][2 * j + 1] = __high2float(b);
+                for (int j = 0; j < 2; ++j) {
+                    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
+                    x[ps][2 * j] = __low2float(b);
+                    x[ps][2 * j + 1] = __high2float(b);
+                }
+            } else {
+                unpack8(*reinterpret_cast<const uint4*>(raw + e0), x[ps]);
             }
         } else {
-            unpack8(*reinterpret_cast<const uint4*>(raw + e0), x[ps]);
+            const int cb = c * E;  // first channel of the piece
+            const uint8_t* src = tile + sw128_offset(i, cb & ~7, 64) + (cb & 7) * 2;
+            if constexpr (F32) {
+                const uint2 u = *reinterpret_cast<const uint2*>(src);
+                const uint32_t wv[2] = {u.x, u.y};
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
+                    x[ps][2 * j] = __low2float(b);
+                    x[ps][2 * j + 1] = __high2float(b);
+                }
+            } else {
+                unpack8(*reinterpret_cast<const uint4*>(src), x[ps]);
+            }
+            if (SRC == 1 && rowf) {
+                const float f = rowf[i];
+#pragma unroll
+                for (int j = 0; j < E; ++j) x[ps][j] *= f;
+            } else if (SRC == 2) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) x[ps][j] *= fast_rcp(gam[i * D + cb + j]);
+            }
         }
     }
     float d[kPass][E], xd[kPass];
@@ -409,7 +439,9 @@ __device__ __forceinline__ void stage_copy_out_prep(void* out, const uint8_t* lo
     for (int ps = 0; ps < kPass; ++ps) {
         const int w = threadIdx.x + ps * kChunkThreads, i = w / kChunks, c = w % kChunks;
         const size_t e0 = ((size_t)(row0 + i) * p.H + h) * D + c * E;
-        const float r = rinv[i], f = r * r * xd[ps];  // (x_hat . dx_hat) / |x|
+        const float r = rinv[i];
+        // x_hat . dx_hat, and the factor of x in the chain (x_hat itself for SRC > 0)
+        const float f = SRC == 0 ? r * r * xd[ps] : xd[ps];
 #pragma unroll
         for (int j = 0; j < E; ++j) d[ps][j] = r * (d[ps][j] - x[ps][j] * f);
         if (i < len) {
@@ -1194,11 +1226,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             p.dbeta[(size_t)(row0 + r) * p.H + h] = db;
         }
         if (PREP) {
-            const __nv_bfloat16* rawq = static_cast<const __nv_bfloat16*>(p.q);
+            // q_hat from the Qb' tile: e^{Gamma_r - Gamma} per row (GDN), 1 / e^{Gamma - Gamma_r}
+            // per element (KDA, whose array still holds them), nothing (DeltaNet)
+            constexpr int kSrc = VAR == DR_KDA ? 2 : 1;
+            const float* rf = VAR == DR_GDN ? Eirow : nullptr;
             if (f32out)
-                stage_copy_out_prep<D, true>(p.dq, dUts, dWys, p, row0, len, h, rawq, rq_s);
+                stage_copy_out_prep<D, true, kSrc>(p.dq, dUts, dWys, p, row0, len, h, nullptr, rq_s, Qs, rf, Gam);
             else
-                stage_copy_out_prep<D, false>(p.dq, dUts, dWys, p, row0, len, h, rawq, rq_s);
+                stage_copy_out_prep<D, false, kSrc>(p.dq, dUts, dWys, p, row0, len, h, nullptr, rq_s, Qs, rf, Gam);
         } else if (f32out)
             stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
         else
@@ -1252,11 +1287,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dk_stage(BoolTag<false>{});
         __syncthreads();
         if (PREP) {
+            // k_hat from the Kr' tile times e^{Gamma - Gamma_r} per row (GDN) or nothing
+            // (DeltaNet); KDA's per-element factors are gone by now (its array already holds
+            // the next item's gates), so it re-reads the raw rows
             const __nv_bfloat16* rawk = static_cast<const __nv_bfloat16*>(p.k);
+            constexpr int kSrc = VAR == DR_KDA ? 0 : 1;
+            const float* rf = VAR == DR_GDN ? Erow : nullptr;
             if (f32out)
-                stage_copy_out_prep<D, true>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s);
+                stage_copy_out_prep<D, true, kSrc>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s, Ks, rf, nullptr);
             else
-                stage_copy_out_prep<D, false>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s);
+                stage_copy_out_prep<D, false, kSrc>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s, Ks, rf, nullptr);
         } else if (f32out)
             stage_copy_out<D, true>(p.dk_, Vs, dOs, p, row0, len, h);
         else
