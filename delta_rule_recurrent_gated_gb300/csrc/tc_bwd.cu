@@ -1339,7 +1339,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 float run = dgC_s[cl] * gC_s[cl];
                 for (int q = 0; q < kG; ++q) run += fq[q * D + cl];
                 for (int q = grp + 1; q < kG; ++q) run += sgq[q * D + cl];
-#pragma unroll
                 float sx[PREP ? kTok : 1];  // sigmoid of the raw gate arguments
                 if (PREP) {
 #pragma unroll
