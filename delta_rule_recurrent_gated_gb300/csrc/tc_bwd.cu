@@ -284,7 +284,7 @@ struct BChunkSmem {
     // of P0 and P4..P7 alternate between consecutive work items of a CTA (ChunkRoles), so
     // that the next item's inputs can be copied in while this item finishes.
     // [64][D] token-row tiles: q -> Qb, k -> Kr, v, dO, Kb
-    // [D][64] channel-row tiles: U^T, dQt^T, -dWyA^T -> dWy^T, -dU^T -> dUt^T
+    // U [64][D] (token rows); [D][64] channel-row tiles: dQt^T, -dWyA^T -> dWy^T, -dU^T -> dUt^T
     static constexpr int kK = kTile, kV = 2 * kTile, kdO = 3 * kTile;
     // five 8 KB tiles: T, then Aqk / P-X / dT-dG / dAqk, which hold S before those
     static constexpr int kT = 8 * kTile, kAq = kT + kCC, kB8a = kAq + kCC, kB8b = kB8a + kCC,
@@ -457,8 +457,8 @@ __device__ __forceinline__ void stage_copy_out_prep(void* out, const uint8_t* lo
     }
 }
 
-// Buffer roles of one work item.  Even items: q in P0, U^T in P4 (then dQt^T), dS in
-// P5..P6 (then Kb in P5, dWy^T in P6), -dU^T in P7.  Odd items: q in P5, U^T in P0 (then
+// Buffer roles of one work item.  Even items: q in P0, U in P4 (then dQt^T), dS in
+// P5..P6 (then Kb in P5, dWy^T in P6), -dU^T in P7.  Odd items: q in P5, U in P0 (then
 // Kb), dS in P6..P7 (then dQt^T in P6, dWy^T in P7), -dU^T in P4.  What an even item
 // still reads after its last product (Kb, Kr) and where it stages dk (P2, P3) is
 // disjoint from where the next odd item's state goes, and the reverse.
@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 
     constexpr uint32_t kDD = D * D * 2;
     uint8_t* Sst = Aqs;  // [D][D] W-layout state at the chunk start, in the four 8 KB tiles
-    // State-side copies of an item: S, dS, U^T, -dU^T, T, e^{Gamma_last} (and KDA's
+    // State-side copies of an item: S, dS, U, -dU^T, T, e^{Gamma_last} (and KDA's
     // gates, one [64][D] fp32 box) on bar_st; token side q, k, v, dO on bar_tok.
     auto issue_state = [&](int itm, bool odd) {
         const int c = itm / p.H, hh = itm % p.H;
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int next = item + gridDim.x;
         const ChunkRoles R = chunk_roles(sm, kTile, odd);
         uint8_t* Qs = R.Q;      // q -> Qb
-        uint8_t* Ust = R.U;     // [D][64] U^T
+        uint8_t* Ust = R.U;     // [64][D] U
         uint8_t* dQs = R.dQ;    // dQt^T = S dO^T
         uint8_t* dSst = R.dS;   // [D][D] W-layout state gradient at the chunk end
         uint8_t* Kbs = R.Kb;    // Kb
@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const Tile tS{smem_u32(Sst), D};
             mma_tiles(tm + C0, tS, true, Tile{smem_u32(dOs), 64}, false, D, 64, D, false);
             mma_tiles(tm + C1, tS, true, Tile{smem_u32(dUts), D}, true, D, 64, D, false);
-            mma_tiles(tm + C_dKC, Tile{smem_u32(dSst), D}, true, Tile{smem_u32(Ust), D}, true, D, 64, D,
+            mma_tiles(tm + C_dKC, Tile{smem_u32(dSst), D}, true, Tile{smem_u32(Ust), 64}, false, D, 64, D,
                       false);
             mma_commit(&bar_mma);
         }
@@ -928,7 +928,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int q = 0; q < 128 / (D / 8); ++q) a += Xs[q * D + c];
             dgC_s[c] = a;
         }
-        // E0: Kb' into its tile; dQt^T -> its tile (U^T is consumed), -dWyA^T -> the dWy
+        // E0: Kb' into its tile; dQt^T -> its tile (U is consumed), -dWyA^T -> the dWy
         // tile (dS is consumed), both scaled by e^{Gamma_r} of their key channel
 #pragma unroll
         for (int n = 0; n < kPer; ++n) {

@@ -22,15 +22,18 @@
 //
 // Kernel 1, tc_prep: one CTA per (chunk, head), fully parallel.  TMA loads the
 // q/k/v tiles, CUDA cores apply the decay, tcgen05 computes the two Gram
-// products, CUDA cores invert the unit-lower-triangular 64x64 matrix (one
-// column per thread, forward substitution), tcgen05 forms Wy, Ut, Aqk Wy,
-// Aqk Ut.  Writes Wy, Qt, KC (tile images), Ut^T, Ot^T, T and e^{Gamma_last}.
+// products, CUDA cores invert the unit-lower-triangular 64x64 matrix (2x2 blocks
+// of 32 rows), tcgen05 forms Wy, Ut, Aqk Wy, Aqk Ut.  Writes Wy, Qt, KC (tile
+// images), Ut, Ot (token rows), T and e^{Gamma_last}.
 // Kernel 2, tc_scan_fwd: one CTA per (sequence, head, value tile of BV rows),
 // sequential over the sequence's chunks.  The state slice W[v0:v0+BV, :] stays
-// in fp32 registers (one row per thread); per chunk two tcgen05 products
-// (W Wy^T, W Qt^T) give U and O, and one more (U^T KC) the state increment.
-// Also stores the chunk-start state S and U for the backward pass.
+// in fp32 registers (half a row per thread); per chunk one tcgen05 product
+// ([Wy; Qt] W^T) gives U and O, and one more (U^T KC) the state increment.
+// Also stores the chunk-start state S and U for the backward pass; o leaves by
+// tensor stores from shared memory.
 #include <cudaTypedefs.h>
+
+#include <cstring>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -520,52 +523,45 @@ __global__ void __launch_bounds__(128, 1)
         fence_async_smem();
         __syncthreads();
 
-        // Wy = T (beta Kb) -> cols [0,D);  Ut^T = (beta v)^T T^T -> cols [128,192) (M = D:
-        // the rows are value channels, so its operand tile is written 16 bytes wide)
+        // Wy = T (beta Kb) -> cols [0,D);  Ut = T (beta v) -> cols [128,128+D)
         if (tid == 0) {
             bulk_s2g(L.T + rec * 8192, Ts, 8192);
             bulk_commit();
             tc_fence_after();
             const Tile tT{smem_u32(Ts), 64}, tY{smem_u32(Ys), 64}, tV{smem_u32(Vs), 64};
             mma_tiles(tm + 0, tT, false, tY, true, 64, D, 64, false);
-            mma_tiles(tm + 128, tV, true, tT, false, D, 64, 64, false);
+            mma_tiles(tm + 128, tT, false, tV, true, 64, D, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        // Wy and Ut^T into their operand tiles; the workspace images (Wy [64][D], Ut^T
-        // [D][64], SW128 tile images) are bulk copies of those tiles
-        {
-            for (int cb = 0; cb < D / 16; ++cb) {
-                float w16[16];
-                tmem_ld16(tl + cb * 16, w16);
-                tmem_ld_wait();
-                if (r >= 0) tile_store16(Xs, r, cb * 16, 64, w16);
-            }
-            const int cv = D == 128 ? tid : r;  // value channel of the M = D accumulator
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                float u16[16];
-                tmem_ld16(tl + 128 + b * 16, u16);
-                tmem_ld_wait();
-                if (cv >= 0) tile_store16(Ks, cv, b * 16, D, u16);  // Ut^T [D][64] (Kr is consumed)
+        // Wy and Ut into their operand tiles (Ut where Kr was, which is consumed); the
+        // workspace images ([64][D] SW128 tile images) are bulk copies of those tiles
+        for (int cb = 0; cb < D / 16; ++cb) {
+            float w16[16], u16[16];
+            tmem_ld16(tl + cb * 16, w16);
+            tmem_ld16(tl + 128 + cb * 16, u16);
+            tmem_ld_wait();
+            if (r >= 0) {
+                tile_store16(Xs, r, cb * 16, 64, w16);
+                tile_store16(Ks, r, cb * 16, 64, u16);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // Aqk Wy -> cols [0,D);  Ot^T / scale = Ut^T Aqk^T -> cols [128,192) (M = D)
+        // Aqk Wy -> cols [0,D);  Ot / scale = Aqk Ut -> cols [128,128+D)
         if (tid == 0) {
             bulk_s2g(L.Wy + rec * kTile, Xs, kTile);
-            bulk_s2g(L.UtT + rec * kTile, Ks, kTile);
+            bulk_s2g(L.Ut + rec * kTile, Ks, kTile);
             bulk_commit();
             tc_fence_after();
-            const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), D};
+            const Tile tA{smem_u32(Aqs), 64}, tW{smem_u32(Xs), 64}, tU{smem_u32(Ks), 64};
             mma_tiles(tm + 0, tA, false, tW, true, 64, D, 64, false);
-            mma_tiles(tm + 128, tU, false, tA, false, D, 64, 64, false);
+            mma_tiles(tm + 128, tA, false, tU, true, 64, D, 64, false);
             mma_commit(&bar_mma);
         }
         ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
@@ -574,29 +570,22 @@ __global__ void __launch_bounds__(128, 1)
 
         {
             uint8_t* qt_img = L.Qt + rec * kTile;
-            uint8_t* otT = L.OtT + rec * kTile;  // [D][64] SW128 tile image of Ot^T
+            uint8_t* ot_img = L.Ot + rec * kTile;  // [64][D] SW128 tile image of Ot
             const float sc = p.scale;
             for (int cb = 0; cb < D / 16; ++cb) {
-                float w16[16], qb[16];
+                float w16[16], o16[16], qb[16];
                 tmem_ld16(tl + cb * 16, w16);
+                tmem_ld16(tl + 128 + cb * 16, o16);
                 tmem_ld_wait();
                 if (r >= 0) {
                     tile_load16(Qs, r, cb * 16, 64, qb);  // Qb' = q e^{Gamma - Gamma_r}
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) qb[j] = sc * (qb[j] * Rf[cb * 16 + j] - w16[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        qb[j] = sc * (qb[j] * Rf[cb * 16 + j] - w16[j]);
+                        o16[j] *= sc;
+                    }
                     tile_store16(qt_img, r, cb * 16, 64, qb);
-                }
-            }
-            const int cv = D == 128 ? tid : r;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                float o16[16];
-                tmem_ld16(tl + 128 + b * 16, o16);
-                tmem_ld_wait();
-                if (cv >= 0) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) o16[j] *= sc;
-                    tile_store16(otT, cv, b * 16, D, o16);
+                    tile_store16(ot_img, r, cb * 16, 64, o16);
                 }
             }
         }
@@ -614,53 +603,58 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ============================================================== tc_scan_fwd
-// Shared memory: the state operand, the U^T operand, and two stages of the
-// per-chunk inputs so the next chunk's tiles load while this chunk computes.
+// Shared memory: the state operand, the U operand, and two stages of the per-chunk
+// inputs so the next chunk's tiles load while this chunk computes.
 template <int D, int BV>
 struct ScanSmem {
     static constexpr int kTile = 64 * D * 2;
     static constexpr int kW = 0;                       // [BV][D] state W (bf16 operand)
-    static constexpr int kUs = BV * D * 2;             // [BV][64] U^T operand
+    static constexpr int kUs = BV * D * 2;             // [64][BV] U operand
     static constexpr int kStage0 = kUs + BV * 128;
-    // stage layout: Wy, Qt, KC [64][D] tiles; Ut^T, Ot^T rows [BV][64]; gC [D] fp32
-    static constexpr int kWy = 0, kQt = kTile, kKC = 2 * kTile, kUt = 3 * kTile,
-                         kOt = kUt + BV * 128, kG = kOt + BV * 128;
+    // stage layout: [Wy; Qt] as one [128][D] tile (column block b holds the 64 Wy rows,
+    // then the 64 Qt rows), KC [64][D]; Ut, Ot [64][BV] (columns v0 .. v0+BV-1 of their
+    // [64][D] images); gC [D] fp32
+    static constexpr int kWQ = 0, kKC = 2 * kTile, kUt = 3 * kTile, kOt = kUt + BV * 128,
+                         kG = kOt + BV * 128;
     static constexpr int kStageBytes = (kG + D * 4 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
     static constexpr uint32_t kStageTx = 3 * kTile + 2 * BV * 128 + D * 4;
 };
 
-// 256 threads: warps 0-3 carry the state chain (U, the state-update product, W);
-// warps 4-7 read the output accumulator of the same rows and store o meanwhile.
-constexpr int kScanFwdThreads = 256;
-
-__device__ __forceinline__ void state_warps_sync() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-// barrier 2 (160 threads): the state warps wait, the first output warp arrives once the
-// chunk-start state image has been read out of the state tile
-__device__ __forceinline__ void state_image_sync() {
-    asm volatile("bar.sync 2, 160;" ::: "memory");
-}
-__device__ __forceinline__ void state_image_arrive() {
-    asm volatile("bar.arrive 2, 160;" ::: "memory");
-}
+// 256 threads, warp w on TMEM lane quarter w % 4 and half w / 4 of the columns.  Per
+// chunk one product [Wy; Qt] W^T (M = 128) gives, in lanes 0..63, Wy S for the writes
+// U = Ut - Wy S and, in lanes 64..127, Qt S for the outputs O = Ot + Qt S (token t of
+// either in lane t, resp. 64 + t), so the threads of quarters 0-1 form U and those of
+// quarters 2-3 form o at the same time, each 16 bytes at a time along a token row.
+// Then U^T KC (M = BV value rows) gives the state increment; each thread updates half a
+// state row (BV = 128: row 32 (w % 4) + lane; BV = 64: the M = 64 row layout).  A ninth
+// warp issues the bulk copies (its lane 0: the state image, the next chunk's tiles, the
+// o boxes), so no epilogue warp waits on their issue.
+constexpr int kScanFwdThreads = 288;
+constexpr int kScanMathThreads = 256;
 
 template <int D, int BV>
-__global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const Params p, const TcLayout L,
-                                                                         int write_o) {
+__global__ void __launch_bounds__(kScanFwdThreads, 1)
+    tc_scan_fwd_kernel(const __grid_constant__ CUtensorMap mo, const Params p, const TcLayout L,
+                       int write_o, int stage_o) {
     using S = ScanSmem<D, BV>;
     constexpr int kTile = S::kTile;
+    constexpr int DH = D / 2;   // key columns of a state thread
+    constexpr int HC = BV / 2;  // value columns of an epilogue thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Ws = sm + S::kW;
     uint8_t* Us = sm + S::kUs;
-    __shared__ uint64_t bar_ld[2], bar_mma, bar_o;
+    __shared__ uint64_t bar_ld[2], bar_mma;
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const bool state_warp = warp < 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool math = tid < kScanMathThreads;   // the eight epilogue / state warps
+    const int hf = (warp >> 2) & 1;             // which half of the columns
+    const int erow = (warp & 3) * 32 + lane;    // row of the stacked product (M = 128)
+    const int etok = erow & 63;                 // its token
+    const bool u_row = erow < 64;               // lanes 0..63: Wy S; 64..127: Qt S
     const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
     const int v0 = blockIdx.y * BV;
     int c0, nc, srow, slen;
@@ -670,9 +664,9 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
         mbar_init(&bar_ld[0], 1);
         mbar_init(&bar_ld[1], 1);
         mbar_init(&bar_mma, 1);
-        mbar_init(&bar_o, 1);
         fence_barrier_init();
         s_fail = 0;
+        if (stage_o) prefetch_tmap(&mo);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -683,24 +677,26 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = (BV == 128) ? (tid & 127) : m64_row();  // value row (or -1)
+    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row();  // state row (or -1)
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
-    // Thread kIss (lane 0 of the first output warp, idle until the products land) issues
-    // the copies: the chunk-start state image and the next chunk's tiles.
-    constexpr int kIss = 128;
-    int issued[2] = {0, 0};   // bulk-load phases per stage (thread kIss)
+    // Thread kIss (lane 0 of the copy warp) issues the copies: the chunk-start state image,
+    // the next chunk's tiles and the o boxes.  Thread 0 issues the products and the U image.
+    constexpr int kIss = kScanMathThreads;
+    int issued[2] = {0, 0};  // bulk-load phases per stage (thread kIss)
 
     auto load_chunk = [&](int ci) {  // thread kIss: fetch chunk ci into stage ci & 1
         const int s = ci & 1;
         uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
         mbar_arrive_expect_tx(&bar_ld[s], S::kStageTx);
-        bulk_g2s(st + S::kWy, L.Wy + rec * kTile, kTile, &bar_ld[s]);
-        bulk_g2s(st + S::kQt, L.Qt + rec * kTile, kTile, &bar_ld[s]);
+        for (int kb = 0; kb < D / 64; ++kb) {
+            bulk_g2s(st + S::kWQ + kb * 16384, L.Wy + rec * kTile + kb * 8192, 8192, &bar_ld[s]);
+            bulk_g2s(st + S::kWQ + kb * 16384 + 8192, L.Qt + rec * kTile + kb * 8192, 8192, &bar_ld[s]);
+        }
         bulk_g2s(st + S::kKC, L.KC + rec * kTile, kTile, &bar_ld[s]);
-        bulk_g2s(st + S::kUt, L.UtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
-        bulk_g2s(st + S::kOt, L.OtT + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
+        bulk_g2s(st + S::kUt, L.Ut + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
+        bulk_g2s(st + S::kOt, L.Ot + rec * kTile + (size_t)v0 * 128, BV * 128, &bar_ld[s]);
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
         if (ci + 1 < nc) {  // the chunk after it into L2, one step ahead of its copy
@@ -708,23 +704,22 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
             bulk_prefetch_l2(L.Wy + rn * kTile, kTile);
             bulk_prefetch_l2(L.Qt + rn * kTile, kTile);
             bulk_prefetch_l2(L.KC + rn * kTile, kTile);
-            bulk_prefetch_l2(L.UtT + rn * kTile + (size_t)v0 * 128, BV * 128);
-            bulk_prefetch_l2(L.OtT + rn * kTile + (size_t)v0 * 128, BV * 128);
+            bulk_prefetch_l2(L.Ut + rn * kTile + (size_t)v0 * 128, BV * 128);
+            bulk_prefetch_l2(L.Ot + rn * kTile + (size_t)v0 * 128, BV * 128);
         }
     };
     if (tid == kIss && nc > 0) load_chunk(0);
 
-    float W[D];  // W[v, :] = S[:, v], fp32 (state warps)
+    float W[DH];  // W[v, hf*DH + c] = S[hf*DH + c, v], fp32
 #pragma unroll
-    for (int c = 0; c < D; ++c)
-        W[c] = (p.h0 && r >= 0 && state_warp) ? p.h0[state_off + (size_t)c * D + v] : 0.f;
-    if (r >= 0 && state_warp) {
+    for (int c = 0; c < DH; ++c) W[c] = (p.h0 && r >= 0) ? p.h0[state_off + (size_t)(hf * DH + c) * D + v] : 0.f;
+    if (r >= 0) {
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = 0; cb < DH / 16; ++cb) {
             float t[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
-            tile_store16(Ws, r, cb * 16, BV, t);
+            tile_store16(Ws, r, hf * DH + cb * 16, BV, t);
         }
     }
     fence_async_smem();
@@ -733,90 +728,119 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
     bool ok = true;
     for (int ci = 0; ci < nc && ok; ++ci) {
         const int s = ci & 1;
-        const uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
+        uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
         const int row0 = srow + ci * 64, len = min(64, slen - ci * 64);
-        if (tid == 0) bulk_wait_read();  // the previous chunk's U^T image has left Us
+        // o of a whole chunk is written in place over its Ot tile and leaves by tensor
+        // stores; a ragged last chunk, and fp32 o, by 16-byte stores of token rows
+        const bool tile_o = write_o && stage_o && len == 64;
+        if (tid == 0) bulk_wait_read();  // the previous chunk's U image has left Us
         ok = mbar_wait(&bar_ld[s], (ci >> 1) & 1, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
 
-        // W Wy^T -> cols [0,64) ;  W Qt^T -> cols [64,128)
+        // [Wy; Qt] W^T -> cols [0, BV)
         if (tid == 0) {
             tc_fence_after();
-            const Tile tW{smem_u32(Ws), BV}, tWy{smem_u32(st + S::kWy), 64}, tQt{smem_u32(st + S::kQt), 64};
-            mma_tiles(tm + 0, tW, false, tWy, false, BV, 64, D, false);
-            mma_commit(&bar_mma);  // the state chain waits for W Wy^T only
-            mma_tiles(tm + 64, tW, false, tQt, false, BV, 64, D, false);
-            mma_commit(&bar_o);
+            mma_tiles(tm, Tile{smem_u32(st + S::kWQ), 128}, false, Tile{smem_u32(Ws), BV}, false, 128, BV, D,
+                      false);
+            mma_commit(&bar_mma);
         }
         if (tid == kIss) {
-            // the chunk-start state rows [v0, v0+BV) of the W-layout state image, then the
-            // next chunk's tiles (stage s^1 was released at the end of ci-1); Ws may be
-            // rewritten once the image has left it
+            // the chunk-start state rows [v0, v0+BV) of the W-layout state image; then,
+            // once the previous chunk's o tiles have left stage s^1, the next chunk's
+            // tiles into it
             uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
             for (int kb = 0; kb < D / 64; ++kb)
                 bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
             bulk_commit();
+            bulk_wait_read_but_newest();
             if (ci + 1 < nc) load_chunk(ci + 1);
-            bulk_wait_read();
         }
-        if (warp == kIss / 32) {
-            __syncwarp();
-            state_image_arrive();
-        }
-
-        if (state_warp) {
-            // no block-wide barrier here: the state chain does not wait for the issuing
-            // thread; a failed wait is reported through s_fail at the end of the chunk
-            if (!mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
-            tc_fence_after();
-            // U = Ut - W Wy^T
-            for (int g = 0; g < 4; g += 2) {
-                float acc[16], acc2[16];
-                tmem_ld16(tl + g * 16, acc);
-                tmem_ld16(tl + (g + 1) * 16, acc2);
+        if (math && !mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
+        tc_fence_after();
+        // U = Ut - Wy S into the U operand (quarters 0-1); o = Ot + Qt S (quarters 2-3)
+        if (math && (u_row || write_o)) {
+            const uint8_t* src = st + (u_row ? S::kUt : S::kOt);
+#pragma unroll 1
+            for (int cb = 0; cb < HC / 16; cb += 2) {
+                const int col = hf * HC + cb * 16;  // first of this pass's 32 value columns
+                float a[16], b[16], x[16], y[16];
+                tmem_ld16(tl + col, a);
+                tmem_ld16(tl + col + 16, b);
                 tmem_ld_wait();
-                if (r >= 0) {
-                    // row r of the swizzled Ut^T rows: 16-byte chunk q sits at q ^ (r % 8)
-                    float ut[16];
-                    const uint8_t* urow = st + S::kUt + r * 128;
-                    auto uchunk = [&](int q) {
-                        return *reinterpret_cast<const uint4*>(urow + (((2 * g + q) ^ (r & 7)) << 4));
-                    };
-                    unpack8(uchunk(0), ut);
-                    unpack8(uchunk(1), ut + 8);
+                tile_load16(src, etok, col, 64, x);
+                tile_load16(src, etok, col + 16, 64, y);
+                if (u_row) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] = ut[j] - acc[j];
-                    tile_store16(Us, r, g * 16, BV, acc);
-                    unpack8(uchunk(2), ut);
-                    unpack8(uchunk(3), ut + 8);
+                    for (int j = 0; j < 16; ++j) {
+                        x[j] -= a[j];
+                        y[j] -= b[j];
+                    }
+                    tile_store16(Us, etok, col, 64, x);
+                    tile_store16(Us, etok, col + 16, 64, y);
+                } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc2[j] = ut[j] - acc2[j];
-                    tile_store16(Us, r, (g + 1) * 16, BV, acc2);
+                    for (int j = 0; j < 16; ++j) {
+                        x[j] += a[j];
+                        y[j] += b[j];
+                    }
+                    if (tile_o) {  // in place: the Ot tile becomes the o box(es)
+                        tile_store16(st + S::kOt, etok, col, 64, x);
+                        tile_store16(st + S::kOt, etok, col + 16, 64, y);
+                    } else if (etok < len) {
+                        const size_t e0 = ((size_t)(row0 + etok) * p.H + h) * D + v0 + col;
+                        if (p.out_dtype == DR_F32) {
+                            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.o) + e0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                d[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                                d[4 + q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+                            }
+                        } else {
+                            uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + e0);
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                d[q] = make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                                                  pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+                                d[2 + q] = make_uint4(pack_bf16(y[8 * q], y[8 * q + 1]), pack_bf16(y[8 * q + 2], y[8 * q + 3]),
+                                                      pack_bf16(y[8 * q + 4], y[8 * q + 5]), pack_bf16(y[8 * q + 6], y[8 * q + 7]));
+                            }
+                        }
+                    }
                 }
             }
-            fence_async_smem();
-            tc_fence_before();
-            state_warps_sync();
-            // U^T KC -> cols [128, 128+D); U^T rows [v0, v0+BV) of the U^T image
-            if (tid == 0) {
-                tc_fence_after();
-                const Tile tU{smem_u32(Us), BV}, tKC{smem_u32(st + S::kKC), 64};
-                mma_tiles(tm + 128, tU, false, tKC, true, BV, D, 64, false);
-                mma_commit(&bar_mma);
-                bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
-                bulk_commit();
-            }
-            const bool ok2 = mbar_wait(&bar_mma, 1, kWaitLimitNs);
-            state_image_sync();  // the state image has left Ws, rewritten below
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // U^T KC -> cols [128, 128+D); the U rows of the U image; the o boxes
+        if (tid == 0) {
             tc_fence_after();
-            if (!ok2) s_fail = 1;
-            const float* gCs = reinterpret_cast<const float*>(st + S::kG);
+            mma_tiles(tm + 128, Tile{smem_u32(Us), 64}, true, Tile{smem_u32(st + S::kKC), 64}, true, BV, D, 64,
+                      false);
+            mma_commit(&bar_mma);
+            bulk_s2g(L.U + rec * kTile + (size_t)v0 * 128, Us, BV * 128);
+            bulk_commit();
+        }
+        if (tid == kIss) {
+            if (tile_o) {
+                for (int b = 0; b < BV / 64; ++b) tma_store_3d(&mo, st + S::kOt + b * 8192, v0 + 64 * b, h, row0);
+                bulk_commit();
+                bulk_wait_read_but_newest();  // the state image has left Ws
+            } else {
+                bulk_wait_read();
+            }
+        }
+        if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
+        __syncthreads();  // the state image has left Ws, rewritten below
+        tc_fence_after();
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + hf * DH;
+        if (math) {
 #pragma unroll
-            for (int cb = 0; cb < D / 16; cb += 2) {
+            for (int cb = 0; cb < DH / 16; cb += 2) {
                 float acc[16], acc2[16];
-                tmem_ld16(tl + 128 + cb * 16, acc);
-                tmem_ld16(tl + 128 + (cb + 1) * 16, acc2);
+                tmem_ld16(tl + 128 + hf * DH + cb * 16, acc);
+                tmem_ld16(tl + 128 + hf * DH + (cb + 1) * 16, acc2);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -827,37 +851,8 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
                     acc2[j] = W[c + 16];
                 }
                 if (r >= 0) {
-                    tile_store16(Ws, r, cb * 16, BV, acc);
-                    tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
-                }
-            }
-        } else if (write_o) {
-            // O = Ot + W Qt^T for rows r, while the state chain proceeds
-            if (!mbar_wait(&bar_o, ci & 1, kWaitLimitNs)) s_fail = 1;
-            tc_fence_after();
-            const size_t stride = (size_t)p.H * D;
-            const size_t base = ((size_t)row0 * p.H + h) * D + v;
-            for (int g = 0; g < 4; ++g) {
-                float oacc[16];
-                tmem_ld16(tl + 64 + g * 16, oacc);
-                tmem_ld_wait();
-                if (r >= 0) {
-                    float ot[16];  // swizzled like the Ut^T rows
-                    const uint8_t* orow = st + S::kOt + r * 128;
-                    unpack8(*reinterpret_cast<const uint4*>(orow + (((2 * g) ^ (r & 7)) << 4)), ot);
-                    unpack8(*reinterpret_cast<const uint4*>(orow + (((2 * g + 1) ^ (r & 7)) << 4)), ot + 8);
-                    const int jmax = min(16, len - g * 16);
-                    if (p.out_dtype == DR_F32) {
-                        float* dst = static_cast<float*>(p.o) + base + (size_t)g * 16 * stride;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (j < jmax) dst[(size_t)j * stride] = ot[j] + oacc[j];
-                    } else {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + base + (size_t)g * 16 * stride;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (j < jmax) dst[(size_t)j * stride] = __float2bfloat16_rn(ot[j] + oacc[j]);
-                    }
+                    tile_store16(Ws, r, hf * DH + cb * 16, BV, acc);
+                    tile_store16(Ws, r, hf * DH + (cb + 1) * 16, BV, acc2);
                 }
             }
         }
@@ -870,9 +865,9 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1) tc_scan_fwd_kernel(const P
     }
 
     if (ok) {
-        if (p.hT && r >= 0 && state_warp) {
+        if (p.hT && r >= 0) {
 #pragma unroll
-            for (int c = 0; c < D; ++c) p.hT[state_off + (size_t)c * D + v] = W[c];
+            for (int c = 0; c < DH; ++c) p.hT[state_off + (size_t)(hf * DH + c) * D + v] = W[c];
         }
     } else {
         record_timeout(p);
@@ -904,35 +899,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 // [rows, H, D] bf16 tensor, box = 64 channels x 1 head x 64 rows, 128B swizzle
-// The write u = U (token-major, out_dtype) from the U^T tile images the forward scan
-// leaves in the workspace: a [D][64] image goes through shared memory, then thread
-// (token i, channels 8c .. 8c+7) writes one 8-channel piece of row i.
+// The write u = U (token-major, out_dtype) from the U tile images the forward scan
+// leaves in the workspace ([64 tokens][D] SW128 images): thread (token i, channels
+// 8c .. 8c+7) moves one 16-byte piece of row i.
 template <int D>
 __global__ void __launch_bounds__(256) unpack_u_kernel(const Params p, const TcLayout L) {
-    __shared__ __align__(16) uint8_t img[64 * D * 2];
     const int chunk = blockIdx.x, h = blockIdx.y;
     int seq, row0, len;
     chunk_info(p, chunk, seq, row0, len);
-    const uint4* src = reinterpret_cast<const uint4*>(L.U + ((size_t)chunk * p.H + h) * (64 * D * 2));
-    for (int w = threadIdx.x; w < 64 * D * 2 / 16; w += blockDim.x)
-        reinterpret_cast<uint4*>(img)[w] = src[w];
-    __syncthreads();
+    const uint8_t* img = L.U + ((size_t)chunk * p.H + h) * (64 * D * 2);
     for (int w = threadIdx.x; w < 64 * (D / 8); w += blockDim.x) {
-        const int i = w % 64, c8 = (w / 64) * 8;
+        const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
         if (i >= len) continue;
-        float x[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-            x[t] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(img + sw128_offset(c8 + t, i, D)));
+        const uint4 piece = *reinterpret_cast<const uint4*>(img + sw128_offset(i, c8, 64));
         const size_t e = ((size_t)(row0 + i) * p.H + h) * D + c8;
         if (p.out_dtype == DR_F32) {
+            float x[8];
+            unpack8(piece, x);
             float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.u) + e);
             d[0] = make_float4(x[0], x[1], x[2], x[3]);
             d[1] = make_float4(x[4], x[5], x[6], x[7]);
         } else {
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.u) + e) =
-                make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                           pack_bf16(x[6], x[7]));
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.u) + e) = piece;
         }
     }
 }
@@ -1003,8 +991,14 @@ cudaError_t launch_scan_fwd(const Params& p, const TcLayout& L, cudaStream_t st,
         if (e != cudaSuccess) return e;
     }
     if (p.N * p.H == 0) return cudaSuccess;
+    // bf16 o leaves whole chunks by tensor stores (a map over [rows, H, D], as the inputs)
+    CUtensorMap mo;
+    std::memset(&mo, 0, sizeof(mo));
+    const bool stage_o = write_o && p.o && p.out_dtype == DR_BF16 &&
+                         make_token_map(&mo, p.o, D, p.H, (long long)p.B * p.T);
     TraceScope ts("tc_scan_fwd", st);
-    tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), kScanFwdThreads, smem, st>>>(p, L, write_o ? 1 : 0);
+    tc_scan_fwd_kernel<D, BV><<<dim3(p.N * p.H, D / BV), kScanFwdThreads, smem, st>>>(
+        mo, p, L, write_o ? 1 : 0, stage_o ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -4,8 +4,8 @@
 // "Tile images" are byte-for-byte copies of SW128 shared-memory tiles (see
 // tc.cuh) so a kernel fetches one with a single untiled bulk copy.
 //   Wy, Qt, KC        : [64 tokens][D] tile images             (64*D*2 bytes)
-//   U, dU             : [D value channels][64 tokens] tile images of U^T and -dU^T
-//   UtT, OtT          : [D][64] tile images of Ut^T and Ot^T   (D*64*2 bytes)
+//   Ut, Ot, U         : [64 tokens][D value channels] tile images
+//   dU                : [D value channels][64 tokens] tile image of -dU^T
 //   T                 : [64][64] tile image of the UT inverse  (8 KB)
 //   S, dS             : [D rows = value channel][D cols = key channel] tile images
 //                       (W layout) of the state at the chunk start / of dL/d(state
@@ -21,7 +21,7 @@
 namespace dr {
 
 struct TcLayout {
-    uint8_t *Wy, *Qt, *KC, *U, *dU, *UtT, *OtT, *T, *S, *dS, *dUx;
+    uint8_t *Wy, *Qt, *KC, *U, *dU, *Ut, *Ot, *T, *S, *dS, *dUx;
     float* gC;
 };
 
@@ -50,8 +50,8 @@ __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
     L.KC = take(recs * s.kd);
     L.U = take(recs * s.kd);
     L.dU = take(recs * s.kd);
-    L.UtT = take(recs * s.kd);
-    L.OtT = take(recs * s.kd);
+    L.Ut = take(recs * s.kd);
+    L.Ot = take(recs * s.kd);
     L.T = take(recs * s.cc);
     L.S = take(recs * s.dd);
     L.dS = take(recs * s.dd);
