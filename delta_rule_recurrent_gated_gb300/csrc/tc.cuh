@@ -171,6 +171,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 lanes x 32 bits, twice: threads 0..15 of the warp receive columns [col, col+16) of
+// TMEM lanes (warp_base + t), threads 16..31 columns [col + OFF, col + OFF + 16) of lanes
+// (warp_base + t - 16).  An M = 64 accumulator keeps its rows in lanes 0..15 of each
+// warp quarter, so this shape gives every thread of the warp half of a row's columns.
+template <int OFF>
+__device__ __forceinline__ void tmem_ld16_x2(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr), "n"(OFF));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -327,6 +344,12 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* v) {
 __device__ __forceinline__ uint32_t warp_lane_base(uint32_t tmem) {
     return tmem + ((uint32_t)((threadIdx.x >> 5) & 3) * 32u << 16);
 }
+// Row of an M = 64 accumulator that tmem_ld16_x2 gives this thread (both halves of the
+// warp read rows 16w..16w+15 of warp quarter w), and which half of the columns.
+__device__ __forceinline__ int m64_row_x2() {
+    return (int)((threadIdx.x >> 5) & 3) * 16 + (int)(threadIdx.x & 15);
+}
+__device__ __forceinline__ int m64_half_x2() { return (int)((threadIdx.x >> 4) & 1); }
 // Row of the accumulator held by this thread for an M = 64 product (rows
 // 16w..16w+15 sit in lanes 0..15 of warp quarter w), or -1.
 __device__ __forceinline__ int m64_row() {

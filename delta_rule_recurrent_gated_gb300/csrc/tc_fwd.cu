@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = m64_row();
+    const int r2 = m64_row_x2(), h2 = m64_half_x2();  // M = 64 row and column half (tmem_ld16_x2)
     bool ok = true;
     bool ld_phase2 = false;  // KDA: the second gate copy was issued
 
@@ -425,21 +425,23 @@ __global__ void __launch_bounds__(128, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
-        // A = diag(beta) strict_lower(Gram) (fp32) and the masked Aqk tile
-        for (int cb = 0; cb < 4; ++cb) {
-            float g16[16], a16[16];
-            tmem_ld16(tl + cb * 16, g16);
-            tmem_ld16(tl + 64 + cb * 16, a16);
-            tmem_ld_wait();
-            if (r >= 0) {
-                const float br = beta_s[r];
+        // A = diag(beta) strict_lower(Gram) (fp32) and the masked Aqk tile; each row's 64
+        // columns are split over two threads (columns 32 h2 + 16 cb + j)
+        {
+            const float br = beta_s[r2];
+            for (int cb = 0; cb < 2; ++cb) {
+                float g16[16], a16[16];
+                tmem_ld16_x2<32>(tl + cb * 16, g16);
+                tmem_ld16_x2<32>(tl + 64 + cb * 16, a16);
+                tmem_ld_wait();
+                const int c0 = h2 * 32 + cb * 16;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int col = cb * 16 + j;
-                    Af[col * 64 + r] = col < r ? br * g16[j] : 0.f;  // column-major A
-                    a16[j] = col <= r ? a16[j] : 0.f;
+                    const int col = c0 + j;
+                    Af[col * 64 + r2] = col < r2 ? br * g16[j] : 0.f;  // column-major A
+                    a16[j] = col <= r2 ? a16[j] : 0.f;
                 }
-                tile_store16(Aqs, r, cb * 16, 64, a16);
+                tile_store16(Aqs, r2, c0, 64, a16);
             }
         }
         tc_fence_before();
@@ -539,15 +541,14 @@ __global__ void __launch_bounds__(128, 1)
 
         // Wy and Ut into their operand tiles (Ut where Kr was, which is consumed); the
         // workspace images ([64][D] SW128 tile images) are bulk copies of those tiles
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = 0; cb < D / 32; ++cb) {
             float w16[16], u16[16];
-            tmem_ld16(tl + cb * 16, w16);
-            tmem_ld16(tl + 128 + cb * 16, u16);
+            tmem_ld16_x2<D / 2>(tl + cb * 16, w16);
+            tmem_ld16_x2<D / 2>(tl + 128 + cb * 16, u16);
             tmem_ld_wait();
-            if (r >= 0) {
-                tile_store16(Xs, r, cb * 16, 64, w16);
-                tile_store16(Ks, r, cb * 16, 64, u16);
-            }
+            const int c0 = h2 * (D / 2) + cb * 16;
+            tile_store16(Xs, r2, c0, 64, w16);
+            tile_store16(Ks, r2, c0, 64, u16);
         }
         fence_async_smem();
         tc_fence_before();
@@ -572,21 +573,20 @@ __global__ void __launch_bounds__(128, 1)
             uint8_t* qt_img = L.Qt + rec * kTile;
             uint8_t* ot_img = L.Ot + rec * kTile;  // [64][D] SW128 tile image of Ot
             const float sc = p.scale;
-            for (int cb = 0; cb < D / 16; ++cb) {
+            for (int cb = 0; cb < D / 32; ++cb) {
                 float w16[16], o16[16], qb[16];
-                tmem_ld16(tl + cb * 16, w16);
-                tmem_ld16(tl + 128 + cb * 16, o16);
+                tmem_ld16_x2<D / 2>(tl + cb * 16, w16);
+                tmem_ld16_x2<D / 2>(tl + 128 + cb * 16, o16);
                 tmem_ld_wait();
-                if (r >= 0) {
-                    tile_load16(Qs, r, cb * 16, 64, qb);  // Qb' = q e^{Gamma - Gamma_r}
+                const int c0 = h2 * (D / 2) + cb * 16;
+                tile_load16(Qs, r2, c0, 64, qb);  // Qb' = q e^{Gamma - Gamma_r}
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        qb[j] = sc * (qb[j] * Rf[cb * 16 + j] - w16[j]);
-                        o16[j] *= sc;
-                    }
-                    tile_store16(qt_img, r, cb * 16, 64, qb);
-                    tile_store16(ot_img, r, cb * 16, 64, o16);
+                for (int j = 0; j < 16; ++j) {
+                    qb[j] = sc * (qb[j] * Rf[c0 + j] - w16[j]);
+                    o16[j] *= sc;
                 }
+                tile_store16(qt_img, r2, c0, 64, qb);
+                tile_store16(ot_img, r2, c0, 64, o16);
             }
         }
     } while (0);
