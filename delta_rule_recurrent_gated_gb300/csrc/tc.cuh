@@ -188,6 +188,18 @@ __device__ __forceinline__ void tmem_ld16_x2(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same shape, 8 columns per half: threads 0..15 columns [col, col+8), threads 16..31
+// columns [col + OFF, col + OFF + 8).
+template <int OFF>
+__device__ __forceinline__ void tmem_ld8_x2(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr), "n"(OFF));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -300,6 +312,16 @@ __device__ __forceinline__ void tile_store16(uint8_t* base, int row, int col0, i
         u.w = pack_bf16(v[8 * h + 6], v[8 * h + 7]);
         *reinterpret_cast<uint4*>(base + sw128_offset(row, col0 + 8 * h, rows)) = u;
     }
+}
+// Write 8 consecutive values (col0 multiple of 8) of one tile row as bf16.
+__device__ __forceinline__ void tile_store8(uint8_t* base, int row, int col0, int rows,
+                                            const float (&v)[8]) {
+    uint4 u;
+    u.x = pack_bf16(v[0], v[1]);
+    u.y = pack_bf16(v[2], v[3]);
+    u.z = pack_bf16(v[4], v[5]);
+    u.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4*>(base + sw128_offset(row, col0, rows)) = u;
 }
 // Read 16 consecutive values (col0 multiple of 16) of one tile row.
 __device__ __forceinline__ void tile_load16(const uint8_t* base, int row, int col0, int rows,

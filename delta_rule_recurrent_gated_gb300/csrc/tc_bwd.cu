@@ -536,8 +536,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = m64_row();                            // row of an M = 64 accumulator, or -1
-    const int cl = D == 128 ? (tid & 127) : r;          // channel of an M = D accumulator, or -1
+    // row of an M = 64 accumulator read with tmem_ld8_x2, and which 8 of a 16-column block
+    const int r2 = m64_row_x2(), h2 = m64_half_x2();
+    const int cl = D == 128 ? (tid & 127) : m64_row();  // channel of an M = D accumulator, or -1
     const int t0 = kTok * grp;                          // first token of this thread's group
     // Element (t0 + k, cl) of a [64][D] SW128 token tile sits at xo[k % 8] + 128 k: the
     // swizzle depends on the row only through k % 8 because t0 is a multiple of 16.
@@ -971,21 +972,20 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // E2: Aqk = tril(Qb Kr^T) ; P = (dO v^T - dQt Kb^T) diag(beta)
 #pragma unroll 1
         for (int cb = grp; cb < 4; cb += kG) {
-            float a[16], p1[16], p2[16];
-            tmem_ld16(tl + C3 + cb * 16, a);
-            tmem_ld16(tl + C4 + cb * 16, p1);
-            tmem_ld16(tl + C2 + cb * 16, p2);
+            float a[8], p1[8], p2[8];
+            tmem_ld8_x2<8>(tl + C3 + cb * 16, a);
+            tmem_ld8_x2<8>(tl + C4 + cb * 16, p1);
+            tmem_ld8_x2<8>(tl + C2 + cb * 16, p2);
             tmem_ld_wait();
-            if (r >= 0) {
+            const int c0 = cb * 16 + h2 * 8;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = cb * 16 + j;
-                    a[j] = col <= r ? a[j] : 0.f;
-                    p1[j] = beta_s[col] * (p1[j] - p2[j]);
-                }
-                tile_store16(Aqs, r, cb * 16, 64, a);
-                tile_store16(B8a, r, cb * 16, 64, p1);
+            for (int j = 0; j < 8; ++j) {
+                const int col = c0 + j;
+                a[j] = col <= r2 ? a[j] : 0.f;
+                p1[j] = beta_s[col] * (p1[j] - p2[j]);
             }
+            tile_store8(Aqs, r2, c0, 64, a);
+            tile_store8(B8a, r2, c0, 64, p1);
         }
         fence_async_smem();
         tc_fence_before();
@@ -1005,14 +1005,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int cb = grp; cb < 4; cb += kG) {
-            float a[16];
-            tmem_ld16(tl + C0 + cb * 16, a);
+            float a[8];
+            tmem_ld8_x2<8>(tl + C0 + cb * 16, a);
             tmem_ld_wait();
-            if (r >= 0) {
+            const int c0 = cb * 16 + h2 * 8;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a[j] = (cb * 16 + j <= r) ? sc * a[j] : 0.f;
-                tile_store16(dAqs, r, cb * 16, 64, a);
-            }
+            for (int j = 0; j < 8; ++j) a[j] = (c0 + j <= r2) ? sc * a[j] : 0.f;
+            tile_store8(dAqs, r2, c0, 64, a);
         }
 #pragma unroll 1
         for (int b = 0; b < kTok / 16; ++b) {
@@ -1057,31 +1056,29 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         //                        = sum_i T[i,j] (dWy Kb^T + dUt v^T)[i,j]
         float dbeta_acc = 0.f;
         {
-            // column r of T: element (16 cb + j, r) at xr[j % 8] + 128 (16 cb + j)
+            // column r2 of T: element (c0 + j, r2) at xr[j] + 128 (c0 + j), c0 a multiple of 8
             uint32_t xr[8];
-            const int rc = r < 0 ? 0 : r;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) xr[k] = (uint32_t)(((((rc >> 3) & 7) ^ k) << 4) + (rc & 7) * 2);
+            for (int k = 0; k < 8; ++k) xr[k] = (uint32_t)(((((r2 >> 3) & 7) ^ k) << 4) + (r2 & 7) * 2);
+            const float br = beta_s[r2];
 #pragma unroll 1
             for (int n = 0; n < 4 / kG; ++n) {
                 const int cb = grp + kG * n;
-                float a[16], b[16];
-                tmem_ld16(tl + C0 + cb * 16, a);
-                tmem_ld16(tl + C1 + cb * 16, b);
+                float a[8], b[8];
+                tmem_ld8_x2<8>(tl + C0 + cb * 16, a);
+                tmem_ld8_x2<8>(tl + C1 + cb * 16, b);
                 tmem_ld_wait();
-                if (r >= 0) {
-                    const float br = beta_s[r];
-                    const uint8_t* tcol = Ts + cb * 16 * 128;
+                const int c0 = cb * 16 + h2 * 8;
+                const uint8_t* tcol = Ts + c0 * 128;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float s = a[j] + b[j];
-                        const float tij = __bfloat162float(
-                            *reinterpret_cast<const __nv_bfloat16*>(tcol + xr[j & 7] + j * 128));
-                        dbeta_acc = fmaf(tij, s, dbeta_acc);
-                        a[j] = br * s;
-                    }
-                    tile_store16(B8b, r, cb * 16, 64, a);
+                for (int j = 0; j < 8; ++j) {
+                    const float s = a[j] + b[j];
+                    const float tij = __bfloat162float(
+                        *reinterpret_cast<const __nv_bfloat16*>(tcol + xr[j] + j * 128));
+                    dbeta_acc = fmaf(tij, s, dbeta_acc);
+                    a[j] = br * s;
                 }
+                tile_store8(B8b, r2, c0, 64, a);
             }
         }
         fence_async_smem();
@@ -1126,10 +1123,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int cb = grp; cb < 4; cb += kG) {
-            float a[16];
-            tmem_ld16(tl + C0 + cb * 16, a);
+            float a[8];
+            tmem_ld8_x2<8>(tl + C0 + cb * 16, a);
             tmem_ld_wait();
-            if (r >= 0) tile_store16(B8a, r, cb * 16, 64, a);
+            tile_store8(B8a, r2, cb * 16 + h2 * 8, 64, a);
         }
         fence_async_smem();
         tc_fence_before();
@@ -1188,23 +1185,24 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         // E6: dA = -T^T X (strictly lower), the A part of dbeta, dG = diag(beta) dA
 #pragma unroll 1
         for (int cb = grp; cb < 4; cb += kG) {
-            float a[16], gm[16];
-            tmem_ld16(tl + C0 + cb * 16, a);
-            tmem_ld16(tl + C6 + cb * 16, gm);
+            float a[8], gm[8];
+            tmem_ld8_x2<8>(tl + C0 + cb * 16, a);
+            tmem_ld8_x2<8>(tl + C6 + cb * 16, gm);
             tmem_ld_wait();
-            if (r >= 0) {
-                const float br = beta_s[r];
+            const float br = beta_s[r2];
+            const int c0 = cb * 16 + h2 * 8;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const bool low = cb * 16 + j < r;  // the Gram above the diagonal may be inf
-                    const float dA = low ? -a[j] : 0.f;
-                    if (low) dbeta_acc = fmaf(dA, gm[j], dbeta_acc);
-                    a[j] = br * dA;  // dG
-                }
-                tile_store16(B8b, r, cb * 16, 64, a);
+            for (int j = 0; j < 8; ++j) {
+                const bool low = c0 + j < r2;  // the Gram above the diagonal may be inf
+                const float dA = low ? -a[j] : 0.f;
+                if (low) dbeta_acc = fmaf(dA, gm[j], dbeta_acc);
+                a[j] = br * dA;  // dG
             }
+            tile_store8(B8b, r2, c0, 64, a);
         }
-        if (grp > 0 && r >= 0) part[(grp - 1) * 64 + r] = dbeta_acc;
+        // the two threads of a row hold the sums over their halves of the columns
+        dbeta_acc += __shfl_xor_sync(0xffffffffu, dbeta_acc, 16);
+        if (grp > 0 && h2 == 0) part[(grp - 1) * 64 + r2] = dbeta_acc;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -1219,11 +1217,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             mma_commit(&bar_mma);
         }
         // while M6 runs: dbeta and the staged dq go out
-        if (grp == 0 && r >= 0 && r < len) {
+        if (grp == 0 && h2 == 0 && r2 < len) {
             float db = dbeta_acc;
-            for (int q = 1; q < kG; ++q) db += part[(q - 1) * 64 + r];
-            if (PREP) db *= beta_s[r] * (1.f - beta_s[r]);  // through beta = sigmoid(b)
-            p.dbeta[(size_t)(row0 + r) * p.H + h] = db;
+            for (int q = 1; q < kG; ++q) db += part[(q - 1) * 64 + r2];
+            if (PREP) db *= beta_s[r2] * (1.f - beta_s[r2]);  // through beta = sigmoid(b)
+            p.dbeta[(size_t)(row0 + r2) * p.H + h] = db;
         }
         if (PREP) {
             // q_hat from the Qb' tile: e^{Gamma_r - Gamma} per row (GDN), 1 / e^{Gamma - Gamma_r}
