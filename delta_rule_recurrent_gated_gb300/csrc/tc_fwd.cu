@@ -178,7 +178,10 @@ __global__ void __launch_bounds__(128, 1)
                 tma_load_3d(Ks + kb * 8192, &mk, &bar_ld, kb * 64, h, row0);
                 tma_load_3d(Vs + kb * 8192, &mv, &bar_ld, kb * 64, h, row0);
             }
-            if (VAR == DR_KDA) tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
+            if (VAR == DR_KDA) {
+                tma_load_3d(Aqs, &mg, &bar_ld, 0, h, row0);
+                tma_prefetch_3d(&mg, 0, h, row0 + 32);  // the second half's gates, into L2
+            }
         }
         // GDN's log-decays (two per lane of warp 0) are read while the tiles land
         float ga0 = 0.f, ga1 = 0.f;
