@@ -58,6 +58,12 @@ __device__ __forceinline__ void zero_pad_rows(uint8_t* tile, int D, int len) {
 }
 
 // ============================================================== tc_scan_bwd
+// 288 threads: warps 0-7 carry the chain (the thread of warp w holds state row r, lane
+// quarter w % 4, and the half w / 4 of its key columns and of the -dU^T tokens); warp 8
+// issues the loads and the dS image.
+constexpr int kScanBwdThreads = 288;
+constexpr int kScanBwdMathThreads = 256;
+
 template <int D, int BV>
 struct BScanSmem {
     static constexpr int kTile = 64 * D * 2;
@@ -74,18 +80,22 @@ struct BScanSmem {
 };
 
 template <int D, int BV>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kScanBwdThreads, 1)
     tc_scan_bwd_kernel(const __grid_constant__ CUtensorMap mdo, const Params p, const TcLayout L) {
     using S = BScanSmem<D, BV>;
     constexpr int kTile = S::kTile;
+    constexpr int DH = D / 2;  // key columns of a state thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* Ws = sm + S::kW;
     uint8_t* dUs = sm + S::kdU;
     __shared__ uint64_t bar_ld[2], bar_mma;
     __shared__ uint32_t tmem_base;
+    __shared__ int s_fail;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const bool math = tid < kScanBwdMathThreads;  // the eight epilogue / state warps
+    const int hf = (warp >> 2) & 1;               // which half of the columns
     const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
     const int v0 = blockIdx.y * BV;
     int c0, nc, srow, slen;
@@ -97,6 +107,7 @@ __global__ void __launch_bounds__(128, 1)
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
         prefetch_tmap(&mdo);
+        s_fail = 0;
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 256);
@@ -107,10 +118,13 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = (BV == 128) ? tid : m64_row();
+    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row();  // state row (or -1)
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
-    int issued[2] = {0, 0}, waited[2] = {0, 0};
+    // Thread kIss (lane 0 of the copy warp) issues the loads and the dS image; thread 0
+    // the products and the -dU^T image.
+    constexpr int kIss = kScanBwdMathThreads;
+    int issued[2] = {0, 0};  // bulk-load phases per stage (thread kIss)
 
     // iteration it handles chunk nc-1-it, in stage it & 1
     auto load_iter = [&](int it) {
@@ -128,18 +142,18 @@ __global__ void __launch_bounds__(128, 1)
         bulk_g2s(st + S::kG, L.gC + rec * D, D * 4, &bar_ld[s]);
         ++issued[s];
     };
-    if (tid == 0 && nc > 0) load_iter(0);
+    if (tid == kIss && nc > 0) load_iter(0);
 
-    float W[D];  // dS[:, v] (the gradient of the state at the current chunk end)
+    float W[DH];  // dS[hf*DH + c, v] (the gradient of the state at the current chunk end)
 #pragma unroll
-    for (int c = 0; c < D; ++c) W[c] = (p.dhT && r >= 0) ? p.dhT[state_off + (size_t)c * D + v] : 0.f;
+    for (int c = 0; c < DH; ++c) W[c] = (p.dhT && r >= 0) ? p.dhT[state_off + (size_t)(hf * DH + c) * D + v] : 0.f;
     if (r >= 0) {
 #pragma unroll
-        for (int cb = 0; cb < D / 16; ++cb) {
+        for (int cb = 0; cb < DH / 16; ++cb) {
             float t[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
-            tile_store16(Ws, r, cb * 16, BV, t);
+            tile_store16(Ws, r, hf * DH + cb * 16, BV, t);
         }
     }
     fence_async_smem();
@@ -148,34 +162,36 @@ __global__ void __launch_bounds__(128, 1)
     bool ok = true;
     for (int it = 0; it < nc && ok; ++it) {
         const int s = it & 1, ci = nc - 1 - it;
-        const uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
+        uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
-        if (tid == 0) {
+        if (tid == kIss) {
+            // the next chunk's tiles into stage s^1 (released at the end of the previous
+            // iteration), then rows [v0, v0+BV) of the W-layout image of dS at this chunk's end
             if (it + 1 < nc) load_iter(it + 1);
-            // rows [v0, v0+BV) of the W-layout image of dS at this chunk's end
             uint8_t* ds_img = L.dS + rec * (size_t)D * D * 2;
             for (int kb = 0; kb < D / 64; ++kb)
                 bulk_s2g(ds_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
             bulk_commit();
         }
         ok = mbar_wait(&bar_ld[s], (it >> 1) & 1, kWaitLimitNs);
-        if (tid == 0) ++waited[s];
         if (__syncthreads_or(!ok)) break;
 
-        // dU^T = dS^T KC^T -> cols [0,64)
+        // dU^T = dS^T KC^T -> cols [0,64); then dO^T Qt -> cols [64, 64+D), which does not
+        // depend on the chain and runs during the -dU^T epilogue
         if (tid == 0) {
             tc_fence_after();
-            const Tile tW{smem_u32(Ws), BV}, tK{smem_u32(st + S::kKC), 64};
-            mma_tiles(tm + 0, tW, false, tK, false, BV, 64, D, false);
+            mma_tiles(tm + 0, Tile{smem_u32(Ws), BV}, false, Tile{smem_u32(st + S::kKC), 64}, false, BV, 64, D,
+                      false);
             mma_commit(&bar_mma);
+            mma_tiles(tm + 64, Tile{smem_u32(st + S::kdO), 64}, true, Tile{smem_u32(st + S::kQt), 64}, true, BV,
+                      D, 64, false);
         }
-        ok = mbar_wait(&bar_mma, 0, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
+        if (math && !mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
         tc_fence_after();
-        for (int g = 0; g < 4; g += 2) {  // two loads in flight per wait
+        if (math) {  // -dU^T for this thread's 32 tokens [32 hf, 32 hf + 32)
             float acc[16], acc2[16];
-            tmem_ld16(tl + g * 16, acc);
-            tmem_ld16(tl + (g + 1) * 16, acc2);
+            tmem_ld16(tl + hf * 32, acc);
+            tmem_ld16(tl + hf * 32 + 16, acc2);
             tmem_ld_wait();
             if (r >= 0) {
 #pragma unroll
@@ -187,78 +203,80 @@ __global__ void __launch_bounds__(128, 1)
                     const uint8_t* xrow = st + S::kdUx + r * 128;
                     float x[16];
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((2 * g + q) ^ (r & 7)) << 4)), x + 8 * q);
-                    }
+                    for (int q = 0; q < 2; ++q)
+                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((4 * hf + q) ^ (r & 7)) << 4)), x + 8 * q);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] += x[j];
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((2 * g + 2 + q) ^ (r & 7)) << 4)), x + 8 * q);
-                    }
+                    for (int q = 0; q < 2; ++q)
+                        unpack8(*reinterpret_cast<const uint4*>(xrow + (((4 * hf + 2 + q) ^ (r & 7)) << 4)), x + 8 * q);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc2[j] += x[j];
                 }
-                tile_store16(dUs, r, g * 16, BV, acc);
-                tile_store16(dUs, r, (g + 1) * 16, BV, acc2);
+                tile_store16(dUs, r, hf * 32, BV, acc);
+                tile_store16(dUs, r, hf * 32 + 16, BV, acc2);
             }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // dO^T Qt - dU^T Wy -> cols [64, 64+D); -dU^T rows [v0, v0+BV) of its image
+        // + (-dU^T) Wy -> cols [64, 64+D); -dU^T rows [v0, v0+BV) of its image
         if (tid == 0) {
             tc_fence_after();
-            const Tile tO{smem_u32(st + S::kdO), 64}, tU{smem_u32(dUs), BV},
-                tQ{smem_u32(st + S::kQt), 64}, tWy{smem_u32(st + S::kWy), 64};
-            mma_tiles(tm + 64, tO, true, tQ, true, BV, D, 64, false);
-            mma_tiles(tm + 64, tU, false, tWy, true, BV, D, 64, true);
+            mma_tiles(tm + 64, Tile{smem_u32(dUs), BV}, false, Tile{smem_u32(st + S::kWy), 64}, true, BV, D, 64,
+                      true);
             mma_commit(&bar_mma);
             bulk_s2g(L.dU + rec * kTile + (size_t)v0 * 128, dUs, BV * 128);
             bulk_commit();
         }
-        ok = mbar_wait(&bar_mma, 1, kWaitLimitNs);
-        if (tid == 0) bulk_wait_read();
-        if (__syncthreads_or(!ok)) break;
+        if (tid == kIss) bulk_wait_read();  // the dS image has left Ws
+        if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
+        if (tid == 0) bulk_wait_read();     // the -dU^T image has left dUs
+        __syncthreads();
         tc_fence_after();
-        const float* gCs = reinterpret_cast<const float*>(st + S::kG);
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + hf * DH;
+        if (math) {
 #pragma unroll
-        for (int cb = 0; cb < D / 16; cb += 2) {  // two loads in flight per wait
-            float acc[16], acc2[16];
-            tmem_ld16(tl + 64 + cb * 16, acc);
-            tmem_ld16(tl + 64 + (cb + 1) * 16, acc2);
-            tmem_ld_wait();
+            for (int cb = 0; cb < DH / 16; cb += 2) {  // two loads in flight per wait
+                float acc[16], acc2[16];
+                tmem_ld16(tl + 64 + hf * DH + cb * 16, acc);
+                tmem_ld16(tl + 64 + hf * DH + (cb + 1) * 16, acc2);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int c = cb * 16 + j;
-                W[c] = fmaf(W[c], gCs[c], acc[j]);
-                acc[j] = W[c];
-                W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
-                acc2[j] = W[c + 16];
-            }
-            if (r >= 0) {
-                tile_store16(Ws, r, cb * 16, BV, acc);
-                tile_store16(Ws, r, (cb + 1) * 16, BV, acc2);
+                for (int j = 0; j < 16; ++j) {
+                    const int c = cb * 16 + j;
+                    W[c] = fmaf(W[c], gCs[c], acc[j]);
+                    acc[j] = W[c];
+                    W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                    acc2[j] = W[c + 16];
+                }
+                if (r >= 0) {
+                    tile_store16(Ws, r, hf * DH + cb * 16, BV, acc);
+                    tile_store16(Ws, r, hf * DH + (cb + 1) * 16, BV, acc2);
+                }
             }
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(s_fail != 0)) {
+            ok = false;
+            break;
+        }
     }
 
     if (ok) {
         if (p.dh0 && r >= 0) {
 #pragma unroll
-            for (int c = 0; c < D; ++c) p.dh0[state_off + (size_t)c * D + v] = W[c];
+            for (int c = 0; c < DH; ++c) p.dh0[state_off + (size_t)(hf * DH + c) * D + v] = W[c];
         }
     } else {
         record_timeout(p);
-        if (tid == 0)
+        if (tid == kIss)  // the latest copy issued into each stage has landed before exit
             for (int s = 0; s < 2; ++s)
-                if (issued[s] > waited[s]) mbar_wait(&bar_ld[s], waited[s] & 1, kWaitLimitNs);
+                if (issued[s] > 0) mbar_wait(&bar_ld[s], (issued[s] - 1) & 1, kWaitLimitNs);
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0 || tid == kIss) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -1453,7 +1471,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
                 if (e != cudaSuccess) return e;
             }
             TraceScope ts("tc_scan_bwd", st);
-            kernel<<<dim3(p.N * p.H, D / bv), 128, smem, st>>>(mdo, p, L);
+            kernel<<<dim3(p.N * p.H, D / bv), kScanBwdThreads, smem, st>>>(mdo, p, L);
             return cudaGetLastError();
         };
         static std::atomic<unsigned long long> s64{0}, s128{0};
