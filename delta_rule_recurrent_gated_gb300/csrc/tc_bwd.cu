@@ -118,8 +118,14 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row();  // state row (or -1)
+    // state row (or -1) and this thread's key columns: BV = 128 gives a thread half a row;
+    // BV = 64 (M = 64 accumulators, read with the two-half-warp shape) a quarter of a row,
+    // and 16 of the tokens of -dU^T
+    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row_x2();
     const int v = v0 + (r < 0 ? 0 : r);
+    constexpr int WC = BV == 128 ? DH : DH / 2;
+    const int h2 = m64_half_x2();
+    const int cbase = hf * DH + (BV == 128 ? 0 : h2 * (DH / 2));
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
     // Thread kIss (lane 0 of the copy warp) issues the loads and the dS image; thread 0
     // the products and the -dU^T image.
@@ -144,16 +150,16 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
     };
     if (tid == kIss && nc > 0) load_iter(0);
 
-    float W[DH];  // dS[hf*DH + c, v] (the gradient of the state at the current chunk end)
+    float W[WC];  // dS[cbase + c, v] (the gradient of the state at the current chunk end)
 #pragma unroll
-    for (int c = 0; c < DH; ++c) W[c] = (p.dhT && r >= 0) ? p.dhT[state_off + (size_t)(hf * DH + c) * D + v] : 0.f;
+    for (int c = 0; c < WC; ++c) W[c] = (p.dhT && r >= 0) ? p.dhT[state_off + (size_t)(cbase + c) * D + v] : 0.f;
     if (r >= 0) {
 #pragma unroll
-        for (int cb = 0; cb < DH / 16; ++cb) {
+        for (int cb = 0; cb < WC / 16; ++cb) {
             float t[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
-            tile_store16(Ws, r, hf * DH + cb * 16, BV, t);
+            tile_store16(Ws, r, cbase + cb * 16, BV, t);
         }
     }
     fence_async_smem();
@@ -188,7 +194,24 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         }
         if (math && !mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
         tc_fence_after();
-        if (math) {  // -dU^T for this thread's 32 tokens [32 hf, 32 hf + 32)
+        if (math && BV == 64) {  // -dU^T for this thread's 16 tokens [32 hf + 16 h2, + 16)
+            float acc[16];
+            tmem_ld16_x2<16>(tl + hf * 32, acc);
+            tmem_ld_wait();
+            const int tb = hf * 32 + h2 * 16;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = -acc[j];
+            if (p.dU) {  // plus the packed -dU^T of the emitted write: row r, swizzled chunks
+                const uint8_t* xrow = st + S::kdUx + r * 128;
+                float x[16];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    unpack8(*reinterpret_cast<const uint4*>(xrow + (((tb / 8 + q) ^ (r & 7)) << 4)), x + 8 * q);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] += x[j];
+            }
+            tile_store16(dUs, r, tb, BV, acc);
+        } else if (math) {  // -dU^T for this thread's 32 tokens [32 hf, 32 hf + 32)
             float acc[16], acc2[16];
             tmem_ld16(tl + hf * 32, acc);
             tmem_ld16(tl + hf * 32 + 16, acc2);
@@ -235,25 +258,33 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         if (tid == 0) bulk_wait_read();     // the -dU^T image has left dUs
         __syncthreads();
         tc_fence_after();
-        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + hf * DH;
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + cbase;
         if (math) {
 #pragma unroll
-            for (int cb = 0; cb < DH / 16; cb += 2) {  // two loads in flight per wait
+            for (int cb = 0; cb < WC / 16; cb += 2) {  // two loads in flight per wait
+                constexpr bool kPair = WC / 16 >= 2;
                 float acc[16], acc2[16];
-                tmem_ld16(tl + 64 + hf * DH + cb * 16, acc);
-                tmem_ld16(tl + 64 + hf * DH + (cb + 1) * 16, acc2);
+                if constexpr (BV == 128) {
+                    tmem_ld16(tl + 64 + hf * DH + cb * 16, acc);
+                    tmem_ld16(tl + 64 + hf * DH + (cb + 1) * 16, acc2);
+                } else {  // the second half-warp reads DH / 2 columns further
+                    tmem_ld16_x2<DH / 2>(tl + 64 + hf * DH + cb * 16, acc);
+                    if (kPair) tmem_ld16_x2<DH / 2>(tl + 64 + hf * DH + (cb + 1) * 16, acc2);
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int c = cb * 16 + j;
                     W[c] = fmaf(W[c], gCs[c], acc[j]);
                     acc[j] = W[c];
-                    W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
-                    acc2[j] = W[c + 16];
+                    if (kPair) {
+                        W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                        acc2[j] = W[c + 16];
+                    }
                 }
                 if (r >= 0) {
-                    tile_store16(Ws, r, hf * DH + cb * 16, BV, acc);
-                    tile_store16(Ws, r, hf * DH + (cb + 1) * 16, BV, acc2);
+                    tile_store16(Ws, r, cbase + cb * 16, BV, acc);
+                    if (kPair) tile_store16(Ws, r, cbase + (cb + 1) * 16, BV, acc2);
                 }
             }
         }
@@ -268,7 +299,7 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
     if (ok) {
         if (p.dh0 && r >= 0) {
 #pragma unroll
-            for (int c = 0; c < DH; ++c) p.dh0[state_off + (size_t)(hf * DH + c) * D + v] = W[c];
+            for (int c = 0; c < WC; ++c) p.dh0[state_off + (size_t)(cbase + c) * D + v] = W[c];
         }
     } else {
         record_timeout(p);

@@ -680,7 +680,13 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = warp_lane_base(tm);
-    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row();  // state row (or -1)
+    // state row of U^T KC (or -1) and this thread's key columns: BV = 128 gives a thread
+    // half a row; BV = 64 (an M = 64 accumulator, read with the two-half-warp shape) a
+    // quarter of a row
+    const int r = !math ? -1 : (BV == 128) ? (tid & 127) : m64_row_x2();
+    constexpr int WC = BV == 128 ? DH : DH / 2;
+    const int cbase = hf * DH + (BV == 128 ? 0 : m64_half_x2() * (DH / 2));
+
     const int v = v0 + (r < 0 ? 0 : r);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
     // Thread kIss (lane 0 of the copy warp) issues the copies: the chunk-start state image,
@@ -713,16 +719,16 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
     };
     if (tid == kIss && nc > 0) load_chunk(0);
 
-    float W[DH];  // W[v, hf*DH + c] = S[hf*DH + c, v], fp32
+    float W[WC];  // W[v, cbase + c] = S[cbase + c, v], fp32
 #pragma unroll
-    for (int c = 0; c < DH; ++c) W[c] = (p.h0 && r >= 0) ? p.h0[state_off + (size_t)(hf * DH + c) * D + v] : 0.f;
+    for (int c = 0; c < WC; ++c) W[c] = (p.h0 && r >= 0) ? p.h0[state_off + (size_t)(cbase + c) * D + v] : 0.f;
     if (r >= 0) {
 #pragma unroll
-        for (int cb = 0; cb < DH / 16; ++cb) {
+        for (int cb = 0; cb < WC / 16; ++cb) {
             float t[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) t[j] = W[cb * 16 + j];
-            tile_store16(Ws, r, hf * DH + cb * 16, BV, t);
+            tile_store16(Ws, r, cbase + cb * 16, BV, t);
         }
     }
     fence_async_smem();
@@ -837,25 +843,33 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
         if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
         __syncthreads();  // the state image has left Ws, rewritten below
         tc_fence_after();
-        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + hf * DH;
+        const float* gCs = reinterpret_cast<const float*>(st + S::kG) + cbase;
         if (math) {
 #pragma unroll
-            for (int cb = 0; cb < DH / 16; cb += 2) {
+            for (int cb = 0; cb < WC / 16; cb += 2) {  // two loads in flight per wait
+                constexpr bool kPair = WC / 16 >= 2;
                 float acc[16], acc2[16];
-                tmem_ld16(tl + 128 + hf * DH + cb * 16, acc);
-                tmem_ld16(tl + 128 + hf * DH + (cb + 1) * 16, acc2);
+                if constexpr (BV == 128) {
+                    tmem_ld16(tl + 128 + hf * DH + cb * 16, acc);
+                    tmem_ld16(tl + 128 + hf * DH + (cb + 1) * 16, acc2);
+                } else {  // the second half-warp reads DH / 2 columns further
+                    tmem_ld16_x2<DH / 2>(tl + 128 + hf * DH + cb * 16, acc);
+                    if (kPair) tmem_ld16_x2<DH / 2>(tl + 128 + hf * DH + (cb + 1) * 16, acc2);
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int c = cb * 16 + j;
                     W[c] = fmaf(W[c], gCs[c], acc[j]);
                     acc[j] = W[c];
-                    W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
-                    acc2[j] = W[c + 16];
+                    if (kPair) {
+                        W[c + 16] = fmaf(W[c + 16], gCs[c + 16], acc2[j]);
+                        acc2[j] = W[c + 16];
+                    }
                 }
                 if (r >= 0) {
-                    tile_store16(Ws, r, hf * DH + cb * 16, BV, acc);
-                    tile_store16(Ws, r, hf * DH + (cb + 1) * 16, BV, acc2);
+                    tile_store16(Ws, r, cbase + cb * 16, BV, acc);
+                    if (kPair) tile_store16(Ws, r, cbase + (cb + 1) * 16, BV, acc2);
                 }
             }
         }
@@ -870,7 +884,7 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
     if (ok) {
         if (p.hT && r >= 0) {
 #pragma unroll
-            for (int c = 0; c < DH; ++c) p.hT[state_off + (size_t)(hf * DH + c) * D + v] = W[c];
+            for (int c = 0; c < WC; ++c) p.hT[state_off + (size_t)(cbase + c) * D + v] = W[c];
         }
     } else {
         record_timeout(p);
