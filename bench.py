@@ -43,35 +43,39 @@ def algorithmic(w, N):
     return flops, byts
 
 
-# DRAM bytes (read + write) per work item (chunk x head) from one ncu capture, with the
-# sha256 of the kernel source it was taken on; reported only while the source is unchanged.
-# profiles/dram_traffic_gdn_b2_t4096_h16_d128.md: 2048 records per launch.  Only the
-# chunk-parallel kernels, whose traffic per record does not depend on the batch.
+_FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
+            "4edc339d709f3de31f5a891fd8b115a850e4b1f42e9a1e0b560ca89e352ca346")
+_BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
+            "0b905a15462f5bbd66f4f466e50794e4701b36d687842bde78419a855cb37ecc")
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
+# from an ncu capture of the timed step of the full-size workload (profiles/
+# dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("tc_bwd_chunk", "gdn", 128): ((355029248 + 77033472) / 2048,
-                                   "delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-                                   "c8049b033855c9dfbb294e2a156d15a9dea3699c8a14770ef7ccb9e3e3db4257"),
-    ("tc_prep", "gdn", 128): ((102339584 + 129750784) / 2048,
-                              "delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
-                              "5e2d369426e2f0a53e16d1974770e159ddfd736a49091534d55d999e76316ab7"),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424774912 + 687097344, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687267328 + 496396288, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541224960 + 361376512, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418498816 + 383116288, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (691221760 + 690995200, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678714112 + 497501184, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541130496 + 361172480, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1694795264 + 637413376, _BWD_SRC),
 }
 
 
 def measured_traffic(name, w):
-    """DRAM bytes per launch of `name` on workload w from the recorded capture, or None."""
-    rec = MEASURED_TRAFFIC.get((name, w.variant, w.dk))
+    """DRAM bytes of one launch of `name` on workload w from the recorded capture, or None
+    (no capture of that workload, or the kernel's source changed since)."""
+    rec = MEASURED_TRAFFIC.get((w.name, name))
     if rec is None:
         return None
-    per_item, src, sha = rec
+    byts, (src, sha) = rec
     try:
         with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), src), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != sha:
                 return None
     except OSError:
         return None
-    if w.lengths is not None or w.varlen_total:
-        return None  # packed sequences: the item count depends on the drawn lengths
-    return per_item * ((w.T + 63) // 64 * w.B * w.H)
+    return byts
 
 
 def kernel_bytes(name, w, N):
@@ -81,13 +85,13 @@ def kernel_bytes(name, w, N):
     recs = chunks * H
     tile, dd = 64 * D * 2, D * D * 2
     g = {"deltanet": 0, "gdn": 4, "kda": 4 * D}[w.variant]
-    if name == "tc_prep":            # q, k, v, beta, g in; Wy, Qt, KC, Ut^T, Ot^T, T, gC out
+    if name == "tc_prep":            # q, k, v, beta, g in; Wy, Qt, KC, Ut, Ot, T, gC out
         return th * (3 * D * 2 + 4 + g) + recs * (5 * tile + 8192 + D * 4)
-    if name == "tc_scan_fwd":        # Wy, Qt, KC, Ut^T, Ot^T, gC in; o, U, S out
+    if name == "tc_scan_fwd":        # Wy, Qt, KC, Ut, Ot, gC in; o, U, S out
         return recs * (5 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
     if name == "tc_scan_bwd":        # KC, Qt, Wy, gC, dO in; dU, dS out
         return recs * (3 * tile + D * 4) + th * D * 2 + recs * (tile + dd)
-    if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, U^T, -dU^T, S, dS, T, gC in;
+    if name == "tc_bwd_chunk":       # q, k, v, dO, beta, g, U, -dU^T, S, dS, T, gC in;
         return (th * (4 * D * 2 + 4 + g) + recs * (2 * tile + 2 * dd + 8192 + D * 4)
                 + th * (3 * D * 2 + 4 + g))             # dq, dk, dv, dbeta, dg out
     return 0
@@ -464,9 +468,13 @@ def time_workload(name, dev, stream, steps, warmup, max_over_ranks, barrier, see
         kern[nm] = (tot + kms, n + 1)
     del prob, t, o, hT
     torch.cuda.empty_cache()
+    trs = {nm: measured_traffic(nm, w) for nm in kern}
+    traffic = (sum(trs[nm] * n / steps for nm, (tot, n) in kern.items())
+               if kern and all(v is not None for v in trs.values()) else None)
     return {"workload": w.name, "value": w.tokens / (ms / 1e3), "unit": "tokens/s",
             "ms_per_step": ms, "steps": steps, "warmup": warmup,
             "roofline_frac": t_roof / (ms / 1e3), "t_roof_ms": t_roof * 1e3,
+            "traffic_bytes_per_step": traffic, "algorithmic_bytes_per_step": byts,
             "kernels_ms": {nm: tot / n for nm, (tot, n) in kern.items()}}
 
 

@@ -49,9 +49,10 @@ def test_kernel_design_bytes(bench):
     assert bench.kernel_bytes("tc_prep", w, 8) == th * (3 * 256 + 4 + 4) + recs * (5 * tile + 8192 + 512)
     assert bench.kernel_bytes("tc_bwd_chunk", w, 8) == (
         th * (8 * 128 + 8) + recs * (2 * tile + 2 * dd + 8192 + 512) + th * (6 * 128 + 8))
-    # the recorded traffic capture scales with the items of the launch
+    # the recorded capture of this workload, while the kernel source is the captured one
     t = bench.measured_traffic("tc_bwd_chunk", w)
-    assert t is None or t == pytest.approx((355029248 + 77033472) / 2048 * recs)
+    assert t is None or t == 1418498816 + 383116288
+    assert bench.measured_traffic("tc_bwd_chunk", inputs.get("gdn_b2_t4096_h16_d128")) is None
 
 
 def test_fp32_peak_and_gdn2_flops(bench):
