@@ -312,11 +312,19 @@ __global__ void __launch_bounds__(128, 1)
                     if (__syncthreads_or(!ok)) break;
                 }
                 if (tid < D) {
-#pragma unroll 8
-                    for (int ii = 0; ii < 32; ++ii) {
-                        if (32 * half + ii < len)
-                            G += PREP ? prep_neg_softplus(Gb[ii * D + tid]) : Gb[ii * D + tid];
-                        Gb[ii * D + tid] = G;
+                    // 16 rows at a time: the loads are issued together, then the dependent sums
+#pragma unroll
+                    for (int i0 = 0; i0 < 32; i0 += 16) {
+                        float x[16];
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii) x[ii] = Gb[(i0 + ii) * D + tid];
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii) {
+                            if (32 * half + i0 + ii < len) G += PREP ? prep_neg_softplus(x[ii]) : x[ii];
+                            x[ii] = G;
+                        }
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii) Gb[(i0 + ii) * D + tid] = x[ii];
                     }
                     if (half == 0) {
                         Gr[tid] = G;
@@ -324,9 +332,22 @@ __global__ void __launch_bounds__(128, 1)
                     }
                 }
                 __syncthreads();
-                // all passes' q, k, v pieces are loaded before the first store
+                // all passes' q, k, v pieces are loaded before the first store; a thread's
+                // channels c8 .. c8+7 are the same in every pass (128 is a multiple of D / 8)
                 constexpr int kIt = 32 * (D / 8) / 128;
                 uint4 qb_[kIt], kb_[kIt], vb_[kIt];
+                float R8[8], E8[8];  // Gamma_r and e^{Gamma_r} of those channels
+                {
+                    const int c8 = (tid % (D / 8)) * 8;
+                    const float4* rp = reinterpret_cast<const float4*>(&Gr[c8]);
+                    const float4 r0 = rp[0], r1 = rp[1];
+                    R8[0] = r0.x; R8[1] = r0.y; R8[2] = r0.z; R8[3] = r0.w;
+                    R8[4] = r1.x; R8[5] = r1.y; R8[6] = r1.z; R8[7] = r1.w;
+                    const float4* ep = reinterpret_cast<const float4*>(&Rf[c8]);
+                    const float4 f0 = ep[0], f1 = ep[1];
+                    E8[0] = f0.x; E8[1] = f0.y; E8[2] = f0.z; E8[3] = f0.w;
+                    E8[4] = f1.x; E8[5] = f1.y; E8[6] = f1.z; E8[7] = f1.w;
+                }
 #pragma unroll
                 for (int u = 0; u < kIt; ++u) {
                     const int w = tid + 128 * u;
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(128, 1)
                     const int w = tid + 128 * u;
                     const int ii = w / (D / 8), c8 = (w % (D / 8)) * 8, i = 32 * half + ii;
                     const uint32_t off = sw128_offset(i, c8, 64);
-                    float q8[8], k8[8], v8[8], G8[8], R8[8], E8[8];
+                    float q8[8], k8[8], v8[8], G8[8];
                     unpack8(qb_[u], q8);
                     unpack8(kb_[u], k8);
                     unpack8(vb_[u], v8);
@@ -357,14 +378,6 @@ __global__ void __launch_bounds__(128, 1)
                     const float4 g0 = gp[0], g1 = gp[1];
                     G8[0] = g0.x; G8[1] = g0.y; G8[2] = g0.z; G8[3] = g0.w;
                     G8[4] = g1.x; G8[5] = g1.y; G8[6] = g1.z; G8[7] = g1.w;
-                    const float4* rp = reinterpret_cast<const float4*>(&Gr[c8]);
-                    const float4 r0 = rp[0], r1 = rp[1];
-                    R8[0] = r0.x; R8[1] = r0.y; R8[2] = r0.z; R8[3] = r0.w;
-                    R8[4] = r1.x; R8[5] = r1.y; R8[6] = r1.z; R8[7] = r1.w;
-                    const float4* ep = reinterpret_cast<const float4*>(&Rf[c8]);
-                    const float4 f0 = ep[0], f1 = ep[1];
-                    E8[0] = f0.x; E8[1] = f0.y; E8[2] = f0.z; E8[3] = f0.w;
-                    E8[4] = f1.x; E8[5] = f1.y; E8[6] = f1.z; E8[7] = f1.w;
                     uint32_t wq[4], wr[4], wb[4], wy[4], wv[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -398,14 +411,15 @@ __global__ void __launch_bounds__(128, 1)
             }
             __syncthreads();
             uint8_t* kc_img = L.KC + rec * kTile;
+            const int c8k = (tid % (D / 8)) * 8;  // the same channels in every pass
+            const float4* lp = reinterpret_cast<const float4*>(&GLs[c8k]);
+            const float4 l0 = lp[0], l1 = lp[1];
+            const float L8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
             for (int w = tid; w < 64 * (D / 8); w += 128) {
                 const int i = w / (D / 8), c8 = (w % (D / 8)) * 8;
                 const uint32_t off = sw128_offset(i, c8, 64);
                 float kr8[8];
                 unpack8(*reinterpret_cast<const uint4*>(Ks + off), kr8);
-                const float4* lp = reinterpret_cast<const float4*>(&GLs[c8]);
-                const float4 l0 = lp[0], l1 = lp[1];
-                const float L8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
                 uint32_t wc[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
