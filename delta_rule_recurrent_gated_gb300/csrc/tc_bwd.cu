@@ -693,18 +693,32 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
     };
     // per-token scalars of an item, read into registers ahead of time: beta (threads
-    // 64..127) and GDN's log-decays (two per lane of warp 1); with input preparation
-    // the raw values, mapped only when the item starts (so no thread waits on the loads
-    // before then)
-    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f;
+    // 64..127) and GDN's log-decays (two per lane of warp 1).  With input preparation the
+    // loads are raw and map_scalars applies the maps (beta = sigmoid(b), g = -softplus(x),
+    // and sigmoid(x) for the chain of dg) at the end of the previous item, where these
+    // warps wait for warp 0's dg scan, so neither the loads nor the maps delay an item.
+    float beta_ld = 0.f, gl0 = 0.f, gl1 = 0.f, sg0 = 0.f, sg1 = 0.f;
+    int scal_len = 0;  // the length of the item whose scalars are held
     auto load_scalars = [&](int itm) {
         const int c = itm / p.H, hh = itm % p.H;
         int sq, r0, ln;
         chunk_info(p, c, sq, r0, ln);
+        scal_len = ln;
         beta_ld = (tid >= 64 && tid < 128 && tid - 64 < ln) ? p.beta[(size_t)(r0 + tid - 64) * p.H + hh] : 0.f;
         if (VAR == DR_GDN && warp == 1) {
             gl0 = 2 * lane < ln ? p.g[(size_t)(r0 + 2 * lane) * p.H + hh] : 0.f;
             gl1 = 2 * lane + 1 < ln ? p.g[(size_t)(r0 + 2 * lane + 1) * p.H + hh] : 0.f;
+        }
+    };
+    auto map_scalars = [&]() {
+        if (!PREP) return;
+        const int ln = scal_len;
+        if (tid >= 64 && tid < 128) beta_ld = tid - 64 < ln ? prep_sigmoid(beta_ld) : 0.f;
+        if (VAR == DR_GDN && warp == 1) {
+            sg0 = prep_sigmoid(gl0);
+            sg1 = prep_sigmoid(gl1);
+            gl0 = 2 * lane < ln ? prep_neg_softplus(gl0) : 0.f;
+            gl1 = 2 * lane + 1 < ln ? prep_neg_softplus(gl1) : 0.f;
         }
     };
     uint32_t n_st = 0, n_tok = 0;  // copy groups issued on bar_st / bar_tok
@@ -712,6 +726,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         for (int c = tid; c < D; c += kChunkThreads) eref[c] = gcr[c] = 1.f;
     if ((int)blockIdx.x < nitems) {
         load_scalars(blockIdx.x);
+        map_scalars();
         if (tid == 0) {
             issue_tok(blockIdx.x, false);
             issue_state(blockIdx.x, false);
@@ -737,8 +752,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         uint8_t* dUts = R.dUt;  // -dU^T -> dUt^T
         float* gC_s = gC_b + (odd ? D : 0);
         fsum = 0.f;
-        if (tid >= 64 && tid < 128)  // with input preparation beta = sigmoid(b)
-            beta_s[tid - 64] = PREP ? (tid - 64 < len ? prep_sigmoid(beta_ld) : 0.f) : beta_ld;
+        if (tid >= 64 && tid < 128) beta_s[tid - 64] = beta_ld;  // mapped already (preparation)
         if (tid == kIssuer && next < nitems) {
             // the next item's q, k, v, dO boxes into L2 now; their loads into shared memory
             // can only be issued once this item's last stage has read those buffers
@@ -785,11 +799,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tot[pt * D + c] = G;
         } else if (VAR == DR_GDN) {
             if (warp == 1) {
-                if (PREP) {  // g = -softplus(x); sigmoid(x) is kept for the chain of dg
-                    sgx[2 * lane] = prep_sigmoid(gl0);
-                    sgx[2 * lane + 1] = prep_sigmoid(gl1);
-                    gl0 = 2 * lane < len ? prep_neg_softplus(gl0) : 0.f;
-                    gl1 = 2 * lane + 1 < len ? prep_neg_softplus(gl1) : 0.f;
+                if (PREP) {  // g = -softplus(x) (mapped already); sigmoid(x) for the chain of dg
+                    sgx[2 * lane] = sg0;
+                    sgx[2 * lane + 1] = sg1;
                 }
                 float x = gl0 + gl1;
 #pragma unroll
@@ -1437,6 +1449,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 if (2 * lane + 1 < len) p.dg[g1] = PREP ? -(e + x - a0) * sgx[2 * lane + 1] : e + x - a0;
             }
         }
+        if (next < nitems) map_scalars();  // the next item's (loaded before E8)
         tc_fence_before();
         __syncthreads();  // Xs, TMEM and the small arrays are reused by the next item
     }
