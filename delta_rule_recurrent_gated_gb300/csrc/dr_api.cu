@@ -110,8 +110,13 @@ size_t path_ws_bytes(const Params& p, Path path) {
 // With DR_FLAG_PREPARE_INPUTS on the fp32 CUDA-core path the prepared q, k, beta, g
 // follow the path's area; the tensor-core kernels prepare their inputs on the fly.
 size_t ws_bytes(const Params& p, Path path, int flags) {
+    if (path == Path::kTensor) {  // with preparation the tensor-core path keeps the row norms
+        Params q = p;
+        q.prepare = (flags & DR_FLAG_PREPARE_INPUTS) ? 1 : 0;
+        return path_ws_bytes(q, path);
+    }
     const size_t base = path_ws_bytes(p, path);
-    if (!(flags & DR_FLAG_PREPARE_INPUTS) || path == Path::kTensor) return base;
+    if (!(flags & DR_FLAG_PREPARE_INPUTS)) return base;
     return align256(base) + dr::prepare_bytes(p);
 }
 

@@ -684,7 +684,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         int sq, r0, ln;
         chunk_info(p, c, sq, r0, ln);
         const ChunkRoles R = chunk_roles(sm, kTile, odd);
-        mbar_arrive_expect_tx(&bar_tok, 4 * kTile);
+        mbar_arrive_expect_tx(&bar_tok, 4 * kTile + (PREP ? 512 : 0));
+        if (PREP) bulk_g2s(rq_s, L.RN + ((size_t)c * p.H + hh) * 128, 512, &bar_tok);  // row norms
         for (int kb = 0; kb < D / 64; ++kb) {
             tma_load_3d(R.Q + kb * 8192, &mq, &bar_tok, kb * 64, hh, r0);
             tma_load_3d(Ks + kb * 8192, &mk, &bar_tok, kb * 64, hh, r0);
@@ -839,29 +840,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             kv_[n] = *reinterpret_cast<const uint4*>(Ks + off);
             qv_[n] = *reinterpret_cast<const uint4*>(Qs + off);
         }
-        if (PREP) {  // L2 norms of the raw rows; the inverse norms are kept for the chain
+        if (PREP) {  // the inverse norms of the raw rows, as tc_prep formed them (with the tiles)
 #pragma unroll
             for (int n = 0; n < kPer; ++n) {
-                float q8[8], k8[8], a = 0.f, b = 0.f;
-                unpack8(qv_[n], q8);
-                unpack8(kv_[n], k8);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    a = fmaf(q8[j], q8[j], a);
-                    b = fmaf(k8[j], k8[j], b);
-                }
-                rq_[n] = a;
-                rk_[n] = b;
-            }
-#pragma unroll
-            for (int n = 0; n < kPer; ++n) {
-                rq_[n] = rsqrtf(lane_group_sum<D / 8>(rq_[n]) + kPrepEps);
-                rk_[n] = rsqrtf(lane_group_sum<D / 8>(rk_[n]) + kPrepEps);
-                const int w = tid + n * kChunkThreads;
-                if (w % (D / 8) == 0) {
-                    rq_s[w / (D / 8)] = rq_[n];
-                    rk_s[w / (D / 8)] = rk_[n];
-                }
+                const int i = (tid + n * kChunkThreads) / (D / 8);
+                rq_[n] = rq_s[i];
+                rk_[n] = rk_s[i];
             }
         }
 #pragma unroll

@@ -212,6 +212,10 @@ __global__ void __launch_bounds__(128, 1)
         if (PREP) {  // raw q, k rows: their inverse norms, applied in the decay pass
             row_inv_norms<D, 128>(Qs, Ks, RQ, RK);
             __syncthreads();
+            if (tid == 0) {  // the norms for the backward chunk kernel (RQ, RK contiguous)
+                bulk_s2g(L.RN + rec * 128, RQ, 512);
+                bulk_commit();
+            }
         }
 
         // decay, per token (DeltaNet, GDN): warp 0 scans the 64 log-decays, two per lane, and
@@ -987,10 +991,10 @@ bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows
 size_t tc_records(const Params& p) { return (size_t)p.num_chunks * p.H; }
 
 TcLayout tc_layout(const Params& p) {
-    return tc_layout_at(p.ws + 256, tc_records(p), p.dk);
+    return tc_layout_at(p.ws + 256, tc_records(p), p.dk, p.prepare != 0);
 }
 
-size_t tc_workspace_bytes(const Params& p) { return tc_layout_bytes(tc_records(p), p.dk); }
+size_t tc_workspace_bytes(const Params& p) { return tc_layout_bytes(tc_records(p), p.dk, p.prepare != 0); }
 
 template <int D, int VAR, bool PREP>
 cudaError_t launch_prep(const Params& p, const TcLayout& L, cudaStream_t st) {

@@ -13,6 +13,9 @@
 //   gC                : [D] fp32, e^{Gamma} at the chunk's last token
 //   dUx               : [D][64] tile image of -dU^T for the gradient of the emitted
 //                       write (dr_bwd_u), packed before the backward scan
+//   RN (with DR_FLAG_PREPARE_INPUTS only)
+//                     : [2][64] fp32, rsqrt(sum x^2 + eps) of the chunk's raw q and k rows,
+//                       written by tc_prep, read by tc_bwd_chunk
 #pragma once
 #include <cstdint>
 
@@ -23,6 +26,7 @@ namespace dr {
 struct TcLayout {
     uint8_t *Wy, *Qt, *KC, *U, *dU, *Ut, *Ot, *T, *S, *dS, *dUx;
     float* gC;
+    float* RN;
 };
 
 __host__ __device__ inline size_t tc_align(size_t x) { return (x + 1023) & ~(size_t)1023; }
@@ -34,13 +38,13 @@ struct TcSizes {
         : kd((size_t)64 * D * 2), dd((size_t)D * D * 2), cc(64 * 64 * 2), g((size_t)D * 4) {}
 };
 
-__host__ inline size_t tc_layout_bytes(size_t recs, int D) {
+__host__ inline size_t tc_layout_bytes(size_t recs, int D, bool prep) {
     TcSizes s(D);
     return tc_align(recs * s.kd) * 8 + tc_align(recs * s.cc) + tc_align(recs * s.dd) * 2 +
-           tc_align(recs * s.g);
+           tc_align(recs * s.g) + (prep ? tc_align(recs * 512) : 0);
 }
 
-__host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
+__host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D, bool prep) {
     TcSizes s(D);
     TcLayout L;
     uint8_t* p = base;
@@ -57,6 +61,7 @@ __host__ inline TcLayout tc_layout_at(uint8_t* base, size_t recs, int D) {
     L.dS = take(recs * s.dd);
     L.dUx = take(recs * s.kd);
     L.gC = reinterpret_cast<float*>(take(recs * s.g));
+    L.RN = prep ? reinterpret_cast<float*>(take(recs * 512)) : nullptr;
     return L;
 }
 

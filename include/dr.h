@@ -84,8 +84,9 @@ enum dr_dtype { DR_BF16 = 0, DR_F32 = 1 };
  * dr_bwd / dr_bwd_u take the same raw tensors and return gradients with respect to
  * them (dq, dk, dbeta, dg chained through the three maps).  On the bf16 tensor-core
  * path the kernels apply the maps on the fly, in fp32, to the raw tiles they load
- * (forward and backward alike; the prepared values are never stored) and chain the
- * gradients before writing them.  On the fp32 CUDA-core path dr_fwd / dr_fwd_u write
+ * (forward and backward alike; the prepared values are never stored, only the two
+ * inverse row norms per token and head, 8 bytes, which dr_workspace_bytes counts and
+ * the backward reads back) and chain the gradients before writing them.  On the fp32 CUDA-core path dr_fwd / dr_fwd_u write
  * q_hat, k_hat (io_dtype), beta and g (fp32) into the workspace (dr_workspace_bytes
  * counts them) and run on those; with DR_FLAG_REUSE_FWD the backward reuses them (the
  * same raw inputs must be passed).  dr_decode applies the maps in its own kernel.

@@ -184,13 +184,16 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
 
 def test_prepare_flag_host_rules(lib):
     """DR_FLAG_PREPARE_INPUTS: accepted by dr_workspace_bytes; the bf16 tensor-core
-    path prepares on the fly and needs no more workspace, the fp32 CUDA-core path
-    adds room for the prepared tensors (two q/k-sized buffers in the io dtype plus
-    fp32 beta and gate); refused by dr_fwd_noalloc; an unknown flag bit stays an
-    error."""
+    path prepares on the fly and keeps only the two inverse row norms per token and
+    head (fp32, 512 bytes per chunk record), the fp32 CUDA-core path adds room for the
+    prepared tensors (two q/k-sized buffers in the io dtype plus fp32 beta and gate);
+    refused by dr_fwd_noalloc; an unknown flag bit stays an error."""
     n = B.DR_FLAG_PREPARE_INPUTS
     for kw in (dict(), dict(variant=B.DR_KDA)):
-        assert B.workspace_bytes(desc(flags=n, **kw)) == B.workspace_bytes(desc(**kw)) > 0
+        d = desc(**kw)
+        recs = (d.T + 63) // 64 * d.B * d.H
+        extra = B.workspace_bytes(desc(flags=n, **kw)) - B.workspace_bytes(d)
+        assert recs * 512 <= extra <= recs * 512 + 1023
     for kw, gate_per_token in ((dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16), 1),
                                (dict(io_dtype=B.DR_F32, d_k=32, d_v=32, chunk=16,
                                      variant=B.DR_KDA), 128),
