@@ -44,21 +44,21 @@ def algorithmic(w, N):
 
 
 _FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
-            "4edc339d709f3de31f5a891fd8b115a850e4b1f42e9a1e0b560ca89e352ca346")
+            "1cb81b05a16537b25013d8d8663ff867b0210c31424a42917f9128baa14dd212")
 _BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-            "0b905a15462f5bbd66f4f466e50794e4701b36d687842bde78419a855cb37ecc")
+            "0bd7bce301b09773ea6d497ffdb76168506e08b8276c05c7b4697638a3a1bd56")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
 # from an ncu capture of the timed step of the full-size workload (profiles/
 # dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424774912 + 687097344, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687267328 + 496396288, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541224960 + 361376512, _BWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418498816 + 383116288, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_prep"): (691221760 + 690995200, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678714112 + 497501184, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541130496 + 361172480, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1694795264 + 637413376, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424884992 + 687267328, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687681280 + 495318528, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541131520 + 360587008, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418619136 + 382836992, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (690833152 + 691175680, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678957056 + 498136320, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541140736 + 361083648, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1698728704 + 637552896, _BWD_SRC),
 }
 
 
