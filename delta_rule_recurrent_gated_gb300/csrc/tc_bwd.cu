@@ -768,7 +768,19 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             }
             if (VAR == DR_KDA) tma_prefetch_3d(&mg, 0, nh, nr0);  // its gates (one box)
         }
-        ok = mbar_wait(&bar_tok, ph, kWaitLimitNs);
+        // two products of M0 read the state side only: thread 0 issues them while the token
+        // tiles land (the state side was issued during the previous item's last stages)
+        bool st_ok = true;
+        if (tid == 0) {
+            st_ok = mbar_wait(&bar_st, ph, kWaitLimitNs);
+            if (st_ok) {
+                tc_fence_after();
+                mma_tiles(tm + C1, Tile{smem_u32(Sst), D}, true, Tile{smem_u32(dUts), D}, true, D, 64, D, false);
+                mma_tiles(tm + C_dKC, Tile{smem_u32(dSst), D}, true, Tile{smem_u32(Ust), 64}, false, D, 64, D,
+                          false);
+            }
+        }
+        ok = mbar_wait(&bar_tok, ph, kWaitLimitNs) && st_ok;
         if (VAR == DR_KDA) ok = ok && mbar_wait(&bar_st, ph, kWaitLimitNs);  // the gates
         if (__syncthreads_or(!ok)) break;
         zero_pad_rows(Qs, D, len);
@@ -933,14 +945,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         ok = mbar_wait(&bar_st, ph, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
 
-        // M0 (M = D): dQt^T = S dO^T -> C0 ; -dWyA^T = S (-dU)^T -> C1 ; dKC^T = dS U^T -> C_dKC
+        // M0 (M = D): dQt^T = S dO^T -> C0 ; -dWyA^T = S (-dU)^T -> C1 and dKC^T = dS U^T -> C_dKC
+        // were issued at the start of the item; the commit covers them
         if (tid == 0) {
             tc_fence_after();
-            const Tile tS{smem_u32(Sst), D};
-            mma_tiles(tm + C0, tS, true, Tile{smem_u32(dOs), 64}, false, D, 64, D, false);
-            mma_tiles(tm + C1, tS, true, Tile{smem_u32(dUts), D}, true, D, 64, D, false);
-            mma_tiles(tm + C_dKC, Tile{smem_u32(dSst), D}, true, Tile{smem_u32(Ust), 64}, false, D, 64, D,
-                      false);
+            mma_tiles(tm + C0, Tile{smem_u32(Sst), D}, true, Tile{smem_u32(dOs), 64}, false, D, 64, D, false);
             mma_commit(&bar_mma);
         }
         // while M0 runs: dgC[c] = sum_v dS[c, v] S[c, v] (eight channels by a block of
