@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
                 bulk_s2g(ds_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
             bulk_commit();
         }
+        if (tid == 0) bulk_wait_read();  // the previous chunk's -dU^T image has left dUs
         ok = mbar_wait(&bar_ld[s], (it >> 1) & 1, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
 
@@ -255,7 +256,6 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         }
         if (tid == kIss) bulk_wait_read();  // the dS image has left Ws
         if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
-        if (tid == 0) bulk_wait_read();     // the -dU^T image has left dUs
         __syncthreads();
         tc_fence_after();
         const float* gCs = reinterpret_cast<const float*>(st + S::kG) + cbase;
