@@ -67,8 +67,11 @@ constexpr int kScanBwdMathThreads = 256;
 template <int D, int BV>
 struct BScanSmem {
     static constexpr int kTile = 64 * D * 2;
-    static constexpr int kW = 0;                 // [BV][D]  dS^T slice (bf16 operand)
-    static constexpr int kdU = BV * D * 2;       // [BV][64] -dU^T operand
+    // [BV][D] dS^T slice (bf16 operand); with 64-row value tiles two of them, the chunk's
+    // and the previous one's, so the update need not wait for the dS image copy
+    static constexpr int kWBufs = BV == 64 ? 2 : 1, kWBytes = BV * D * 2;
+    static constexpr int kW = 0;
+    static constexpr int kdU = kWBufs * kWBytes;  // [BV][64] -dU^T operand
     static constexpr int kStage0 = kdU + BV * 128;
     // stage layout: KC, Qt, Wy [64][D] tiles; dO [64 tokens][BV] tile; gC [D] fp32;
     // rows [v0, v0+BV) of the -dU^T image of the emitted write's gradient (dr_bwd_u)
@@ -76,6 +79,7 @@ struct BScanSmem {
                          kG = kdO + BV * 128, kdUx = kG + D * 4;
     static constexpr int kStageBytes = (kdUx + BV * 128 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
+    static_assert(kBytes <= 232448 - 1024, "shared memory of one CTA");
     static constexpr uint32_t kStageTx = 3 * kTile + BV * 128 + D * 4;
 };
 
@@ -170,14 +174,19 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         const int s = it & 1, ci = nc - 1 - it;
         uint8_t* st = sm + S::kStage0 + s * S::kStageBytes;
         const size_t rec = (size_t)(c0 + ci) * p.H + h;
+        // this chunk's dS operand, and the one its update writes
+        uint8_t* Wc = Ws + (S::kWBufs == 2 ? (it & 1) * S::kWBytes : 0);
+        uint8_t* Wn = Ws + (S::kWBufs == 2 ? ((it + 1) & 1) * S::kWBytes : 0);
         if (tid == kIss) {
             // the next chunk's tiles into stage s^1 (released at the end of the previous
             // iteration), then rows [v0, v0+BV) of the W-layout image of dS at this chunk's end
             if (it + 1 < nc) load_iter(it + 1);
             uint8_t* ds_img = L.dS + rec * (size_t)D * D * 2;
             for (int kb = 0; kb < D / 64; ++kb)
-                bulk_s2g(ds_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
+                bulk_s2g(ds_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Wc + kb * BV * 128, BV * 128);
             bulk_commit();
+            // two dS tiles: the previous dS image has left the one this chunk's update writes
+            if (S::kWBufs == 2) bulk_wait_read_but_newest();
         }
         if (tid == 0) bulk_wait_read();  // the previous chunk's -dU^T image has left dUs
         ok = mbar_wait(&bar_ld[s], (it >> 1) & 1, kWaitLimitNs);
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         // depend on the chain and runs during the -dU^T epilogue
         if (tid == 0) {
             tc_fence_after();
-            mma_tiles(tm + 0, Tile{smem_u32(Ws), BV}, false, Tile{smem_u32(st + S::kKC), 64}, false, BV, 64, D,
+            mma_tiles(tm + 0, Tile{smem_u32(Wc), BV}, false, Tile{smem_u32(st + S::kKC), 64}, false, BV, 64, D,
                       false);
             mma_commit(&bar_mma);
             mma_tiles(tm + 64, Tile{smem_u32(st + S::kdO), 64}, true, Tile{smem_u32(st + S::kQt), 64}, true, BV,
@@ -254,9 +263,9 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
             bulk_s2g(L.dU + rec * kTile + (size_t)v0 * 128, dUs, BV * 128);
             bulk_commit();
         }
-        if (tid == kIss) bulk_wait_read();  // the dS image has left Ws
+        if (S::kWBufs == 1 && tid == kIss) bulk_wait_read();  // the dS image has left Ws
         if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
-        __syncthreads();
+        if (S::kWBufs == 1) __syncthreads();
         tc_fence_after();
         const float* gCs = reinterpret_cast<const float*>(st + S::kG) + cbase;
         if (math) {
@@ -283,8 +292,8 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
                     }
                 }
                 if (r >= 0) {
-                    tile_store16(Ws, r, cbase + cb * 16, BV, acc);
-                    if (kPair) tile_store16(Ws, r, cbase + (cb + 1) * 16, BV, acc2);
+                    tile_store16(Wn, r, cbase + cb * 16, BV, acc);
+                    if (kPair) tile_store16(Wn, r, cbase + (cb + 1) * 16, BV, acc2);
                 }
             }
         }

@@ -629,8 +629,11 @@ __global__ void __launch_bounds__(128, 1)
 template <int D, int BV>
 struct ScanSmem {
     static constexpr int kTile = 64 * D * 2;
-    static constexpr int kW = 0;                       // [BV][D] state W (bf16 operand)
-    static constexpr int kUs = BV * D * 2;             // [64][BV] U operand
+    // [BV][D] state W (bf16 operand); with 64-row value tiles two of them, the chunk's
+    // and the next one's, so the state update need not wait for the state image copy
+    static constexpr int kWBufs = BV == 64 ? 2 : 1, kWBytes = BV * D * 2;
+    static constexpr int kW = 0;
+    static constexpr int kUs = kWBufs * kWBytes;       // [64][BV] U operand
     static constexpr int kStage0 = kUs + BV * 128;
     // stage layout: [Wy; Qt] as one [128][D] tile (column block b holds the 64 Wy rows,
     // then the 64 Qt rows), KC [64][D]; Ut, Ot [64][BV] (columns v0 .. v0+BV-1 of their
@@ -639,6 +642,7 @@ struct ScanSmem {
                          kG = kOt + BV * 128;
     static constexpr int kStageBytes = (kG + D * 4 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kStage0 + 2 * kStageBytes + 1024;
+    static_assert(kBytes <= 232448 - 1024, "shared memory of one CTA");
     static constexpr uint32_t kStageTx = 3 * kTile + 2 * BV * 128 + D * 4;
 };
 
@@ -761,6 +765,9 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
         // o of a whole chunk is written in place over its Ot tile and leaves by tensor
         // stores; a ragged last chunk, and fp32 o, by 16-byte stores of token rows
         const bool tile_o = write_o && stage_o && len == 64;
+        // this chunk's state operand, and the one its state update writes
+        uint8_t* Wc = Ws + (S::kWBufs == 2 ? (ci & 1) * S::kWBytes : 0);
+        uint8_t* Wn = Ws + (S::kWBufs == 2 ? ((ci + 1) & 1) * S::kWBytes : 0);
         if (tid == 0) bulk_wait_read();  // the previous chunk's U image has left Us
         ok = mbar_wait(&bar_ld[s], (ci >> 1) & 1, kWaitLimitNs);
         if (__syncthreads_or(!ok)) break;
@@ -768,17 +775,17 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
         // [Wy; Qt] W^T -> cols [0, BV)
         if (tid == 0) {
             tc_fence_after();
-            mma_tiles(tm, Tile{smem_u32(st + S::kWQ), 128}, false, Tile{smem_u32(Ws), BV}, false, 128, BV, D,
+            mma_tiles(tm, Tile{smem_u32(st + S::kWQ), 128}, false, Tile{smem_u32(Wc), BV}, false, 128, BV, D,
                       false);
             mma_commit(&bar_mma);
         }
         if (tid == kIss) {
             // the chunk-start state rows [v0, v0+BV) of the W-layout state image; then,
-            // once the previous chunk's o tiles have left stage s^1, the next chunk's
-            // tiles into it
+            // once the previous chunk's o tiles have left stage s^1 (and, with two state
+            // tiles, the previous state image the other tile), the next chunk's tiles
             uint8_t* s_img = L.S + rec * (size_t)D * D * 2;
             for (int kb = 0; kb < D / 64; ++kb)
-                bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Ws + kb * BV * 128, BV * 128);
+                bulk_s2g(s_img + (size_t)kb * D * 128 + (size_t)v0 * 128, Wc + kb * BV * 128, BV * 128);
             bulk_commit();
             bulk_wait_read_but_newest();
             if (ci + 1 < nc) load_chunk(ci + 1);
@@ -853,13 +860,17 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
             if (tile_o) {
                 for (int b = 0; b < BV / 64; ++b) tma_store_3d(&mo, st + S::kOt + b * 8192, v0 + 64 * b, h, row0);
                 bulk_commit();
-                bulk_wait_read_but_newest();  // the state image has left Ws
-            } else {
-                bulk_wait_read();
+            }
+            // one state tile: the state image has left it before the update rewrites it
+            if (S::kWBufs == 1) {
+                if (tile_o)
+                    bulk_wait_read_but_newest();
+                else
+                    bulk_wait_read();
             }
         }
         if (math && !mbar_wait(&bar_mma, 1, kWaitLimitNs)) s_fail = 1;
-        __syncthreads();  // the state image has left Ws, rewritten below
+        if (S::kWBufs == 1) __syncthreads();  // the state image has left Ws, rewritten below
         tc_fence_after();
         const float* gCs = reinterpret_cast<const float*>(st + S::kG) + cbase;
         if (math) {
@@ -886,8 +897,8 @@ __global__ void __launch_bounds__(kScanFwdThreads, 1)
                     }
                 }
                 if (r >= 0) {
-                    tile_store16(Ws, r, cbase + cb * 16, BV, acc);
-                    if (kPair) tile_store16(Ws, r, cbase + (cb + 1) * 16, BV, acc2);
+                    tile_store16(Wn, r, cbase + cb * 16, BV, acc);
+                    if (kPair) tile_store16(Wn, r, cbase + (cb + 1) * 16, BV, acc2);
                 }
             }
         }
