@@ -188,21 +188,25 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
             // two dS tiles: the previous dS image has left the one this chunk's update writes
             if (S::kWBufs == 2) bulk_wait_read_but_newest();
         }
-        if (tid == 0) bulk_wait_read();  // the previous chunk's -dU^T image has left dUs
-        ok = mbar_wait(&bar_ld[s], (it >> 1) & 1, kWaitLimitNs);
-        if (__syncthreads_or(!ok)) break;
-
+        // no block barrier here: the previous iteration ended with one (its update is
+        // complete), and the threads that read this chunk's stage wait for it themselves
+        const uint32_t ldph = (it >> 1) & 1;
         // dU^T = dS^T KC^T -> cols [0,64); then dO^T Qt -> cols [64, 64+D), which does not
         // depend on the chain and runs during the -dU^T epilogue
         if (tid == 0) {
-            tc_fence_after();
-            mma_tiles(tm + 0, Tile{smem_u32(Wc), BV}, false, Tile{smem_u32(st + S::kKC), 64}, false, BV, 64, D,
-                      false);
-            mma_commit(&bar_mma);
-            mma_tiles(tm + 64, Tile{smem_u32(st + S::kdO), 64}, true, Tile{smem_u32(st + S::kQt), 64}, true, BV,
-                      D, 64, false);
+            if (mbar_wait(&bar_ld[s], ldph, kWaitLimitNs)) {
+                tc_fence_after();
+                mma_tiles(tm + 0, Tile{smem_u32(Wc), BV}, false, Tile{smem_u32(st + S::kKC), 64}, false, BV, 64,
+                          D, false);
+                mma_commit(&bar_mma);
+                mma_tiles(tm + 64, Tile{smem_u32(st + S::kdO), 64}, true, Tile{smem_u32(st + S::kQt), 64}, true,
+                          BV, D, 64, false);
+            } else {
+                s_fail = 1;
+            }
         }
-        if (math && !mbar_wait(&bar_mma, 0, kWaitLimitNs)) s_fail = 1;
+        if (math && (!mbar_wait(&bar_mma, 0, kWaitLimitNs) || !mbar_wait(&bar_ld[s], ldph, kWaitLimitNs)))
+            s_fail = 1;
         tc_fence_after();
         if (math && BV == 64) {  // -dU^T for this thread's 16 tokens [32 hf + 16 h2, + 16)
             float acc[16];
@@ -252,7 +256,10 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        if (__syncthreads_or(s_fail != 0)) {
+            ok = false;
+            break;
+        }
 
         // + (-dU^T) Wy -> cols [64, 64+D); -dU^T rows [v0, v0+BV) of its image
         if (tid == 0) {
@@ -297,6 +304,7 @@ __global__ void __launch_bounds__(kScanBwdThreads, 1)
                 }
             }
         }
+        if (tid == 0) bulk_wait_read();  // the -dU^T image has left dUs before the next epilogue
         fence_async_smem();
         tc_fence_before();
         if (__syncthreads_or(s_fail != 0)) {
