@@ -44,21 +44,21 @@ def algorithmic(w, N):
 
 
 _FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
-            "1cb81b05a16537b25013d8d8663ff867b0210c31424a42917f9128baa14dd212")
+            "4f0e051b2df760d834e63a9e3e31ee1a92d2c8591d394d3a0dd7e574cb3b4434")
 _BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-            "455b7892682197f83e2104d9926b922ddc9f29859e344c4b0b0e6c1ae1acd48e")
+            "9f16e087f44647aaf51c598544c1528d391854d0e0d690074cd082d20bbf726a")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
 # from an ncu capture of the timed step of the full-size workload (profiles/
 # dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424736256 + 687255296, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (686689024 + 495737600, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541112064 + 360923392, _BWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418497280 + 382756352, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_prep"): (690806528 + 691228160, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678980864 + 497375488, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541134848 + 361299968, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1692093696 + 637578240, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (425014528 + 687373824, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687610112 + 495004416, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541140224 + 359937280, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418521856 + 382640640, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (690923008 + 691225344, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678699264 + 498061312, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541133056 + 360072704, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1695348480 + 637328640, _BWD_SRC),
 }
 
 
