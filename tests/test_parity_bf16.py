@@ -60,6 +60,23 @@ def test_fwd_bwd_packed(variant):
     compare(w, x, run_gpu(w, x), run_oracle(w, x))
 
 
+# 128 (sequence, head) units or more: the scans take 128-row value tiles, the shape of the
+# full-size workloads, here with ragged tails and packed sequences at a size the oracle
+# runs whole
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fwd_bwd_many_units_ragged(variant):
+    w = inputs.small(variant, B=8, T=130, H=16, dk=128, dv=128)
+    x = inputs.make(w, seed=11)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_fwd_bwd_many_units_packed(variant):
+    w = inputs.small(variant, H=16, dk=128, dv=128, lengths=[200, 64, 1, 130, 0, 65, 191, 7])
+    x = inputs.make(w, seed=12)
+    compare(w, x, run_gpu(w, x), run_oracle(w, x))
+
+
 @pytest.mark.parametrize("variant", ["gdn", "kda"])
 def test_backward_recompute_matches_reuse(variant):
     w = inputs.small(variant, B=2, T=300, H=2, dk=128, dv=128)
