@@ -27,6 +27,8 @@
 // state-side products dO S^T, dU S^T, U dS^T and rowsum(dS * S), then the rest).
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "tc.cuh"
 #include "tc_layout.cuh"
@@ -537,7 +539,7 @@ __device__ __forceinline__ ChunkRoles chunk_roles(uint8_t* sm, int kTile, bool o
     return ChunkRoles{P(0), P(4), P(4), P(5), P(5), P(6), P(7)};
 }
 
-template <int D, int VAR, bool PREP>
+template <int D, int VAR, bool PREP, bool F32OUT>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, grp = warp >> 2, lane = tid & 31;
     const int nitems = p.num_chunks * p.H;  // work item = (chunk, head), item = chunk * H + h
     const float sc = p.scale;
-    const bool f32out = p.grad_dtype == DR_F32;
+    constexpr bool f32out = F32OUT;  // fp32 gradients (else bf16): one compact loop per type
 
     if (tid == 0) {
         mbar_init(&bar_st, 1);
@@ -1557,20 +1559,26 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         }
         return cudaGetLastError();
     };
-    static std::atomic<unsigned long long> a0{0}, a1{0}, a2{0}, a3{0}, a4{0}, a5{0};
+    // one attribute flag per instantiation (variant x preparation x gradient type)
+    static std::atomic<unsigned long long> attr[12];
+    auto pick = [&](auto var, auto prep) -> cudaError_t {
+        constexpr int V = decltype(var)::value;
+        constexpr bool P = decltype(prep)::value;
+        constexpr int slot = (V * 2 + (P ? 1 : 0)) * 2;
+        if (p.grad_dtype == DR_F32)
+            return chunk_launch(tc_bwd_chunk_kernel<D, V, P, true>, BChunkSmem<D, V>::kBytes, attr[slot + 1]);
+        return chunk_launch(tc_bwd_chunk_kernel<D, V, P, false>, BChunkSmem<D, V>::kBytes, attr[slot]);
+    };
+    using DN = std::integral_constant<int, DR_DELTANET>;
+    using GD = std::integral_constant<int, DR_GDN>;
+    using KD = std::integral_constant<int, DR_KDA>;
     switch (p.variant * 2 + (p.prepare ? 1 : 0)) {
-        case 2 * DR_DELTANET:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET, false>, BChunkSmem<D, DR_DELTANET>::kBytes, a0);
-        case 2 * DR_DELTANET + 1:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_DELTANET, true>, BChunkSmem<D, DR_DELTANET>::kBytes, a3);
-        case 2 * DR_GDN:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN, false>, BChunkSmem<D, DR_GDN>::kBytes, a1);
-        case 2 * DR_GDN + 1:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_GDN, true>, BChunkSmem<D, DR_GDN>::kBytes, a4);
-        case 2 * DR_KDA:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA, false>, BChunkSmem<D, DR_KDA>::kBytes, a2);
-        default:
-            return chunk_launch(tc_bwd_chunk_kernel<D, DR_KDA, true>, BChunkSmem<D, DR_KDA>::kBytes, a5);
+        case 2 * DR_DELTANET: return pick(DN{}, std::false_type{});
+        case 2 * DR_DELTANET + 1: return pick(DN{}, std::true_type{});
+        case 2 * DR_GDN: return pick(GD{}, std::false_type{});
+        case 2 * DR_GDN + 1: return pick(GD{}, std::true_type{});
+        case 2 * DR_KDA: return pick(KD{}, std::false_type{});
+        default: return pick(KD{}, std::true_type{});
     }
 }
 

@@ -38,3 +38,31 @@ def test_bf16_o_against_oracle(variant, shape):
     assert np.all(err <= np.abs(r) * 2.0 ** -9 + tol), float(err.max())
     # hT is written in fp32 either way
     assert float(np.max(np.abs(got["hT"] - ref["hT"]))) <= tolerance(w, ref["hT"])
+
+
+# bf16 gradients (the step the benchmark times writes dq, dk, dv in bf16): each within the
+# same bound, half a bf16 ulp of the value over the tolerance; dbeta, dg and dh0 are fp32
+GRAD_CASES = [
+    ("gdn", dict(B=8, T=130, H=16)),      # 128-row value tiles, a ragged last chunk
+    ("kda", dict(B=2, T=200, H=2)),       # 64-row value tiles
+    ("deltanet", dict(H=2, lengths=[100, 0, 64, 1, 191, 7])),  # packed
+]
+
+
+@pytest.mark.parametrize("variant,shape", GRAD_CASES)
+def test_bf16_gradients_against_oracle(variant, shape):
+    w = inputs.small(variant, dk=128, dv=128, **shape)
+    x = inputs.make(w, seed=82)
+    got = run_gpu(w, x, out="bf16", grad="bf16")
+    ref = run_oracle(w, x)
+    for name in ("dq", "dk", "dv", "dbeta", "dg", "dh0"):
+        if ref.get(name) is None or got.get(name) is None:
+            continue
+        r = ref[name]
+        g = got[name].astype(np.float64)
+        assert np.all(np.isfinite(g)), name
+        err = np.abs(g - r)
+        tol = tolerance(w, r)
+        record(w, f"{name} (bf16)", float(err.max()) if err.size else 0.0,
+               float(np.abs(r).max()) if r.size else 0.0, tol)
+        assert np.all(err <= np.abs(r) * 2.0 ** -9 + tol), (name, float(err.max()))
