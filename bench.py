@@ -46,19 +46,19 @@ def algorithmic(w, N):
 _FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
             "4f0e051b2df760d834e63a9e3e31ee1a92d2c8591d394d3a0dd7e574cb3b4434")
 _BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-            "9f16e087f44647aaf51c598544c1528d391854d0e0d690074cd082d20bbf726a")
+            "89a3139adb29964150c184b63c62a4fc75cd821736a3372a74fc94a0228036d4")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
 # from an ncu capture of the timed step of the full-size workload (profiles/
 # dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (425014528 + 687373824, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687610112 + 495004416, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541140224 + 359937280, _BWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418521856 + 382640640, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_prep"): (690923008 + 691225344, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678699264 + 498061312, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541133056 + 360072704, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1695348480 + 637328640, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424871168 + 687171328, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687655936 + 495103232, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541115136 + 360482560, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418457600 + 383343104, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (690775552 + 691168256, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (679926528 + 497256192, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541209856 + 360693760, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1691661312 + 637162496, _BWD_SRC),
 }
 
 
