@@ -590,9 +590,9 @@ __global__ void __launch_bounds__(128, 1)
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
 
+        // Qt in place over Qb' (each thread rewrites the elements it read), Ot in the
+        // consumed v tile; their [64][D] SW128 workspace images are bulk copies of the tiles
         {
-            uint8_t* qt_img = L.Qt + rec * kTile;
-            uint8_t* ot_img = L.Ot + rec * kTile;  // [64][D] SW128 tile image of Ot
             const float sc = p.scale;
             for (int cb = 0; cb < D / 32; ++cb) {
                 float w16[16], o16[16], qb[16];
@@ -606,9 +606,16 @@ __global__ void __launch_bounds__(128, 1)
                     qb[j] = sc * (qb[j] * Rf[c0 + j] - w16[j]);
                     o16[j] *= sc;
                 }
-                tile_store16(qt_img, r2, c0, 64, qb);
-                tile_store16(ot_img, r2, c0, 64, o16);
+                tile_store16(Qs, r2, c0, 64, qb);
+                tile_store16(Vs, r2, c0, 64, o16);
             }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(L.Qt + rec * kTile, Qs, kTile);
+            bulk_s2g(L.Ot + rec * kTile, Vs, kTile);
+            bulk_commit();
         }
     } while (0);
 
