@@ -39,6 +39,7 @@ using namespace tc;
 
 bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows);
 bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows, int box_rows);
+bool make_out_map(CUtensorMap* m, void* ptr, int D, int H, long long rows, bool f32);
 TcLayout tc_layout(const Params& p);
 cudaError_t tc_fwd(const Params& p, cudaStream_t st, bool write_o);
 
@@ -543,7 +544,9 @@ template <int D, int VAR, bool PREP, bool F32OUT>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     tc_bwd_chunk_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-                        const __grid_constant__ CUtensorMap mg, const Params p, const TcLayout L) {
+                        const __grid_constant__ CUtensorMap mg, const __grid_constant__ CUtensorMap mgq,
+                        const __grid_constant__ CUtensorMap mgk, const __grid_constant__ CUtensorMap mgv,
+                        const Params p, const TcLayout L) {
     using S = BChunkSmem<D, VAR>;
     constexpr int kTile = S::kTile;
     extern __shared__ uint8_t smem_raw[];
@@ -594,6 +597,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         prefetch_tmap(&mv);
         prefetch_tmap(&mdo);
         if (VAR == DR_KDA) prefetch_tmap(&mg);
+        if (!PREP) {
+            prefetch_tmap(&mgq);
+            prefetch_tmap(&mgk);
+            prefetch_tmap(&mgv);
+        }
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -674,6 +682,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     auto stage_base = [&](uint8_t* lo, uint8_t* hi, bool f32) -> uint8_t* {
         const int esz = f32 ? 4 : 2;
         return (t0 >= 32 ? hi : lo) + (t0 & 31) * D * esz + (cl < 0 ? 0 : cl) * esz;
+    };
+    // a whole chunk's staged rows leave as two tensor stores of 32 tokens (thread kIssuer,
+    // after the staging barrier); the copy warp waits for them to read the staging tiles
+    // before anything refills those
+    auto tensor_out = [&](const CUtensorMap* map, const uint8_t* lo, const uint8_t* hi, int hh, int r0) {
+        tma_store_3d(map, lo, 0, hh, r0);
+        tma_store_3d(map, hi, 0, hh, r0 + 32);
+        bulk_commit();
     };
     // dGamma of this thread's channel and tokens (KDA), or its share of each token's
     // dGamma (GDN), is accumulated in TMEM columns C1 + t0 .. + kTok - 1 from E4 on
@@ -763,6 +779,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         chunk_info(p, chunk, seq, row0, len);
         const int next = item + gridDim.x;
         const ChunkRoles R = chunk_roles(sm, kTile, odd);
+        // dq, dk, dv by tensor stores for whole chunks; per thread for a ragged chunk and with
+        // input preparation (whose write-out chains every row through its norm)
+        const bool tstore = !PREP && len == 64;
         uint8_t* Qs = R.Q;      // q -> Qb
         uint8_t* Ust = R.U;     // [64][D] U
         uint8_t* dQs = R.dQ;    // dQt^T = S dO^T
@@ -1186,11 +1205,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dv_stage(BoolTag<true>{});
         else
             dv_stage(BoolTag<false>{});
+        fence_async_smem();
         __syncthreads();
-        if (f32out)
+        if (tstore) {
+            if (tid == kIssuer) tensor_out(&mgv, Vs, dOs, h, row0);
+        } else if (f32out) {
             stage_copy_out<D, true>(p.dv_, Vs, dOs, p, row0, len, h);
-        else
+        } else {
             stage_copy_out<D, false>(p.dv_, Vs, dOs, p, row0, len, h);
+        }
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
@@ -1252,6 +1275,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dq_stage(BoolTag<true>{});
         else
             dq_stage(BoolTag<false>{});
+        fence_async_smem();  // the staged dq rows may leave by a tensor store
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
@@ -1305,11 +1329,17 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 stage_copy_out_prep<D, true, kSrc>(p.dq, dUts, dWys, p, row0, len, h, nullptr, rq_s, Qs, rf, Gam);
             else
                 stage_copy_out_prep<D, false, kSrc>(p.dq, dUts, dWys, p, row0, len, h, nullptr, rq_s, Qs, rf, Gam);
-        } else if (f32out)
+        } else if (tstore) {
+            if (tid == kIssuer) tensor_out(&mgq, dUts, dWys, h, row0);
+        } else if (f32out) {
             stage_copy_out<D, true>(p.dq, dUts, dWys, p, row0, len, h);
-        else
+        } else {
             stage_copy_out<D, false>(p.dq, dUts, dWys, p, row0, len, h);
+        }
         fence_async_smem();  // generic accesses of the buffers the next item's state goes to
+        // the dv and dq stores have read their staging tiles before the next item's state
+        // side and the dk stage refill them
+        if (tid == kIssuer) bulk_wait_read();
         ok = mma_done();
         if (__syncthreads_or(!ok)) break;
         tc_fence_after();
@@ -1356,8 +1386,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dk_stage(BoolTag<true>{});
         else
             dk_stage(BoolTag<false>{});
+        fence_async_smem();
         __syncthreads();
-        if (PREP) {
+        if (tstore) {
+            if (tid == kIssuer) tensor_out(&mgk, Vs, dOs, h, row0);
+        } else if (PREP) {
             // k_hat from the Kr' tile times e^{Gamma - Gamma_r} per row (GDN) or nothing
             // (DeltaNet); KDA's per-element factors are gone by now (its array already holds
             // the next item's gates), so it re-reads the raw rows
@@ -1368,15 +1401,19 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 stage_copy_out_prep<D, true, kSrc>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s, Ks, rf, nullptr);
             else
                 stage_copy_out_prep<D, false, kSrc>(p.dk_, Vs, dOs, p, row0, len, h, rawk, rk_s, Ks, rf, nullptr);
-        } else if (f32out)
+        } else if (f32out) {
             stage_copy_out<D, true>(p.dk_, Vs, dOs, p, row0, len, h);
-        else
+        } else {
             stage_copy_out<D, false>(p.dk_, Vs, dOs, p, row0, len, h);
+        }
         // the next item's token side goes into the Kb / Kr / staging tiles
         fence_async_smem();
         __syncthreads();
         if (next < nitems) {
-            if (tid == kIssuer) issue_tok(next, !odd);
+            if (tid == kIssuer) {
+                bulk_wait_read();  // the dk store has read the staging tiles
+                issue_tok(next, !odd);
+            }
             load_scalars(next);
             ++n_tok;
         }
@@ -1471,6 +1508,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         for (uint32_t q = (uint32_t)it; q < n_st; ++q) mbar_wait(&bar_st, q & 1, kWaitLimitNs);
         for (uint32_t q = (uint32_t)it; q < n_tok; ++q) mbar_wait(&bar_tok, q & 1, kWaitLimitNs);
     }
+    if (tid == kIssuer) bulk_wait_all();  // the last item's gradient stores
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
@@ -1512,6 +1550,11 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         !make_token_map(&mv, p.v, D, p.H, rows) || !make_token_map(&mdo, p.dO, D, p.H, rows))
         return cudaErrorInvalidValue;
     if (p.variant == DR_KDA ? !make_gate_map(&mg, p.g, D, p.H, rows, 64) : !make_token_map(&mg, p.q, D, p.H, rows))
+        return cudaErrorInvalidValue;
+    CUtensorMap mgq, mgk, mgv;  // dq, dk, dv written by tensor stores
+    const bool gf32 = p.grad_dtype == DR_F32;
+    if (!make_out_map(&mgq, p.dq, D, p.H, rows, gf32) || !make_out_map(&mgk, p.dk_, D, p.H, rows, gf32) ||
+        !make_out_map(&mgv, p.dv_, D, p.H, rows, gf32))
         return cudaErrorInvalidValue;
     if (p.dU && p.num_chunks > 0) {
         TraceScope ts("pack_dux", st);
@@ -1555,7 +1598,7 @@ cudaError_t tc_bwd_d(const Params& p, cudaStream_t st, bool reuse) {
         const int grid = (int)(items < nsm ? items : nsm);
         {
             TraceScope ts("tc_bwd_chunk", st);
-            kernel<<<grid, kChunkThreads, smem, st>>>(mq, mk, mv, mdo, mg, p, L);
+            kernel<<<grid, kChunkThreads, smem, st>>>(mq, mk, mv, mdo, mg, mgq, mgk, mgv, p, L);
         }
         return cudaGetLastError();
     };

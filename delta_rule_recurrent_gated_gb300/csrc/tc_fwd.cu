@@ -991,6 +991,21 @@ bool make_token_map(CUtensorMap* m, const void* ptr, int D, int H, long long row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output rows [rows][H][D] (bf16 or fp32) written by tensor stores: one box is the D values
+// of 32 consecutive tokens of one head, dense (no swizzle) in shared memory
+bool make_out_map(CUtensorMap* m, void* ptr, int D, int H, long long rows, bool f32) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int esz = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)D * esz, (cuuint64_t)H * D * esz};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, 32};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr,
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp32 per-key-channel gates [rows][H][D]: one box is the D gates of box_rows tokens of
 // one head, dense (no swizzle) in shared memory
 bool make_gate_map(CUtensorMap* m, const void* ptr, int D, int H, long long rows, int box_rows) {
