@@ -44,21 +44,21 @@ def algorithmic(w, N):
 
 
 _FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
-            "4f0e051b2df760d834e63a9e3e31ee1a92d2c8591d394d3a0dd7e574cb3b4434")
+            "cc35122664e52feb61b1e5bc8fceccfdd30e7d046d1767f11a1e4d53cd275fc8")
 _BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-            "89a3139adb29964150c184b63c62a4fc75cd821736a3372a74fc94a0228036d4")
+            "638af57cea24d29a4a850f3e3216b1f75b92fc4648c177b102cf261e21c53151")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
 # from an ncu capture of the timed step of the full-size workload (profiles/
 # dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (424871168 + 687171328, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687655936 + 495103232, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541115136 + 360482560, _BWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418457600 + 383343104, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_prep"): (690775552 + 691168256, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (679926528 + 497256192, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541209856 + 360693760, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1691661312 + 637162496, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (430415872 + 686169600, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687848192 + 495548928, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541123584 + 360243968, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418461184 + 383065600, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (693804544 + 691300096, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678966272 + 497432576, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541111552 + 360175616, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1690303232 + 637799424, _BWD_SRC),
 }
 
 
