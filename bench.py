@@ -46,19 +46,19 @@ def algorithmic(w, N):
 _FWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_fwd.cu",
             "cc35122664e52feb61b1e5bc8fceccfdd30e7d046d1767f11a1e4d53cd275fc8")
 _BWD_SRC = ("delta_rule_recurrent_gated_gb300/csrc/tc_bwd.cu",
-            "638af57cea24d29a4a850f3e3216b1f75b92fc4648c177b102cf261e21c53151")
+            "da69fd81708bc3ef9f74f066f270bd673f5db1a4875a46a25e1090022b9b71bc")
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel,
 # from an ncu capture of the timed step of the full-size workload (profiles/
 # dram_traffic_gdn_kda_b8_t4096_h16_d128.md), with the source file it was taken on
 MEASURED_TRAFFIC = {
-    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (430415872 + 686169600, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687848192 + 495548928, _FWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541123584 + 360243968, _BWD_SRC),
-    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418461184 + 383065600, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_prep"): (693804544 + 691300096, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (678966272 + 497432576, _FWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541111552 + 360175616, _BWD_SRC),
-    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1690303232 + 637799424, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_prep"): (430136832 + 686508800, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_fwd"): (687477504 + 495796992, _FWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_scan_bwd"): (541128192 + 360294912, _BWD_SRC),
+    ("gdn_h0_b8_t4096_h16_d128", "tc_bwd_chunk"): (1418410240 + 383005184, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_prep"): (693737472 + 691343360, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_fwd"): (679206400 + 497192192, _FWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_scan_bwd"): (541140224 + 360376832, _BWD_SRC),
+    ("kda_b8_t4096_h16_d128", "tc_bwd_chunk"): (1691225856 + 637511680, _BWD_SRC),
 }
 
 

@@ -597,10 +597,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         prefetch_tmap(&mv);
         prefetch_tmap(&mdo);
         if (VAR == DR_KDA) prefetch_tmap(&mg);
+        prefetch_tmap(&mgv);
         if (!PREP) {
             prefetch_tmap(&mgq);
             prefetch_tmap(&mgk);
-            prefetch_tmap(&mgv);
         }
     }
     if (warp == 0) {
@@ -779,9 +779,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         chunk_info(p, chunk, seq, row0, len);
         const int next = item + gridDim.x;
         const ChunkRoles R = chunk_roles(sm, kTile, odd);
-        // dq, dk, dv by tensor stores for whole chunks; per thread for a ragged chunk and with
-        // input preparation (whose write-out chains every row through its norm)
-        const bool tstore = !PREP && len == 64;
+        // dq, dk, dv by tensor stores for whole chunks; per thread for a ragged chunk, and dq,
+        // dk with input preparation (whose write-out chains every row through its norm)
+        const bool tstore = !PREP && len == 64, tstore_v = len == 64;
         uint8_t* Qs = R.Q;      // q -> Qb
         uint8_t* Ust = R.U;     // [64][D] U
         uint8_t* dQs = R.dQ;    // dQt^T = S dO^T
@@ -1207,7 +1207,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             dv_stage(BoolTag<false>{});
         fence_async_smem();
         __syncthreads();
-        if (tstore) {
+        if (tstore_v) {
             if (tid == kIssuer) tensor_out(&mgv, Vs, dOs, h, row0);
         } else if (f32out) {
             stage_copy_out<D, true>(p.dv_, Vs, dOs, p, row0, len, h);

@@ -51,7 +51,7 @@ def test_kernel_design_bytes(bench):
         th * (8 * 128 + 8) + recs * (2 * tile + 2 * dd + 8192 + 512) + th * (6 * 128 + 8))
     # the recorded capture of this workload, while the kernel source is the captured one
     t = bench.measured_traffic("tc_bwd_chunk", w)
-    assert t is None or t == 1418461184 + 383065600
+    assert t is None or t == 1418410240 + 383005184
     assert bench.measured_traffic("tc_bwd_chunk", inputs.get("gdn_b2_t4096_h16_d128")) is None
 
 
