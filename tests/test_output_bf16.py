@@ -43,15 +43,16 @@ def test_bf16_o_against_oracle(variant, shape):
 # bf16 gradients (the step the benchmark times writes dq, dk, dv in bf16): each within the
 # same bound, half a bf16 ulp of the value over the tolerance; dbeta, dg and dh0 are fp32
 GRAD_CASES = [
-    ("gdn", dict(B=8, T=130, H=16)),      # 128-row value tiles, a ragged last chunk
-    ("kda", dict(B=2, T=200, H=2)),       # 64-row value tiles
-    ("deltanet", dict(H=2, lengths=[100, 0, 64, 1, 191, 7])),  # packed
+    ("gdn", 128, dict(B=8, T=130, H=16)),      # 128-row value tiles, a ragged last chunk
+    ("kda", 128, dict(B=2, T=200, H=2)),       # 64-row value tiles
+    ("deltanet", 128, dict(H=2, lengths=[100, 0, 64, 1, 191, 7])),  # packed
+    ("gdn", 64, dict(B=2, T=200, H=3)),        # d = 64: 64-channel rows per store
 ]
 
 
-@pytest.mark.parametrize("variant,shape", GRAD_CASES)
-def test_bf16_gradients_against_oracle(variant, shape):
-    w = inputs.small(variant, dk=128, dv=128, **shape)
+@pytest.mark.parametrize("variant,d,shape", GRAD_CASES)
+def test_bf16_gradients_against_oracle(variant, d, shape):
+    w = inputs.small(variant, dk=d, dv=d, **shape)
     x = inputs.make(w, seed=82)
     got = run_gpu(w, x, out="bf16", grad="bf16")
     ref = run_oracle(w, x)
